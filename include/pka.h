@@ -1,0 +1,203 @@
+/*
+ * pka.h -- C ABI of the paged-KV attention forward for GB300 (sm_103a).
+ *
+ * One serving-engine attention step over a paged KV pool:
+ *   pka_reshape_and_cache   write this step's K/V rows into the pool,
+ *   pka_paged_attn_forward  attention of a mixed, decode-first batch over
+ *                           the pool (split-KV decode, causal / chunked
+ *                           prefill, optional shared-prefix cascade),
+ *   pka_cascade_merge       log-sum-exp merge of two partial attentions.
+ *
+ * Sources, cited by page title and section:
+ *  [FA/FI]   "FlashAttention y FlashInfer: los dos grandes backends de atencion
+ *            en GPU" (vllm-arch-zh.pages.dev/es/attention/flash)
+ *  [blog]    "El especialista del plato estrella: el backend de atencion de
+ *            vLLM (FlashAttention, FlashInfer y la asimetria prefill/decode)"
+ *            (blog.lo0.es)
+ *  [backend] "AttentionBackend: capa de abstraccion de backends de atencion"
+ *            (vllm-arch-zh.pages.dev/es/attention/backend)
+ *
+ * Common rules for every entry point
+ *  - Device buffers are owned by the caller; the library never allocates or
+ *    frees device memory and never synchronises the stream, except
+ *    pka_check_status, which synchronises on purpose.
+ *  - Work is enqueued on `stream` (a cudaStream_t / CUstream passed as
+ *    void*; NULL is the legacy default stream) and runs asynchronously.
+ *  - Tensors are dense, row-major, with 16-byte aligned base addresses.
+ *  - bf16 means IEEE bfloat16 (the upper half of a binary32).
+ *  - Every call returns a pka_status; on a non-OK status nothing was
+ *    enqueued and pka_last_error() describes the reason.  No C++ exception
+ *    crosses this boundary.
+ *  - A device-side check that fails (an out-of-pool slot or block id, or a
+ *    pipeline wait that exceeded its time limit) never traps: the access is
+ *    skipped, a sticky error word is set, and the next pka_check_status
+ *    returns PKA_ERR_DEVICE_CHECK.
+ */
+#ifndef PKA_H
+#define PKA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKA_OK = 0,
+    PKA_ERR_INVALID_ARG = -1,  /* a bad argument (null pointer, size, alignment, block size) */
+    PKA_ERR_UNSUPPORTED = -2,  /* valid, but not a shape this build serves */
+    PKA_ERR_WORKSPACE = -3,    /* workspace missing, too small or misaligned */
+    PKA_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed */
+    PKA_ERR_DEVICE_CHECK = -5  /* a device-side check failed (see pka_check_status) */
+} pka_status;
+
+/*
+ * Batch metadata, the per-step fields of CommonAttentionMetadata
+ * ([backend] "Archivos clave": query_start_loc, seq_lens, block_table_tensor;
+ * [FA/FI] "Responsabilidades": decode-first order; [backend] "Flujo de datos":
+ * build(common_prefix_len, ...)).  The struct itself lives in host memory;
+ * the three array pointers are device pointers.
+ *
+ *  query_start_loc  int32 [num_seqs+1]; qsl[0] = 0, nondecreasing,
+ *                   qsl[num_seqs] = num_tokens.  Sequence s owns query
+ *                   tokens [qsl[s], qsl[s+1]).
+ *  seq_lens         int32 [num_seqs]; L_s >= 1, the whole KV length of s
+ *                   including this step's tokens (already written by
+ *                   pka_reshape_and_cache).  Prior context c_s = L_s - q_s.
+ *  block_table      int32 [num_seqs, block_table_stride]; entry n of row s
+ *                   is the physical block holding keys [n*bs, (n+1)*bs) of
+ *                   s.  Entries past ceil(L_s/bs) are never read.
+ *  num_decodes      the first num_decodes sequences are decodes: exactly one
+ *                   query token each ([FA/FI] "Responsabilidades": decode
+ *                   first, then prefill).
+ *  max_query_len    host upper bound on q_s over the prefill sequences.
+ *  max_seq_len      host upper bound on L_s over all sequences.
+ *  common_prefix_len  0, or a multiple of block_size P such that the first
+ *                   P/bs block-table entries of every sequence are the same
+ *                   blocks and P <= c_s for every s ([blog] "Que aporta
+ *                   FlashInfer: JIT y cascade attention").
+ *  split_kv_tokens  0 = automatic; else the number of keys per decode split
+ *                   (rounded up to the kernel's stage size).
+ */
+typedef struct {
+    const int32_t *query_start_loc;
+    const int32_t *seq_lens;
+    const int32_t *block_table;
+    int32_t block_table_stride;
+    int32_t num_seqs;
+    int32_t num_decodes;
+    int32_t max_query_len;
+    int32_t max_seq_len;
+    int32_t common_prefix_len;
+    int32_t split_kv_tokens;
+} pka_meta;
+
+/*
+ * Write this step's K/V rows into the paged pool (the cache-update op of
+ * [FA/FI] "Responsabilidades", unified_kv_cache_update).
+ *
+ *  key, value     device bf16 [num_tokens, num_kv_heads, head_size]
+ *  kv_cache       device bf16 [num_blocks, 2, block_size, num_kv_heads,
+ *                 head_size] ([FA/FI] "Flujo de datos", get_kv_cache_shape;
+ *                 index 0 of the second axis is K, 1 is V), written in place
+ *  slot_mapping   device int64 [num_tokens]; slot = block*block_size +
+ *                 offset; a negative slot is padding and is skipped
+ *
+ * For every token t with slot >= 0 the K row and the V row land byte for
+ * byte at (slot/block_size, slot%block_size); nothing else is written.
+ * A slot >= num_blocks*block_size is skipped and flagged on the device.
+ * Duplicate slots in one call are a caller error (the winner is undefined).
+ * Errors: PKA_ERR_INVALID_ARG for null pointers, num_tokens < 0,
+ * block_size not a multiple of 16 ([FA/FI] "Flujo de datos": "Block size must
+ * be a multiple of 16"), head_size not a multiple of 8.
+ */
+pka_status pka_reshape_and_cache(const void *key, const void *value, void *kv_cache,
+                                 const int64_t *slot_mapping, int32_t num_tokens,
+                                 int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                 int64_t num_blocks, void *stream);
+
+/*
+ * Bytes of device workspace pka_paged_attn_forward needs for this batch
+ * (split-KV and cascade partial results, fp32).  Same shape arguments as the
+ * forward; depends only on host-side fields of `meta`.  Returns 0 when the
+ * arguments are invalid.
+ */
+size_t pka_workspace_size(const pka_meta *meta, int32_t num_tokens, int32_t num_heads,
+                          int32_t num_kv_heads, int32_t head_size, int32_t block_size);
+
+/*
+ * Attention forward of one layer over the paged pool ([backend] "Archivos
+ * clave": AttentionImpl.forward(layer, query, key, value, kv_cache,
+ * attn_metadata, output); [FA/FI] "Responsabilidades": Q/K/V reshaped to
+ * [num_tokens, num_heads, head_size]; [blog] "Como lee el backend el KV
+ * paginado": the kernel gathers the physical blocks through the block table).
+ *
+ * For query token t of sequence s (t = qsl[s] + i), head h, kv head
+ * k = h / (num_heads/num_kv_heads), key j admitted iff !causal || j <= c_s+i:
+ *     x_j  = scale * <q[t,h], K_j>,        K_j = kv_cache[bt[s][j/bs], 0, j%bs, k]
+ *     lse  = ln sum_j exp(x_j)
+ *     out  = sum_j exp(x_j - lse) * V_j,   V_j = kv_cache[bt[s][j/bs], 1, j%bs, k]
+ * With common_prefix_len P > 0 the result is the same, computed as the
+ * cascade of [blog] "Que aporta FlashInfer": the shared prefix keys [0, P)
+ * are attended once for all queries and merged with each sequence's own
+ * suffix [P, L_s) by log-sum-exp.
+ *
+ *  query      device bf16 [num_tokens, num_heads, head_size]
+ *  kv_cache   device bf16 [num_blocks, 2, block_size, num_kv_heads, head_size]
+ *  meta       host pointer to the batch metadata above
+ *  out        device bf16 [num_tokens, num_heads, head_size]; must not alias
+ *             query; every row of every query token is written
+ *  lse        device fp32 [num_tokens, num_heads], natural-log units
+ *             ([backend] "Limites y fallos": the lse base must be known),
+ *             or NULL
+ *  scale      softmax scale (1/sqrt(head_size) in the usual case)
+ *  causal     1: bottom-right causal mask; 0: every key [0, L_s) admitted
+ *  workspace  device buffer of at least pka_workspace_size(...) bytes,
+ *             256-byte aligned (may be NULL when that size is 0)
+ *
+ * Served shapes: head_size 64 or 128; num_kv_heads in {1, 2, 4, 8};
+ * num_heads/num_kv_heads <= 8 for decodes; block_size a multiple of 16
+ * (PKA_ERR_INVALID_ARG otherwise, as [FA/FI] "Limites y fallos" and
+ * [backend] "Limites y fallos" require); other shapes PKA_ERR_UNSUPPORTED.
+ */
+pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const pka_meta *meta,
+                                  void *out, float *lse, int32_t num_tokens, int32_t num_heads,
+                                  int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                  int64_t num_blocks, float scale, int32_t causal,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Log-sum-exp merge of two partial attentions of the same queries over
+ * disjoint key sets ([blog] "Que aporta FlashInfer: JIT y cascade attention":
+ * the prefix result is combined with each request's suffix; [FA/FI] "Limites
+ * y fallos": the softmax combine across shards; [backend] "Limites y fallos":
+ * natural-log lse).  Per row r = t*num_heads + h:
+ *     lse = ln(exp(lse_a) + exp(lse_b))
+ *     out = exp(lse_a - lse) * out_a + exp(lse_b - lse) * out_b
+ * A side with lse = -inf holds no keys and is the identity.
+ *
+ *  out_a, out_b  device bf16 [num_tokens, num_heads, head_size]
+ *  lse_a, lse_b  device fp32 [num_tokens, num_heads], natural log
+ *  out           device bf16, same shape (may alias out_a or out_b)
+ *  lse_out       device fp32 [num_tokens, num_heads] or NULL (may alias)
+ */
+pka_status pka_cascade_merge(const void *out_a, const float *lse_a, const void *out_b,
+                             const float *lse_b, void *out, float *lse_out, int32_t num_tokens,
+                             int32_t num_heads, int32_t head_size, void *stream);
+
+/*
+ * Synchronise `stream`, then read and clear the sticky device error word.
+ * Returns PKA_OK, PKA_ERR_DEVICE_CHECK (with the failing check named by
+ * pka_last_error), or PKA_ERR_CUDA when the stream itself reports an error.
+ */
+pka_status pka_check_status(void *stream);
+
+/* Thread-local description of the last non-OK status on this thread. */
+const char *pka_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKA_H */

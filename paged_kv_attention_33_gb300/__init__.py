@@ -1,0 +1,194 @@
+"""GB300-native paged-KV attention forward: Python binding of libpka.so.
+
+Thin ctypes marshalling over the C ABI declared in include/pka.h: tensor
+shapes become size arguments, tensors become device pointers, the current
+torch CUDA stream becomes the stream argument.  Every step of the attention
+runs in the library's CUDA kernels; there is no CPU or PyTorch fallback, and
+every call raises if the library cannot be loaded.
+
+Entry points (same names as the C ABI without the ``pka_`` prefix):
+    reshape_and_cache(key, value, kv_cache, slot_mapping)
+    paged_attn_forward(query, kv_cache, meta, out, lse=None, scale=None, causal=True)
+    cascade_merge(out_a, lse_a, out_b, lse_b, out, lse_out=None)
+    workspace_size(meta, num_tokens, num_heads, num_kv_heads, head_size, block_size)
+    check_status()
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+from . import build as _build
+
+__all__ = ["Meta", "PkaError", "reshape_and_cache", "paged_attn_forward", "cascade_merge",
+           "workspace_size", "check_status", "load_library", "library_path"]
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_lock = threading.Lock()
+_lib = None
+
+STATUS = {0: "PKA_OK", -1: "PKA_ERR_INVALID_ARG", -2: "PKA_ERR_UNSUPPORTED",
+          -3: "PKA_ERR_WORKSPACE", -4: "PKA_ERR_CUDA", -5: "PKA_ERR_DEVICE_CHECK"}
+
+
+class PkaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class _CMeta(ctypes.Structure):
+    _fields_ = [("query_start_loc", _P), ("seq_lens", _P), ("block_table", _P),
+                ("block_table_stride", _I32), ("num_seqs", _I32), ("num_decodes", _I32),
+                ("max_query_len", _I32), ("max_seq_len", _I32), ("common_prefix_len", _I32),
+                ("split_kv_tokens", _I32)]
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libpka.so (building it first if asked and it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise RuntimeError(f"libpka.so not built ({path}); run "
+                                   "paged_kv_attention_33_gb300.build.build()")
+            path = _build.build()
+        lib = ctypes.CDLL(path)
+        lib.pka_reshape_and_cache.argtypes = [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I64, _P]
+        lib.pka_reshape_and_cache.restype = ctypes.c_int
+        lib.pka_workspace_size.argtypes = [ctypes.POINTER(_CMeta), _I32, _I32, _I32, _I32, _I32]
+        lib.pka_workspace_size.restype = ctypes.c_size_t
+        lib.pka_paged_attn_forward.argtypes = [_P, _P, ctypes.POINTER(_CMeta), _P, _P, _I32,
+                                               _I32, _I32, _I32, _I32, _I64, ctypes.c_float,
+                                               _I32, _P, ctypes.c_size_t, _P]
+        lib.pka_paged_attn_forward.restype = ctypes.c_int
+        lib.pka_cascade_merge.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P]
+        lib.pka_cascade_merge.restype = ctypes.c_int
+        lib.pka_check_status.argtypes = [_P]
+        lib.pka_check_status.restype = ctypes.c_int
+        lib.pka_last_error.argtypes = []
+        lib.pka_last_error.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _check(rc: int):
+    if rc != 0:
+        msg = load_library().pka_last_error().decode(errors="replace")
+        raise PkaError(rc, msg)
+
+
+def _stream(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+class Meta:
+    """Batch metadata: device tensors plus the host-side sizes the plan needs.
+
+    query_start_loc int32 [S+1], seq_lens int32 [S], block_table int32
+    [S, stride] live on the device; num_decodes, max_query_len, max_seq_len,
+    common_prefix_len and split_kv_tokens are host integers.
+    """
+
+    def __init__(self, query_start_loc, seq_lens, block_table, num_decodes, max_query_len,
+                 max_seq_len, common_prefix_len=0, split_kv_tokens=0):
+        self.query_start_loc = query_start_loc
+        self.seq_lens = seq_lens
+        self.block_table = block_table
+        self.num_decodes = int(num_decodes)
+        self.max_query_len = int(max_query_len)
+        self.max_seq_len = int(max_seq_len)
+        self.common_prefix_len = int(common_prefix_len)
+        self.split_kv_tokens = int(split_kv_tokens)
+
+    @classmethod
+    def from_host(cls, query_start_loc, seq_lens, block_table, num_decodes, device,
+                  common_prefix_len=0, split_kv_tokens=0):
+        """Build from host (numpy) arrays, copying them to `device`."""
+        import numpy as np
+        import torch
+
+        qsl = np.asarray(query_start_loc, dtype=np.int32)
+        sl = np.asarray(seq_lens, dtype=np.int32)
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        ql = np.diff(qsl)
+        nd = int(num_decodes)
+        max_q = int(ql[nd:].max()) if len(ql) > nd else 1
+        max_s = int(sl.max()) if len(sl) else 1
+        return cls(torch.from_numpy(qsl).to(device), torch.from_numpy(sl).to(device),
+                   torch.from_numpy(bt).to(device), nd, max_q, max_s, common_prefix_len,
+                   split_kv_tokens)
+
+    def _c(self) -> _CMeta:
+        return _CMeta(self.query_start_loc.data_ptr(), self.seq_lens.data_ptr(),
+                      self.block_table.data_ptr(), self.block_table.shape[1],
+                      self.seq_lens.shape[0], self.num_decodes, self.max_query_len,
+                      self.max_seq_len, self.common_prefix_len, self.split_kv_tokens)
+
+
+def reshape_and_cache(key, value, kv_cache, slot_mapping, stream=None) -> None:
+    """Scatter key/value [T, Hkv, D] rows into kv_cache [NB, 2, bs, Hkv, D] at slot_mapping."""
+    lib = load_library()
+    nb, two, bs, hkv, d = kv_cache.shape
+    _check(lib.pka_reshape_and_cache(_ptr(key), _ptr(value), _ptr(kv_cache), _ptr(slot_mapping),
+                                     key.shape[0], hkv, d, bs, nb, _stream(stream)))
+
+
+def workspace_size(meta: Meta, num_tokens, num_heads, num_kv_heads, head_size, block_size) -> int:
+    lib = load_library()
+    cm = meta._c()
+    return int(lib.pka_workspace_size(ctypes.byref(cm), num_tokens, num_heads, num_kv_heads,
+                                      head_size, block_size))
+
+
+def paged_attn_forward(query, kv_cache, meta: Meta, out, lse=None, scale=None, causal=True,
+                       workspace=None, stream=None) -> None:
+    """out[T, H, D] (bf16) and lse[T, H] (fp32, ln) of the paged attention forward."""
+    import torch
+
+    lib = load_library()
+    T, H, D = query.shape
+    nb, _, bs, hkv, _ = kv_cache.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    cm = meta._c()
+    need = int(lib.pka_workspace_size(ctypes.byref(cm), T, H, hkv, D, bs))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.pka_paged_attn_forward(_ptr(query), _ptr(kv_cache), ctypes.byref(cm), _ptr(out),
+                                      _ptr(lse), T, H, hkv, D, bs, nb, float(scale),
+                                      1 if causal else 0, _ptr(workspace), ws_bytes,
+                                      _stream(stream)))
+
+
+def cascade_merge(out_a, lse_a, out_b, lse_b, out, lse_out=None, stream=None) -> None:
+    """Log-sum-exp merge of two partial attentions ([T, H, D] bf16 + [T, H] fp32 ln)."""
+    lib = load_library()
+    T, H, D = out_a.shape
+    _check(lib.pka_cascade_merge(_ptr(out_a), _ptr(lse_a), _ptr(out_b), _ptr(lse_b), _ptr(out),
+                                 _ptr(lse_out), T, H, D, _stream(stream)))
+
+
+def check_status(stream=None) -> None:
+    """Synchronise the stream and raise if a device-side check failed."""
+    _check(load_library().pka_check_status(_stream(stream)))

@@ -1,0 +1,346 @@
+// api.cu -- the C ABI (include/pka.h): argument checks, the host-side plan of
+// one forward (decode/prefill partition, split-KV size, workspace carve-up),
+// TMA descriptor encoding and the launch sequence on the caller's stream.
+//
+// The plan uses host-side sizes only (the metadata arrays stay on the device),
+// so a forward enqueues kernels and never waits on the GPU; this is the
+// analogue of the metadata builder's ahead-of-time schedule on the
+// "FlashAttention y FlashInfer" page ("Responsabilidades").
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "pka.h"
+
+namespace pka {
+
+static thread_local char g_msg[512] = "";
+
+static pka_status fail(pka_status st, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+static pka_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(PKA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+static bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ------------------------------------------------------------ device facts
+static int sm_count()
+{
+    static std::mutex mu;
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 148;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+// ------------------------------------------------------------ tensor maps
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// The pool [num_blocks, 2, block_size, num_kv_heads, head_size] seen as the
+// 3-D tensor (head_size, num_kv_heads, num_blocks*2*block_size); one box is
+// {64 dims, 1 head, 16 rows}, 128-byte swizzled.
+CUresult encode_kv_map(CUtensorMap *map, const void *cache, int32_t head_size,
+                       int32_t num_kv_heads, int32_t block_size, int64_t num_blocks)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return CUDA_ERROR_NOT_FOUND;
+    cuuint64_t dims[3] = {cuuint64_t(head_size), cuuint64_t(num_kv_heads),
+                          cuuint64_t(num_blocks) * 2 * cuuint64_t(block_size)};
+    cuuint64_t strides[2] = {cuuint64_t(head_size) * 2, cuuint64_t(num_kv_heads) * head_size * 2};
+    cuuint32_t box[3] = {64, 1, 16};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(cache), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+// ------------------------------------------------------------ planning
+Workspace plan_workspace(const DecodePlan &dp, int32_t num_tokens, int32_t num_decodes,
+                         int32_t num_heads, int32_t head_size, bool cascade)
+{
+    Workspace w;
+    size_t off = 0;
+    const size_t rows_part = size_t(num_decodes) * dp.max_splits * num_heads;
+    w.o_part = off;
+    off = round256(off + rows_part * head_size * 4);
+    w.lse_part = off;
+    off = round256(off + rows_part * 4);
+    const size_t rows_all = cascade ? size_t(num_tokens) * num_heads : 0;
+    w.o_pre = off;
+    off = round256(off + rows_all * head_size * 4);
+    w.lse_pre = off;
+    off = round256(off + rows_all * 4);
+    const size_t rows_pf = cascade ? size_t(num_tokens - num_decodes) * num_heads : 0;
+    w.o_suf = off;
+    off = round256(off + rows_pf * head_size * 4);
+    w.lse_suf = off;
+    off = round256(off + rows_pf * 4);
+    w.total = off;
+    return w;
+}
+
+// Checks shared by pka_workspace_size and pka_paged_attn_forward.
+static pka_status check_shape(const pka_meta *m, int32_t num_tokens, int32_t num_heads,
+                              int32_t num_kv_heads, int32_t head_size, int32_t block_size)
+{
+    if (!m)
+        return fail(PKA_ERR_INVALID_ARG, "meta is NULL");
+    if (block_size <= 0 || block_size % 16 != 0)
+        return fail(PKA_ERR_INVALID_ARG, "Block size must be a multiple of 16 (got %d).",
+                    block_size);
+    if (head_size <= 0 || head_size % 8 != 0 || head_size > 256)
+        return fail(PKA_ERR_INVALID_ARG,
+                    "head_size must be a positive multiple of 8 not above 256 (got %d)",
+                    head_size);
+    if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0)
+        return fail(PKA_ERR_INVALID_ARG,
+                    "num_heads (%d) must be a positive multiple of num_kv_heads (%d)", num_heads,
+                    num_kv_heads);
+    if (num_tokens < 0 || m->num_seqs < 0 || m->num_decodes < 0 ||
+        m->num_decodes > m->num_seqs || m->num_decodes > num_tokens)
+        return fail(PKA_ERR_INVALID_ARG,
+                    "inconsistent sizes: num_tokens %d, num_seqs %d, num_decodes %d", num_tokens,
+                    m->num_seqs, m->num_decodes);
+    if (m->num_seqs > 0 && m->max_seq_len < 1)
+        return fail(PKA_ERR_INVALID_ARG, "max_seq_len must be >= 1");
+    if (m->num_seqs > m->num_decodes && m->max_query_len < 1)
+        return fail(PKA_ERR_INVALID_ARG, "max_query_len must be >= 1 when prefills are present");
+    if (m->common_prefix_len < 0 || m->common_prefix_len % block_size != 0 ||
+        (m->common_prefix_len > 0 && m->common_prefix_len >= m->max_seq_len))
+        return fail(PKA_ERR_INVALID_ARG,
+                    "common_prefix_len (%d) must be a multiple of block_size below max_seq_len",
+                    m->common_prefix_len);
+    if (m->split_kv_tokens < 0)
+        return fail(PKA_ERR_INVALID_ARG, "split_kv_tokens must be >= 0");
+    if (m->num_seqs > 0 &&
+        int64_t(m->block_table_stride) * block_size < int64_t(m->max_seq_len))
+        return fail(PKA_ERR_INVALID_ARG,
+                    "block_table_stride %d too small for max_seq_len %d at block_size %d",
+                    m->block_table_stride, m->max_seq_len, block_size);
+    if (head_size != 64 && head_size != 128)
+        return fail(PKA_ERR_UNSUPPORTED, "head_size %d is not built (64, 128)", head_size);
+    if (num_kv_heads != 1 && num_kv_heads != 2 && num_kv_heads != 4 && num_kv_heads != 8)
+        return fail(PKA_ERR_UNSUPPORTED, "num_kv_heads %d is not built (1, 2, 4, 8)",
+                    num_kv_heads);
+    if (m->num_decodes > 0 && num_heads / num_kv_heads > 8)
+        return fail(PKA_ERR_UNSUPPORTED, "decode query-head group %d above 8",
+                    num_heads / num_kv_heads);
+    if (m->num_decodes > 65535)
+        return fail(PKA_ERR_UNSUPPORTED, "more than 65535 decodes in one call");
+    return PKA_OK;
+}
+
+}  // namespace pka
+
+using namespace pka;
+
+extern "C" {
+
+const char *pka_last_error(void) { return g_msg; }
+
+pka_status pka_reshape_and_cache(const void *key, const void *value, void *kv_cache,
+                                 const int64_t *slot_mapping, int32_t num_tokens,
+                                 int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                 int64_t num_blocks, void *stream)
+{
+    if (num_tokens < 0)
+        return fail(PKA_ERR_INVALID_ARG, "num_tokens < 0");
+    if (block_size <= 0 || block_size % 16 != 0)
+        return fail(PKA_ERR_INVALID_ARG, "Block size must be a multiple of 16 (got %d).",
+                    block_size);
+    if (head_size <= 0 || head_size % 8 != 0 || num_kv_heads <= 0 || num_blocks <= 0)
+        return fail(PKA_ERR_INVALID_ARG,
+                    "bad shape: head_size %d (multiple of 8), num_kv_heads %d, num_blocks %lld",
+                    head_size, num_kv_heads, static_cast<long long>(num_blocks));
+    if (num_tokens == 0)
+        return PKA_OK;
+    if (!key || !value || !kv_cache || !slot_mapping)
+        return fail(PKA_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(key, 16) || !aligned(value, 16) || !aligned(kv_cache, 16) ||
+        !aligned(slot_mapping, 8))
+        return fail(PKA_ERR_INVALID_ARG, "misaligned pointer (16 bytes required)");
+    cudaError_t e = launch_reshape_and_cache(key, value, kv_cache, slot_mapping, num_tokens,
+                                             num_kv_heads, head_size, block_size, num_blocks,
+                                             static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "reshape_and_cache launch");
+    return PKA_OK;
+}
+
+size_t pka_workspace_size(const pka_meta *meta, int32_t num_tokens, int32_t num_heads,
+                          int32_t num_kv_heads, int32_t head_size, int32_t block_size)
+{
+    if (check_shape(meta, num_tokens, num_heads, num_kv_heads, head_size, block_size) != PKA_OK)
+        return 0;
+    const bool cascade = meta->common_prefix_len > 0;
+    const int32_t kv_begin = meta->common_prefix_len;
+    DecodePlan dp = plan_decode(meta->split_kv_tokens, meta->num_decodes, meta->max_seq_len,
+                                kv_begin, num_kv_heads, sm_count());
+    return plan_workspace(dp, num_tokens, meta->num_decodes, num_heads, head_size, cascade).total;
+}
+
+pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const pka_meta *meta,
+                                  void *out, float *lse, int32_t num_tokens, int32_t num_heads,
+                                  int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                  int64_t num_blocks, float scale, int32_t causal,
+                                  void *workspace, size_t workspace_bytes, void *stream)
+{
+    pka_status st = check_shape(meta, num_tokens, num_heads, num_kv_heads, head_size, block_size);
+    if (st != PKA_OK)
+        return st;
+    if (num_tokens == 0 || meta->num_seqs == 0)
+        return PKA_OK;
+    if (!query || !kv_cache || !out || !meta->query_start_loc || !meta->seq_lens ||
+        !meta->block_table)
+        return fail(PKA_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(query, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) ||
+        (lse && !aligned(lse, 4)))
+        return fail(PKA_ERR_INVALID_ARG, "misaligned pointer (16 bytes required)");
+    if (query == out)
+        return fail(PKA_ERR_INVALID_ARG, "out must not alias query");
+    if (num_blocks <= 0)
+        return fail(PKA_ERR_INVALID_ARG, "num_blocks must be positive");
+    if (num_blocks * 2 * int64_t(block_size) >= (int64_t(1) << 31))
+        return fail(PKA_ERR_UNSUPPORTED, "pool has more than 2^31 token rows");
+    if (!(scale > 0.f) || scale != scale || scale > 1e30f)
+        return fail(PKA_ERR_INVALID_ARG, "scale must be a positive finite number");
+
+    const bool cascade = meta->common_prefix_len > 0;
+    const int32_t kv_begin = meta->common_prefix_len;
+    const int num_prefills = meta->num_seqs - meta->num_decodes;
+    if (num_prefills > 0)
+        return fail(PKA_ERR_UNSUPPORTED, "prefill sequences are not served by this build yet");
+    if (cascade)
+        return fail(PKA_ERR_UNSUPPORTED, "cascade is not served by this build yet");
+
+    Fwd f;
+    f.query = query;
+    f.kv_cache = kv_cache;
+    f.qsl = meta->query_start_loc;
+    f.seq_lens = meta->seq_lens;
+    f.block_table = meta->block_table;
+    f.bt_stride = meta->block_table_stride;
+    f.num_seqs = meta->num_seqs;
+    f.num_decodes = meta->num_decodes;
+    f.max_query_len = meta->max_query_len;
+    f.max_seq_len = meta->max_seq_len;
+    f.common_prefix_len = meta->common_prefix_len;
+    f.out = out;
+    f.lse = lse;
+    f.num_tokens = num_tokens;
+    f.num_heads = num_heads;
+    f.num_kv_heads = num_kv_heads;
+    f.head_size = head_size;
+    f.block_size = block_size;
+    f.num_blocks = num_blocks;
+    f.scale = scale;
+    f.causal = causal;
+    f.stream = static_cast<cudaStream_t>(stream);
+    f.num_sms = sm_count();
+
+    DecodePlan dp = plan_decode(meta->split_kv_tokens, meta->num_decodes, meta->max_seq_len,
+                                kv_begin, num_kv_heads, f.num_sms);
+    Workspace ws = plan_workspace(dp, num_tokens, meta->num_decodes, num_heads, head_size, cascade);
+    if (ws.total > 0 && (!workspace || workspace_bytes < ws.total || !aligned(workspace, 256)))
+        return fail(PKA_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)",
+                    ws.total, workspace_bytes);
+    char *wsp = static_cast<char *>(workspace);
+
+    CUtensorMap kv_map;
+    CUresult cr = encode_kv_map(&kv_map, kv_cache, head_size, num_kv_heads, block_size, num_blocks);
+    if (cr != CUDA_SUCCESS)
+        return fail(PKA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(cr));
+
+    cudaError_t e = launch_decode(f, dp, ws, wsp, kv_map, kv_begin, false);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "decode launch");
+    e = launch_decode_combine(f, dp, ws, wsp, kv_begin, false);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "decode combine launch");
+    return PKA_OK;
+}
+
+pka_status pka_cascade_merge(const void *out_a, const float *lse_a, const void *out_b,
+                             const float *lse_b, void *out, float *lse_out, int32_t num_tokens,
+                             int32_t num_heads, int32_t head_size, void *stream)
+{
+    if (num_tokens < 0 || num_heads <= 0 || head_size <= 0 || head_size % 8 != 0)
+        return fail(PKA_ERR_INVALID_ARG, "bad shape: tokens %d heads %d head_size %d",
+                    num_tokens, num_heads, head_size);
+    if (num_tokens == 0)
+        return PKA_OK;
+    if (!out_a || !lse_a || !out_b || !lse_b || !out)
+        return fail(PKA_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(out_a, 16) || !aligned(out_b, 16) || !aligned(out, 16) || !aligned(lse_a, 4) ||
+        !aligned(lse_b, 4) || (lse_out && !aligned(lse_out, 4)))
+        return fail(PKA_ERR_INVALID_ARG, "misaligned pointer (16 bytes required)");
+    cudaError_t e = launch_cascade_merge(out_a, lse_a, out_b, lse_b, out, lse_out, num_tokens,
+                                         num_heads, head_size, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cascade_merge launch");
+    return PKA_OK;
+}
+
+pka_status pka_check_status(void *stream)
+{
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "stream synchronize");
+    const uint32_t bits = kv_write_take_error() | decode_take_error();
+    if (bits == 0)
+        return PKA_OK;
+    char buf[256] = "";
+    if (bits & kErrSlotOutOfPool)
+        strcat(buf, " slot_mapping entry outside the pool;");
+    if (bits & kErrBlockOutOfPool)
+        strcat(buf, " block_table entry outside the pool;");
+    if (bits & kErrWaitTimeout)
+        strcat(buf, " pipeline wait timed out;");
+    if (bits & kErrTmemAlloc)
+        strcat(buf, " tensor-memory allocation failed;");
+    if (bits & kErrBadMetadata)
+        strcat(buf, " seq_lens/query_start_loc outside the stated bounds;");
+    return fail(PKA_ERR_DEVICE_CHECK, "device check failed:%s", buf);
+}
+
+}  // extern "C"

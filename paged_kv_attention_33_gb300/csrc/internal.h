@@ -1,0 +1,88 @@
+// internal.h -- host-side interface between the C ABI (api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pka.h"
+
+namespace pka {
+
+// Everything one forward launch needs, validated by api.cu.
+struct Fwd {
+    const void *query;
+    const void *kv_cache;
+    const int32_t *qsl;
+    const int32_t *seq_lens;
+    const int32_t *block_table;
+    int32_t bt_stride;
+    int32_t num_seqs;
+    int32_t num_decodes;
+    int32_t max_query_len;
+    int32_t max_seq_len;
+    int32_t common_prefix_len;
+    void *out;
+    float *lse;
+    int32_t num_tokens;
+    int32_t num_heads;
+    int32_t num_kv_heads;
+    int32_t head_size;
+    int32_t block_size;
+    int64_t num_blocks;
+    float scale;
+    int32_t causal;
+    cudaStream_t stream;
+    int num_sms;
+};
+
+// Split-KV plan of the decode part of a batch.
+struct DecodePlan {
+    int32_t stage_keys;    // keys per pipeline stage (16 * 8/num_kv_heads)
+    int32_t split_tokens;  // keys per split, a multiple of stage_keys
+    int32_t max_splits;    // ceil(max decode KV length / split_tokens)
+};
+
+// Workspace carve-up (byte offsets from the workspace base, 256-aligned).
+struct Workspace {
+    size_t o_part, lse_part;   // decode split partials
+    size_t o_pre, lse_pre;     // cascade: shared-prefix partial of every token
+    size_t o_suf, lse_suf;     // cascade: suffix partial of every prefill token
+    size_t total;
+};
+
+DecodePlan plan_decode(int32_t requested_split, int32_t num_decodes, int32_t max_seq_len,
+                       int32_t kv_begin, int32_t num_kv_heads, int num_sms);
+Workspace plan_workspace(const DecodePlan &dp, int32_t num_tokens, int32_t num_decodes,
+                         int32_t num_heads, int32_t head_size, bool cascade);
+
+// kv_write.cu
+cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *cache,
+                                     const int64_t *slots, int32_t num_tokens,
+                                     int32_t num_kv_heads, int32_t head_size,
+                                     int32_t block_size, int64_t num_blocks, cudaStream_t st);
+uint32_t kv_write_take_error();
+
+// decode.cu: split-KV decode over sequences [0, num_decodes) and keys
+// [kv_begin, L_s).  partial_only: write fp32 partials for every split (the
+// cascade merges them later) instead of finishing single-split sequences.
+cudaError_t launch_decode(const Fwd &f, const DecodePlan &dp, const Workspace &ws, char *wsp,
+                          const CUtensorMap &kv_map, int32_t kv_begin, bool partial_only);
+// Merge the decode split partials (and, for a cascade, the prefix partial)
+// into out/lse for the decode tokens.
+cudaError_t launch_decode_combine(const Fwd &f, const DecodePlan &dp, const Workspace &ws,
+                                  char *wsp, int32_t kv_begin, bool with_prefix);
+uint32_t decode_take_error();
+
+// merge.cu
+cudaError_t launch_cascade_merge(const void *out_a, const float *lse_a, const void *out_b,
+                                 const float *lse_b, void *out, float *lse_out,
+                                 int32_t num_tokens, int32_t num_heads, int32_t head_size,
+                                 cudaStream_t st);
+
+// tensor maps (api.cu)
+CUresult encode_kv_map(CUtensorMap *map, const void *cache, int32_t head_size,
+                       int32_t num_kv_heads, int32_t block_size, int64_t num_blocks);
+
+}  // namespace pka

@@ -1,0 +1,140 @@
+"""GPU parity of the cache write and the split-KV decode path against the fp64
+oracle (all calls go through the C ABI)."""
+import numpy as np
+import pytest
+
+from paged_kv_attention_33_gb300 import workloads as W
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+
+def _spec(H, Hkv, D, bs, ctx, **kw):
+    return W.BatchSpec(f"d_{H}_{Hkv}_{D}_{bs}", H, Hkv, D, bs, decode_ctx=list(ctx), **kw)
+
+
+def test_tiny_decode_named(oracle):
+    b = W.make_batch(W.named_spec("tiny_decode"), seed=2001)
+    G.check_batch(oracle, b, label="tiny_decode")
+
+
+@pytest.mark.parametrize("split", [0, 64, 128, 192])
+def test_tiny_decode_forced_splits(oracle, split):
+    b = W.make_batch(W.named_spec("tiny_decode"), seed=2002)
+    G.check_batch(oracle, b, split_kv_tokens=split, label=f"split {split}")
+
+
+# lengths 1, one short of / exactly / one past a 16-key slice and a block
+EDGE_CTX = [0, 14, 15, 16, 31, 32, 63, 64, 65, 127, 128, 129, 200, 511]
+
+
+@pytest.mark.parametrize("H,Hkv,D,bs", [
+    (8, 2, 64, 16),     # group 4, two kv heads (4 slices per stage)
+    (32, 8, 128, 16),   # the decode-heavy shape
+    (8, 1, 128, 32),    # group 8, one kv head
+    (8, 4, 64, 64),     # group 2
+    (8, 8, 128, 128),   # group 1
+    (64, 8, 128, 128),  # group 8, the cascade shape
+])
+def test_decode_edges(oracle, H, Hkv, D, bs):
+    b = W.make_batch(_spec(H, Hkv, D, bs, EDGE_CTX, table_pad=3), seed=2100 + H + Hkv + bs)
+    for split in (0, 16 * (8 // Hkv), 48 * (8 // Hkv)):
+        G.check_batch(oracle, b, split_kv_tokens=split, label=f"split {split}")
+
+
+def test_decode_many_splits_ragged(oracle):
+    rng = np.random.Generator(np.random.PCG64(5))
+    ctx = rng.integers(1, 3000, size=24).tolist()
+    b = W.make_batch(_spec(32, 8, 128, 16, ctx), seed=2200)
+    G.check_batch(oracle, b, split_kv_tokens=64, label="64-key splits")
+    G.check_batch(oracle, b, label="auto split")
+
+
+def test_decode_heavy_full_size_sampled(oracle):
+    """The decode-heavy batch at full size in the benchmark's launch
+    configuration (automatic split), checked on sampled rows."""
+    spec = W.named_spec("decode_heavy")
+    b = W.make_batch(spec, seed=1002, device="cuda")
+    rows = W.sample_rows(b, 384, seed=3)
+    G.check_batch(oracle, b, rows=rows, label="decode_heavy", threads=16)
+
+
+def test_out_of_pool_slot_is_flagged():
+    import torch
+
+    import paged_kv_attention_33_gb300 as pka
+
+    sp = _spec(8, 2, 64, 16, [5, 9], pool_blocks=4)
+    b = W.make_batch(sp, seed=2300)
+    cache = G.to_dev(b.cache, "cuda")
+    slots = b.slot_mapping.copy()
+    slots[1] = 4 * 16          # one past the pool: skipped and flagged
+    before = cache.clone()
+    pka.reshape_and_cache(G.to_dev(b.key, "cuda"), G.to_dev(b.value, "cuda"), cache,
+                          torch.from_numpy(slots).cuda())
+    with pytest.raises(pka.PkaError) as e:
+        pka.check_status()
+    assert e.value.status == -5
+    pka.check_status()         # the error word was cleared
+    # the good token landed, nothing else changed
+    assert int((cache.view(torch.int16) != before.view(torch.int16)).sum()) > 0
+
+
+def test_out_of_pool_block_is_flagged():
+    import torch
+
+    import paged_kv_attention_33_gb300 as pka
+
+    sp = _spec(8, 2, 64, 16, [40, 9])
+    b = W.make_batch(sp, seed=2301)
+    table = b.block_table.copy()
+    table[0, 1] = b.num_blocks + 7   # outside the pool
+    meta = pka.Meta.from_host(b.query_start_loc, b.seq_lens, table, 2, "cuda")
+    q = G.to_dev(b.query, "cuda")
+    out = torch.empty_like(q)
+    pka.paged_attn_forward(q, G.to_dev(b.cache, "cuda"), meta, out, scale=sp.softmax_scale)
+    with pytest.raises(pka.PkaError) as e:
+        pka.check_status()
+    assert e.value.status == -5
+    pka.check_status()
+
+
+def test_cascade_merge_kernel(oracle):
+    """pka_cascade_merge against the oracle's merge on the same bf16 inputs,
+    including rows where one or both sides are empty (lse = -inf)."""
+    import torch
+
+    import paged_kv_attention_33_gb300 as pka
+
+    rng = np.random.Generator(np.random.PCG64(9))
+    T, H, D = 37, 8, 128
+    oa = W.f32_to_bf16_bits(rng.standard_normal((T, H, D), dtype=np.float32))
+    ob = W.f32_to_bf16_bits(rng.standard_normal((T, H, D), dtype=np.float32))
+    la = (rng.standard_normal((T, H)) * 3).astype(np.float32)
+    lb = (rng.standard_normal((T, H)) * 3).astype(np.float32)
+    la[0, :] = -np.inf
+    lb[1, :] = -np.inf
+    la[2, :] = -np.inf
+    lb[2, :] = -np.inf
+    dev = "cuda"
+    out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+    lo = torch.empty((T, H), dtype=torch.float32, device=dev)
+    pka.cascade_merge(W.to_device(oa, dev), torch.from_numpy(la).to(dev), W.to_device(ob, dev),
+                      torch.from_numpy(lb).to(dev), out, lo)
+    pka.check_status()
+    f = lambda x: W.bf16_bits_to_f32(x).astype(np.float64).reshape(T * H, D)
+    o_ref, l_ref = oracle.lse_merge(f(oa), la.astype(np.float64).ravel(), f(ob),
+                                    lb.astype(np.float64).ravel())
+    got = W.bf16_bits_to_f32(W.to_host_bits(out)).astype(np.float64).reshape(T * H, D)
+    assert np.max(np.abs(got - o_ref)) <= 2e-2
+    lg = lo.cpu().numpy().astype(np.float64).ravel()
+    both = np.isneginf(l_ref)
+    assert np.all(np.isneginf(lg[both]))
+    assert np.all(got[both] == 0)
+    assert np.max(np.abs(lg[~both] - l_ref[~both])) <= 1e-3
+    # in place (out aliases out_a)
+    a = W.to_device(oa, dev)
+    la_t = torch.from_numpy(la).to(dev)
+    pka.cascade_merge(a, la_t, W.to_device(ob, dev), torch.from_numpy(lb).to(dev), a, la_t)
+    pka.check_status()
+    assert torch.equal(a.view(torch.int16), out.view(torch.int16))
