@@ -1,0 +1,484 @@
+"""Benchmark of one paged-KV attention step on GB300.
+
+A step is one pass of the hot path over one synthetic batch: the cache write
+of this step's new K/V rows (reshape_and_cache) followed by the attention
+forward (paged_attn_forward: split-KV decode + combine, prefill, cascade as
+the batch needs).  The headline workload is the decode-heavy batch: 128
+decode requests, prior context ~ U[512, 8192], 32 query heads over 8 kv heads,
+head_size 128, block_size 16, pages shuffled across the pool.  Its value is
+KV bytes read per second (GB/s); its KV (about 2.3 GB) is far larger than L2,
+so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  Flags:
+  --gpus N --steps K --warmup W   (N > 1: launched by torchrun, one replica per GPU)
+  --impl reference                the fp64 CPU oracle on a bounded sample, on the host cores
+  --workload NAME                 another named workload (for profiling runs)
+  --no-cpu-baseline               skip the oracle timing (profiling runs)
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_attention_33_gb300 import accounting as A  # noqa: E402
+from paged_kv_attention_33_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged-attn decode KV GB/s & prefill TFLOP/s, % of GB300 roofline"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+SEED_OF = {"tiny_decode": 1001, "decode_heavy": 1002, "prefill": 1003, "mixed": 1004,
+           "cascade": 1005}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+# --------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock, power and throttle reasons."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str | None, interval_ms: int = 50):
+        self.proc = None
+        self.lines = []
+        self.gpu_id = gpu_id
+        self.interval_ms = interval_ms
+        self.t_start = None
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=timestamp," + ",".join(self.FIELDS),
+               "--format=csv,noheader,nounits", f"-lms={self.interval_ms}"]
+        if self.gpu_id:
+            cmd.append(f"--id={self.gpu_id}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+        self.t_start = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        if self.proc is None or not self.lines:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        loaded = [x for x in sm if x > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_uuid(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# --------------------------------------------------------------------- workload
+class Step:
+    """Device-resident inputs of one workload and the call sequence of a step."""
+
+    def __init__(self, name, dev, max_decodes=None):
+        import dataclasses
+
+        import torch
+
+        import paged_kv_attention_33_gb300 as pka
+
+        self.torch = torch
+        self.pka = pka
+        self.spec = W.named_spec(name)
+        if max_decodes is not None:
+            self.spec = dataclasses.replace(self.spec,
+                                            decode_ctx=self.spec.decode_ctx[:max_decodes])
+        self.name = name
+        self.batch = W.make_batch(self.spec, seed=SEED_OF[name], device=dev)
+        b = self.batch
+        self.dev = dev
+        self.slots = torch.from_numpy(b.slot_mapping).to(dev)
+        self.meta = pka.Meta.from_host(b.query_start_loc, b.seq_lens, b.block_table,
+                                       self.spec.num_decodes, dev,
+                                       common_prefix_len=self.spec.common_prefix_len)
+        T = b.num_tokens
+        self.out = torch.empty((T, self.spec.num_heads, self.spec.head_size),
+                               dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((T, self.spec.num_heads), dtype=torch.float32, device=dev)
+        need = pka.workspace_size(self.meta, T, self.spec.num_heads, self.spec.num_kv_heads,
+                                  self.spec.head_size, self.spec.block_size)
+        self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+
+    def run(self, q=None, k=None, v=None, slots=None, meta=None):
+        b = self.batch
+        self.pka.reshape_and_cache(b.key if k is None else k, b.value if v is None else v,
+                                   b.cache, self.slots if slots is None else slots)
+        self.pka.paged_attn_forward(b.query if q is None else q, b.cache,
+                                    self.meta if meta is None else meta, self.out, self.lse,
+                                    scale=self.spec.softmax_scale, causal=self.spec.causal,
+                                    workspace=self.ws)
+
+
+def units(spec):
+    """(KV bytes, prefill flops) of one step."""
+    return A.decode_kv_bytes(spec, spec.common_prefix_len), A.prefill_flops(spec)
+
+
+# --------------------------------------------------------------------- reference arm
+def oracle_sample_rows(batch, seqs):
+    H = batch.spec.num_heads
+    rows = []
+    for s in seqs:
+        t0, t1 = int(batch.query_start_loc[s]), int(batch.query_start_loc[s + 1])
+        for t in range(t0, t1):
+            rows.extend(range(t * H, (t + 1) * H))
+    return np.asarray(rows, dtype=np.int64)
+
+
+def time_oracle(name, seqs, threads):
+    """Oracle on the whole heads of `seqs` of the workload; returns
+    (seconds, KV bytes those sequences read, sample description)."""
+    from oracle import Oracle
+
+    spec = W.named_spec(name)
+    b = W.make_batch(spec, seed=SEED_OF[name], device="cpu")
+    cache = b.cache
+    orc = Oracle()
+    orc.reshape_and_cache(b.key, b.value, cache, b.slot_mapping)
+    rows = oracle_sample_rows(b, seqs)
+    t0 = time.perf_counter()
+    orc.paged_attention(b.query, cache, b.query_start_loc, b.seq_lens, b.block_table,
+                        spec.softmax_scale, spec.causal, rows=rows, threads=threads)
+    dt = time.perf_counter() - t0
+    row_bytes = spec.num_kv_heads * spec.head_size * 2 * 2
+    nbytes = sum(int(b.seq_lens[s]) for s in seqs) * row_bytes
+    return dt, nbytes, f"{name}: sequences {seqs[0]}..{seqs[-1]} ({len(seqs)} of " \
+                       f"{len(b.seq_lens)}), all {spec.num_heads} heads, fp64"
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+
+    threads = oracle.cpu_threads()
+    name = args.workload
+    spec = W.named_spec(name)
+    per_step = list(range(0, min(spec.num_decodes, 16)))  # bounded sample per step
+    times = []
+    nbytes = 0
+    for i in range(args.warmup + args.steps):
+        dt, nb, desc = time_oracle(name, per_step, threads)
+        if i >= args.warmup:
+            times.append(dt)
+            nbytes = nb
+    sec = sum(times) / len(times)
+    value = nbytes / sec / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": name, "sample_per_step": desc}, "impl": "reference",
+        "cpu_baseline": {"kind": "oracle", "cores": threads, "sample": desc, "value": value,
+                         "unit": "GB/s"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------- our arm
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("decode.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_attention_33_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload):
+    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary,
+    or None when the kernel source changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"decode_kernel_{workload}_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return rec.get("traffic_bytes_per_launch")
+
+
+def run_ours(args):
+    import torch
+
+    import paged_kv_attention_33_gb300 as pka
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device(dev))
+    pka.load_library()
+    peaks, peaks_kind = load_peaks()
+    st = Step(args.workload, dev, args.max_decodes)
+    spec = st.spec
+    if args.profile:
+        return run_profile(args, st)
+    kv_bytes, pf_flops = units(spec)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    # warm-up (at least W steps, and at least ~1 s so that clocks settle)
+    t_end = time.time() + 1.0
+    n = 0
+    while n < args.warmup or time.time() < t_end:
+        st.run()
+        n += 1
+        if n % 50 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    pka.check_status()
+
+    # timed region: K steps, per-step events around the decode kernel
+    ev_k0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_k1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for e in ev_k0 + ev_k1:
+        e.record(stream)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_uuid(torch, local))
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    # keep the region long enough for clock samples: repeat the K-step block
+    launches0 = pka.kernel_launches()
+    e0.record(stream)
+    for i in range(args.steps):
+        pka.set_kernel_events(pka.KERNEL_DECODE, ev_k0[i], ev_k1[i])
+        st.run()
+    pka.set_kernel_events(pka.KERNEL_DECODE, None, None)
+    e1.record(stream)
+    launches = pka.kernel_launches() - launches0
+    torch.cuda.synchronize()
+    barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    k_ms = sum(a.elapsed_time(b) for a, b in zip(ev_k0, ev_k1)) / args.steps
+    # clocks: keep loading the GPU for ~1 s more so that nvidia-smi sees it busy
+    t_end = time.time() + 1.0
+    while time.time() < t_end:
+        for _ in range(20):
+            st.run()
+        torch.cuda.synchronize()
+    sampler.stop()
+    pka.check_status()
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([ms, k_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, k_ms = float(t[0]), float(t[1])
+    value = world * kv_bytes / (ms * 1e-3) / 1e9
+
+    # end to end through the public API with host buffers
+    b = st.batch
+    host = {
+        "q": b.query.cpu().pin_memory(), "k": b.key.cpu().pin_memory(),
+        "v": b.value.cpu().pin_memory(),
+        "slots": torch.from_numpy(b.slot_mapping).pin_memory(),
+        "qsl": torch.from_numpy(b.query_start_loc).pin_memory(),
+        "sl": torch.from_numpy(b.seq_lens).pin_memory(),
+        "bt": torch.from_numpy(np.ascontiguousarray(b.block_table)).pin_memory(),
+    }
+    dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    out_host = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    lse_host = torch.empty(st.lse.shape, dtype=st.lse.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_host.numel() * out_host.element_size() + lse_host.numel() * lse_host.element_size()
+    meta_e2e = pka.Meta(dbuf["qsl"], dbuf["sl"], dbuf["bt"], st.meta.num_decodes,
+                        st.meta.max_query_len, st.meta.max_seq_len, st.meta.common_prefix_len)
+
+    def e2e_step():
+        for k in host:
+            dbuf[k].copy_(host[k], non_blocking=True)
+        st.run(q=dbuf["q"], k=dbuf["k"], v=dbuf["v"], slots=dbuf["slots"], meta=meta_e2e)
+        out_host.copy_(st.out, non_blocking=True)
+        lse_host.copy_(st.lse, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = f0.elapsed_time(f1) / args.steps
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+    pka.check_status()
+
+    # roofline of the dominant kernel (the split-KV decode kernel)
+    achieved = kv_bytes / (k_ms * 1e-3) / 1e9
+    peak = float(peaks["hbm_gbs"])
+    roofline = {"bound": "hbm", "kernel": "paged_decode_kernel", "achieved": achieved,
+                "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": f"{peaks_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                if peaks_kind == "measured" else "fallback 6.8 TB/s",
+                "frac_of_nominal_8tbs": achieved / 8000.0,
+                "kernel_ms": k_ms, "algorithmic_bytes_per_launch": kv_bytes,
+                "traffic": committed_traffic(args.workload)}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "num_decodes": spec.num_decodes,
+                   "num_prefills": len(spec.prefill), "num_heads": spec.num_heads,
+                   "num_kv_heads": spec.num_kv_heads, "head_size": spec.head_size,
+                   "block_size": spec.block_size, "kv_bytes_per_step": kv_bytes,
+                   "l2": "inputs larger than L2 (KV per step >> 129 MB), no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "roofline": roofline,
+        "e2e": {"value": world * kv_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": sampler.summary(),
+        "timed_region": "CUDA events on the launching stream; decode kernel timed per launch "
+                        "with events recorded by the library around it",
+    }
+    if pf_flops:
+        line["prefill_tflops"] = pf_flops / (ms * 1e-3) / 1e12
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        threads = oracle.cpu_threads()
+        seqs = list(range(spec.num_decodes)) if spec.num_decodes else [0]
+        dt, nb, desc = time_oracle(args.workload, seqs, threads)
+        line["cpu_baseline"] = {"value": nb / dt / 1e9, "unit": "GB/s", "cores": threads,
+                                "kind": "oracle", "sample": desc, "seconds": dt}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def run_profile(args, st):
+    """Short run for profilers: W warm-up steps and K steps, no clock sampler,
+    no host-buffer leg, no oracle."""
+    import torch
+
+    for _ in range(args.warmup):
+        st.run()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        st.run()
+    e1.record()
+    torch.cuda.synchronize()
+    st.pka.check_status()
+    ms = e0.elapsed_time(e1) / args.steps
+    kv_bytes, _ = units(st.spec)
+    print(json.dumps({"profile_run": True, "workload": args.workload,
+                      "num_decodes": st.spec.num_decodes, "ms_per_step": ms,
+                      "kv_bytes_per_step": kv_bytes,
+                      "GBps_step": kv_bytes / (ms * 1e-3) / 1e9}), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="pka", choices=["pka", "reference"])
+    ap.add_argument("--workload", default="decode_heavy", choices=list(W.NAMED))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="short run for a profiler: W + K steps only")
+    ap.add_argument("--max-decodes", type=int, default=None,
+                    help="keep only the first N decode requests (small profiling case)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

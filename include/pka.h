@@ -193,6 +193,22 @@ pka_status pka_cascade_merge(const void *out_a, const float *lse_a, const void *
  */
 pka_status pka_check_status(void *stream);
 
+/*
+ * Instrumentation for timing one kernel with CUDA events.  With start/stop
+ * non-NULL (cudaEvent_t passed as void*), every later pka_paged_attn_forward
+ * on this thread records `start` on its stream right before it launches the
+ * kernel named by `kernel` (PKA_KERNEL_DECODE: the split-KV decode kernel;
+ * PKA_KERNEL_PREFILL: the prefill kernel) and `stop` right after it.  NULL
+ * start/stop turns the recording off.  The events stay owned by the caller.
+ * Errors: PKA_ERR_INVALID_ARG for an unknown kernel id.
+ */
+enum { PKA_KERNEL_DECODE = 0, PKA_KERNEL_PREFILL = 1 };
+pka_status pka_set_kernel_events(int32_t kernel, void *start, void *stop);
+
+/* Number of kernels the library has launched from this thread so far
+ * (instrumentation; counts every launch of every entry point). */
+uint64_t pka_kernel_launches(void);
+
 /* Thread-local description of the last non-OK status on this thread. */
 const char *pka_last_error(void);
 

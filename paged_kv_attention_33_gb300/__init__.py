@@ -23,7 +23,9 @@ import threading
 from . import build as _build
 
 __all__ = ["Meta", "PkaError", "reshape_and_cache", "paged_attn_forward", "cascade_merge",
-           "workspace_size", "check_status", "load_library", "library_path"]
+           "workspace_size", "check_status", "set_kernel_events", "kernel_launches",
+           "load_library",
+           "library_path", "KERNEL_DECODE", "KERNEL_PREFILL"]
 
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
@@ -75,6 +77,10 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pka_paged_attn_forward.restype = ctypes.c_int
         lib.pka_cascade_merge.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P]
         lib.pka_cascade_merge.restype = ctypes.c_int
+        lib.pka_set_kernel_events.argtypes = [_I32, _P, _P]
+        lib.pka_set_kernel_events.restype = ctypes.c_int
+        lib.pka_kernel_launches.argtypes = []
+        lib.pka_kernel_launches.restype = ctypes.c_uint64
         lib.pka_check_status.argtypes = [_P]
         lib.pka_check_status.restype = ctypes.c_int
         lib.pka_last_error.argtypes = []
@@ -187,6 +193,24 @@ def cascade_merge(out_a, lse_a, out_b, lse_b, out, lse_out=None, stream=None) ->
     T, H, D = out_a.shape
     _check(lib.pka_cascade_merge(_ptr(out_a), _ptr(lse_a), _ptr(out_b), _ptr(lse_b), _ptr(out),
                                  _ptr(lse_out), T, H, D, _stream(stream)))
+
+
+KERNEL_DECODE = 0
+KERNEL_PREFILL = 1
+
+
+def set_kernel_events(kernel: int, start=None, stop=None) -> None:
+    """Record torch CUDA events `start`/`stop` around the named kernel in every
+    later forward on this thread (None turns it off)."""
+    def raw(e):
+        return None if e is None else ctypes.c_void_p(e.cuda_event)
+
+    _check(load_library().pka_set_kernel_events(kernel, raw(start), raw(stop)))
+
+
+def kernel_launches() -> int:
+    """Kernels the library has launched from this thread so far."""
+    return int(load_library().pka_kernel_launches())
 
 
 def check_status(stream=None) -> None:

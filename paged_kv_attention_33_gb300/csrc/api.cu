@@ -22,6 +22,24 @@
 namespace pka {
 
 static thread_local char g_msg[512] = "";
+// Optional timing events per kernel kind (pka_set_kernel_events).
+static thread_local cudaEvent_t g_ev_start[2] = {nullptr, nullptr};
+static thread_local cudaEvent_t g_ev_stop[2] = {nullptr, nullptr};
+
+static thread_local uint64_t g_launches = 0;
+void count_launch() { ++g_launches; }
+
+static void record_start(int which, cudaStream_t st)
+{
+    if (g_ev_start[which])
+        cudaEventRecord(g_ev_start[which], st);
+}
+
+static void record_stop(int which, cudaStream_t st)
+{
+    if (g_ev_stop[which])
+        cudaEventRecord(g_ev_stop[which], st);
+}
 
 static pka_status fail(pka_status st, const char *fmt, ...)
 {
@@ -75,23 +93,32 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
+CUresult encode_3d_bf16(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1,
+                        uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes,
+                        uint32_t box0, uint32_t box1, uint32_t box2)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return CUDA_ERROR_NOT_FOUND;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    cuuint32_t box[3] = {box0, box1, box2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 // The pool [num_blocks, 2, block_size, num_kv_heads, head_size] seen as the
 // 3-D tensor (head_size, num_kv_heads, num_blocks*2*block_size); one box is
 // {64 dims, 1 head, 16 rows}, 128-byte swizzled.
 CUresult encode_kv_map(CUtensorMap *map, const void *cache, int32_t head_size,
                        int32_t num_kv_heads, int32_t block_size, int64_t num_blocks)
 {
-    auto fn = encode_fn();
-    if (!fn)
-        return CUDA_ERROR_NOT_FOUND;
-    cuuint64_t dims[3] = {cuuint64_t(head_size), cuuint64_t(num_kv_heads),
-                          cuuint64_t(num_blocks) * 2 * cuuint64_t(block_size)};
-    cuuint64_t strides[2] = {cuuint64_t(head_size) * 2, cuuint64_t(num_kv_heads) * head_size * 2};
-    cuuint32_t box[3] = {64, 1, 16};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(cache), dims, strides,
-              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return encode_3d_bf16(map, cache, uint64_t(head_size), uint64_t(num_kv_heads),
+                          uint64_t(num_blocks) * 2 * uint64_t(block_size),
+                          uint64_t(head_size) * 2, uint64_t(num_kv_heads) * head_size * 2, 64, 1,
+                          16);
 }
 
 // ------------------------------------------------------------ planning
@@ -178,6 +205,17 @@ extern "C" {
 
 const char *pka_last_error(void) { return g_msg; }
 
+uint64_t pka_kernel_launches(void) { return g_launches; }
+
+pka_status pka_set_kernel_events(int32_t kernel, void *start, void *stop)
+{
+    if (kernel != PKA_KERNEL_DECODE && kernel != PKA_KERNEL_PREFILL)
+        return fail(PKA_ERR_INVALID_ARG, "unknown kernel id %d", kernel);
+    g_ev_start[kernel] = static_cast<cudaEvent_t>(start);
+    g_ev_stop[kernel] = static_cast<cudaEvent_t>(stop);
+    return PKA_OK;
+}
+
 pka_status pka_reshape_and_cache(const void *key, const void *value, void *kv_cache,
                                  const int64_t *slot_mapping, int32_t num_tokens,
                                  int32_t num_kv_heads, int32_t head_size, int32_t block_size,
@@ -248,8 +286,9 @@ pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const
     const bool cascade = meta->common_prefix_len > 0;
     const int32_t kv_begin = meta->common_prefix_len;
     const int num_prefills = meta->num_seqs - meta->num_decodes;
-    if (num_prefills > 0)
-        return fail(PKA_ERR_UNSUPPORTED, "prefill sequences are not served by this build yet");
+    if (num_prefills > kMaxPrefillSeqsPerCall)
+        return fail(PKA_ERR_UNSUPPORTED, "more than %d prefill sequences in one call",
+                    kMaxPrefillSeqsPerCall);
     if (cascade)
         return fail(PKA_ERR_UNSUPPORTED, "cascade is not served by this build yet");
 
@@ -291,12 +330,21 @@ pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const
     if (cr != CUDA_SUCCESS)
         return fail(PKA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(cr));
 
+    record_start(PKA_KERNEL_DECODE, f.stream);
     cudaError_t e = launch_decode(f, dp, ws, wsp, kv_map, kv_begin, false);
+    record_stop(PKA_KERNEL_DECODE, f.stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "decode launch");
     e = launch_decode_combine(f, dp, ws, wsp, kv_begin, false);
     if (e != cudaSuccess)
         return cuda_fail(e, "decode combine launch");
+    if (num_prefills > 0) {
+        record_start(PKA_KERNEL_PREFILL, f.stream);
+        e = launch_prefill(f, wsp, ws, 0, INT32_MAX, causal ? 1 : 0, false);
+        record_stop(PKA_KERNEL_PREFILL, f.stream);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "prefill launch");
+    }
     return PKA_OK;
 }
 
@@ -326,7 +374,7 @@ pka_status pka_check_status(void *stream)
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "stream synchronize");
-    const uint32_t bits = kv_write_take_error() | decode_take_error();
+    const uint32_t bits = kv_write_take_error() | decode_take_error() | prefill_take_error();
     if (bits == 0)
         return PKA_OK;
     char buf[256] = "";

@@ -487,6 +487,7 @@ static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Wor
     p.o_part = reinterpret_cast<float *>(wsp + ws.o_part);
     p.lse_part = reinterpret_cast<float *>(wsp + ws.lse_part);
     dim3 grid(dp.max_splits, f.num_decodes);
+    count_launch();
     paged_decode_kernel<D><<<grid, kDecodeThreads, Cfg::kSmemBytes, f.stream>>>(kv_map, p);
     return cudaGetLastError();
 }
@@ -524,6 +525,7 @@ cudaError_t launch_decode_combine(const Fwd &f, const DecodePlan &dp, const Work
     p.lse = f.lse;
     const int64_t warps = int64_t(f.num_decodes) * f.num_heads;
     const unsigned grid = static_cast<unsigned>((warps * 32 + 255) / 256);
+    count_launch();
     if (f.head_size == 128)
         decode_combine_kernel<128><<<grid, 256, 0, f.stream>>>(p);
     else

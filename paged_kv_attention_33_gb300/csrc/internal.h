@@ -81,7 +81,21 @@ cudaError_t launch_cascade_merge(const void *out_a, const float *lse_a, const vo
                                  int32_t num_tokens, int32_t num_heads, int32_t head_size,
                                  cudaStream_t st);
 
-// tensor maps (api.cu)
+// Per-thread count of kernel launches (api.cu), bumped by every launcher.
+void count_launch();
+
+// prefill.cu: causal (or not) attention of the prefill sequences
+// [num_decodes, num_seqs) over keys [kv_lo, min(kv_cap, L_s)).  partial:
+// write fp32 partials (cascade) into ws.o_suf / ws.lse_suf instead of out/lse.
+cudaError_t launch_prefill(const Fwd &f, char *wsp, const Workspace &ws, int32_t kv_lo,
+                           int32_t kv_cap, int32_t causal, bool partial);
+uint32_t prefill_take_error();
+constexpr int kMaxPrefillSeqsPerCall = 4096;
+
+// tensor maps (api.cu): a 3-D bf16 tensor (d0 contiguous), 128-byte swizzle
+CUresult encode_3d_bf16(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1,
+                        uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes,
+                        uint32_t box0, uint32_t box1, uint32_t box2);
 CUresult encode_kv_map(CUtensorMap *map, const void *cache, int32_t head_size,
                        int32_t num_kv_heads, int32_t block_size, int64_t num_blocks);
 

@@ -71,6 +71,7 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *c
     const int32_t row_vecs = num_kv_heads * head_size * 2 / 16;
     const int64_t threads = static_cast<int64_t>(num_tokens) * 32;
     const unsigned grid = static_cast<unsigned>((threads + kKvwThreads - 1) / kKvwThreads);
+    count_launch();
     reshape_and_cache_kernel<<<grid, kKvwThreads, 0, st>>>(
         static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
         static_cast<uint4 *>(cache), slots, num_tokens, row_vecs, block_size, num_blocks);

@@ -65,6 +65,7 @@ cudaError_t launch_cascade_merge(const void *out_a, const float *lse_a, const vo
     if (rows == 0)
         return cudaSuccess;
     const unsigned grid = static_cast<unsigned>((rows * 32 + 255) / 256);
+    count_launch();
     cascade_merge_kernel<<<grid, 256, 0, st>>>(
         static_cast<const uint4 *>(out_a), lse_a, static_cast<const uint4 *>(out_b), lse_b,
         static_cast<uint4 *>(out), lse_out, rows, head_size * 2 / 16);

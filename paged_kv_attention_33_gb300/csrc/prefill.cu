@@ -1,0 +1,607 @@
+// prefill.cu -- varlen causal prefill / chunked prefill on the fifth-generation
+// tensor cores (tcgen05) with accumulators in tensor memory (TMEM).
+//
+// What it computes (the "El especialista del plato estrella" blog, "Por que
+// prefill y decode son problemas opuestos"): N queries against N (+ prior
+// context) keys, N^2 d flops over N d bytes, so it is bound by the tensor
+// cores.  For sequence s with q_s queries after c_s cached tokens, query i
+// admits keys j <= c_s + i (bottom-right causal alignment), keys read through
+// the block table (the blog's "Como lee el backend el KV paginado").
+//
+// Work item: (sequence s, 128-query tile, query head h), in a persistent grid
+// (one CTA per SM, items taken round-robin, the heaviest causal tiles of each
+// sequence first).  Roles inside the CTA (256 threads):
+//   warp 0      TMA producer: the Q tile once per item, then K and V tiles of
+//               128 keys into a two-stage ring, one TMA box per page (paged
+//               gather straight from the pool, 128-byte swizzled);
+//   warp 1      MMA issuer (one thread): S = Q K^T into one of two TMEM
+//               buffers (M=128, N=128, K=head_size), then O += P V with P read
+//               from TMEM (M=128, N=head_size, K=128 keys);
+//   warp 2      TMEM allocator;
+//   warps 4-7   softmax: thread r owns query row r; it reads its S row from
+//               TMEM, applies the mask and the online softmax (base-2, scale
+//               folded in), writes P back over S as bf16, rescales its O row
+//               in TMEM when its running max moved, and at the end writes
+//               out = O / l and lse.
+// TMEM columns: S buffers [0,128) and [128,256), O [256, 256+head_size).
+#include <math.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tcgen05.cuh"
+
+namespace pka {
+
+constexpr int kBM = 128;             // query rows per tile
+constexpr int kBN = 128;             // keys per tile
+constexpr int kPfThreads = 256;
+constexpr int kPfStages = 2;
+constexpr int kMaxPrefillSeqs = 4096;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kPfNegInf = -INFINITY;
+constexpr float kPfLn2 = 0.69314718055994530942f;
+
+struct PrefillParams {
+    const int32_t *qsl;
+    const int32_t *seq_lens;
+    const int32_t *block_table;
+    int32_t bt_stride;
+    int32_t first_seq;  // prefill sequences are [first_seq, num_seqs)
+    int32_t num_seqs;
+    int32_t num_tokens;
+    int32_t num_heads;
+    int32_t group;
+    int32_t block_size;
+    int32_t box_rows;  // rows per K/V TMA box: min(block_size, 128)
+    int32_t num_blocks;
+    int32_t kv_lo;     // first key attended
+    int32_t kv_cap;    // keys >= kv_cap are not attended
+    int32_t causal;
+    float scale_log2;
+    int32_t partial;     // 0: bf16 out + ln lse; 1: fp32 partial + log2 lse
+    int32_t token_base;  // partial rows are (t - token_base) * H + h
+    __nv_bfloat16 *out;
+    float *lse;
+    float *o_part;
+    float *lse_part;
+};
+
+template <int D>
+struct PfCfg {
+    static constexpr int kHalves = D / 64;
+    static constexpr int kHalfBytes = 128 * 128;        // 128 rows x 128 B
+    static constexpr int kTileBytes = kHalves * kHalfBytes;  // Q, K or V tile
+    static constexpr int kQOff = 0;
+    static constexpr int kKOff = kTileBytes;
+    static constexpr int kVOff = kKOff + kPfStages * kTileBytes;
+    static constexpr int kBarOff = kVOff + kPfStages * kTileBytes;
+    static constexpr int kNumBars = 16;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;   // tmem base, abort flag
+    static constexpr int kPrefixOff = kMiscOff + 16;
+    static constexpr size_t kSmemBytes = kPrefixOff + (kMaxPrefillSeqs + 1) * 4 + 1024;
+    static constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, 0, 0);
+    static constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, 0, 1);
+};
+
+struct PfItem {
+    int s, h, t0, rows, qidx0, ctx, L, kv_hi, n_kv;
+};
+
+__device__ __forceinline__ bool pf_item(const PrefillParams &p, const int32_t *prefix, int nseq,
+                                        int item, PfItem &it)
+{
+    const int tiles = prefix[nseq];
+    if (item >= tiles * p.num_heads)
+        return false;
+    it.h = item % p.num_heads;
+    const int r = item / p.num_heads;
+    int lo = 0, hi = nseq;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= r)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    it.s = p.first_seq + lo;
+    const int ntile = prefix[lo + 1] - prefix[lo];
+    const int qt = ntile - 1 - (r - prefix[lo]);  // heaviest tile of the sequence first
+    const int q0 = p.qsl[it.s];
+    const int qlen = p.qsl[it.s + 1] - q0;
+    it.L = p.seq_lens[it.s];
+    it.ctx = it.L - qlen;
+    it.qidx0 = qt * kBM;
+    it.t0 = q0 + it.qidx0;
+    it.rows = min(kBM, qlen - it.qidx0);
+    int kv_hi = p.causal ? min(it.L, it.ctx + it.qidx0 + it.rows) : it.L;
+    kv_hi = min(kv_hi, p.kv_cap);
+    it.kv_hi = kv_hi;
+    it.n_kv = kv_hi > p.kv_lo ? (kv_hi - p.kv_lo + kBN - 1) / kBN : 0;
+    return true;
+}
+
+// Bounded wait that also gives up once another role has given up.
+__device__ __forceinline__ bool pf_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
+{
+    if (mbar_test(bar, parity))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1; it < kWaitIterCap; ++it) {
+        if (mbar_test(bar, parity))
+            return true;
+        if ((it & 127u) == 0) {
+            if (*abort_flag)
+                return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs)
+                break;
+        }
+    }
+    flag_error(kErrWaitTimeout);
+    *abort_flag = 1;
+    return false;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPfThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
+                      const __grid_constant__ CUtensorMap kv_map, const PrefillParams p)
+{
+    using Cfg = PfCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kBarOff);
+    uint64_t *q_full = bars + 0;
+    uint64_t *q_empty = bars + 1;
+    uint64_t *k_full = bars + 2;   // [kPfStages]
+    uint64_t *v_full = bars + 4;   // [kPfStages]
+    uint64_t *kv_empty = bars + 6; // [kPfStages]
+    uint64_t *s_full = bars + 8;   // [2]
+    uint64_t *p_full = bars + 10;  // [2]
+    uint64_t *o_done = bars + 12;
+    uint64_t *o_free = bars + 13;
+    uint64_t *drain = bars + 14;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + Cfg::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kMiscOff + 4);
+    int32_t *prefix = reinterpret_cast<int32_t *>(smem + Cfg::kPrefixOff);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int nseq = p.num_seqs - p.first_seq;
+
+    // ---- prefix sums of 128-query tiles per prefill sequence (block-wide scan)
+    {
+        __shared__ int32_t part[kPfThreads];
+        const int per = (nseq + kPfThreads - 1) / kPfThreads;
+        const int a = min(nseq, int(threadIdx.x) * per);
+        const int b = min(nseq, a + per);
+        int sum = 0;
+        for (int k = a; k < b; ++k) {
+            const int s = p.first_seq + k;
+            const int ql = p.qsl[s + 1] - p.qsl[s];
+            sum += ql > 0 ? (ql + kBM - 1) / kBM : 0;
+        }
+        part[threadIdx.x] = sum;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int run = 0;
+            for (int i = 0; i < kPfThreads; ++i) {
+                const int v = part[i];
+                part[i] = run;
+                run += v;
+            }
+            prefix[nseq] = run;
+        }
+        __syncthreads();
+        int run = part[threadIdx.x];
+        for (int k = a; k < b; ++k) {
+            prefix[k] = run;
+            const int s = p.first_seq + k;
+            const int ql = p.qsl[s + 1] - p.qsl[s];
+            run += ql > 0 ? (ql + kBM - 1) / kBM : 0;
+        }
+    }
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        for (int i = 0; i < kPfStages; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 4);
+        }
+        mbar_init(o_done, 1);
+        mbar_init(o_free, 4);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(tmem_holder, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_holder;
+    const uint32_t tS = tbase;          // two S buffers of 128 columns
+    const uint32_t tO = tbase + 256;    // O, D columns
+
+    if (warp == 0) {
+        // ================================================================ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&q_map);
+            tma_prefetch_desc(&kv_map);
+            const uint64_t pol_kv = l2_policy_evict_last();
+            const uint64_t pol_q = l2_policy_evict_first();
+            uint32_t li = 0, kv_it = 0;
+            PfItem it;
+            for (int item = blockIdx.x; pf_item(p, prefix, nseq, item, it); item += gridDim.x) {
+                if (it.n_kv == 0)
+                    continue;
+                if (li > 0 && !pf_wait(q_empty, (li - 1) & 1, abort_flag))
+                    goto producer_done;
+                mbar_arrive_expect_tx(q_full, Cfg::kTileBytes);
+                for (int hf = 0; hf < Cfg::kHalves; ++hf)
+                    tma_load_3d(smem + Cfg::kQOff + hf * Cfg::kHalfBytes, &q_map, q_full, hf * 64,
+                                it.h, it.t0, pol_q);
+                const int kvh = it.h / p.group;
+                const int32_t *bt = p.block_table + int64_t(it.s) * p.bt_stride;
+                for (int jt = 0; jt < it.n_kv; ++jt, ++kv_it) {
+                    const int st = kv_it % kPfStages;
+                    const uint32_t rnd = kv_it / kPfStages;
+                    if (rnd > 0 && !pf_wait(&kv_empty[st], (rnd - 1) & 1, abort_flag))
+                        goto producer_done;
+                    const int key0 = p.kv_lo + jt * kBN;
+                    const int nvalid = min(kBN, it.kv_hi - key0);
+                    const int nbox = (nvalid + p.box_rows - 1) / p.box_rows;
+                    const uint32_t bytes = nbox * p.box_rows * 128 * Cfg::kHalves;
+                    for (int kv = 0; kv < 2; ++kv) {
+                        uint64_t *bar = kv == 0 ? &k_full[st] : &v_full[st];
+                        uint8_t *tile = smem + (kv == 0 ? Cfg::kKOff : Cfg::kVOff) +
+                                        st * Cfg::kTileBytes;
+                        mbar_arrive_expect_tx(bar, bytes);
+                        for (int bx = 0; bx < nbox; ++bx) {
+                            const int key = key0 + bx * p.box_rows;
+                            const int col = key / p.block_size;
+                            int blk = col < p.bt_stride ? bt[col] : -1;
+                            if (blk < 0 || blk >= p.num_blocks) {
+                                flag_error(kErrBlockOutOfPool);
+                                blk = 0;
+                            }
+                            const int row = (blk * 2 + kv) * p.block_size + key % p.block_size;
+                            for (int hf = 0; hf < Cfg::kHalves; ++hf)
+                                tma_load_3d(tile + hf * Cfg::kHalfBytes + bx * p.box_rows * 128,
+                                            &kv_map, bar, hf * 64, kvh, row, pol_kv);
+                        }
+                    }
+                }
+                ++li;
+            }
+        }
+    producer_done:;
+    } else if (warp == 1) {
+        // ================================================================ MMA issuer
+        const uint32_t sQ = smem_addr(smem + Cfg::kQOff);
+        uint32_t li = 0, kv_it = 0, s_it = 0;
+        PfItem it;
+        for (int item = blockIdx.x; pf_item(p, prefix, nseq, item, it); item += gridDim.x) {
+            if (it.n_kv == 0)
+                continue;
+            if (!pf_wait(q_full, li & 1, abort_flag))
+                goto mma_done;
+            tc_fence_after();
+            for (int jt = 0; jt <= it.n_kv; ++jt) {
+                if (jt < it.n_kv) {
+                    // ---- S[jt] = Q K[jt]^T
+                    const uint32_t n = kv_it + jt;
+                    const int st = n % kPfStages;
+                    if (!pf_wait(&k_full[st], (n / kPfStages) & 1, abort_flag))
+                        goto mma_done;
+                    tc_fence_after();
+                    const uint32_t sb = (s_it + jt) & 1;
+                    const uint32_t sK = smem_addr(smem + Cfg::kKOff + st * Cfg::kTileBytes);
+                    if (lane == 0) {
+#pragma unroll
+                        for (int k = 0; k < D / 16; ++k) {
+                            const uint32_t off = (k >> 2) * Cfg::kHalfBytes + (k & 3) * 32;
+                            mma_ss(tS + sb * 128, smem_desc_sw128(sQ + off, 16, 1024),
+                                   smem_desc_sw128(sK + off, 16, 1024), Cfg::kIdescS, k > 0);
+                        }
+                        mma_commit(&s_full[sb]);
+                        if (jt == it.n_kv - 1)
+                            mma_commit(q_empty);
+                    }
+                    __syncwarp();
+                }
+                if (jt > 0) {
+                    // ---- O += P[jt-1] V[jt-1]
+                    const int jp = jt - 1;
+                    const uint32_t n = kv_it + jp;
+                    const int st = n % kPfStages;
+                    const uint32_t sn = s_it + jp;
+                    const uint32_t sb = sn & 1;
+                    if (!pf_wait(&p_full[sb], (sn >> 1) & 1, abort_flag))
+                        goto mma_done;
+                    if (!pf_wait(&v_full[st], (n / kPfStages) & 1, abort_flag))
+                        goto mma_done;
+                    uint8_t *vt = smem + Cfg::kVOff + st * Cfg::kTileBytes;
+                    const int nvalid = it.kv_hi - (p.kv_lo + jp * kBN);
+                    if (nvalid < kBN) {
+                        // rows past the last key may hold anything (or nothing was
+                        // loaded there): zero them so that P = 0 meets finite V
+                        for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+                            uint4 *base = reinterpret_cast<uint4 *>(vt + hf * Cfg::kHalfBytes +
+                                                                     nvalid * 128);
+                            const int n16 = (kBN - nvalid) * 8;
+                            for (int i = lane; i < n16; i += 32)
+                                base[i] = make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
+                    }
+                    if (jp == 0 && li > 0 && !pf_wait(o_free, (li - 1) & 1, abort_flag))
+                        goto mma_done;
+                    __syncwarp();
+                    tc_fence_after();
+                    const uint32_t sV = smem_addr(vt);
+                    if (lane == 0) {
+#pragma unroll
+                        for (int k = 0; k < kBN / 16; ++k)
+                            mma_ts(tO, tS + sb * 128 + k * 8,
+                                   smem_desc_sw128(sV + k * 2048, Cfg::kHalfBytes, 1024),
+                                   Cfg::kIdescPV, (jp > 0 || k > 0) ? 1u : 0u);
+                        mma_commit(o_done);
+                        mma_commit(&kv_empty[st]);
+                    }
+                    __syncwarp();
+                }
+            }
+            kv_it += it.n_kv;
+            s_it += it.n_kv;
+            ++li;
+        }
+    mma_done:
+        if (lane == 0) {
+            mma_commit(drain);  // all issued MMAs have finished once this fires
+            mbar_wait(drain, 0);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ================================================================ softmax
+        const int wq = warp - 4;  // TMEM lane quarter of this warp
+        const int r = wq * 32 + lane;
+        const uint32_t lane_off = uint32_t(wq * 32) << 16;
+        uint32_t s_it = 0, pv_n = 0;
+        PfItem it;
+        for (int item = blockIdx.x; pf_item(p, prefix, nseq, item, it); item += gridDim.x) {
+            const bool valid = r < it.rows;
+            const int t = it.t0 + r;
+            if (it.n_kv == 0) {
+                if (valid && p.partial) {
+                    const int64_t row = int64_t(t - p.token_base) * p.num_heads + it.h;
+                    for (int d = 0; d < D; ++d)
+                        p.o_part[row * D + d] = 0.f;
+                    p.lse_part[row] = kPfNegInf;
+                }
+                continue;
+            }
+            const int pos = it.ctx + it.qidx0 + r;
+            int hi_row = p.causal ? min(it.L, pos + 1) : it.L;
+            hi_row = min(hi_row, p.kv_cap);
+            float m = kPfNegInf, l = 0.f;
+            for (int jt = 0; jt < it.n_kv; ++jt) {
+                const uint32_t sn = s_it + jt;
+                const uint32_t sb = sn & 1;
+                if (!pf_wait(&s_full[sb], (sn >> 1) & 1, abort_flag))
+                    goto softmax_done;
+                tc_fence_after();
+                const uint32_t ts = tS + sb * 128 + lane_off;
+                float x[kBN];
+                {
+                    uint32_t raw[32];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        tmem_ld32(ts + c * 32, raw);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            x[c * 32 + i] = __uint_as_float(raw[i]);
+                    }
+                }
+                const int key0 = p.kv_lo + jt * kBN;
+                const int lim = hi_row - key0;  // columns c < lim are admitted
+                float mx = kPfNegInf;
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) {
+                    x[c] = c < lim ? x[c] * p.scale_log2 : kPfNegInf;
+                    mx = fmaxf(mx, x[c]);
+                }
+                const float m_new = fmaxf(m, mx);
+                const float base = m_new == kPfNegInf ? 0.f : m_new;
+                float sum = 0.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float p0 = fast_exp2(x[c * 32 + 2 * i] - base);
+                        const float p1 = fast_exp2(x[c * 32 + 2 * i + 1] - base);
+                        sum += p0 + p1;
+                        pk[i] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(ts + c * 16, pk);
+                }
+                tmem_wait_st();
+                const float alpha = fast_exp2(m - base);
+                l = l * alpha + sum;
+                m = m_new;
+                if (jt > 0) {
+                    if (!pf_wait(o_done, pv_n & 1, abort_flag))
+                        goto softmax_done;
+                    ++pv_n;
+                    tc_fence_after();
+                    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t o[32];
+                            tmem_ld32(tO + lane_off + c * 32, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                            tmem_st32(tO + lane_off + c * 32, o);
+                        }
+                        tmem_wait_st();
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&p_full[sb]);
+            }
+            // ---- epilogue: out = O / l, lse
+            if (!pf_wait(o_done, pv_n & 1, abort_flag))
+                goto softmax_done;
+            ++pv_n;
+            tc_fence_after();
+            {
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const float lse2 = m + log2f(l);
+                const int64_t orow = int64_t(t) * p.num_heads + it.h;
+                const int64_t prow = int64_t(t - p.token_base) * p.num_heads + it.h;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + lane_off + c * 32, o);
+                    tmem_wait_ld();
+                    if (valid) {
+                        if (p.partial) {
+                            float4 *dst = reinterpret_cast<float4 *>(p.o_part + prow * D + c * 32);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv,
+                                                     __uint_as_float(o[4 * i + 1]) * inv,
+                                                     __uint_as_float(o[4 * i + 2]) * inv,
+                                                     __uint_as_float(o[4 * i + 3]) * inv);
+                        } else {
+                            uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D + c * 32);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                dst[i] = make_uint4(
+                                    pack_bf16x2(__uint_as_float(o[8 * i]) * inv,
+                                                __uint_as_float(o[8 * i + 1]) * inv),
+                                    pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv,
+                                                __uint_as_float(o[8 * i + 3]) * inv),
+                                    pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv,
+                                                __uint_as_float(o[8 * i + 5]) * inv),
+                                    pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv,
+                                                __uint_as_float(o[8 * i + 7]) * inv));
+                        }
+                    }
+                }
+                if (valid) {
+                    if (p.partial)
+                        p.lse_part[prow] = lse2;
+                    else if (p.lse)
+                        p.lse[orow] = lse2 * kPfLn2;
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(o_free);
+            s_it += it.n_kv;
+        }
+    softmax_done:;
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 2)
+        tmem_dealloc(tbase, kTmemCols);
+}
+
+// --------------------------------------------------------------------- host
+static CUresult encode_q_map(CUtensorMap *map, const void *q, int32_t num_tokens,
+                             int32_t num_heads, int32_t head_size)
+{
+    return encode_3d_bf16(map, q, head_size, num_heads, num_tokens,
+                          uint64_t(head_size) * 2, uint64_t(num_heads) * head_size * 2, 64, 1,
+                          kBM);
+}
+
+template <int D>
+static cudaError_t launch_prefill_d(const Fwd &f, const PrefillParams &p, int grid)
+{
+    using Cfg = PfCfg<D>;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(Cfg::kSmemBytes));
+        if (e != cudaSuccess)
+            return e;
+        configured_device = dev;
+    }
+    CUtensorMap q_map, kv_map;
+    if (encode_q_map(&q_map, f.query, f.num_tokens, f.num_heads, D) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    if (encode_3d_bf16(&kv_map, f.kv_cache, D, f.num_kv_heads,
+                       uint64_t(f.num_blocks) * 2 * f.block_size, uint64_t(D) * 2,
+                       uint64_t(f.num_kv_heads) * D * 2, 64, 1, p.box_rows) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    count_launch();
+    prefill_tc_kernel<D><<<grid, kPfThreads, Cfg::kSmemBytes, f.stream>>>(q_map, kv_map, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefill(const Fwd &f, char *wsp, const Workspace &ws, int32_t kv_lo,
+                           int32_t kv_cap, int32_t causal, bool partial)
+{
+    const int nseq = f.num_seqs - f.num_decodes;
+    if (nseq <= 0)
+        return cudaSuccess;
+    PrefillParams p;
+    p.qsl = f.qsl;
+    p.seq_lens = f.seq_lens;
+    p.block_table = f.block_table;
+    p.bt_stride = f.bt_stride;
+    p.first_seq = f.num_decodes;
+    p.num_seqs = f.num_seqs;
+    p.num_tokens = f.num_tokens;
+    p.num_heads = f.num_heads;
+    p.group = f.num_heads / f.num_kv_heads;
+    p.block_size = f.block_size;
+    p.box_rows = std::min(f.block_size, 128);
+    p.num_blocks = static_cast<int32_t>(f.num_blocks);
+    p.kv_lo = kv_lo;
+    p.kv_cap = kv_cap;
+    p.causal = causal;
+    p.scale_log2 = f.scale * 1.4426950408889634f;
+    p.partial = partial ? 1 : 0;
+    p.token_base = f.num_decodes;
+    p.out = static_cast<__nv_bfloat16 *>(f.out);
+    p.lse = f.lse;
+    p.o_part = reinterpret_cast<float *>(wsp + ws.o_suf);
+    p.lse_part = reinterpret_cast<float *>(wsp + ws.lse_suf);
+    // persistent grid: one CTA per SM, but no more CTAs than tiles
+    const int64_t tiles_upper =
+        (int64_t(f.num_tokens - f.num_decodes) + int64_t(nseq) * (kBM - 1)) / kBM * f.num_heads;
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(f.num_sms, tiles_upper)));
+    if (f.head_size == 128)
+        return launch_prefill_d<128>(f, p, grid);
+    return launch_prefill_d<64>(f, p, grid);
+}
+
+uint32_t prefill_take_error() { return take_device_error(); }
+
+}  // namespace pka
