@@ -452,11 +452,12 @@ def run_profile(args, st):
     torch.cuda.synchronize()
     st.pka.check_status()
     ms = e0.elapsed_time(e1) / args.steps
-    kv_bytes, _ = units(st.spec)
+    kv_bytes, flops = units(st.spec)
     print(json.dumps({"profile_run": True, "workload": args.workload,
                       "num_decodes": st.spec.num_decodes, "ms_per_step": ms,
-                      "kv_bytes_per_step": kv_bytes,
-                      "GBps_step": kv_bytes / (ms * 1e-3) / 1e9}), flush=True)
+                      "kv_bytes_per_step": kv_bytes, "prefill_flops_per_step": flops,
+                      "GBps_step": kv_bytes / (ms * 1e-3) / 1e9,
+                      "TFLOPs_step": flops / (ms * 1e-3) / 1e12}), flush=True)
     return 0
 
 

@@ -289,8 +289,6 @@ pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const
     if (num_prefills > kMaxPrefillSeqsPerCall)
         return fail(PKA_ERR_UNSUPPORTED, "more than %d prefill sequences in one call",
                     kMaxPrefillSeqsPerCall);
-    if (cascade)
-        return fail(PKA_ERR_UNSUPPORTED, "cascade is not served by this build yet");
 
     Fwd f;
     f.query = query;
@@ -330,21 +328,40 @@ pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const
     if (cr != CUDA_SUCCESS)
         return fail(PKA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(cr));
 
+    cudaError_t e;
+    if (cascade) {
+        // [blog] "Que aporta FlashInfer: JIT y cascade attention": the shared
+        // prefix once for every query (tensor cores, no mask), each sequence's
+        // own suffix [P, L_s), then a log-sum-exp merge of the parts.
+        PrefillPass pre{0, kv_begin, 0, true, reinterpret_cast<float *>(wsp + ws.o_pre),
+                        reinterpret_cast<float *>(wsp + ws.lse_pre), 0};
+        record_start(PKA_KERNEL_PREFILL, f.stream);
+        e = launch_prefill(f, pre);
+        record_stop(PKA_KERNEL_PREFILL, f.stream);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cascade prefix launch");
+    }
     record_start(PKA_KERNEL_DECODE, f.stream);
-    cudaError_t e = launch_decode(f, dp, ws, wsp, kv_map, kv_begin, false);
+    e = launch_decode(f, dp, ws, wsp, kv_map, kv_begin, cascade);
     record_stop(PKA_KERNEL_DECODE, f.stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "decode launch");
-    e = launch_decode_combine(f, dp, ws, wsp, kv_begin, false);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "decode combine launch");
     if (num_prefills > 0) {
-        record_start(PKA_KERNEL_PREFILL, f.stream);
-        e = launch_prefill(f, wsp, ws, 0, INT32_MAX, causal ? 1 : 0, false);
-        record_stop(PKA_KERNEL_PREFILL, f.stream);
+        PrefillPass pf{kv_begin, INT32_MAX, causal ? 1 : 0, false,
+                       cascade ? reinterpret_cast<float *>(wsp + ws.o_suf) : nullptr,
+                       cascade ? reinterpret_cast<float *>(wsp + ws.lse_suf) : nullptr,
+                       meta->num_decodes};
+        if (!cascade)
+            record_start(PKA_KERNEL_PREFILL, f.stream);
+        e = launch_prefill(f, pf);
+        if (!cascade)
+            record_stop(PKA_KERNEL_PREFILL, f.stream);
         if (e != cudaSuccess)
             return cuda_fail(e, "prefill launch");
     }
+    e = launch_decode_combine(f, dp, ws, wsp, kv_begin, cascade);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "combine launch");
     return PKA_OK;
 }
 

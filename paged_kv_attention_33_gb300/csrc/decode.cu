@@ -118,6 +118,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const int s = blockIdx.y;
     const int split = blockIdx.x;
     const int L = p.seq_lens[s];
+    if (p.kv_begin > 0 && L <= p.kv_begin) {
+        // cascade suffix pass: the decode's query must come after the shared prefix
+        if (threadIdx.x == 0 && split == 0)
+            flag_error(kErrBadMetadata);
+        return;
+    }
     const int key_begin = p.kv_begin + split * p.split_tokens;
     if (key_begin >= L)
         return;  // whole CTA: this split lies past the end of the sequence
@@ -351,77 +357,101 @@ struct CombineParams {
     int32_t max_splits;
     int32_t kv_begin;
     int32_t with_prefix;
-    const float *o_part;
+    const float *o_part;   // decode split partials
     const float *lse_part;
-    const float *o_pre;    // [T, H, D] (cascade)
-    const float *lse_pre;  // [T, H], log2 units
+    const float *o_pre;    // cascade: shared-prefix partial of every token [T, H, D]
+    const float *lse_pre;
+    const float *o_suf;    // cascade: suffix partial of every prefill token
+    const float *lse_suf;
     __nv_bfloat16 *out;
     float *lse;
 };
 
-// One warp per (decode sequence, head): warp-shuffle max and sum of the
-// splits' log2-sum-exp values, then the weighted sum of their normalised
-// partial outputs (the same merge as the cascade merge, over n parts).
+// One warp per (token, head) row: warp-shuffle max and sum of the parts'
+// log2-sum-exp values, then the weighted sum of their normalised partial
+// outputs -- the cascade merge, over n parts.  Parts of a decode token: its
+// splits (and the shared prefix in a cascade); of a prefill token in a
+// cascade: its suffix and the shared prefix.
 template <int D>
 __global__ void __launch_bounds__(256) decode_combine_kernel(const CombineParams p)
 {
     constexpr int kPer = D / 32;
-    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t gw = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (gw >= p.num_decodes * p.num_heads)
+    const int64_t nrows = int64_t(p.with_prefix ? p.num_tokens : p.num_decodes) * p.num_heads;
+    if (gw >= nrows)
         return;
-    const int s = gw / p.num_heads;
-    const int h = gw - s * p.num_heads;
-    const int L = p.seq_lens[s];
-    const int n = max(0, (L - p.kv_begin + p.split_tokens - 1) / p.split_tokens);
-    if (n <= 1 && !p.with_prefix)
-        return;  // finished by the decode kernel itself
-    const int t = p.qsl[s];
-    if (n > p.max_splits || t < 0 || t >= p.num_tokens)
-        return;  // flagged by the decode kernel
-    const int64_t base = static_cast<int64_t>(s) * p.max_splits * p.num_heads + h;
-    const float lpre = p.with_prefix ? p.lse_pre[static_cast<int64_t>(t) * p.num_heads + h]
-                                     : kNegInf;
-    float mx = lpre;
+    const int t = static_cast<int>(gw / p.num_heads);  // decode s owns token s
+    const int h = static_cast<int>(gw - int64_t(t) * p.num_heads);
+    const int64_t row = int64_t(t) * p.num_heads + h;
+    const float *parts_o[2];
+    float parts_l[2];
+    int nextra = 0;
+    if (p.with_prefix) {
+        parts_o[nextra] = p.o_pre + row * D;
+        parts_l[nextra++] = p.lse_pre[row];
+    }
+    int n = 0;
+    int64_t base = 0;
+    if (t < p.num_decodes) {
+        const int L = p.seq_lens[t];
+        n = max(0, (L - p.kv_begin + p.split_tokens - 1) / p.split_tokens);
+        if (n <= 1 && !p.with_prefix)
+            return;  // finished by the decode kernel itself
+        if (n > p.max_splits || p.qsl[t] != t)
+            return;  // flagged by the decode kernel
+        base = int64_t(t) * p.max_splits * p.num_heads + h;
+    } else {
+        const int64_t srow = int64_t(t - p.num_decodes) * p.num_heads + h;
+        parts_o[nextra] = p.o_suf + srow * D;
+        parts_l[nextra++] = p.lse_suf[srow];
+    }
+    float mx = kNegInf;
+    for (int e = 0; e < nextra; ++e)
+        mx = fmaxf(mx, parts_l[e]);
     for (int j = lane; j < n; j += 32)
-        mx = fmaxf(mx, p.lse_part[base + static_cast<int64_t>(j) * p.num_heads]);
+        mx = fmaxf(mx, p.lse_part[base + int64_t(j) * p.num_heads]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float ws = 0.f;
-    for (int j = lane; j < n; j += 32)
-        ws += exp2f(p.lse_part[base + static_cast<int64_t>(j) * p.num_heads] - mx);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        ws += __shfl_xor_sync(0xffffffffu, ws, o);
     float acc[kPer];
 #pragma unroll
     for (int e = 0; e < kPer; ++e)
         acc[e] = 0.f;
-    for (int j = 0; j < n; ++j) {
-        const int64_t row = base + static_cast<int64_t>(j) * p.num_heads;
-        const float w = exp2f(p.lse_part[row] - mx);
-        const float *src = p.o_part + row * D + lane * kPer;
+    float ws = 0.f;
+    if (mx != kNegInf) {
+        for (int j = lane; j < n; j += 32)
+            ws += exp2f(p.lse_part[base + int64_t(j) * p.num_heads] - mx);
 #pragma unroll
-        for (int e = 0; e < kPer; ++e)
-            acc[e] += w * src[e];
-    }
-    if (p.with_prefix) {
-        const float w = exp2f(lpre - mx);
-        ws += w;
-        const float *src = p.o_pre + (static_cast<int64_t>(t) * p.num_heads + h) * D + lane * kPer;
+        for (int o = 16; o > 0; o >>= 1)
+            ws += __shfl_xor_sync(0xffffffffu, ws, o);
+        for (int j = 0; j < n; ++j) {
+            const int64_t prow = base + int64_t(j) * p.num_heads;
+            const float w = exp2f(p.lse_part[prow] - mx);
+            const float *src = p.o_part + prow * D + lane * kPer;
 #pragma unroll
-        for (int e = 0; e < kPer; ++e)
-            acc[e] += w * src[e];
+            for (int e = 0; e < kPer; ++e)
+                acc[e] += w * src[e];
+        }
+        for (int x = 0; x < nextra; ++x) {
+            if (parts_l[x] == kNegInf)
+                continue;  // an empty part contributes nothing, whatever it holds
+            const float w = exp2f(parts_l[x] - mx);
+            ws += w;
+            const float *src = parts_o[x] + lane * kPer;
+#pragma unroll
+            for (int e = 0; e < kPer; ++e)
+                acc[e] += w * src[e];
+        }
     }
-    const float inv = 1.f / ws;
-    __nv_bfloat16 *dst = p.out + (static_cast<int64_t>(t) * p.num_heads + h) * D + lane * kPer;
+    const float inv = ws > 0.f ? 1.f / ws : 0.f;
+    __nv_bfloat16 *dst = p.out + row * D + lane * kPer;
 #pragma unroll
     for (int e = 0; e < kPer; e += 2)
         *reinterpret_cast<__nv_bfloat162 *>(dst + e) =
             __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
     if (lane == 0 && p.lse)
-        p.lse[static_cast<int64_t>(t) * p.num_heads + h] = (mx + log2f(ws)) * kLn2;
+        p.lse[row] = ws > 0.f ? (mx + log2f(ws)) * kLn2 : kNegInf;
 }
 
 // --------------------------------------------------------------------- host
@@ -505,7 +535,7 @@ cudaError_t launch_decode(const Fwd &f, const DecodePlan &dp, const Workspace &w
 cudaError_t launch_decode_combine(const Fwd &f, const DecodePlan &dp, const Workspace &ws,
                                   char *wsp, int32_t kv_begin, bool with_prefix)
 {
-    if (f.num_decodes == 0 || (dp.max_splits <= 1 && !with_prefix))
+    if (!with_prefix && (f.num_decodes == 0 || dp.max_splits <= 1))
         return cudaSuccess;
     CombineParams p;
     p.qsl = f.qsl;
@@ -521,9 +551,11 @@ cudaError_t launch_decode_combine(const Fwd &f, const DecodePlan &dp, const Work
     p.lse_part = reinterpret_cast<const float *>(wsp + ws.lse_part);
     p.o_pre = reinterpret_cast<const float *>(wsp + ws.o_pre);
     p.lse_pre = reinterpret_cast<const float *>(wsp + ws.lse_pre);
+    p.o_suf = reinterpret_cast<const float *>(wsp + ws.o_suf);
+    p.lse_suf = reinterpret_cast<const float *>(wsp + ws.lse_suf);
     p.out = static_cast<__nv_bfloat16 *>(f.out);
     p.lse = f.lse;
-    const int64_t warps = int64_t(f.num_decodes) * f.num_heads;
+    const int64_t warps = int64_t(with_prefix ? f.num_tokens : f.num_decodes) * f.num_heads;
     const unsigned grid = static_cast<unsigned>((warps * 32 + 255) / 256);
     count_launch();
     if (f.head_size == 128)

@@ -69,8 +69,9 @@ uint32_t kv_write_take_error();
 // cascade merges them later) instead of finishing single-split sequences.
 cudaError_t launch_decode(const Fwd &f, const DecodePlan &dp, const Workspace &ws, char *wsp,
                           const CUtensorMap &kv_map, int32_t kv_begin, bool partial_only);
-// Merge the decode split partials (and, for a cascade, the prefix partial)
-// into out/lse for the decode tokens.
+// Merge the decode split partials into out/lse for the decode tokens; for a
+// cascade (with_prefix) also merge every token with its shared-prefix partial
+// (decode tokens: splits + prefix; prefill tokens: suffix partial + prefix).
 cudaError_t launch_decode_combine(const Fwd &f, const DecodePlan &dp, const Workspace &ws,
                                   char *wsp, int32_t kv_begin, bool with_prefix);
 uint32_t decode_take_error();
@@ -84,11 +85,23 @@ cudaError_t launch_cascade_merge(const void *out_a, const float *lse_a, const vo
 // Per-thread count of kernel launches (api.cu), bumped by every launcher.
 void count_launch();
 
-// prefill.cu: causal (or not) attention of the prefill sequences
-// [num_decodes, num_seqs) over keys [kv_lo, min(kv_cap, L_s)).  partial:
-// write fp32 partials (cascade) into ws.o_suf / ws.lse_suf instead of out/lse.
-cudaError_t launch_prefill(const Fwd &f, char *wsp, const Workspace &ws, int32_t kv_lo,
-                           int32_t kv_cap, int32_t causal, bool partial);
+// prefill.cu: one pass of the tensor-core kernel.
+//  shared_prefix = false: the prefill sequences [num_decodes, num_seqs), keys
+//    [kv_lo, min(kv_cap, L_s)), causal or not;
+//  shared_prefix = true: every token of the batch against keys [0, kv_cap) of
+//    the prefix all sequences share (block-table row 0), no mask.
+//  o_part == nullptr: write bf16 out / ln lse; else fp32 partials (normalised)
+//    and log2 lse at rows (t - token_base) * num_heads + h.
+struct PrefillPass {
+    int32_t kv_lo;
+    int32_t kv_cap;
+    int32_t causal;
+    bool shared_prefix;
+    float *o_part;
+    float *lse_part;
+    int32_t token_base;
+};
+cudaError_t launch_prefill(const Fwd &f, const PrefillPass &pass);
 uint32_t prefill_take_error();
 constexpr int kMaxPrefillSeqsPerCall = 4096;
 

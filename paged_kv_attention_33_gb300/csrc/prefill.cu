@@ -27,6 +27,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <numeric>
 
 #include "common.cuh"
 #include "internal.h"
@@ -54,7 +55,7 @@ struct PrefillParams {
     int32_t num_heads;
     int32_t group;
     int32_t block_size;
-    int32_t box_rows;  // rows per K/V TMA box: min(block_size, 128)
+    int32_t box_rows;  // rows per K/V TMA box: gcd(block_size, 128)
     int32_t num_blocks;
     int32_t kv_lo;     // first key attended
     int32_t kv_cap;    // keys >= kv_cap are not attended
@@ -62,6 +63,8 @@ struct PrefillParams {
     float scale_log2;
     int32_t partial;     // 0: bf16 out + ln lse; 1: fp32 partial + log2 lse
     int32_t token_base;  // partial rows are (t - token_base) * H + h
+    int32_t shared_prefix;  // 1: every token of the batch against keys [0, kv_cap) of
+                            //    block-table row 0 (the cascade's shared prefix)
     __nv_bfloat16 *out;
     float *lse;
     float *o_part;
@@ -92,6 +95,24 @@ struct PfItem {
 __device__ __forceinline__ bool pf_item(const PrefillParams &p, const int32_t *prefix, int nseq,
                                         int item, PfItem &it)
 {
+    if (p.shared_prefix) {
+        // one pseudo-sequence: all tokens of the batch, keys [0, kv_cap) of the
+        // prefix every sequence shares, no mask (the prefix precedes every query)
+        const int tiles = (p.num_tokens + kBM - 1) / kBM;
+        if (item >= tiles * p.num_heads)
+            return false;
+        it.h = item % p.num_heads;
+        const int qt = tiles - 1 - item / p.num_heads;
+        it.s = 0;
+        it.t0 = qt * kBM;
+        it.rows = min(kBM, p.num_tokens - it.t0);
+        it.qidx0 = 0;
+        it.L = p.kv_cap;
+        it.ctx = p.kv_cap;
+        it.kv_hi = p.kv_cap;
+        it.n_kv = (p.kv_cap + kBN - 1) / kBN;
+        return true;
+    }
     const int tiles = prefix[nseq];
     if (item >= tiles * p.num_heads)
         return false;
@@ -119,6 +140,11 @@ __device__ __forceinline__ bool pf_item(const PrefillParams &p, const int32_t *p
     kv_hi = min(kv_hi, p.kv_cap);
     it.kv_hi = kv_hi;
     it.n_kv = kv_hi > p.kv_lo ? (kv_hi - p.kv_lo + kBN - 1) / kBN : 0;
+    if (p.kv_lo > 0 && it.ctx < p.kv_lo) {
+        // a cascade suffix pass needs every query after the shared prefix
+        flag_error(kErrBadMetadata);
+        it.n_kv = 0;
+    }
     return true;
 }
 
@@ -169,7 +195,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int nseq = p.num_seqs - p.first_seq;
+    const int nseq = p.shared_prefix ? 0 : p.num_seqs - p.first_seq;
 
     // ---- prefix sums of 128-query tiles per prefill sequence (block-wide scan)
     {
@@ -564,11 +590,10 @@ static cudaError_t launch_prefill_d(const Fwd &f, const PrefillParams &p, int gr
     return cudaGetLastError();
 }
 
-cudaError_t launch_prefill(const Fwd &f, char *wsp, const Workspace &ws, int32_t kv_lo,
-                           int32_t kv_cap, int32_t causal, bool partial)
+cudaError_t launch_prefill(const Fwd &f, const PrefillPass &pass)
 {
     const int nseq = f.num_seqs - f.num_decodes;
-    if (nseq <= 0)
+    if (!pass.shared_prefix && nseq <= 0)
         return cudaSuccess;
     PrefillParams p;
     p.qsl = f.qsl;
@@ -581,22 +606,29 @@ cudaError_t launch_prefill(const Fwd &f, char *wsp, const Workspace &ws, int32_t
     p.num_heads = f.num_heads;
     p.group = f.num_heads / f.num_kv_heads;
     p.block_size = f.block_size;
-    p.box_rows = std::min(f.block_size, 128);
+    // boxes never straddle a block: key offsets are multiples of both
+    // block_size (prefix length) and 128 (tile), so use their gcd
+    p.box_rows = std::gcd(f.block_size, 128);
     p.num_blocks = static_cast<int32_t>(f.num_blocks);
-    p.kv_lo = kv_lo;
-    p.kv_cap = kv_cap;
-    p.causal = causal;
+    p.kv_lo = pass.kv_lo;
+    p.kv_cap = pass.kv_cap;
+    p.causal = pass.causal;
     p.scale_log2 = f.scale * 1.4426950408889634f;
-    p.partial = partial ? 1 : 0;
-    p.token_base = f.num_decodes;
+    p.partial = pass.o_part != nullptr ? 1 : 0;
+    p.token_base = pass.token_base;
+    p.shared_prefix = pass.shared_prefix ? 1 : 0;
     p.out = static_cast<__nv_bfloat16 *>(f.out);
     p.lse = f.lse;
-    p.o_part = reinterpret_cast<float *>(wsp + ws.o_suf);
-    p.lse_part = reinterpret_cast<float *>(wsp + ws.lse_suf);
-    // persistent grid: one CTA per SM, but no more CTAs than tiles
-    const int64_t tiles_upper =
-        (int64_t(f.num_tokens - f.num_decodes) + int64_t(nseq) * (kBM - 1)) / kBM * f.num_heads;
-    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(f.num_sms, tiles_upper)));
+    p.o_part = pass.o_part;
+    p.lse_part = pass.lse_part;
+    int64_t items;
+    if (pass.shared_prefix)
+        items = int64_t((f.num_tokens + kBM - 1) / kBM) * f.num_heads;
+    else
+        items = (int64_t(f.num_tokens - f.num_decodes) + int64_t(nseq) * (kBM - 1)) / kBM *
+                f.num_heads;
+    // persistent grid: one CTA per SM, but no more CTAs than work items
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(f.num_sms, items)));
     if (f.head_size == 128)
         return launch_prefill_d<128>(f, p, grid);
     return launch_prefill_d<64>(f, p, grid);

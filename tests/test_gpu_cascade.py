@@ -1,0 +1,65 @@
+"""GPU parity of the shared-prefix cascade: prefix attended once on the tensor
+cores, per-sequence suffixes by the decode / prefill kernels, merged by
+log-sum-exp; compared with the oracle's cascade and with plain attention."""
+import numpy as np
+import pytest
+
+from paged_kv_attention_33_gb300 import workloads as W
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+
+def test_cascade_small_decodes(oracle):
+    sp = W.BatchSpec("c1", 16, 2, 128, 16, decode_ctx=[64, 65, 100, 200, 64 + 15],
+                     common_prefix_len=64)
+    G.check_batch(oracle, W.make_batch(sp, seed=4001), label="cascade decodes")
+
+
+@pytest.mark.parametrize("bs,P", [(16, 128), (64, 256), (128, 128)])
+def test_cascade_with_prefill_chunks(oracle, bs, P):
+    sp = W.BatchSpec("c2", 32, 8, 128, bs, decode_ctx=[P, P + 7, P + 300],
+                     prefill=[(40, P), (130, P + 50), (1, P + 1)], common_prefix_len=P)
+    G.check_batch(oracle, W.make_batch(sp, seed=4100 + bs), label=f"cascade bs={bs}")
+
+
+def test_cascade_equals_plain(oracle):
+    """The same batch with and without the cascade gives the same rows (both
+    within tolerance of the oracle's plain attention)."""
+    sp = W.BatchSpec("c3", 64, 8, 128, 128, decode_ctx=[256 + k * 37 for k in range(12)],
+                     common_prefix_len=256)
+    b = W.make_batch(sp, seed=4200)
+    res_c = G.check_batch(oracle, b, label="cascade")
+    sp0 = W.BatchSpec("c3p", 64, 8, 128, 128, decode_ctx=sp.decode_ctx)
+    b0 = W.Batch(sp0, b.query, b.key, b.value, b.cache, b.slot_mapping, b.query_start_loc,
+                 b.seq_lens, b.block_table, b.num_blocks)
+    res_p = G.check_batch(oracle, b0, label="plain")
+    assert res_c["out_max_abs"] <= 2e-2 and res_p["out_max_abs"] <= 2e-2
+
+
+def test_cascade_named_full_size_sampled(oracle):
+    """256 decodes sharing a 4096-token prefix (bs 128, H 64, Hkv 8) at full
+    size, in the benchmark's launch configuration, on sampled rows."""
+    b = W.make_batch(W.named_spec("cascade"), seed=1005, device="cuda")
+    rows = W.sample_rows(b, 512, seed=6)
+    G.check_batch(oracle, b, rows=rows, label="cascade full", threads=16)
+
+
+def test_cascade_precondition_is_flagged():
+    """A prefill chunk whose queries start inside the shared prefix breaks the
+    cascade's premise; the kernel flags it instead of computing garbage."""
+    import torch
+
+    import paged_kv_attention_33_gb300 as pka
+
+    sp = W.BatchSpec("c4", 8, 2, 64, 16, decode_ctx=[40], prefill=[(20, 40)],
+                     common_prefix_len=32)
+    b = W.make_batch(sp, seed=4300)
+    meta = pka.Meta.from_host(b.query_start_loc, b.seq_lens, b.block_table, 1, "cuda",
+                              common_prefix_len=48)   # 48 > ctx of... decode ctx 40
+    q = G.to_dev(b.query, "cuda")
+    out = torch.empty_like(q)
+    pka.paged_attn_forward(q, G.to_dev(b.cache, "cuda"), meta, out, scale=sp.softmax_scale)
+    with pytest.raises(pka.PkaError) as e:
+        pka.check_status()
+    assert e.value.status == -5
