@@ -168,6 +168,35 @@ pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const
                                   void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * pka_paged_attn_forward for callers that cannot allocate device memory.
+ * The pages have no counterpart of this entry point.
+ *
+ * Some callers cannot provide a workspace: an engine that reserved almost
+ * all of HBM for its KV pool at start-up, a plugin host that only passes
+ * input and output pointers, or a serving loop that must not call cudaMalloc
+ * because it can synchronise the device.  This entry point takes the same
+ * arguments as pka_paged_attn_forward minus the workspace; its scratch (the
+ * fp32 split-KV and cascade partials) is a 16 MiB buffer built into the
+ * library's device image, which every GPU that loads the library holds until
+ * the process exits.  It allocates and frees nothing.
+ *
+ *  - A batch whose pka_workspace_size is above 16 MiB is rejected with
+ *    PKA_ERR_WORKSPACE (and a message naming both sizes); nothing is enqueued.
+ *  - The first call on a device looks up the buffer's device address once
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - Every call shares the one buffer and leaves its contents behind (each
+ *    call writes all of what it later reads).  Calls that overlap on the GPU
+ *    (other streams, other host threads) race on it: serialise them.
+ */
+pka_status pka_paged_attn_forward_noalloc(const void *query, const void *kv_cache,
+                                          const pka_meta *meta, void *out, float *lse,
+                                          int32_t num_tokens, int32_t num_heads,
+                                          int32_t num_kv_heads, int32_t head_size,
+                                          int32_t block_size, int64_t num_blocks, float scale,
+                                          int32_t causal, void *stream);
+
+/*
  * Log-sum-exp merge of two partial attentions of the same queries over
  * disjoint key sets ([blog] "Que aporta FlashInfer: JIT y cascade attention":
  * the prefix result is combined with each request's suffix; [FA/FI] "Limites

@@ -23,7 +23,7 @@ import threading
 from . import build as _build
 
 __all__ = ["Meta", "PkaError", "reshape_and_cache", "paged_attn_forward", "cascade_merge",
-           "workspace_size", "check_status", "set_kernel_events", "kernel_launches",
+           "paged_attn_forward_noalloc", "workspace_size", "check_status", "set_kernel_events", "kernel_launches",
            "load_library",
            "library_path", "KERNEL_DECODE", "KERNEL_PREFILL"]
 
@@ -75,6 +75,10 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
                                                _I32, _I32, _I32, _I32, _I64, ctypes.c_float,
                                                _I32, _P, ctypes.c_size_t, _P]
         lib.pka_paged_attn_forward.restype = ctypes.c_int
+        lib.pka_paged_attn_forward_noalloc.argtypes = [_P, _P, ctypes.POINTER(_CMeta), _P, _P,
+                                                       _I32, _I32, _I32, _I32, _I32, _I64,
+                                                       ctypes.c_float, _I32, _P]
+        lib.pka_paged_attn_forward_noalloc.restype = ctypes.c_int
         lib.pka_cascade_merge.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P]
         lib.pka_cascade_merge.restype = ctypes.c_int
         lib.pka_set_kernel_events.argtypes = [_I32, _P, _P]
@@ -185,6 +189,23 @@ def paged_attn_forward(query, kv_cache, meta: Meta, out, lse=None, scale=None, c
                                       _ptr(lse), T, H, hkv, D, bs, nb, float(scale),
                                       1 if causal else 0, _ptr(workspace), ws_bytes,
                                       _stream(stream)))
+
+
+def paged_attn_forward_noalloc(query, kv_cache, meta: Meta, out, lse=None, scale=None,
+                               causal=True, stream=None) -> None:
+    """paged_attn_forward without a workspace: for callers that cannot allocate
+    device memory, the library's built-in 16 MiB scratch holds the partial
+    results.  Batches that need more raise PkaError (PKA_ERR_WORKSPACE).
+    Calls that overlap on the GPU share that scratch and must be serialised."""
+    lib = load_library()
+    T, H, D = query.shape
+    nb, _, bs, hkv, _ = kv_cache.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    cm = meta._c()
+    _check(lib.pka_paged_attn_forward_noalloc(_ptr(query), _ptr(kv_cache), ctypes.byref(cm),
+                                              _ptr(out), _ptr(lse), T, H, hkv, D, bs, nb,
+                                              float(scale), 1 if causal else 0, _stream(stream)))
 
 
 def cascade_merge(out_a, lse_a, out_b, lse_b, out, lse_out=None, stream=None) -> None:

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpka.so")
 
-SOURCES = ["api.cu", "kv_write.cu", "decode.cu", "merge.cu", "prefill.cu"]
+SOURCES = ["api.cu", "kv_write.cu", "decode.cu", "merge.cu", "prefill.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -50,6 +50,14 @@ static pka_status fail(pka_status st, const char *fmt, ...)
     return st;
 }
 
+void set_last_error(const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+    va_end(ap);
+}
+
 static pka_status cuda_fail(cudaError_t e, const char *what)
 {
     return fail(PKA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));

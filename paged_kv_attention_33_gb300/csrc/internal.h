@@ -82,6 +82,9 @@ cudaError_t launch_cascade_merge(const void *out_a, const float *lse_a, const vo
                                  int32_t num_tokens, int32_t num_heads, int32_t head_size,
                                  cudaStream_t st);
 
+// Set the thread-local message pka_last_error() returns (api.cu).
+void set_last_error(const char *fmt, ...);
+
 // Per-thread count of kernel launches (api.cu), bumped by every launcher.
 void count_launch();
 

@@ -1,0 +1,85 @@
+"""The allocation-free forward entry point (pka_paged_attn_forward_noalloc).
+
+It serves callers that cannot allocate device memory -- an engine that gave
+nearly all of HBM to its KV pool, a plugin host that only passes input and
+output pointers, a loop that must not call cudaMalloc -- by keeping the
+partial results in a scratch buffer built into the library.  Here its output
+is checked against the regular entry point (which takes a workspace) on the
+same inputs, for two calls in a row, so the second call also runs over the
+first call's leftovers.  This file is collected last on purpose.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import paged_kv_attention_33_gb300 as pka
+from paged_kv_attention_33_gb300 import workloads as W
+from tests import gpu_util as G
+
+
+def _run_both(spec, seed, split):
+    import torch
+
+    dev = "cuda"
+    b = W.make_batch(spec, seed=seed)
+    cache = G.to_dev(b.cache, dev)
+    pka.reshape_and_cache(G.to_dev(b.key, dev), G.to_dev(b.value, dev), cache,
+                          torch.from_numpy(b.slot_mapping).to(dev))
+    meta = pka.Meta.from_host(b.query_start_loc, b.seq_lens, b.block_table, spec.num_decodes,
+                              dev, common_prefix_len=spec.common_prefix_len,
+                              split_kv_tokens=split)
+    need = pka.workspace_size(meta, b.num_tokens, spec.num_heads, spec.num_kv_heads,
+                              spec.head_size, spec.block_size)
+    assert 0 < need <= 16 << 20
+    q = G.to_dev(b.query, dev)
+    T, H = q.shape[:2]
+    ref = torch.empty_like(q)
+    ref_lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    pka.paged_attn_forward(q, cache, meta, ref, ref_lse, scale=spec.softmax_scale)
+    results = []
+    for _ in range(2):
+        out = torch.full_like(q, float("nan"))
+        lse = torch.full((T, H), float("nan"), dtype=torch.float32, device=dev)
+        pka.paged_attn_forward_noalloc(q, cache, meta, out, lse, scale=spec.softmax_scale)
+        results.append((out, lse))
+    pka.check_status()
+    return ref, ref_lse, results
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", ["decode_splits", "cascade_mixed"])
+def test_noalloc_matches_workspace_entry_point(case):
+    if case == "decode_splits":
+        rng = np.random.Generator(np.random.PCG64(11))
+        spec = W.BatchSpec("na1", 32, 8, 128, 16,
+                           decode_ctx=rng.integers(1, 3000, size=24).tolist())
+        split = 256
+    else:
+        spec = W.BatchSpec("na2", 32, 8, 128, 64, decode_ctx=[128, 300, 1000],
+                           prefill=[(100, 128), (70, 200)], common_prefix_len=128)
+        split = 64
+    ref, ref_lse, results = _run_both(spec, seed=5001, split=split)
+    r = W.bf16_bits_to_f32(W.to_host_bits(ref)).astype(np.float64)
+    rl = ref_lse.cpu().numpy().astype(np.float64)
+    for k, (out, lse) in enumerate(results):
+        o = W.bf16_bits_to_f32(W.to_host_bits(out)).astype(np.float64)
+        lo = lse.cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(o)) and np.all(np.isfinite(lo)), f"call {k}"
+        err = np.abs(o - r)
+        assert err.max() <= G.OUT_MAX_ABS and err.mean() <= G.OUT_MEAN_ABS, f"call {k}"
+        assert np.abs(lo - rl).max() <= G.LSE_ABS, f"call {k}"
+
+
+def test_noalloc_rejects_batches_above_its_scratch():
+    """A batch whose partials need more than the built-in 16 MiB is refused
+    with PKA_ERR_WORKSPACE before anything is enqueued."""
+    lib = pka.load_library()
+    m = pka._CMeta(16, 16, 16, 1024, 256, 256, 1, 16384, 0, 16)
+    need = lib.pka_workspace_size(ctypes.byref(m), 256, 32, 8, 128, 16)
+    assert need > 16 << 20
+    rc = lib.pka_paged_attn_forward_noalloc(256, 512, ctypes.byref(m), 1024, None, 256, 32, 8,
+                                            128, 16, 100000, 0.088, 1, None)
+    assert rc == -3
+    msg = lib.pka_last_error().decode()
+    assert "16777216" in msg and str(need) in msg
