@@ -261,55 +261,75 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
     if (warp == 0) {
         // ================================================================ producer
+        // Lane b owns TMA box b of every K/V tile (one page-sized box per lane),
+        // so the block-table lookups of a tile are one parallel load, issued for
+        // the next tile before waiting for a free stage.
         if (lane == 0) {
             tma_prefetch_desc(&q_map);
             tma_prefetch_desc(&kv_map);
-            const uint64_t pol_kv = l2_policy_evict_last();
-            const uint64_t pol_q = l2_policy_evict_first();
-            uint32_t li = 0, kv_it = 0;
-            PfItem it;
-            for (int item = blockIdx.x; pf_item(p, prefix, nseq, item, it); item += gridDim.x) {
-                if (it.n_kv == 0)
-                    continue;
-                if (li > 0 && !pf_wait(q_empty, (li - 1) & 1, abort_flag))
-                    goto producer_done;
+        }
+        const uint64_t pol_kv = l2_policy_evict_last();
+        const uint64_t pol_q = l2_policy_evict_first();
+        uint32_t li = 0, kv_it = 0;
+        PfItem it;
+        for (int item = blockIdx.x; pf_item(p, prefix, nseq, item, it); item += gridDim.x) {
+            if (it.n_kv == 0)
+                continue;
+            const int kvh = it.h / p.group;
+            const int32_t *bt = p.block_table + int64_t(it.s) * p.bt_stride;
+            auto lane_block = [&](int jt) -> int {
+                const int key0 = p.kv_lo + jt * kBN;
+                const int nbox = (min(kBN, it.kv_hi - key0) + p.box_rows - 1) / p.box_rows;
+                if (lane >= nbox)
+                    return -1;
+                const int col = (key0 + lane * p.box_rows) / p.block_size;
+                int blk = col < p.bt_stride ? bt[col] : -1;
+                if (blk < 0 || blk >= p.num_blocks) {
+                    flag_error(kErrBlockOutOfPool);
+                    blk = 0;  // keep the byte count whole; the result is flagged
+                }
+                return blk;
+            };
+            int blk_next = lane_block(0);
+            if (li > 0 && !pf_wait(q_empty, (li - 1) & 1, abort_flag))
+                goto producer_done;
+            if (lane == 0) {
                 mbar_arrive_expect_tx(q_full, Cfg::kTileBytes);
                 for (int hf = 0; hf < Cfg::kHalves; ++hf)
-                    tma_load_3d(smem + Cfg::kQOff + hf * Cfg::kHalfBytes, &q_map, q_full, hf * 64,
-                                it.h, it.t0, pol_q);
-                const int kvh = it.h / p.group;
-                const int32_t *bt = p.block_table + int64_t(it.s) * p.bt_stride;
-                for (int jt = 0; jt < it.n_kv; ++jt, ++kv_it) {
-                    const int st = kv_it % kPfStages;
-                    const uint32_t rnd = kv_it / kPfStages;
-                    if (rnd > 0 && !pf_wait(&kv_empty[st], (rnd - 1) & 1, abort_flag))
-                        goto producer_done;
-                    const int key0 = p.kv_lo + jt * kBN;
-                    const int nvalid = min(kBN, it.kv_hi - key0);
-                    const int nbox = (nvalid + p.box_rows - 1) / p.box_rows;
-                    const uint32_t bytes = nbox * p.box_rows * 128 * Cfg::kHalves;
-                    for (int kv = 0; kv < 2; ++kv) {
-                        uint64_t *bar = kv == 0 ? &k_full[st] : &v_full[st];
-                        uint8_t *tile = smem + (kv == 0 ? Cfg::kKOff : Cfg::kVOff) +
-                                        st * Cfg::kTileBytes;
-                        mbar_arrive_expect_tx(bar, bytes);
-                        for (int bx = 0; bx < nbox; ++bx) {
-                            const int key = key0 + bx * p.box_rows;
-                            const int col = key / p.block_size;
-                            int blk = col < p.bt_stride ? bt[col] : -1;
-                            if (blk < 0 || blk >= p.num_blocks) {
-                                flag_error(kErrBlockOutOfPool);
-                                blk = 0;
-                            }
-                            const int row = (blk * 2 + kv) * p.block_size + key % p.block_size;
-                            for (int hf = 0; hf < Cfg::kHalves; ++hf)
-                                tma_load_3d(tile + hf * Cfg::kHalfBytes + bx * p.box_rows * 128,
-                                            &kv_map, bar, hf * 64, kvh, row, pol_kv);
-                        }
-                    }
-                }
-                ++li;
+                    tma_load_3d(smem + Cfg::kQOff + hf * Cfg::kHalfBytes, &q_map, q_full,
+                                hf * 64, it.h, it.t0, pol_q);
             }
+            for (int jt = 0; jt < it.n_kv; ++jt, ++kv_it) {
+                const int blk = blk_next;
+                if (jt + 1 < it.n_kv)
+                    blk_next = lane_block(jt + 1);
+                const int st = kv_it % kPfStages;
+                const uint32_t rnd = kv_it / kPfStages;
+                if (rnd > 0 && !pf_wait(&kv_empty[st], (rnd - 1) & 1, abort_flag))
+                    goto producer_done;
+                const int key0 = p.kv_lo + jt * kBN;
+                const int nbox = (min(kBN, it.kv_hi - key0) + p.box_rows - 1) / p.box_rows;
+                const uint32_t bytes = nbox * p.box_rows * 128 * Cfg::kHalves;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&k_full[st], bytes);
+                    mbar_arrive_expect_tx(&v_full[st], bytes);
+                }
+                __syncwarp();
+                if (lane < nbox) {
+                    const int key = key0 + lane * p.box_rows;
+                    const int row_k = (blk * 2) * p.block_size + key % p.block_size;
+                    const int row_v = row_k + p.block_size;
+                    uint8_t *kt = smem + Cfg::kKOff + st * Cfg::kTileBytes + lane * p.box_rows * 128;
+                    uint8_t *vt = smem + Cfg::kVOff + st * Cfg::kTileBytes + lane * p.box_rows * 128;
+                    for (int hf = 0; hf < Cfg::kHalves; ++hf)
+                        tma_load_3d(kt + hf * Cfg::kHalfBytes, &kv_map, &k_full[st], hf * 64,
+                                    kvh, row_k, pol_kv);
+                    for (int hf = 0; hf < Cfg::kHalves; ++hf)
+                        tma_load_3d(vt + hf * Cfg::kHalfBytes, &kv_map, &v_full[st], hf * 64,
+                                    kvh, row_v, pol_kv);
+                }
+            }
+            ++li;
         }
     producer_done:;
     } else if (warp == 1) {
@@ -428,51 +448,56 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     goto softmax_done;
                 tc_fence_after();
                 const uint32_t ts = tS + sb * 128 + lane_off;
-                float x[kBN];
-                {
-                    uint32_t raw[32];
+                uint32_t x[4][32];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        tmem_ld32(ts + c * 32, raw);
-                        tmem_wait_ld();
+                for (int c = 0; c < 4; ++c)
+                    tmem_ld32(ts + c * 32, x[c]);
+                tmem_wait_ld();
+                const int lim = hi_row - (p.kv_lo + jt * kBN);  // columns c < lim admitted
+                // scaled, masked logits (base 2) and their row max in four chains
+                float mx4[4] = {kPfNegInf, kPfNegInf, kPfNegInf, kPfNegInf};
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            x[c * 32 + i] = __uint_as_float(raw[i]);
+                for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float v =
+                            c * 32 + i < lim ? __uint_as_float(x[c][i]) * p.scale_log2 : kPfNegInf;
+                        x[c][i] = __float_as_uint(v);
+                        mx4[i & 3] = fmaxf(mx4[i & 3], v);
                     }
                 }
-                const int key0 = p.kv_lo + jt * kBN;
-                const int lim = hi_row - key0;  // columns c < lim are admitted
-                float mx = kPfNegInf;
-#pragma unroll
-                for (int c = 0; c < kBN; ++c) {
-                    x[c] = c < lim ? x[c] * p.scale_log2 : kPfNegInf;
-                    mx = fmaxf(mx, x[c]);
-                }
-                const float m_new = fmaxf(m, mx);
+                const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+                // The reference max m moves only when the row max passes it by more
+                // than 8 (a factor 256): every p stays <= 256 and the O rescale in
+                // TMEM is rarely needed.  The result is exact either way, since lse
+                // and the final 1/l use the same reference.
+                const float m_new = mx > m + 8.f ? mx : m;
                 const float base = m_new == kPfNegInf ? 0.f : m_new;
-                float sum = 0.f;
+                float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float p0 = fast_exp2(x[c * 32 + 2 * i] - base);
-                        const float p1 = fast_exp2(x[c * 32 + 2 * i + 1] - base);
-                        sum += p0 + p1;
+                        const float p0 = fast_exp2(__uint_as_float(x[c][2 * i]) - base);
+                        const float p1 = fast_exp2(__uint_as_float(x[c][2 * i + 1]) - base);
+                        sum4[(2 * i) & 3] += p0;
+                        sum4[(2 * i + 1) & 3] += p1;
                         pk[i] = pack_bf16x2(p0, p1);
                     }
                     tmem_st16(ts + c * 16, pk);
                 }
                 tmem_wait_st();
-                const float alpha = fast_exp2(m - base);
-                l = l * alpha + sum;
+                const float alpha = fast_exp2(m - base);  // 1 when m did not move
+                l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+                const bool moved = m_new != m;
                 m = m_new;
                 if (jt > 0) {
                     if (!pf_wait(o_done, pv_n & 1, abort_flag))
                         goto softmax_done;
                     ++pv_n;
                     tc_fence_after();
-                    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                    if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
                         for (int c = 0; c < D / 32; ++c) {
                             uint32_t o[32];
