@@ -53,6 +53,19 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(values, device):
+    """Element-wise max of a list of floats over all ranks (identity at N=1).
+    Each replica times its own work; the job's time is the slowest rank's."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
 # --------------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi samples of SM clock, power and throttle reasons."""
@@ -332,12 +345,7 @@ def run_ours(args):
         torch.cuda.synchronize()
     sampler.stop()
     pka.check_status()
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([ms, k_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, k_ms = float(t[0]), float(t[1])
+    ms, k_ms = max_over_ranks([ms, k_ms], dev)
     value = world * kv_bytes / (ms * 1e-3) / 1e9
 
     # end to end through the public API with host buffers
@@ -377,13 +385,7 @@ def run_ours(args):
     f1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    e2e_ms = f0.elapsed_time(f1) / args.steps
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t[0])
+    e2e_ms = max_over_ranks([f0.elapsed_time(f1) / args.steps], dev)[0]
     pka.check_status()
 
     # roofline of the dominant kernel (the split-KV decode kernel)

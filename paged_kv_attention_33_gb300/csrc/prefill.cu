@@ -8,22 +8,29 @@
 // admits keys j <= c_s + i (bottom-right causal alignment), keys read through
 // the block table (the blog's "Como lee el backend el KV paginado").
 //
-// Work item: (sequence s, 128-query tile, query head h), in a persistent grid
-// (one CTA per SM, items taken round-robin, the heaviest causal tiles of each
-// sequence first).  Roles inside the CTA (256 threads):
-//   warp 0      TMA producer: the Q tile once per item, then K and V tiles of
-//               128 keys into a two-stage ring, one TMA box per page (paged
-//               gather straight from the pool, 128-byte swizzled);
-//   warp 1      MMA issuer (one thread): S = Q K^T into one of two TMEM
-//               buffers (M=128, N=128, K=head_size), then O += P V with P read
-//               from TMEM (M=128, N=head_size, K=128 keys);
+// Work item: (sequence s, 256-query super-tile, query head h) = two 128-row
+// tiles A and B that share every K/V tile, in a persistent grid (one CTA per
+// SM, items round-robin, the heaviest causal tiles of each sequence first).
+// Roles (384 threads, three warpgroups):
+//   warp 0      TMA producer: Q tiles once per item, K and V tiles of 128 keys
+//               into a two-stage ring, one TMA box per page straight from the
+//               pool (128-byte swizzled), block ids looked up one per lane;
+//   warp 1      MMA issuer (one thread).  Per K/V tile j it issues
+//                 PV_A(j-1), S_A(j), PV_B(j-1), S_B(j)
+//               so that while one softmax warpgroup works on its S tile the
+//               tensor core runs the other tile's MMAs;
+//               S = Q K^T: M=128, N=128, K=head_size, both operands in smem;
+//               O += P V: M=128, N=head_size, K=128 keys, P read from TMEM;
 //   warp 2      TMEM allocator;
-//   warps 4-7   softmax: thread r owns query row r; it reads its S row from
-//               TMEM, applies the mask and the online softmax (base-2, scale
-//               folded in), writes P back over S as bf16, rescales its O row
-//               in TMEM when its running max moved, and at the end writes
-//               out = O / l and lse.
-// TMEM columns: S buffers [0,128) and [128,256), O [256, 256+head_size).
+//   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: thread r owns
+//               query row r; it reads its S row from TMEM, masks (only on
+//               tiles that need it), runs the base-2 online softmax with the
+//               scale folded into one FFMA per element, writes P back over S
+//               as bf16, rescales its O row in TMEM when its reference max
+//               moved by more than 8, and at the end writes out = O / l and lse.
+// Registers: the producer warpgroup gives registers back (setmaxnreg) to the
+// two softmax warpgroups: 128 x 88 + 256 x 208 = 64512 = 384 x 168 at launch.
+// TMEM columns: S_A [0,128), S_B [128,256), O_A [256, 256+D), O_B [256+D, 256+2D).
 #include <math.h>
 
 #include <algorithm>
@@ -37,12 +44,14 @@ namespace pka {
 
 constexpr int kBM = 128;             // query rows per tile
 constexpr int kBN = 128;             // keys per tile
-constexpr int kPfThreads = 256;
+constexpr int kSuper = 2 * kBM;      // query rows per work item (tiles A and B)
+constexpr int kPfThreads = 384;
 constexpr int kPfStages = 2;
 constexpr int kMaxPrefillSeqs = 4096;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kPfNegInf = -INFINITY;
 constexpr float kPfLn2 = 0.69314718055994530942f;
+constexpr float kRescaleThreshold = 8.f;  // log2 units: p stays <= 256
 
 struct PrefillParams {
     const int32_t *qsl;
@@ -74,76 +83,99 @@ struct PrefillParams {
 template <int D>
 struct PfCfg {
     static constexpr int kHalves = D / 64;
-    static constexpr int kHalfBytes = 128 * 128;        // 128 rows x 128 B
-    static constexpr int kTileBytes = kHalves * kHalfBytes;  // Q, K or V tile
-    static constexpr int kQOff = 0;
-    static constexpr int kKOff = kTileBytes;
+    static constexpr int kHalfBytes = 128 * 128;             // 128 rows x 128 B
+    static constexpr int kTileBytes = kHalves * kHalfBytes;  // one Q, K or V tile
+    static constexpr int kQOff = 0;                          // Q_A, then Q_B
+    static constexpr int kKOff = 2 * kTileBytes;
     static constexpr int kVOff = kKOff + kPfStages * kTileBytes;
     static constexpr int kBarOff = kVOff + kPfStages * kTileBytes;
-    static constexpr int kNumBars = 16;
-    static constexpr int kMiscOff = kBarOff + kNumBars * 8;   // tmem base, abort flag
+    static constexpr int kNumBars = 24;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
     static constexpr int kPrefixOff = kMiscOff + 16;
     static constexpr size_t kSmemBytes = kPrefixOff + (kMaxPrefillSeqs + 1) * 4 + 1024;
     static constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, 0, 0);
     static constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, 0, 1);
+    static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
+// One work item: two query tiles (A = rows [0,128), B = rows [128,256) of the
+// super-tile) of one head against the K/V tiles of one sequence.
 struct PfItem {
-    int s, h, t0, rows, qidx0, ctx, L, kv_hi, n_kv;
+    int s, h, t0, ctx, L, qidx0;
+    int rows[2];   // valid query rows of tile A / B (0: tile absent)
+    int n_kv[2];   // K/V tiles tile A / B attends
+    int n_kv_all;  // K/V tiles the item loads (max of the two)
+    int kv_hi;     // keys [kv_lo, kv_hi) are loaded
 };
+
+__device__ __forceinline__ int pf_tiles_of(int kv_lo, int hi)
+{
+    return hi > kv_lo ? (hi - kv_lo + kBN - 1) / kBN : 0;
+}
 
 __device__ __forceinline__ bool pf_item(const PrefillParams &p, const int32_t *prefix, int nseq,
                                         int item, PfItem &it)
 {
+    int qlen;
     if (p.shared_prefix) {
         // one pseudo-sequence: all tokens of the batch, keys [0, kv_cap) of the
         // prefix every sequence shares, no mask (the prefix precedes every query)
-        const int tiles = (p.num_tokens + kBM - 1) / kBM;
+        const int tiles = (p.num_tokens + kSuper - 1) / kSuper;
         if (item >= tiles * p.num_heads)
             return false;
         it.h = item % p.num_heads;
-        const int qt = tiles - 1 - item / p.num_heads;
+        const int st_idx = tiles - 1 - item / p.num_heads;
         it.s = 0;
-        it.t0 = qt * kBM;
-        it.rows = min(kBM, p.num_tokens - it.t0);
-        it.qidx0 = 0;
+        qlen = p.num_tokens;
+        it.t0 = st_idx * kSuper;
+        it.qidx0 = it.t0;
         it.L = p.kv_cap;
         it.ctx = p.kv_cap;
-        it.kv_hi = p.kv_cap;
-        it.n_kv = (p.kv_cap + kBN - 1) / kBN;
-        return true;
+    } else {
+        const int tiles = prefix[nseq];
+        if (item >= tiles * p.num_heads)
+            return false;
+        it.h = item % p.num_heads;
+        const int r = item / p.num_heads;
+        int lo = 0, hi = nseq;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (prefix[mid] <= r)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        it.s = p.first_seq + lo;
+        const int ntile = prefix[lo + 1] - prefix[lo];
+        const int st_idx = ntile - 1 - (r - prefix[lo]);  // heaviest super-tile first
+        const int q0 = p.qsl[it.s];
+        qlen = p.qsl[it.s + 1] - q0;
+        it.L = p.seq_lens[it.s];
+        it.ctx = it.L - qlen;
+        it.qidx0 = st_idx * kSuper;
+        it.t0 = q0 + it.qidx0;
     }
-    const int tiles = prefix[nseq];
-    if (item >= tiles * p.num_heads)
-        return false;
-    it.h = item % p.num_heads;
-    const int r = item / p.num_heads;
-    int lo = 0, hi = nseq;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (prefix[mid] <= r)
-            lo = mid;
-        else
-            hi = mid;
+    it.rows[0] = max(0, min(kBM, qlen - it.qidx0));
+    it.rows[1] = max(0, min(kBM, qlen - it.qidx0 - kBM));
+    int all_hi = 0;
+    for (int tl = 0; tl < 2; ++tl) {
+        int hi = 0;
+        if (it.rows[tl] > 0) {
+            if (p.shared_prefix || !p.causal)
+                hi = it.L;
+            else
+                hi = min(it.L, it.ctx + it.qidx0 + tl * kBM + it.rows[tl]);
+            hi = min(hi, p.kv_cap);
+        }
+        it.n_kv[tl] = it.rows[tl] > 0 ? pf_tiles_of(p.kv_lo, hi) : 0;
+        all_hi = max(all_hi, hi);
     }
-    it.s = p.first_seq + lo;
-    const int ntile = prefix[lo + 1] - prefix[lo];
-    const int qt = ntile - 1 - (r - prefix[lo]);  // heaviest tile of the sequence first
-    const int q0 = p.qsl[it.s];
-    const int qlen = p.qsl[it.s + 1] - q0;
-    it.L = p.seq_lens[it.s];
-    it.ctx = it.L - qlen;
-    it.qidx0 = qt * kBM;
-    it.t0 = q0 + it.qidx0;
-    it.rows = min(kBM, qlen - it.qidx0);
-    int kv_hi = p.causal ? min(it.L, it.ctx + it.qidx0 + it.rows) : it.L;
-    kv_hi = min(kv_hi, p.kv_cap);
-    it.kv_hi = kv_hi;
-    it.n_kv = kv_hi > p.kv_lo ? (kv_hi - p.kv_lo + kBN - 1) / kBN : 0;
-    if (p.kv_lo > 0 && it.ctx < p.kv_lo) {
+    it.kv_hi = all_hi;
+    it.n_kv_all = max(it.n_kv[0], it.n_kv[1]);
+    if (!p.shared_prefix && p.kv_lo > 0 && it.ctx < p.kv_lo) {
         // a cascade suffix pass needs every query after the shared prefix
         flag_error(kErrBadMetadata);
-        it.n_kv = 0;
+        it.n_kv[0] = it.n_kv[1] = it.n_kv_all = 0;
     }
     return true;
 }
@@ -169,6 +201,198 @@ __device__ __forceinline__ bool pf_wait(uint64_t *bar, uint32_t parity, volatile
     return false;
 }
 
+template <uint32_t N>
+__device__ __forceinline__ void reg_dealloc()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <uint32_t N>
+__device__ __forceinline__ void reg_alloc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+struct PfBars {
+    uint64_t *q_full, *q_empty, *k_full, *v_full, *kv_empty;
+    uint64_t *s_full, *p_full, *o_done, *o_free;  // [2] each: tile A, tile B
+    uint64_t *drain;
+};
+
+// ---------------------------------------------------------------- softmax role
+template <int D>
+__device__ __forceinline__ void pf_softmax(const PrefillParams &p, const int32_t *prefix,
+                                           int nseq, const PfBars &bars, int tl, uint32_t tS,
+                                           uint32_t tO, volatile int *abort_flag)
+{
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int wq = warp & 3;  // TMEM lane quarter of this warp
+    const int r = wq * 32 + lane;
+    const uint32_t lane_off = uint32_t(wq * 32) << 16;
+    const uint32_t ts = tS + lane_off;
+    uint32_t s_n = 0, pv_n = 0;
+    PfItem it;
+    for (int item = blockIdx.x; pf_item(p, prefix, nseq, item, it); item += gridDim.x) {
+        const int rows = it.rows[tl];
+        const int nkv = it.n_kv[tl];
+        const bool valid = r < rows;
+        const int t = it.t0 + tl * kBM + r;
+        if (rows == 0)
+            continue;
+        if (nkv == 0) {
+            // no admitted key at all: an empty part (cascade partial mode only)
+            if (valid && p.partial) {
+                const int64_t row = int64_t(t - p.token_base) * p.num_heads + it.h;
+                for (int d = 0; d < D; ++d)
+                    p.o_part[row * D + d] = 0.f;
+                p.lse_part[row] = kPfNegInf;
+            }
+            continue;
+        }
+        int hi_row;
+        if (p.shared_prefix || !p.causal)
+            hi_row = it.L;
+        else
+            hi_row = min(it.L, it.ctx + it.qidx0 + tl * kBM + r + 1);
+        hi_row = min(hi_row, p.kv_cap);
+        float m = kPfNegInf, l = 0.f;
+        for (int jt = 0; jt < nkv; ++jt, ++s_n) {
+            if (!pf_wait(&bars.s_full[tl], s_n & 1, abort_flag))
+                return;
+            tc_fence_after();
+            uint32_t x[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                tmem_ld32(ts + c * 32, x[c]);
+            tmem_wait_ld();
+            const int lim = hi_row - (p.kv_lo + jt * kBN);  // columns c < lim admitted
+            const bool full_tile = __all_sync(0xffffffffu, lim >= kBN);
+            // row max of the raw logits (four chains); the scale is positive so
+            // max and scaling commute
+            float mx4[4] = {kPfNegInf, kPfNegInf, kPfNegInf, kPfNegInf};
+            if (full_tile) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(x[c][i]));
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float v = c * 32 + i < lim ? __uint_as_float(x[c][i]) : kPfNegInf;
+                        x[c][i] = __float_as_uint(v);
+                        mx4[i & 3] = fmaxf(mx4[i & 3], v);
+                    }
+            }
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
+            // The reference max m moves only when the row max passes it by more
+            // than the threshold: every p stays <= 2^8 and the O rescale in TMEM
+            // is rare.  Exact either way: lse and 1/l use the same reference.
+            const float m_new = mx > m + kRescaleThreshold ? mx : m;
+            const float base = m_new == kPfNegInf ? 0.f : m_new;
+            float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float p0 =
+                        fast_exp2(fmaf(__uint_as_float(x[c][2 * i]), p.scale_log2, -base));
+                    const float p1 =
+                        fast_exp2(fmaf(__uint_as_float(x[c][2 * i + 1]), p.scale_log2, -base));
+                    sum4[(2 * i) & 3] += p0;
+                    sum4[(2 * i + 1) & 3] += p1;
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+                tmem_st16(ts + c * 16, pk);
+            }
+            tmem_wait_st();
+            const float alpha = fast_exp2(m - base);  // exactly 1 when m did not move
+            l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+            const bool moved = m_new != m;
+            m = m_new;
+            if (jt > 0) {
+                // O holds PV of the previous tiles: wait for the last one, then
+                // rescale the rows whose reference moved
+                if (!pf_wait(&bars.o_done[tl], pv_n & 1, abort_flag))
+                    return;
+                ++pv_n;
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, moved)) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + lane_off + c * 32, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(tO + lane_off + c * 32, o);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars.p_full[tl]);
+        }
+        // ---- epilogue: out = O / l, lse
+        if (!pf_wait(&bars.o_done[tl], pv_n & 1, abort_flag))
+            return;
+        ++pv_n;
+        tc_fence_after();
+        {
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float lse2 = m + log2f(l);
+            const int64_t orow = int64_t(t) * p.num_heads + it.h;
+            const int64_t prow = int64_t(t - p.token_base) * p.num_heads + it.h;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tO + lane_off + c * 32, o);
+                tmem_wait_ld();
+                if (valid) {
+                    if (p.partial) {
+                        float4 *dst = reinterpret_cast<float4 *>(p.o_part + prow * D + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv,
+                                                 __uint_as_float(o[4 * i + 1]) * inv,
+                                                 __uint_as_float(o[4 * i + 2]) * inv,
+                                                 __uint_as_float(o[4 * i + 3]) * inv);
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * i]) * inv,
+                                                            __uint_as_float(o[8 * i + 1]) * inv),
+                                                pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv,
+                                                            __uint_as_float(o[8 * i + 3]) * inv),
+                                                pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv,
+                                                            __uint_as_float(o[8 * i + 5]) * inv),
+                                                pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv,
+                                                            __uint_as_float(o[8 * i + 7]) * inv));
+                    }
+                }
+            }
+            if (valid) {
+                if (p.partial)
+                    p.lse_part[prow] = lse2;
+                else if (p.lse)
+                    p.lse[orow] = lse2 * kPfLn2;
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&bars.o_free[tl]);
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
@@ -178,17 +402,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kBarOff);
-    uint64_t *q_full = bars + 0;
-    uint64_t *q_empty = bars + 1;
-    uint64_t *k_full = bars + 2;   // [kPfStages]
-    uint64_t *v_full = bars + 4;   // [kPfStages]
-    uint64_t *kv_empty = bars + 6; // [kPfStages]
-    uint64_t *s_full = bars + 8;   // [2]
-    uint64_t *p_full = bars + 10;  // [2]
-    uint64_t *o_done = bars + 12;
-    uint64_t *o_free = bars + 13;
-    uint64_t *drain = bars + 14;
+    uint64_t *b = reinterpret_cast<uint64_t *>(smem + Cfg::kBarOff);
+    PfBars bars;
+    bars.q_full = b + 0;
+    bars.q_empty = b + 1;
+    bars.k_full = b + 2;     // [kPfStages]
+    bars.v_full = b + 4;     // [kPfStages]
+    bars.kv_empty = b + 6;   // [kPfStages]
+    bars.s_full = b + 8;     // [2]
+    bars.p_full = b + 10;    // [2]
+    bars.o_done = b + 12;    // [2]
+    bars.o_free = b + 14;    // [2]
+    bars.drain = b + 16;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + Cfg::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kMiscOff + 4);
     int32_t *prefix = reinterpret_cast<int32_t *>(smem + Cfg::kPrefixOff);
@@ -197,17 +422,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int lane = threadIdx.x & 31;
     const int nseq = p.shared_prefix ? 0 : p.num_seqs - p.first_seq;
 
-    // ---- prefix sums of 128-query tiles per prefill sequence (block-wide scan)
+    // ---- prefix sums of 256-query super-tiles per prefill sequence
     {
         __shared__ int32_t part[kPfThreads];
         const int per = (nseq + kPfThreads - 1) / kPfThreads;
         const int a = min(nseq, int(threadIdx.x) * per);
-        const int b = min(nseq, a + per);
+        const int e = min(nseq, a + per);
         int sum = 0;
-        for (int k = a; k < b; ++k) {
+        for (int k = a; k < e; ++k) {
             const int s = p.first_seq + k;
             const int ql = p.qsl[s + 1] - p.qsl[s];
-            sum += ql > 0 ? (ql + kBM - 1) / kBM : 0;
+            sum += ql > 0 ? (ql + kSuper - 1) / kSuper : 0;
         }
         part[threadIdx.x] = sum;
         __syncthreads();
@@ -222,29 +447,29 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         __syncthreads();
         int run = part[threadIdx.x];
-        for (int k = a; k < b; ++k) {
+        for (int k = a; k < e; ++k) {
             prefix[k] = run;
             const int s = p.first_seq + k;
             const int ql = p.qsl[s + 1] - p.qsl[s];
-            run += ql > 0 ? (ql + kBM - 1) / kBM : 0;
+            run += ql > 0 ? (ql + kSuper - 1) / kSuper : 0;
         }
     }
 
     if (threadIdx.x == 0) {
-        mbar_init(q_full, 1);
-        mbar_init(q_empty, 1);
+        mbar_init(bars.q_full, 1);
+        mbar_init(bars.q_empty, 1);
         for (int i = 0; i < kPfStages; ++i) {
-            mbar_init(&k_full[i], 1);
-            mbar_init(&v_full[i], 1);
-            mbar_init(&kv_empty[i], 1);
+            mbar_init(&bars.k_full[i], 1);
+            mbar_init(&bars.v_full[i], 1);
+            mbar_init(&bars.kv_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], 4);
+            mbar_init(&bars.s_full[i], 1);
+            mbar_init(&bars.p_full[i], 4);
+            mbar_init(&bars.o_done[i], 1);
+            mbar_init(&bars.o_free[i], 4);
         }
-        mbar_init(o_done, 1);
-        mbar_init(o_free, 4);
-        mbar_init(drain, 1);
+        mbar_init(bars.drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -256,320 +481,210 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_holder;
-    const uint32_t tS = tbase;          // two S buffers of 128 columns
-    const uint32_t tO = tbase + 256;    // O, D columns
 
-    if (warp == 0) {
-        // ================================================================ producer
-        // Lane b owns TMA box b of every K/V tile (one page-sized box per lane),
-        // so the block-table lookups of a tile are one parallel load, issued for
-        // the next tile before waiting for a free stage.
-        if (lane == 0) {
-            tma_prefetch_desc(&q_map);
-            tma_prefetch_desc(&kv_map);
-        }
-        const uint64_t pol_kv = l2_policy_evict_last();
-        const uint64_t pol_q = l2_policy_evict_first();
-        uint32_t li = 0, kv_it = 0;
-        PfItem it;
-        for (int item = blockIdx.x; pf_item(p, prefix, nseq, item, it); item += gridDim.x) {
-            if (it.n_kv == 0)
-                continue;
-            const int kvh = it.h / p.group;
-            const int32_t *bt = p.block_table + int64_t(it.s) * p.bt_stride;
-            auto lane_block = [&](int jt) -> int {
-                const int key0 = p.kv_lo + jt * kBN;
-                const int nbox = (min(kBN, it.kv_hi - key0) + p.box_rows - 1) / p.box_rows;
-                if (lane >= nbox)
-                    return -1;
-                const int col = (key0 + lane * p.box_rows) / p.block_size;
-                int blk = col < p.bt_stride ? bt[col] : -1;
-                if (blk < 0 || blk >= p.num_blocks) {
-                    flag_error(kErrBlockOutOfPool);
-                    blk = 0;  // keep the byte count whole; the result is flagged
-                }
-                return blk;
-            };
-            int blk_next = lane_block(0);
-            if (li > 0 && !pf_wait(q_empty, (li - 1) & 1, abort_flag))
-                goto producer_done;
+    if (warp < 4) {
+        reg_dealloc<88>();
+        if (warp == 0) {
+            // ============================================================ producer
             if (lane == 0) {
-                mbar_arrive_expect_tx(q_full, Cfg::kTileBytes);
-                for (int hf = 0; hf < Cfg::kHalves; ++hf)
-                    tma_load_3d(smem + Cfg::kQOff + hf * Cfg::kHalfBytes, &q_map, q_full,
-                                hf * 64, it.h, it.t0, pol_q);
+                tma_prefetch_desc(&q_map);
+                tma_prefetch_desc(&kv_map);
             }
-            for (int jt = 0; jt < it.n_kv; ++jt, ++kv_it) {
-                const int blk = blk_next;
-                if (jt + 1 < it.n_kv)
-                    blk_next = lane_block(jt + 1);
-                const int st = kv_it % kPfStages;
-                const uint32_t rnd = kv_it / kPfStages;
-                if (rnd > 0 && !pf_wait(&kv_empty[st], (rnd - 1) & 1, abort_flag))
-                    goto producer_done;
-                const int key0 = p.kv_lo + jt * kBN;
-                const int nbox = (min(kBN, it.kv_hi - key0) + p.box_rows - 1) / p.box_rows;
-                const uint32_t bytes = nbox * p.box_rows * 128 * Cfg::kHalves;
+            const uint64_t pol_kv = l2_policy_evict_last();
+            const uint64_t pol_q = l2_policy_evict_first();
+            uint32_t li = 0, kv_it = 0;
+            PfItem it;
+            for (int item = blockIdx.x; pf_item(p, prefix, nseq, item, it); item += gridDim.x) {
+                if (it.n_kv_all == 0)
+                    continue;
+                const int kvh = it.h / p.group;
+                const int32_t *bt = p.block_table + int64_t(it.s) * p.bt_stride;
+                const int kv_hi = it.kv_hi;
+                // lane b owns TMA box b of every K/V tile; its block id is looked
+                // up for the next tile before waiting for a free stage
+                auto lane_block = [&](int jt) -> int {
+                    const int key0 = p.kv_lo + jt * kBN;
+                    const int nbox = (min(kBN, kv_hi - key0) + p.box_rows - 1) / p.box_rows;
+                    if (lane >= nbox)
+                        return -1;
+                    const int col = (key0 + lane * p.box_rows) / p.block_size;
+                    int blk = col < p.bt_stride ? bt[col] : -1;
+                    if (blk < 0 || blk >= p.num_blocks) {
+                        flag_error(kErrBlockOutOfPool);
+                        blk = 0;  // keep the byte count whole; the result is flagged
+                    }
+                    return blk;
+                };
+                int blk_next = lane_block(0);
+                if (li > 0 && !pf_wait(bars.q_empty, (li - 1) & 1, abort_flag))
+                    break;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&k_full[st], bytes);
-                    mbar_arrive_expect_tx(&v_full[st], bytes);
+                    const int ntiles = it.rows[1] > 0 ? 2 : 1;
+                    mbar_arrive_expect_tx(bars.q_full, ntiles * Cfg::kTileBytes);
+                    for (int tl = 0; tl < ntiles; ++tl)
+                        for (int hf = 0; hf < Cfg::kHalves; ++hf)
+                            tma_load_3d(smem + Cfg::kQOff + tl * Cfg::kTileBytes +
+                                            hf * Cfg::kHalfBytes,
+                                        &q_map, bars.q_full, hf * 64, it.h, it.t0 + tl * kBM,
+                                        pol_q);
                 }
-                __syncwarp();
-                if (lane < nbox) {
-                    const int key = key0 + lane * p.box_rows;
-                    const int row_k = (blk * 2) * p.block_size + key % p.block_size;
-                    const int row_v = row_k + p.block_size;
-                    uint8_t *kt = smem + Cfg::kKOff + st * Cfg::kTileBytes + lane * p.box_rows * 128;
-                    uint8_t *vt = smem + Cfg::kVOff + st * Cfg::kTileBytes + lane * p.box_rows * 128;
-                    for (int hf = 0; hf < Cfg::kHalves; ++hf)
-                        tma_load_3d(kt + hf * Cfg::kHalfBytes, &kv_map, &k_full[st], hf * 64,
-                                    kvh, row_k, pol_kv);
-                    for (int hf = 0; hf < Cfg::kHalves; ++hf)
-                        tma_load_3d(vt + hf * Cfg::kHalfBytes, &kv_map, &v_full[st], hf * 64,
-                                    kvh, row_v, pol_kv);
-                }
-            }
-            ++li;
-        }
-    producer_done:;
-    } else if (warp == 1) {
-        // ================================================================ MMA issuer
-        const uint32_t sQ = smem_addr(smem + Cfg::kQOff);
-        uint32_t li = 0, kv_it = 0, s_it = 0;
-        PfItem it;
-        for (int item = blockIdx.x; pf_item(p, prefix, nseq, item, it); item += gridDim.x) {
-            if (it.n_kv == 0)
-                continue;
-            if (!pf_wait(q_full, li & 1, abort_flag))
-                goto mma_done;
-            tc_fence_after();
-            for (int jt = 0; jt <= it.n_kv; ++jt) {
-                if (jt < it.n_kv) {
-                    // ---- S[jt] = Q K[jt]^T
-                    const uint32_t n = kv_it + jt;
-                    const int st = n % kPfStages;
-                    if (!pf_wait(&k_full[st], (n / kPfStages) & 1, abort_flag))
-                        goto mma_done;
-                    tc_fence_after();
-                    const uint32_t sb = (s_it + jt) & 1;
-                    const uint32_t sK = smem_addr(smem + Cfg::kKOff + st * Cfg::kTileBytes);
+                bool stop = false;
+                for (int jt = 0; jt < it.n_kv_all; ++jt, ++kv_it) {
+                    const int blk = blk_next;
+                    if (jt + 1 < it.n_kv_all)
+                        blk_next = lane_block(jt + 1);
+                    const int st = kv_it % kPfStages;
+                    const uint32_t rnd = kv_it / kPfStages;
+                    if (rnd > 0 && !pf_wait(&bars.kv_empty[st], (rnd - 1) & 1, abort_flag)) {
+                        stop = true;
+                        break;
+                    }
+                    const int key0 = p.kv_lo + jt * kBN;
+                    const int nbox = (min(kBN, kv_hi - key0) + p.box_rows - 1) / p.box_rows;
+                    const uint32_t bytes = nbox * p.box_rows * 128 * Cfg::kHalves;
                     if (lane == 0) {
-#pragma unroll
-                        for (int k = 0; k < D / 16; ++k) {
-                            const uint32_t off = (k >> 2) * Cfg::kHalfBytes + (k & 3) * 32;
-                            mma_ss(tS + sb * 128, smem_desc_sw128(sQ + off, 16, 1024),
-                                   smem_desc_sw128(sK + off, 16, 1024), Cfg::kIdescS, k > 0);
-                        }
-                        mma_commit(&s_full[sb]);
-                        if (jt == it.n_kv - 1)
-                            mma_commit(q_empty);
+                        mbar_arrive_expect_tx(&bars.k_full[st], bytes);
+                        mbar_arrive_expect_tx(&bars.v_full[st], bytes);
                     }
                     __syncwarp();
+                    if (lane < nbox) {
+                        const int key = key0 + lane * p.box_rows;
+                        const int row_k = (blk * 2) * p.block_size + key % p.block_size;
+                        const int row_v = row_k + p.block_size;
+                        uint8_t *kt =
+                            smem + Cfg::kKOff + st * Cfg::kTileBytes + lane * p.box_rows * 128;
+                        uint8_t *vt =
+                            smem + Cfg::kVOff + st * Cfg::kTileBytes + lane * p.box_rows * 128;
+                        for (int hf = 0; hf < Cfg::kHalves; ++hf)
+                            tma_load_3d(kt + hf * Cfg::kHalfBytes, &kv_map, &bars.k_full[st],
+                                        hf * 64, kvh, row_k, pol_kv);
+                        for (int hf = 0; hf < Cfg::kHalves; ++hf)
+                            tma_load_3d(vt + hf * Cfg::kHalfBytes, &kv_map, &bars.v_full[st],
+                                        hf * 64, kvh, row_v, pol_kv);
+                    }
                 }
-                if (jt > 0) {
-                    // ---- O += P[jt-1] V[jt-1]
-                    const int jp = jt - 1;
-                    const uint32_t n = kv_it + jp;
-                    const int st = n % kPfStages;
-                    const uint32_t sn = s_it + jp;
-                    const uint32_t sb = sn & 1;
-                    if (!pf_wait(&p_full[sb], (sn >> 1) & 1, abort_flag))
-                        goto mma_done;
-                    if (!pf_wait(&v_full[st], (n / kPfStages) & 1, abort_flag))
-                        goto mma_done;
-                    uint8_t *vt = smem + Cfg::kVOff + st * Cfg::kTileBytes;
-                    const int nvalid = it.kv_hi - (p.kv_lo + jp * kBN);
-                    if (nvalid < kBN) {
-                        // rows past the last key may hold anything (or nothing was
-                        // loaded there): zero them so that P = 0 meets finite V
-                        for (int hf = 0; hf < Cfg::kHalves; ++hf) {
-                            uint4 *base = reinterpret_cast<uint4 *>(vt + hf * Cfg::kHalfBytes +
-                                                                     nvalid * 128);
-                            const int n16 = (kBN - nvalid) * 8;
-                            for (int i = lane; i < n16; i += 32)
-                                base[i] = make_uint4(0, 0, 0, 0);
-                        }
-                        fence_proxy_async_smem();
-                    }
-                    if (jp == 0 && li > 0 && !pf_wait(o_free, (li - 1) & 1, abort_flag))
-                        goto mma_done;
-                    __syncwarp();
-                    tc_fence_after();
-                    const uint32_t sV = smem_addr(vt);
-                    if (lane == 0) {
-#pragma unroll
-                        for (int k = 0; k < kBN / 16; ++k)
-                            mma_ts(tO, tS + sb * 128 + k * 8,
-                                   smem_desc_sw128(sV + k * 2048, Cfg::kHalfBytes, 1024),
-                                   Cfg::kIdescPV, (jp > 0 || k > 0) ? 1u : 0u);
-                        mma_commit(o_done);
-                        mma_commit(&kv_empty[st]);
-                    }
-                    __syncwarp();
-                }
+                if (stop)
+                    break;
+                ++li;
             }
-            kv_it += it.n_kv;
-            s_it += it.n_kv;
-            ++li;
-        }
-    mma_done:
-        if (lane == 0) {
-            mma_commit(drain);  // all issued MMAs have finished once this fires
-            mbar_wait(drain, 0);
-        }
-        __syncwarp();
-    } else if (warp >= 4) {
-        // ================================================================ softmax
-        const int wq = warp - 4;  // TMEM lane quarter of this warp
-        const int r = wq * 32 + lane;
-        const uint32_t lane_off = uint32_t(wq * 32) << 16;
-        uint32_t s_it = 0, pv_n = 0;
-        PfItem it;
-        for (int item = blockIdx.x; pf_item(p, prefix, nseq, item, it); item += gridDim.x) {
-            const bool valid = r < it.rows;
-            const int t = it.t0 + r;
-            if (it.n_kv == 0) {
-                if (valid && p.partial) {
-                    const int64_t row = int64_t(t - p.token_base) * p.num_heads + it.h;
-                    for (int d = 0; d < D; ++d)
-                        p.o_part[row * D + d] = 0.f;
-                    p.lse_part[row] = kPfNegInf;
-                }
-                continue;
-            }
-            const int pos = it.ctx + it.qidx0 + r;
-            int hi_row = p.causal ? min(it.L, pos + 1) : it.L;
-            hi_row = min(hi_row, p.kv_cap);
-            float m = kPfNegInf, l = 0.f;
-            for (int jt = 0; jt < it.n_kv; ++jt) {
-                const uint32_t sn = s_it + jt;
-                const uint32_t sb = sn & 1;
-                if (!pf_wait(&s_full[sb], (sn >> 1) & 1, abort_flag))
-                    goto softmax_done;
+        } else if (warp == 1) {
+            // ============================================================ MMA issuer
+            const uint32_t sQ = smem_addr(smem + Cfg::kQOff);
+            uint32_t li = 0, kv_it = 0;
+            uint32_t p_cnt[2] = {0, 0}, item_cnt[2] = {0, 0};
+            PfItem it;
+            bool ok = true;
+            for (int item = blockIdx.x; ok && pf_item(p, prefix, nseq, item, it);
+                 item += gridDim.x) {
+                if (it.n_kv_all == 0)
+                    continue;
+                if (!pf_wait(bars.q_full, li & 1, abort_flag))
+                    break;
                 tc_fence_after();
-                const uint32_t ts = tS + sb * 128 + lane_off;
-                uint32_t x[4][32];
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    tmem_ld32(ts + c * 32, x[c]);
-                tmem_wait_ld();
-                const int lim = hi_row - (p.kv_lo + jt * kBN);  // columns c < lim admitted
-                // scaled, masked logits (base 2) and their row max in four chains
-                float mx4[4] = {kPfNegInf, kPfNegInf, kPfNegInf, kPfNegInf};
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float v =
-                            c * 32 + i < lim ? __uint_as_float(x[c][i]) * p.scale_log2 : kPfNegInf;
-                        x[c][i] = __float_as_uint(v);
-                        mx4[i & 3] = fmaxf(mx4[i & 3], v);
-                    }
-                }
-                const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-                // The reference max m moves only when the row max passes it by more
-                // than 8 (a factor 256): every p stays <= 256 and the O rescale in
-                // TMEM is rarely needed.  The result is exact either way, since lse
-                // and the final 1/l use the same reference.
-                const float m_new = mx > m + 8.f ? mx : m;
-                const float base = m_new == kPfNegInf ? 0.f : m_new;
-                float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float p0 = fast_exp2(__uint_as_float(x[c][2 * i]) - base);
-                        const float p1 = fast_exp2(__uint_as_float(x[c][2 * i + 1]) - base);
-                        sum4[(2 * i) & 3] += p0;
-                        sum4[(2 * i + 1) & 3] += p1;
-                        pk[i] = pack_bf16x2(p0, p1);
-                    }
-                    tmem_st16(ts + c * 16, pk);
-                }
-                tmem_wait_st();
-                const float alpha = fast_exp2(m - base);  // 1 when m did not move
-                l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
-                const bool moved = m_new != m;
-                m = m_new;
-                if (jt > 0) {
-                    if (!pf_wait(o_done, pv_n & 1, abort_flag))
-                        goto softmax_done;
-                    ++pv_n;
-                    tc_fence_after();
-                    if (__any_sync(0xffffffffu, moved)) {
-#pragma unroll
-                        for (int c = 0; c < D / 32; ++c) {
-                            uint32_t o[32];
-                            tmem_ld32(tO + lane_off + c * 32, o);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                            tmem_st32(tO + lane_off + c * 32, o);
+                const int n = it.n_kv_all;
+                for (int jt = 0; jt <= n && ok; ++jt) {
+                    const uint32_t kn = kv_it + jt;
+                    const int st = kn % kPfStages;
+                    if (jt < n) {
+                        if (!pf_wait(&bars.k_full[st], (kn / kPfStages) & 1, abort_flag)) {
+                            ok = false;
+                            break;
                         }
-                        tmem_wait_st();
+                        tc_fence_after();
                     }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&p_full[sb]);
-            }
-            // ---- epilogue: out = O / l, lse
-            if (!pf_wait(o_done, pv_n & 1, abort_flag))
-                goto softmax_done;
-            ++pv_n;
-            tc_fence_after();
-            {
-                const float inv = l > 0.f ? 1.f / l : 0.f;
-                const float lse2 = m + log2f(l);
-                const int64_t orow = int64_t(t) * p.num_heads + it.h;
-                const int64_t prow = int64_t(t - p.token_base) * p.num_heads + it.h;
+                    for (int tl = 0; tl < 2 && ok; ++tl) {
+                        const int nk = it.n_kv[tl];
+                        // ---- O_tl += P_tl V of the previous K/V tile
+                        if (jt > 0 && jt - 1 < nk) {
+                            const int jp = jt - 1;
+                            const uint32_t pn = kv_it + jp;
+                            const int pst = pn % kPfStages;
+                            if (!pf_wait(&bars.p_full[tl], p_cnt[tl] & 1, abort_flag) ||
+                                !pf_wait(&bars.v_full[pst], (pn / kPfStages) & 1, abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            ++p_cnt[tl];
+                            const int nvalid = it.kv_hi - (p.kv_lo + jp * kBN);
+                            const bool first_reader = tl == 0 || jp >= it.n_kv[0];
+                            if (jp == n - 1 && nvalid < kBN && first_reader) {
+                                // rows past the last key may hold anything (or nothing
+                                // was loaded there): zero them once, before the first
+                                // PV that reads this tile, so that P = 0 meets finite V
+                                uint8_t *vt = smem + Cfg::kVOff + pst * Cfg::kTileBytes;
+                                for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+                                    uint4 *zb = reinterpret_cast<uint4 *>(
+                                        vt + hf * Cfg::kHalfBytes + nvalid * 128);
+                                    const int n16 = (kBN - nvalid) * 8;
+                                    for (int i = lane; i < n16; i += 32)
+                                        zb[i] = make_uint4(0, 0, 0, 0);
+                                }
+                                fence_proxy_async_smem();
+                                __syncwarp();
+                            }
+                            if (jp == 0 && item_cnt[tl] > 0 &&
+                                !pf_wait(&bars.o_free[tl], (item_cnt[tl] - 1) & 1, abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t sV = smem_addr(smem + Cfg::kVOff + pst * Cfg::kTileBytes);
+                            if (lane == 0) {
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + lane_off + c * 32, o);
-                    tmem_wait_ld();
-                    if (valid) {
-                        if (p.partial) {
-                            float4 *dst = reinterpret_cast<float4 *>(p.o_part + prow * D + c * 32);
+                                for (int k = 0; k < kBN / 16; ++k)
+                                    mma_ts(tbase + 256 + tl * D, tbase + tl * 128 + k * 8,
+                                           smem_desc_sw128(sV + k * 2048, Cfg::kHalfBytes, 1024),
+                                           Cfg::kIdescPV, (jp > 0 || k > 0) ? 1u : 0u);
+                                mma_commit(&bars.o_done[tl]);
+                            }
+                            __syncwarp();
+                        }
+                        // ---- S_tl = Q_tl K^T of this K/V tile
+                        if (jt < nk) {
+                            const uint32_t sK = smem_addr(smem + Cfg::kKOff + st * Cfg::kTileBytes);
+                            const uint32_t sQt = sQ + tl * Cfg::kTileBytes;
+                            if (lane == 0) {
 #pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv,
-                                                     __uint_as_float(o[4 * i + 1]) * inv,
-                                                     __uint_as_float(o[4 * i + 2]) * inv,
-                                                     __uint_as_float(o[4 * i + 3]) * inv);
-                        } else {
-                            uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D + c * 32);
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                dst[i] = make_uint4(
-                                    pack_bf16x2(__uint_as_float(o[8 * i]) * inv,
-                                                __uint_as_float(o[8 * i + 1]) * inv),
-                                    pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv,
-                                                __uint_as_float(o[8 * i + 3]) * inv),
-                                    pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv,
-                                                __uint_as_float(o[8 * i + 5]) * inv),
-                                    pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv,
-                                                __uint_as_float(o[8 * i + 7]) * inv));
+                                for (int k = 0; k < D / 16; ++k) {
+                                    const uint32_t off = (k >> 2) * Cfg::kHalfBytes + (k & 3) * 32;
+                                    mma_ss(tbase + tl * 128, smem_desc_sw128(sQt + off, 16, 1024),
+                                           smem_desc_sw128(sK + off, 16, 1024), Cfg::kIdescS,
+                                           k > 0);
+                                }
+                                mma_commit(&bars.s_full[tl]);
+                            }
+                            __syncwarp();
                         }
                     }
+                    if (!ok)
+                        break;
+                    if (lane == 0) {
+                        if (jt == n - 1)
+                            mma_commit(bars.q_empty);  // Q is free once the last S is done
+                        if (jt > 0)
+                            mma_commit(&bars.kv_empty[(kv_it + jt - 1) % kPfStages]);
+                    }
+                    __syncwarp();
                 }
-                if (valid) {
-                    if (p.partial)
-                        p.lse_part[prow] = lse2;
-                    else if (p.lse)
-                        p.lse[orow] = lse2 * kPfLn2;
-                }
+                if (!ok)
+                    break;
+                for (int tl = 0; tl < 2; ++tl)
+                    if (it.n_kv[tl] > 0)
+                        ++item_cnt[tl];
+                kv_it += n;
+                ++li;
             }
-            tc_fence_before();
+            if (lane == 0) {
+                mma_commit(bars.drain);  // fires once every issued MMA has finished
+                mbar_wait(bars.drain, 0);
+            }
             __syncwarp();
-            if (lane == 0)
-                mbar_arrive(o_free);
-            s_it += it.n_kv;
         }
-    softmax_done:;
+    } else {
+        reg_alloc<208>();
+        const int tl = (warp - 4) / 4;  // warps 4-7: tile A, warps 8-11: tile B
+        pf_softmax<D>(p, prefix, nseq, bars, tl, tbase + tl * 128, tbase + 256 + tl * D,
+                      abort_flag);
     }
 
     tc_fence_before();
@@ -580,14 +695,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 }
 
 // --------------------------------------------------------------------- host
-static CUresult encode_q_map(CUtensorMap *map, const void *q, int32_t num_tokens,
-                             int32_t num_heads, int32_t head_size)
-{
-    return encode_3d_bf16(map, q, head_size, num_heads, num_tokens,
-                          uint64_t(head_size) * 2, uint64_t(num_heads) * head_size * 2, 64, 1,
-                          kBM);
-}
-
 template <int D>
 static cudaError_t launch_prefill_d(const Fwd &f, const PrefillParams &p, int grid)
 {
@@ -604,7 +711,8 @@ static cudaError_t launch_prefill_d(const Fwd &f, const PrefillParams &p, int gr
         configured_device = dev;
     }
     CUtensorMap q_map, kv_map;
-    if (encode_q_map(&q_map, f.query, f.num_tokens, f.num_heads, D) != CUDA_SUCCESS)
+    if (encode_3d_bf16(&q_map, f.query, D, f.num_heads, f.num_tokens, uint64_t(D) * 2,
+                       uint64_t(f.num_heads) * D * 2, 64, 1, kBM) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     if (encode_3d_bf16(&kv_map, f.kv_cache, D, f.num_kv_heads,
                        uint64_t(f.num_blocks) * 2 * f.block_size, uint64_t(D) * 2,
@@ -648,10 +756,10 @@ cudaError_t launch_prefill(const Fwd &f, const PrefillPass &pass)
     p.lse_part = pass.lse_part;
     int64_t items;
     if (pass.shared_prefix)
-        items = int64_t((f.num_tokens + kBM - 1) / kBM) * f.num_heads;
+        items = int64_t((f.num_tokens + kSuper - 1) / kSuper) * f.num_heads;
     else
-        items = (int64_t(f.num_tokens - f.num_decodes) + int64_t(nseq) * (kBM - 1)) / kBM *
-                f.num_heads;
+        items = (int64_t(f.num_tokens - f.num_decodes) + int64_t(nseq) * (kSuper - 1)) /
+                kSuper * f.num_heads;
     // persistent grid: one CTA per SM, but no more CTAs than work items
     const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(f.num_sms, items)));
     if (f.head_size == 128)
