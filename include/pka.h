@@ -77,8 +77,10 @@ typedef enum {
  *                   P/bs block-table entries of every sequence are the same
  *                   blocks and P <= c_s for every s ([blog] "Que aporta
  *                   FlashInfer: JIT y cascade attention").
- *  split_kv_tokens  0 = automatic; else the number of keys per decode split
- *                   (rounded up to the kernel's stage size).
+ *  split_kv_tokens  0 = automatic (the decode work is divided evenly over one
+ *                   CTA per SM); else a target number of keys per CTA, which
+ *                   uses fewer CTAs when the batch is small (a tuning and
+ *                   test knob; results are the same either way).
  */
 typedef struct {
     const int32_t *query_start_loc;
@@ -185,8 +187,9 @@ pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const
  *  - The first call on a device looks up the buffer's device address once
  *    (cudaGetSymbolAddress, with that device current); make that first call
  *    before any stream capture.
- *  - Every call shares the one buffer and leaves its contents behind (each
- *    call writes all of what it later reads).  Calls that overlap on the GPU
+ *  - Every call shares the one buffer and leaves its contents behind; each
+ *    call clears what must start at zero (its per-sequence counters) and
+ *    writes all the rest before reading it.  Calls that overlap on the GPU
  *    (other streams, other host threads) race on it: serialise them.
  */
 pka_status pka_paged_attn_forward_noalloc(const void *query, const void *kv_cache,

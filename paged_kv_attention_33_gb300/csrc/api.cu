@@ -135,11 +135,15 @@ Workspace plan_workspace(const DecodePlan &dp, int32_t num_tokens, int32_t num_d
 {
     Workspace w;
     size_t off = 0;
-    const size_t rows_part = size_t(num_decodes) * dp.max_splits * num_heads;
+    // one partial per (CTA, sequence) piece: slot ids b + s < grid + chunk
+    const size_t slots = num_decodes > 0 ? size_t(dp.grid) + dp.chunk : 0;
+    const size_t rows_part = slots * dp.rows_per_slot * num_heads;
     w.o_part = off;
     off = round256(off + rows_part * head_size * 4);
     w.lse_part = off;
     off = round256(off + rows_part * 4);
+    w.counters = off;
+    off = round256(off + size_t(dp.chunk) * 4);
     const size_t rows_all = cascade ? size_t(num_tokens) * num_heads : 0;
     w.o_pre = off;
     off = round256(off + rows_all * head_size * 4);
@@ -260,8 +264,8 @@ size_t pka_workspace_size(const pka_meta *meta, int32_t num_tokens, int32_t num_
         return 0;
     const bool cascade = meta->common_prefix_len > 0;
     const int32_t kv_begin = meta->common_prefix_len;
-    DecodePlan dp = plan_decode(meta->split_kv_tokens, meta->num_decodes, meta->max_seq_len,
-                                kv_begin, num_kv_heads, sm_count());
+    DecodePlan dp = plan_decode(meta->split_kv_tokens, meta->num_decodes, num_kv_heads,
+                                sm_count());
     return plan_workspace(dp, num_tokens, meta->num_decodes, num_heads, head_size, cascade).total;
 }
 
@@ -323,8 +327,8 @@ pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const
     f.stream = static_cast<cudaStream_t>(stream);
     f.num_sms = sm_count();
 
-    DecodePlan dp = plan_decode(meta->split_kv_tokens, meta->num_decodes, meta->max_seq_len,
-                                kv_begin, num_kv_heads, f.num_sms);
+    DecodePlan dp = plan_decode(meta->split_kv_tokens, meta->num_decodes, num_kv_heads,
+                                f.num_sms);
     Workspace ws = plan_workspace(dp, num_tokens, meta->num_decodes, num_heads, head_size, cascade);
     if (ws.total > 0 && (!workspace || workspace_bytes < ws.total || !aligned(workspace, 256)))
         return fail(PKA_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)",
@@ -367,9 +371,11 @@ pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const
         if (e != cudaSuccess)
             return cuda_fail(e, "prefill launch");
     }
-    e = launch_decode_combine(f, dp, ws, wsp, kv_begin, cascade);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "combine launch");
+    if (cascade) {
+        e = launch_cascade_prefill_combine(f, ws, wsp);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cascade combine launch");
+    }
     return PKA_OK;
 }
 

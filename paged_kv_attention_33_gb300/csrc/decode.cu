@@ -1,4 +1,4 @@
-// decode.cu -- split-KV paged decode and its log-sum-exp combine.
+// decode.cu -- paged decode (split-KV, stream-K) with the split combine fused in.
 //
 // What it computes (the "El especialista del plato estrella" blog,
 // "Por que prefill y decode son problemas opuestos"): one query token per
@@ -7,9 +7,15 @@
 // for all query heads of its kv head at the same time (GQA packing), and is
 // staged into shared memory by TMA ahead of use.
 //
-// Grid: one CTA per (decode sequence s, split j).  Split j covers keys
-// [kv_begin + j*C, min(kv_begin + (j+1)*C, L_s)), C = split_tokens.  CTAs of
-// splits past the end of their sequence exit at once.
+// Grid: persistent, one CTA per SM, stream-K.  The decodes' keys
+// [kv_begin, L_s) are cut into stages of 16*(8/Hkv) keys; the flattened list
+// of all stages (sequence after sequence) is divided into equal, contiguous
+// ranges, one per CTA, so every CTA streams the same number of bytes and its
+// TMA ring never drains between sequences.  A CTA's range covers one or more
+// "pieces" (the part of one sequence inside the range).  A sequence covered by
+// one piece is finished by that CTA; otherwise each piece writes an fp32
+// partial and the last CTA to finish a piece of that sequence (an atomic
+// counter per sequence) merges them -- the split combine fused into the kernel.
 //
 // CTA: 8 consumer warps + 1 producer warp.  A pipeline stage holds 8 "units";
 // unit u is 16 consecutive keys of kv head k = u % Hkv, slice r = u / Hkv of the
@@ -30,9 +36,12 @@
 // The tensor work is g FLOP per byte of KV, far below the ridge point, so the
 // warp-level mma is ample; the kernel is bound by HBM.
 //
-// At the end the warps of the same kv head (when Hkv < 8) are merged through
-// shared memory and the CTA writes either the final bf16 row and lse (single
-// split) or a normalised fp32 partial and its log2-sum-exp for the combine.
+// At the end of a piece every warp writes its rows straight from registers:
+// the final bf16 rows and lse, or (several pieces, or Hkv < 8 where several
+// warps share a kv head) a normalised fp32 partial and its log2-sum-exp.
+// Failure path: every wait is bounded; a warp whose wait gives up raises a
+// CTA-wide abort flag, stops computing and writing, but still walks the same
+// stage and piece sequence so that every named barrier is reached by all.
 #include <math.h>
 
 #include <algorithm>
@@ -54,19 +63,24 @@ struct DecodeParams {
     int32_t group;
     int32_t block_size;
     int32_t num_blocks;
-    int32_t split_tokens;
-    int32_t max_splits;
-    int32_t kv_begin;
-    int32_t partial_only;
-    float scale_log2;  // softmax scale * log2(e)
+    int32_t seq0;         // first decode sequence of this launch
+    int32_t nseq;         // decodes in this launch (<= kMaxDecodeChunk)
+    int32_t kv_begin;     // first key (cascade suffix: the shared prefix length)
+    int32_t target_keys;  // 0, or keys per CTA to aim for (fewer CTAs)
+    int32_t cascade;      // merge the shared-prefix partial into every row
+    float scale_log2;     // softmax scale * log2(e)
     __nv_bfloat16 *out;
     float *lse;
-    float *o_part;    // [num_decodes, max_splits, H, D]
-    float *lse_part;  // [num_decodes, max_splits, H], log2 units
+    float *o_part;        // [slots, R, H, D] normalised partials
+    float *lse_part;      // [slots, R, H], log2 units
+    int32_t *counters;    // [nseq] pieces finished per sequence (zeroed per launch)
+    const float *o_pre;   // cascade: shared-prefix partial [T, H, D]
+    const float *lse_pre; // [T, H], log2 units
 };
 
 constexpr int kConsumerWarps = 8;
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxDecodeChunk = 4096;
 constexpr float kNegInf = -INFINITY;
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -77,10 +91,11 @@ struct DecodeCfg {
     static constexpr int kKvBytes = kConsumerWarps * kUnitBytes;   // all units of K (or V)
     static constexpr int kStageBytes = 2 * kKvBytes;
     static constexpr int kStages = (D == 128) ? 3 : 6;
-    static constexpr int kScratchFloats = 16 + 8 * D;              // per warp: m, l, O^T
-    static constexpr size_t kSmemBytes =
-        size_t(kStages) * kStageBytes + 2 * kStages * sizeof(uint64_t) + 1024;
-    static_assert(kConsumerWarps * kScratchFloats * 4 <= kStages * kStageBytes, "scratch");
+    static constexpr int kBarOff = kStages * kStageBytes;
+    static constexpr int kMiscOff = kBarOff + 2 * kStages * 8;    // last-piece flag, abort flag
+    static constexpr int kPrefixOff = kMiscOff + 16;
+    static constexpr size_t kSmemBytes = kPrefixOff + (kMaxDecodeChunk + 1) * 4 + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
 __device__ __forceinline__ float warp_max_heads(float v)
@@ -104,6 +119,40 @@ __device__ __forceinline__ void consumer_sync()
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
+// Bounded wait that also gives up at once when another warp of the CTA gave up.
+__device__ __forceinline__ bool dec_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
+{
+    if (mbar_test(bar, parity))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1; it < kWaitIterCap; ++it) {
+        if (mbar_test(bar, parity))
+            return true;
+        if ((it & 127u) == 0) {
+            if (*abort_flag)
+                return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs)
+                break;
+        }
+    }
+    flag_error(kErrWaitTimeout);
+    *abort_flag = 1;
+    return false;
+}
+
+// Stages of decode s (at least one, so every decode owns a piece).
+__device__ __forceinline__ int dec_stages(const DecodeParams &p, int s, int stage_keys)
+{
+    const int n = p.seq_lens[p.seq0 + s] - p.kv_begin;
+    return n > 0 ? (n + stage_keys - 1) / stage_keys : 1;
+}
+
+// CTA whose range [floor(b*TS/G), floor((b+1)*TS/G)) holds stage x.
+__device__ __forceinline__ int cta_of_stage(int64_t x, int64_t total, int grid)
+{
+    return static_cast<int>(((x + 1) * grid + total - 1) / total - 1);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p)
@@ -112,83 +161,142 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::kStages * Cfg::kStageBytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::kBarOff);
     uint64_t *empty = full + Cfg::kStages;
+    volatile int *last_flag = reinterpret_cast<volatile int *>(smem + Cfg::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kMiscOff + 4);
+    int32_t *prefix = reinterpret_cast<int32_t *>(smem + Cfg::kPrefixOff);
 
-    const int s = blockIdx.y;
-    const int split = blockIdx.x;
-    const int L = p.seq_lens[s];
-    if (p.kv_begin > 0 && L <= p.kv_begin) {
-        // cascade suffix pass: the decode's query must come after the shared prefix
-        if (threadIdx.x == 0 && split == 0)
-            flag_error(kErrBadMetadata);
-        return;
-    }
-    const int key_begin = p.kv_begin + split * p.split_tokens;
-    if (key_begin >= L)
-        return;  // whole CTA: this split lies past the end of the sequence
-    const int key_end = min(L, key_begin + p.split_tokens);
-    const int nsplit = (L - p.kv_begin + p.split_tokens - 1) / p.split_tokens;
-    const int t = p.qsl[s];
-    if (nsplit > p.max_splits || t < 0 || t >= p.num_tokens) {
-        // seq_lens above the stated max_seq_len, or a token index outside the
-        // batch: nothing is read or written for this sequence
-        if (threadIdx.x == 0 && split == 0)
-            flag_error(kErrBadMetadata);
-        return;
-    }
     const int Hkv = p.num_kv_heads;
     const int R = kConsumerWarps / Hkv;
     const int stage_keys = 16 * R;
-    const int nstage = (key_end - key_begin + stage_keys - 1) / stage_keys;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int nseq = p.nseq;
+
+    // ---- stage prefix sums over the decodes of this launch (block-wide scan)
+    {
+        __shared__ int32_t part[kDecodeThreads];
+        const int per = (nseq + kDecodeThreads - 1) / kDecodeThreads;
+        const int a = min(nseq, int(threadIdx.x) * per);
+        const int e = min(nseq, a + per);
+        int sum = 0;
+        for (int k = a; k < e; ++k)
+            sum += dec_stages(p, k, stage_keys);
+        part[threadIdx.x] = sum;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int run = 0;
+            for (int i = 0; i < kDecodeThreads; ++i) {
+                const int v = part[i];
+                part[i] = run;
+                run += v;
+            }
+            prefix[nseq] = run;
+        }
+        __syncthreads();
+        int run = part[threadIdx.x];
+        for (int k = a; k < e; ++k) {
+            prefix[k] = run;
+            run += dec_stages(p, k, stage_keys);
+        }
+        __syncthreads();
+    }
+    const int64_t total = prefix[nseq];
+    int grid = gridDim.x;
+    if (p.target_keys > 0) {
+        const int64_t per_cta = (int64_t(p.target_keys) + stage_keys - 1) / stage_keys;
+        const int64_t want = (total + per_cta - 1) / per_cta;
+        grid = want < 1 ? 1 : (want < grid ? static_cast<int>(want) : grid);
+    }
+    // every CTA of the effective grid must own at least one stage, so that the
+    // CTAs [bf, bl] of a sequence are exactly its pieces
+    if (total < grid)
+        grid = static_cast<int>(total);
+    const int b = blockIdx.x;
+    if (b >= grid)
+        return;  // whole CTA (uniform): not needed for this batch
+    const int64_t lo = int64_t(b) * total / grid;
+    const int64_t hi = int64_t(b + 1) * total / grid;
+    if (lo >= hi)
+        return;  // whole CTA (uniform): no stage falls in its range
+    // first sequence of the range: the largest s with prefix[s] <= lo
+    int s_first;
+    {
+        int a = 0, e = nseq;
+        while (e - a > 1) {
+            const int mid = (a + e) >> 1;
+            if (prefix[mid] <= lo)
+                a = mid;
+            else
+                e = mid;
+        }
+        s_first = a;
+    }
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < Cfg::kStages; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kConsumerWarps);
         }
+        *abort_flag = 0;
+        *last_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
+        // lane = one (unit, K|V, 64-dim half) box of every stage; its block id is
+        // looked up for the next stage before waiting for a free slot
         if (lane == 0)
             tma_prefetch_desc(&kv_map);
         const uint64_t policy = l2_policy_evict_first();
-        const int32_t *bt = p.block_table + static_cast<int64_t>(s) * p.bt_stride;
-        constexpr int kOps = kConsumerWarps * 2 * Cfg::kHalves;  // (unit, K|V, half)
-        for (int i = 0; i < nstage; ++i) {
-            const int slot = i % Cfg::kStages;
-            const int round = i / Cfg::kStages;
-            if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1))
-                break;
-            const int k0 = key_begin + i * stage_keys;
-            const int slices = min(R, (key_end - k0 + 15) / 16);
-            if (lane == 0)
-                mbar_arrive_expect_tx(&full[slot],
-                                      static_cast<uint32_t>(slices * Hkv * 2 * Cfg::kUnitBytes));
-            __syncwarp();
-            uint8_t *stage = smem + slot * Cfg::kStageBytes;
-            for (int op = lane; op < kOps; op += 32) {
-                const int u = op % kConsumerWarps;
-                const int kv = (op / kConsumerWarps) & 1;
-                const int half = op / (2 * kConsumerWarps);
-                const int r = u / Hkv;
-                const int k = u % Hkv;
+        constexpr int kOps = kConsumerWarps * 2 * Cfg::kHalves;  // <= 32
+        const int u = lane % kConsumerWarps;
+        const int kv = (lane / kConsumerWarps) & 1;
+        const int half = lane / (2 * kConsumerWarps);
+        const int r = u / Hkv;
+        const int k = u % Hkv;
+        int s = s_first;
+        auto lookup = [&](int64_t x, int seq, int &row, int &slices) {
+            const int L = p.seq_lens[p.seq0 + seq];
+            const int k0 = p.kv_begin + int(x - prefix[seq]) * stage_keys;
+            slices = max(0, min(R, (L - k0 + 15) / 16));
+            row = -1;
+            if (lane < kOps && r < slices) {
                 const int ks = k0 + 16 * r;
-                if (r >= slices)
-                    continue;
                 const int col = ks / p.block_size;
+                const int32_t *bt = p.block_table + int64_t(p.seq0 + seq) * p.bt_stride;
                 int blk = col < p.bt_stride ? bt[col] : -1;
                 if (blk < 0 || blk >= p.num_blocks) {
                     flag_error(kErrBlockOutOfPool);
                     blk = 0;  // keep the transaction count whole; result is flagged
                 }
-                const int row = (blk * 2 + kv) * p.block_size + (ks % p.block_size);
-                uint8_t *dst = stage + kv * Cfg::kKvBytes + u * Cfg::kUnitBytes + half * 2048;
+                row = (blk * 2 + kv) * p.block_size + (ks % p.block_size);
+            }
+        };
+        int row_next, slices_next;
+        lookup(lo, s, row_next, slices_next);
+        for (int64_t x = lo; x < hi; ++x) {
+            const int i = int(x - lo);
+            const int row = row_next, slices = slices_next;
+            if (x + 1 < hi) {
+                while (prefix[s + 1] <= x + 1)
+                    ++s;
+                lookup(x + 1, s, row_next, slices_next);
+            }
+            const int slot = i % Cfg::kStages;
+            const int round = i / Cfg::kStages;
+            if (round > 0 && !dec_wait(&empty[slot], (round - 1) & 1, abort_flag))
+                break;
+            if (lane == 0)
+                mbar_arrive_expect_tx(&full[slot],
+                                      static_cast<uint32_t>(slices * Hkv * 2 * Cfg::kUnitBytes));
+            __syncwarp();
+            if (row >= 0) {
+                uint8_t *dst = smem + slot * Cfg::kStageBytes + kv * Cfg::kKvBytes +
+                               u * Cfg::kUnitBytes + half * 2048;
                 tma_load_3d(dst, &kv_map, &full[slot], half * 64, k, row, policy);
             }
         }
@@ -200,28 +308,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const int k = u % Hkv;
     const int r = u / Hkv;
     const int g = p.group;
-    const int tq = lane & 3;  // thread-in-quad
+    const int tq = lane & 3;   // thread-in-quad
     const int gq = lane >> 2;  // quad index
-
-    // Q^T as B fragments: column n = query head k*g + gq, rows = dims.
-    uint32_t qf[D / 16][2];
-    {
-        const bool live = gq < g;
-        const uint32_t *qrow =
-            p.query + ((static_cast<int64_t>(t) * p.num_heads + k * g + (live ? gq : 0)) * D) / 2;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            qf[kk][0] = live ? __ldg(qrow + (16 * kk + 2 * tq) / 2) : 0u;
-            qf[kk][1] = live ? __ldg(qrow + (16 * kk + 8 + 2 * tq) / 2) : 0u;
-        }
-    }
-
-    float o[D / 16][4];
-#pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt)
-        o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-    float m0 = kNegInf, m1 = kNegInf, l0 = 0.f, l1 = 0.f;
-    bool ok = true;
+    const int H = p.num_heads;
 
     // ldmatrix lane addressing (rows = keys of the unit tile)
     const uint32_t k_row = (lane & 7) + ((lane >> 3) & 1) * 8;  // K: non-transposed A
@@ -229,15 +318,46 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const uint32_t v_row = (lane & 7) + (lane >> 4) * 8;  // V: transposed A
     const uint32_t v_chunk = (lane >> 3) & 1;
 
-    for (int i = 0; i < nstage; ++i) {
-        const int slot = i % Cfg::kStages;
-        if (!mbar_wait(&full[slot], (i / Cfg::kStages) & 1)) {
-            ok = false;
-            break;
+    uint32_t qf[D / 16][2];
+    float o[D / 16][4];
+    float m0, m1, l0, l1;
+    int s = s_first;
+    int t = 0, L = 0;
+    bool ok = true;
+    auto begin_piece = [&]() {
+        t = p.qsl[p.seq0 + s];
+        L = p.seq_lens[p.seq0 + s];
+        if (t < 0 || t >= p.num_tokens) {
+            flag_error(kErrBadMetadata);
+            t = 0;
         }
-        const int ks = key_begin + i * stage_keys + 16 * r;
-        const int valid = min(16, key_end - ks);
-        if (valid > 0) {
+        if (p.kv_begin > 0 && L <= p.kv_begin)
+            flag_error(kErrBadMetadata);  // a cascade decode must come after the prefix
+        // Q^T as B fragments: column n = query head k*g + gq, rows = dims
+        const bool live = gq < g;
+        const uint32_t *qrow =
+            p.query + ((static_cast<int64_t>(t) * H + k * g + (live ? gq : 0)) * D) / 2;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            qf[kk][0] = live ? __ldg(qrow + (16 * kk + 2 * tq) / 2) : 0u;
+            qf[kk][1] = live ? __ldg(qrow + (16 * kk + 8 + 2 * tq) / 2) : 0u;
+        }
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt)
+            o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        m0 = m1 = kNegInf;
+        l0 = l1 = 0.f;
+    };
+    begin_piece();
+
+    for (int64_t x = lo; x < hi; ++x) {
+        const int i = int(x - lo);
+        const int slot = i % Cfg::kStages;
+        if (ok && !dec_wait(&full[slot], (i / Cfg::kStages) & 1, abort_flag))
+            ok = false;
+        const int ks = p.kv_begin + int(x - prefix[s]) * stage_keys + 16 * r;
+        const int valid = min(16, L - ks);
+        if (ok && valid > 0) {
             const uint32_t kbase =
                 smem_addr(smem + slot * Cfg::kStageBytes + u * Cfg::kUnitBytes);
             const uint32_t vbase = kbase + Cfg::kKvBytes;
@@ -284,204 +404,186 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             }
         }
         __syncwarp();
-        if (lane == 0)
+        if (ok && lane == 0)
             mbar_arrive(&empty[slot]);
-    }
 
-    l0 = warp_sum_heads(l0);
-    l1 = warp_sum_heads(l1);
-
-    // ------------------------------------------------------------ finalise
-    consumer_sync();  // every warp is done with the stage buffers
-    float *scr = reinterpret_cast<float *>(smem) + warp * Cfg::kScratchFloats;
-    if (gq == 0) {
-        scr[2 * tq] = m0;
-        scr[2 * tq + 1] = m1;
-        scr[8 + 2 * tq] = l0;
-        scr[8 + 2 * tq + 1] = l1;
-    }
-#pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) {
-        const int d = 16 * mt + gq;
-        scr[16 + d * 8 + 2 * tq] = o[mt][0];
-        scr[16 + d * 8 + 2 * tq + 1] = o[mt][1];
-        scr[16 + (d + 8) * 8 + 2 * tq] = o[mt][2];
-        scr[16 + (d + 8) * 8 + 2 * tq + 1] = o[mt][3];
-    }
-    consumer_sync();
-    if (!ok)
-        return;
-
-    const bool direct = (nsplit == 1) && !p.partial_only;
-    const float *all = reinterpret_cast<const float *>(smem);
-    const int total = Hkv * g * D;
-    for (int idx = threadIdx.x; idx < total; idx += kConsumerWarps * 32) {
-        const int d = idx % D;
-        const int hn = idx / D;
-        const int kh = hn / g;
-        const int n = hn - kh * g;
-        float M = kNegInf;
-        for (int rr = 0; rr < R; ++rr)
-            M = fmaxf(M, all[(rr * Hkv + kh) * Cfg::kScratchFloats + n]);
-        float W = 0.f, acc = 0.f;
-        for (int rr = 0; rr < R; ++rr) {
-            const float *w = all + (rr * Hkv + kh) * Cfg::kScratchFloats;
-            const float e = (w[n] == kNegInf) ? 0.f : exp2f(w[n] - M);
-            W += e * w[8 + n];
-            acc += e * w[16 + d * 8 + n];
-        }
-        const int h = kh * g + n;
-        const float val = acc / W;
-        const float lse2 = M + log2f(W);
+        if (x + 1 < hi && x + 1 < prefix[s + 1])
+            continue;  // the piece goes on
+        // ------------------------------------------------------------ end of a piece
+        const float lr0 = warp_sum_heads(l0);
+        const float lr1 = warp_sum_heads(l1);
+        const int bf = cta_of_stage(prefix[s], total, grid);
+        const int bl = cta_of_stage(prefix[s + 1] - 1, total, grid);
+        const int np = bl - bf + 1;
+        const bool direct = np == 1 && R == 1 && !p.cascade;
+        const int n0 = 2 * tq, n1 = 2 * tq + 1;  // the two heads of this thread
+        const float i0 = lr0 > 0.f ? 1.f / lr0 : 0.f;
+        const float i1 = lr1 > 0.f ? 1.f / lr1 : 0.f;
         if (direct) {
-            p.out[(static_cast<int64_t>(t) * p.num_heads + h) * D + d] = __float2bfloat16_rn(val);
-            if (d == 0 && p.lse)
-                p.lse[static_cast<int64_t>(t) * p.num_heads + h] = lse2 * kLn2;
+            if (ok) {
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    const int d = 16 * mt + gq;
+                    if (n0 < g) {
+                        __nv_bfloat16 *dst = p.out + (int64_t(t) * H + k * g + n0) * D;
+                        dst[d] = __float2bfloat16_rn(o[mt][0] * i0);
+                        dst[d + 8] = __float2bfloat16_rn(o[mt][2] * i0);
+                    }
+                    if (n1 < g) {
+                        __nv_bfloat16 *dst = p.out + (int64_t(t) * H + k * g + n1) * D;
+                        dst[d] = __float2bfloat16_rn(o[mt][1] * i1);
+                        dst[d + 8] = __float2bfloat16_rn(o[mt][3] * i1);
+                    }
+                }
+                if (gq == 0 && p.lse) {
+                    if (n0 < g)
+                        p.lse[int64_t(t) * H + k * g + n0] = (m0 + log2f(lr0)) * kLn2;
+                    if (n1 < g)
+                        p.lse[int64_t(t) * H + k * g + n1] = (m1 + log2f(lr1)) * kLn2;
+                }
+            }
         } else {
-            const int64_t row = (static_cast<int64_t>(s) * p.max_splits + split) * p.num_heads + h;
-            p.o_part[row * D + d] = val;
-            if (d == 0)
-                p.lse_part[row] = lse2;
+            const int slot_id = b + s;  // unique per (CTA, sequence) piece
+            const int64_t prow = (int64_t(slot_id) * R + r) * H + k * g;
+            if (ok) {
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    const int d = 16 * mt + gq;
+                    if (n0 < g) {
+                        float *dst = p.o_part + (prow + n0) * D;
+                        dst[d] = o[mt][0] * i0;
+                        dst[d + 8] = o[mt][2] * i0;
+                    }
+                    if (n1 < g) {
+                        float *dst = p.o_part + (prow + n1) * D;
+                        dst[d] = o[mt][1] * i1;
+                        dst[d + 8] = o[mt][3] * i1;
+                    }
+                }
+                if (gq == 0) {
+                    if (n0 < g)
+                        p.lse_part[prow + n0] = lr0 > 0.f ? m0 + log2f(lr0) : kNegInf;
+                    if (n1 < g)
+                        p.lse_part[prow + n1] = lr1 > 0.f ? m1 + log2f(lr1) : kNegInf;
+                }
+            }
+            __threadfence();
+            consumer_sync();  // all eight warps reach it, failed or not
+            if (threadIdx.x == 0)
+                *last_flag = (atomicAdd(&p.counters[s], 1) == np - 1) ? 1 : 0;
+            consumer_sync();
+            if (*last_flag && !*abort_flag) {
+                // every piece of this sequence is written: merge them
+                __threadfence();
+                const int nparts = np * R;
+                for (int idx = threadIdx.x; idx < H * D; idx += kConsumerWarps * 32) {
+                    const int h = idx / D;
+                    const int d = idx - h * D;
+                    const int64_t row_out = int64_t(t) * H + h;
+                    float M = p.cascade ? __ldcg(p.lse_pre + row_out) : kNegInf;
+                    for (int q = 0; q < nparts; ++q) {
+                        const int64_t row = (int64_t(bf + q / R + s) * R + q % R) * H + h;
+                        M = fmaxf(M, __ldcg(p.lse_part + row));
+                    }
+                    float W = 0.f, acc = 0.f;
+                    if (M != kNegInf) {
+                        for (int q = 0; q < nparts; ++q) {
+                            const int64_t row = (int64_t(bf + q / R + s) * R + q % R) * H + h;
+                            const float lq = __ldcg(p.lse_part + row);
+                            if (lq == kNegInf)
+                                continue;  // an empty part adds nothing, whatever it holds
+                            const float w = exp2f(lq - M);
+                            W += w;
+                            acc += w * __ldcg(p.o_part + row * D + d);
+                        }
+                        if (p.cascade) {
+                            const float lq = __ldcg(p.lse_pre + row_out);
+                            if (lq != kNegInf) {
+                                const float w = exp2f(lq - M);
+                                W += w;
+                                acc += w * __ldcg(p.o_pre + row_out * D + d);
+                            }
+                        }
+                    }
+                    p.out[row_out * D + d] = __float2bfloat16_rn(W > 0.f ? acc / W : 0.f);
+                    if (d == 0 && p.lse)
+                        p.lse[row_out] = W > 0.f ? (M + log2f(W)) * kLn2 : kNegInf;
+                }
+            }
+        }
+        if (x + 1 < hi) {
+            ++s;
+            begin_piece();
         }
     }
 }
 
 // --------------------------------------------------------------------- combine
+// Cascade only: every prefill token's suffix partial (from the prefill kernel)
+// merged with its shared-prefix partial -- the log-sum-exp merge of two parts.
+// One warp per (token, head) row, lanes along head_size.
 struct CombineParams {
-    const int32_t *qsl;
-    const int32_t *seq_lens;
     int32_t num_tokens;
     int32_t num_decodes;
     int32_t num_heads;
-    int32_t split_tokens;
-    int32_t max_splits;
-    int32_t kv_begin;
-    int32_t with_prefix;
-    const float *o_part;   // decode split partials
-    const float *lse_part;
-    const float *o_pre;    // cascade: shared-prefix partial of every token [T, H, D]
+    const float *o_pre;  // [T, H, D]
     const float *lse_pre;
-    const float *o_suf;    // cascade: suffix partial of every prefill token
+    const float *o_suf;  // [T - num_decodes, H, D]
     const float *lse_suf;
     __nv_bfloat16 *out;
     float *lse;
 };
 
-// One warp per (token, head) row: warp-shuffle max and sum of the parts'
-// log2-sum-exp values, then the weighted sum of their normalised partial
-// outputs -- the cascade merge, over n parts.  Parts of a decode token: its
-// splits (and the shared prefix in a cascade); of a prefill token in a
-// cascade: its suffix and the shared prefix.
 template <int D>
-__global__ void __launch_bounds__(256) decode_combine_kernel(const CombineParams p)
+__global__ void __launch_bounds__(256) cascade_prefill_combine_kernel(const CombineParams p)
 {
     constexpr int kPer = D / 32;
     const int64_t gw = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t nrows = int64_t(p.with_prefix ? p.num_tokens : p.num_decodes) * p.num_heads;
+    const int64_t nrows = int64_t(p.num_tokens - p.num_decodes) * p.num_heads;
     if (gw >= nrows)
         return;
-    const int t = static_cast<int>(gw / p.num_heads);  // decode s owns token s
-    const int h = static_cast<int>(gw - int64_t(t) * p.num_heads);
-    const int64_t row = int64_t(t) * p.num_heads + h;
-    const float *parts_o[2];
-    float parts_l[2];
-    int nextra = 0;
-    if (p.with_prefix) {
-        parts_o[nextra] = p.o_pre + row * D;
-        parts_l[nextra++] = p.lse_pre[row];
-    }
-    int n = 0;
-    int64_t base = 0;
-    if (t < p.num_decodes) {
-        const int L = p.seq_lens[t];
-        n = max(0, (L - p.kv_begin + p.split_tokens - 1) / p.split_tokens);
-        if (n <= 1 && !p.with_prefix)
-            return;  // finished by the decode kernel itself
-        if (n > p.max_splits || p.qsl[t] != t)
-            return;  // flagged by the decode kernel
-        base = int64_t(t) * p.max_splits * p.num_heads + h;
-    } else {
-        const int64_t srow = int64_t(t - p.num_decodes) * p.num_heads + h;
-        parts_o[nextra] = p.o_suf + srow * D;
-        parts_l[nextra++] = p.lse_suf[srow];
-    }
-    float mx = kNegInf;
-    for (int e = 0; e < nextra; ++e)
-        mx = fmaxf(mx, parts_l[e]);
-    for (int j = lane; j < n; j += 32)
-        mx = fmaxf(mx, p.lse_part[base + int64_t(j) * p.num_heads]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float acc[kPer];
-#pragma unroll
-    for (int e = 0; e < kPer; ++e)
-        acc[e] = 0.f;
-    float ws = 0.f;
+    const int64_t srow = gw;
+    const int64_t row = int64_t(p.num_decodes) * p.num_heads + gw;
+    const float la = p.lse_suf[srow], lb = p.lse_pre[row];
+    const float mx = fmaxf(la, lb);
+    float wa = 0.f, wb = 0.f;
     if (mx != kNegInf) {
-        for (int j = lane; j < n; j += 32)
-            ws += exp2f(p.lse_part[base + int64_t(j) * p.num_heads] - mx);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            ws += __shfl_xor_sync(0xffffffffu, ws, o);
-        for (int j = 0; j < n; ++j) {
-            const int64_t prow = base + int64_t(j) * p.num_heads;
-            const float w = exp2f(p.lse_part[prow] - mx);
-            const float *src = p.o_part + prow * D + lane * kPer;
-#pragma unroll
-            for (int e = 0; e < kPer; ++e)
-                acc[e] += w * src[e];
-        }
-        for (int x = 0; x < nextra; ++x) {
-            if (parts_l[x] == kNegInf)
-                continue;  // an empty part contributes nothing, whatever it holds
-            const float w = exp2f(parts_l[x] - mx);
-            ws += w;
-            const float *src = parts_o[x] + lane * kPer;
-#pragma unroll
-            for (int e = 0; e < kPer; ++e)
-                acc[e] += w * src[e];
-        }
+        wa = la == kNegInf ? 0.f : exp2f(la - mx);
+        wb = lb == kNegInf ? 0.f : exp2f(lb - mx);
     }
+    const float ws = wa + wb;
     const float inv = ws > 0.f ? 1.f / ws : 0.f;
+    const float *a = p.o_suf + srow * D + lane * kPer;
+    const float *bb = p.o_pre + row * D + lane * kPer;
     __nv_bfloat16 *dst = p.out + row * D + lane * kPer;
 #pragma unroll
-    for (int e = 0; e < kPer; e += 2)
-        *reinterpret_cast<__nv_bfloat162 *>(dst + e) =
-            __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+    for (int e = 0; e < kPer; e += 2) {
+        const float x0 = (wa > 0.f ? wa * a[e] : 0.f) + (wb > 0.f ? wb * bb[e] : 0.f);
+        const float x1 = (wa > 0.f ? wa * a[e + 1] : 0.f) + (wb > 0.f ? wb * bb[e + 1] : 0.f);
+        *reinterpret_cast<__nv_bfloat162 *>(dst + e) = __floats2bfloat162_rn(x0 * inv, x1 * inv);
+    }
     if (lane == 0 && p.lse)
         p.lse[row] = ws > 0.f ? (mx + log2f(ws)) * kLn2 : kNegInf;
 }
 
 // --------------------------------------------------------------------- host
-DecodePlan plan_decode(int32_t requested_split, int32_t num_decodes, int32_t max_seq_len,
-                       int32_t kv_begin, int32_t num_kv_heads, int num_sms)
+DecodePlan plan_decode(int32_t split_kv_tokens, int32_t num_decodes, int32_t num_kv_heads,
+                       int num_sms)
 {
     DecodePlan dp;
     dp.stage_keys = 16 * (kConsumerWarps / num_kv_heads);
-    const int64_t span = std::max<int64_t>(1, int64_t(max_seq_len) - kv_begin);
-    int64_t split;
-    if (requested_split > 0) {
-        split = requested_split;
-    } else {
-        // About eight CTAs per SM over the batch, taking the mean decode length
-        // as 60% of the longest; at least four stages per CTA.
-        const double total = 0.6 * double(num_decodes) * double(span);
-        split = static_cast<int64_t>(total / (8.0 * std::max(1, num_sms))) + 1;
-        split = std::max<int64_t>(split, 4 * dp.stage_keys);
-    }
-    split = (split + dp.stage_keys - 1) / dp.stage_keys * dp.stage_keys;
-    split = std::min<int64_t>(split, (span + dp.stage_keys - 1) / dp.stage_keys * dp.stage_keys);
-    dp.split_tokens = static_cast<int32_t>(split);
-    dp.max_splits = static_cast<int32_t>((span + split - 1) / split);
+    dp.grid = std::max(1, num_sms);
+    dp.chunk = std::min(num_decodes, kMaxDecodeChunk);
+    dp.target_keys = split_kv_tokens;
+    dp.rows_per_slot = kConsumerWarps / num_kv_heads;
     return dp;
 }
 
 template <int D>
 static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Workspace &ws,
                                    char *wsp, const CUtensorMap &kv_map, int32_t kv_begin,
-                                   bool partial_only)
+                                   bool cascade)
 {
     using Cfg = DecodeCfg<D>;
     static int configured_device = -1;
@@ -507,61 +609,65 @@ static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Wor
     p.group = f.num_heads / f.num_kv_heads;
     p.block_size = f.block_size;
     p.num_blocks = static_cast<int32_t>(f.num_blocks);
-    p.split_tokens = dp.split_tokens;
-    p.max_splits = dp.max_splits;
     p.kv_begin = kv_begin;
-    p.partial_only = partial_only ? 1 : 0;
+    p.target_keys = dp.target_keys;
+    p.cascade = cascade ? 1 : 0;
     p.scale_log2 = f.scale * 1.4426950408889634f;
     p.out = static_cast<__nv_bfloat16 *>(f.out);
     p.lse = f.lse;
     p.o_part = reinterpret_cast<float *>(wsp + ws.o_part);
     p.lse_part = reinterpret_cast<float *>(wsp + ws.lse_part);
-    dim3 grid(dp.max_splits, f.num_decodes);
-    count_launch();
-    paged_decode_kernel<D><<<grid, kDecodeThreads, Cfg::kSmemBytes, f.stream>>>(kv_map, p);
-    return cudaGetLastError();
+    p.counters = reinterpret_cast<int32_t *>(wsp + ws.counters);
+    p.o_pre = reinterpret_cast<const float *>(wsp + ws.o_pre);
+    p.lse_pre = reinterpret_cast<const float *>(wsp + ws.lse_pre);
+    // one launch per chunk of at most kMaxDecodeChunk decodes (stream ordered,
+    // so chunks reuse the same partial slots and counters)
+    for (int32_t seq0 = 0; seq0 < f.num_decodes; seq0 += dp.chunk) {
+        p.seq0 = seq0;
+        p.nseq = std::min(dp.chunk, f.num_decodes - seq0);
+        cudaError_t e = cudaMemsetAsync(p.counters, 0, size_t(p.nseq) * 4, f.stream);
+        if (e != cudaSuccess)
+            return e;
+        count_launch();
+        paged_decode_kernel<D><<<dp.grid, kDecodeThreads, Cfg::kSmemBytes, f.stream>>>(kv_map, p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_decode(const Fwd &f, const DecodePlan &dp, const Workspace &ws, char *wsp,
-                          const CUtensorMap &kv_map, int32_t kv_begin, bool partial_only)
+                          const CUtensorMap &kv_map, int32_t kv_begin, bool cascade)
 {
     if (f.num_decodes == 0)
         return cudaSuccess;
     if (f.head_size == 128)
-        return launch_decode_d<128>(f, dp, ws, wsp, kv_map, kv_begin, partial_only);
-    return launch_decode_d<64>(f, dp, ws, wsp, kv_map, kv_begin, partial_only);
+        return launch_decode_d<128>(f, dp, ws, wsp, kv_map, kv_begin, cascade);
+    return launch_decode_d<64>(f, dp, ws, wsp, kv_map, kv_begin, cascade);
 }
 
-cudaError_t launch_decode_combine(const Fwd &f, const DecodePlan &dp, const Workspace &ws,
-                                  char *wsp, int32_t kv_begin, bool with_prefix)
+cudaError_t launch_cascade_prefill_combine(const Fwd &f, const Workspace &ws, char *wsp)
 {
-    if (!with_prefix && (f.num_decodes == 0 || dp.max_splits <= 1))
+    const int64_t warps = int64_t(f.num_tokens - f.num_decodes) * f.num_heads;
+    if (warps == 0)
         return cudaSuccess;
     CombineParams p;
-    p.qsl = f.qsl;
-    p.seq_lens = f.seq_lens;
     p.num_tokens = f.num_tokens;
     p.num_decodes = f.num_decodes;
     p.num_heads = f.num_heads;
-    p.split_tokens = dp.split_tokens;
-    p.max_splits = dp.max_splits;
-    p.kv_begin = kv_begin;
-    p.with_prefix = with_prefix ? 1 : 0;
-    p.o_part = reinterpret_cast<const float *>(wsp + ws.o_part);
-    p.lse_part = reinterpret_cast<const float *>(wsp + ws.lse_part);
     p.o_pre = reinterpret_cast<const float *>(wsp + ws.o_pre);
     p.lse_pre = reinterpret_cast<const float *>(wsp + ws.lse_pre);
     p.o_suf = reinterpret_cast<const float *>(wsp + ws.o_suf);
     p.lse_suf = reinterpret_cast<const float *>(wsp + ws.lse_suf);
     p.out = static_cast<__nv_bfloat16 *>(f.out);
     p.lse = f.lse;
-    const int64_t warps = int64_t(with_prefix ? f.num_tokens : f.num_decodes) * f.num_heads;
     const unsigned grid = static_cast<unsigned>((warps * 32 + 255) / 256);
     count_launch();
     if (f.head_size == 128)
-        decode_combine_kernel<128><<<grid, 256, 0, f.stream>>>(p);
+        cascade_prefill_combine_kernel<128><<<grid, 256, 0, f.stream>>>(p);
     else
-        decode_combine_kernel<64><<<grid, 256, 0, f.stream>>>(p);
+        cascade_prefill_combine_kernel<64><<<grid, 256, 0, f.stream>>>(p);
     return cudaGetLastError();
 }
 

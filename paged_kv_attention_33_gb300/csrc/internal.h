@@ -37,23 +37,26 @@ struct Fwd {
     int num_sms;
 };
 
-// Split-KV plan of the decode part of a batch.
+// Plan of the decode part of a batch (persistent stream-K grid).
 struct DecodePlan {
-    int32_t stage_keys;    // keys per pipeline stage (16 * 8/num_kv_heads)
-    int32_t split_tokens;  // keys per split, a multiple of stage_keys
-    int32_t max_splits;    // ceil(max decode KV length / split_tokens)
+    int32_t stage_keys;     // keys per pipeline stage (16 * 8/num_kv_heads)
+    int32_t grid;           // CTAs of the persistent grid (SM count)
+    int32_t chunk;          // decodes per launch (at most 4096)
+    int32_t target_keys;    // 0, or keys per CTA to aim for (fewer CTAs)
+    int32_t rows_per_slot;  // partial rows per (CTA, sequence) piece and head: 8/num_kv_heads
 };
 
 // Workspace carve-up (byte offsets from the workspace base, 256-aligned).
 struct Workspace {
-    size_t o_part, lse_part;   // decode split partials
+    size_t o_part, lse_part;   // decode piece partials
+    size_t counters;           // pieces finished per decode (int32)
     size_t o_pre, lse_pre;     // cascade: shared-prefix partial of every token
     size_t o_suf, lse_suf;     // cascade: suffix partial of every prefill token
     size_t total;
 };
 
-DecodePlan plan_decode(int32_t requested_split, int32_t num_decodes, int32_t max_seq_len,
-                       int32_t kv_begin, int32_t num_kv_heads, int num_sms);
+DecodePlan plan_decode(int32_t split_kv_tokens, int32_t num_decodes, int32_t num_kv_heads,
+                       int num_sms);
 Workspace plan_workspace(const DecodePlan &dp, int32_t num_tokens, int32_t num_decodes,
                          int32_t num_heads, int32_t head_size, bool cascade);
 
@@ -64,16 +67,13 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *c
                                      int32_t block_size, int64_t num_blocks, cudaStream_t st);
 uint32_t kv_write_take_error();
 
-// decode.cu: split-KV decode over sequences [0, num_decodes) and keys
-// [kv_begin, L_s).  partial_only: write fp32 partials for every split (the
-// cascade merges them later) instead of finishing single-split sequences.
+// decode.cu: paged decode of sequences [0, num_decodes) over keys
+// [kv_begin, L_s), stream-K over a persistent grid with the split combine
+// fused in; cascade: every row is also merged with its shared-prefix partial.
 cudaError_t launch_decode(const Fwd &f, const DecodePlan &dp, const Workspace &ws, char *wsp,
-                          const CUtensorMap &kv_map, int32_t kv_begin, bool partial_only);
-// Merge the decode split partials into out/lse for the decode tokens; for a
-// cascade (with_prefix) also merge every token with its shared-prefix partial
-// (decode tokens: splits + prefix; prefill tokens: suffix partial + prefix).
-cudaError_t launch_decode_combine(const Fwd &f, const DecodePlan &dp, const Workspace &ws,
-                                  char *wsp, int32_t kv_begin, bool with_prefix);
+                          const CUtensorMap &kv_map, int32_t kv_begin, bool cascade);
+// Cascade: merge every prefill token's suffix partial with its prefix partial.
+cudaError_t launch_cascade_prefill_combine(const Fwd &f, const Workspace &ws, char *wsp);
 uint32_t decode_take_error();
 
 // merge.cu

@@ -72,8 +72,9 @@ extern "C" pka_status pka_paged_attn_forward_noalloc(
             return PKA_ERR_CUDA;
         }
     }
-    // The partial results are written in full before they are read, so the
-    // leftovers of an earlier call need no clearing.
+    // The forward zeroes the per-sequence counters it keeps in the scratch on
+    // every call and writes the partial results in full before reading them,
+    // so an earlier call's leftovers do no harm.
     return pka_paged_attn_forward(query, kv_cache, meta, out, lse, num_tokens, num_heads,
                                   num_kv_heads, head_size, block_size, num_blocks, scale, causal,
                                   scratch, need > 0 ? pka::kNoallocScratchBytes : 0, stream);

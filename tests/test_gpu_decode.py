@@ -1,5 +1,8 @@
-"""GPU parity of the cache write and the split-KV decode path against the fp64
-oracle (all calls go through the C ABI)."""
+"""GPU parity of the cache write and the stream-K split-KV decode path against
+the fp64 oracle (all calls go through the C ABI).  split_kv_tokens sets the
+keys per CTA: small values spread a sequence over many CTAs (fused merge of
+many pieces), 1 << 30 puts the whole batch on one CTA (every sequence one
+piece)."""
 import numpy as np
 import pytest
 
@@ -18,7 +21,7 @@ def test_tiny_decode_named(oracle):
     G.check_batch(oracle, b, label="tiny_decode")
 
 
-@pytest.mark.parametrize("split", [0, 64, 128, 192])
+@pytest.mark.parametrize("split", [0, 64, 128, 192, 1 << 30])
 def test_tiny_decode_forced_splits(oracle, split):
     b = W.make_batch(W.named_spec("tiny_decode"), seed=2002)
     G.check_batch(oracle, b, split_kv_tokens=split, label=f"split {split}")
@@ -38,7 +41,7 @@ EDGE_CTX = [0, 14, 15, 16, 31, 32, 63, 64, 65, 127, 128, 129, 200, 511]
 ])
 def test_decode_edges(oracle, H, Hkv, D, bs):
     b = W.make_batch(_spec(H, Hkv, D, bs, EDGE_CTX, table_pad=3), seed=2100 + H + Hkv + bs)
-    for split in (0, 16 * (8 // Hkv), 48 * (8 // Hkv)):
+    for split in (0, 16 * (8 // Hkv), 48 * (8 // Hkv), 1 << 30):
         G.check_batch(oracle, b, split_kv_tokens=split, label=f"split {split}")
 
 
@@ -46,8 +49,9 @@ def test_decode_many_splits_ragged(oracle):
     rng = np.random.Generator(np.random.PCG64(5))
     ctx = rng.integers(1, 3000, size=24).tolist()
     b = W.make_batch(_spec(32, 8, 128, 16, ctx), seed=2200)
-    G.check_batch(oracle, b, split_kv_tokens=64, label="64-key splits")
-    G.check_batch(oracle, b, label="auto split")
+    G.check_batch(oracle, b, split_kv_tokens=64, label="64 keys per CTA")
+    G.check_batch(oracle, b, split_kv_tokens=1000, label="1000 keys per CTA")
+    G.check_batch(oracle, b, label="auto")
 
 
 def test_decode_heavy_full_size_sampled(oracle):

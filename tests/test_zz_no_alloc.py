@@ -75,10 +75,12 @@ def test_noalloc_rejects_batches_above_its_scratch():
     """A batch whose partials need more than the built-in 16 MiB is refused
     with PKA_ERR_WORKSPACE before anything is enqueued."""
     lib = pka.load_library()
-    m = pka._CMeta(16, 16, 16, 1024, 256, 256, 1, 16384, 0, 16)
-    need = lib.pka_workspace_size(ctypes.byref(m), 256, 32, 8, 128, 16)
+    # a cascade over 8192 prefill tokens: the shared-prefix partials alone are
+    # 8192 x 32 heads x 128 x 4 bytes
+    m = pka._CMeta(16, 16, 16, 1024, 2, 0, 4096, 16384, 16, 0)
+    need = lib.pka_workspace_size(ctypes.byref(m), 8192, 32, 8, 128, 16)
     assert need > 16 << 20
-    rc = lib.pka_paged_attn_forward_noalloc(256, 512, ctypes.byref(m), 1024, None, 256, 32, 8,
+    rc = lib.pka_paged_attn_forward_noalloc(256, 512, ctypes.byref(m), 1024, None, 8192, 32, 8,
                                             128, 16, 100000, 0.088, 1, None)
     assert rc == -3
     msg = lib.pka_last_error().decode()
