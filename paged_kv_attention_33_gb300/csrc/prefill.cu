@@ -13,8 +13,9 @@
 // SM, items round-robin, the heaviest causal tiles of each sequence first).
 // Roles (384 threads, three warpgroups):
 //   warp 0      TMA producer: Q tiles once per item, K and V tiles of 128 keys
-//               into a two-stage ring, one TMA box per page straight from the
-//               pool (128-byte swizzled), block ids looked up one per lane;
+//               into two-stage rings (K one tile ahead of V, each freed by its
+//               own barrier), one TMA box per page straight from the pool
+//               (128-byte swizzled), block ids looked up one per lane;
 //   warp 1      MMA issuer (one thread).  Per K/V tile j it issues
 //                 PV_A(j-1), S_A(j), PV_B(j-1), S_B(j)
 //               so that while one softmax warpgroup works on its S tile the
@@ -214,7 +215,7 @@ __device__ __forceinline__ void reg_alloc()
 }
 
 struct PfBars {
-    uint64_t *q_full, *q_empty, *k_full, *v_full, *kv_empty;
+    uint64_t *q_full, *q_empty, *k_full, *v_full, *k_empty, *v_empty;
     uint64_t *s_full, *p_full, *o_done, *o_free;  // [2] each: tile A, tile B
     uint64_t *drain;
 };
@@ -408,7 +409,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     bars.q_empty = b + 1;
     bars.k_full = b + 2;     // [kPfStages]
     bars.v_full = b + 4;     // [kPfStages]
-    bars.kv_empty = b + 6;   // [kPfStages]
+    bars.k_empty = b + 6;    // [kPfStages]: K tile free once the S MMAs read it
+    bars.v_empty = b + 18;   // [kPfStages]: V tile free once the PV MMAs read it
     bars.s_full = b + 8;     // [2]
     bars.p_full = b + 10;    // [2]
     bars.o_done = b + 12;    // [2]
@@ -461,7 +463,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int i = 0; i < kPfStages; ++i) {
             mbar_init(&bars.k_full[i], 1);
             mbar_init(&bars.v_full[i], 1);
-            mbar_init(&bars.kv_empty[i], 1);
+            mbar_init(&bars.k_empty[i], 1);
+            mbar_init(&bars.v_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars.s_full[i], 1);
@@ -528,41 +531,49 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                                         &q_map, bars.q_full, hf * 64, it.h, it.t0 + tl * kBM,
                                         pol_q);
                 }
-                bool stop = false;
-                for (int jt = 0; jt < it.n_kv_all; ++jt, ++kv_it) {
-                    const int blk = blk_next;
-                    if (jt + 1 < it.n_kv_all)
-                        blk_next = lane_block(jt + 1);
-                    const int st = kv_it % kPfStages;
-                    const uint32_t rnd = kv_it / kPfStages;
-                    if (rnd > 0 && !pf_wait(&bars.kv_empty[st], (rnd - 1) & 1, abort_flag)) {
-                        stop = true;
-                        break;
-                    }
+                // K runs one tile ahead of V: K(j+1) is issued before V(j), and
+                // each has its own free barrier, so the next K tile streams in
+                // while the PV MMAs of the current tile still hold V
+                const uint32_t kv_base = kv_it;
+                auto issue = [&](int which, int jt, int blk) -> bool {
+                    const uint32_t n = kv_base + jt;
+                    const int st = n % kPfStages;
+                    const uint32_t rnd = n / kPfStages;
+                    uint64_t *emp = which ? &bars.v_empty[st] : &bars.k_empty[st];
+                    if (rnd > 0 && !pf_wait(emp, (rnd - 1) & 1, abort_flag))
+                        return false;
                     const int key0 = p.kv_lo + jt * kBN;
                     const int nbox = (min(kBN, kv_hi - key0) + p.box_rows - 1) / p.box_rows;
                     const uint32_t bytes = nbox * p.box_rows * 128 * Cfg::kHalves;
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(&bars.k_full[st], bytes);
-                        mbar_arrive_expect_tx(&bars.v_full[st], bytes);
-                    }
+                    uint64_t *bar = which ? &bars.v_full[st] : &bars.k_full[st];
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(bar, bytes);
                     __syncwarp();
                     if (lane < nbox) {
                         const int key = key0 + lane * p.box_rows;
-                        const int row_k = (blk * 2) * p.block_size + key % p.block_size;
-                        const int row_v = row_k + p.block_size;
-                        uint8_t *kt =
-                            smem + Cfg::kKOff + st * Cfg::kTileBytes + lane * p.box_rows * 128;
-                        uint8_t *vt =
-                            smem + Cfg::kVOff + st * Cfg::kTileBytes + lane * p.box_rows * 128;
+                        const int row = (blk * 2 + which) * p.block_size + key % p.block_size;
+                        uint8_t *dst = smem + (which ? Cfg::kVOff : Cfg::kKOff) +
+                                       st * Cfg::kTileBytes + lane * p.box_rows * 128;
                         for (int hf = 0; hf < Cfg::kHalves; ++hf)
-                            tma_load_3d(kt + hf * Cfg::kHalfBytes, &kv_map, &bars.k_full[st],
-                                        hf * 64, kvh, row_k, pol_kv);
-                        for (int hf = 0; hf < Cfg::kHalves; ++hf)
-                            tma_load_3d(vt + hf * Cfg::kHalfBytes, &kv_map, &bars.v_full[st],
-                                        hf * 64, kvh, row_v, pol_kv);
+                            tma_load_3d(dst + hf * Cfg::kHalfBytes, &kv_map, bar, hf * 64, kvh,
+                                        row, pol_kv);
                     }
+                    return true;
+                };
+                bool stop = !issue(0, 0, blk_next);
+                for (int jt = 0; jt < it.n_kv_all && !stop; ++jt) {
+                    const int blk_v = blk_next;
+                    if (jt + 1 < it.n_kv_all) {
+                        blk_next = lane_block(jt + 1);
+                        if (!issue(0, jt + 1, blk_next)) {
+                            stop = true;
+                            break;
+                        }
+                    }
+                    if (!issue(1, jt, blk_v))
+                        stop = true;
                 }
+                kv_it += it.n_kv_all;
                 if (stop)
                     break;
                 ++li;
@@ -636,6 +647,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                                            smem_desc_sw128(sV + k * 2048, Cfg::kHalfBytes, 1024),
                                            Cfg::kIdescPV, (jp > 0 || k > 0) ? 1u : 0u);
                                 mma_commit(&bars.o_done[tl]);
+                                if (tl == (jp < it.n_kv[1] ? 1 : 0))
+                                    mma_commit(&bars.v_empty[pst]);  // last reader of V(jp)
                             }
                             __syncwarp();
                         }
@@ -652,18 +665,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                                            k > 0);
                                 }
                                 mma_commit(&bars.s_full[tl]);
+                                if (tl == (jt < it.n_kv[1] ? 1 : 0))
+                                    mma_commit(&bars.k_empty[st]);  // last reader of K(jt)
                             }
                             __syncwarp();
                         }
                     }
                     if (!ok)
                         break;
-                    if (lane == 0) {
-                        if (jt == n - 1)
-                            mma_commit(bars.q_empty);  // Q is free once the last S is done
-                        if (jt > 0)
-                            mma_commit(&bars.kv_empty[(kv_it + jt - 1) % kPfStages]);
-                    }
+                    if (lane == 0 && jt == n - 1)
+                        mma_commit(bars.q_empty);  // Q is free once the last S is done
                     __syncwarp();
                 }
                 if (!ok)
