@@ -420,6 +420,12 @@ def run_ours(args):
     }
     if pf_flops:
         line["prefill_tflops"] = pf_flops / (ms * 1e-3) / 1e12
+    if args.workload != "prefill" and not args.no_prefill:
+        # the metric's second half: prefill TFLOP/s on the varlen prefill workload
+        # (8 prompts, 1024..8192 tokens), timed in the same run
+        del st
+        torch.cuda.empty_cache()
+        line["prefill"] = measure_prefill(args, dev, peaks, peaks_kind)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
 
@@ -435,6 +441,47 @@ def run_ours(args):
 
         dist.destroy_process_group()
     return 0
+
+
+def measure_prefill(args, dev, peaks, peaks_kind):
+    """Prefill workload: step and kernel time (CUDA events on the launching
+    stream, the kernel bracketed by the library), TFLOP/s and the fraction of
+    the measured dense bf16 peak (burst: the kernel is timed on its own)."""
+    import torch
+
+    import paged_kv_attention_33_gb300 as pka
+
+    st = Step("prefill", dev)
+    _, flops = units(st.spec)
+    for _ in range(max(3, args.warmup)):
+        st.run()
+    torch.cuda.synchronize()
+    steps = max(5, min(args.steps, 50))
+    k0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    k1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for e in k0 + k1:
+        e.record()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        pka.set_kernel_events(pka.KERNEL_PREFILL, k0[i], k1[i])
+        st.run()
+    pka.set_kernel_events(pka.KERNEL_PREFILL, None, None)
+    e1.record()
+    torch.cuda.synchronize()
+    pka.check_status()
+    ms, k_ms = max_over_ranks([e0.elapsed_time(e1) / steps,
+                               sum(a.elapsed_time(b) for a, b in zip(k0, k1)) / steps], dev)
+    peak = float(peaks.get("bf16_tflops", PEAKS_FALLBACK["bf16_tflops"]))
+    achieved = flops / (k_ms * 1e-3) / 1e12
+    return {"workload": "prefill", "steps": steps, "flops_per_step": flops,
+            "ms_per_step": ms, "tflops": flops / (ms * 1e-3) / 1e12,
+            "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel", "achieved": achieved,
+                         "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_source": f"{peaks_kind} dense bf16 burst (bf16_tflops)",
+                         "kernel_ms": k_ms, "traffic": None}}
 
 
 def run_profile(args, st):
@@ -471,6 +518,8 @@ def main():
     ap.add_argument("--impl", default="pka", choices=["pka", "reference"])
     ap.add_argument("--workload", default="decode_heavy", choices=list(W.NAMED))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the prefill sub-measurement")
     ap.add_argument("--profile", action="store_true",
                     help="short run for a profiler: W + K steps only")
     ap.add_argument("--max-decodes", type=int, default=None,
