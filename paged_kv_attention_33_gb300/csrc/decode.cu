@@ -153,6 +153,71 @@ __device__ __forceinline__ int cta_of_stage(int64_t x, int64_t total, int grid)
     return static_cast<int>(((x + 1) * grid + total - 1) / total - 1);
 }
 
+// Merge the nparts partials of decode s (token t): part q lives in slot
+// (bf + q / R + s), sub-row q % R; in a cascade the shared-prefix partial of
+// the token is one more part.  Warp w takes heads w, w+8, ...; every load of
+// a part is independent of the others, so they overlap.
+template <int D>
+__device__ __forceinline__ void merge_pieces(const DecodeParams &p, int t, int s, int bf,
+                                             int nparts, int R, int warp, int lane)
+{
+    constexpr int kPer = D / 32;  // dims per lane
+    const int H = p.num_heads;
+    for (int h = warp; h < H; h += kConsumerWarps) {
+        const int64_t row_out = int64_t(t) * H + h;
+        const float l_pre = p.cascade ? __ldcg(p.lse_pre + row_out) : kNegInf;
+        float M = l_pre;
+        for (int q = lane; q < nparts; q += 32)
+            M = fmaxf(M, __ldcg(p.lse_part + (int64_t(bf + q / R + s) * R + q % R) * H + h));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float acc[kPer];
+#pragma unroll
+        for (int e = 0; e < kPer; ++e)
+            acc[e] = 0.f;
+        float W = 0.f;
+        if (M != kNegInf) {
+#pragma unroll 4
+            for (int q = 0; q < nparts; ++q) {
+                const int64_t row = (int64_t(bf + q / R + s) * R + q % R) * H + h;
+                const float lq = __ldcg(p.lse_part + row);
+                // an empty part adds nothing, whatever its row holds
+                const float w = lq == kNegInf ? 0.f : exp2f(lq - M);
+                W += w;
+                const float *src = p.o_part + row * D + lane * kPer;
+                if constexpr (kPer == 4) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
+                    acc[0] += w * v.x;
+                    acc[1] += w * v.y;
+                    acc[2] += w * v.z;
+                    acc[3] += w * v.w;
+                } else {
+                    const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
+                    acc[0] += w * v.x;
+                    acc[1] += w * v.y;
+                }
+            }
+            if (l_pre != kNegInf) {
+                const float w = exp2f(l_pre - M);
+                W += w;
+                const float *src = p.o_pre + row_out * D + lane * kPer;
+#pragma unroll
+                for (int e = 0; e < kPer; ++e)
+                    acc[e] += w * __ldcg(src + e);
+            }
+        }
+        const float inv = W > 0.f ? 1.f / W : 0.f;
+        __nv_bfloat16 *dst = p.out + row_out * D + lane * kPer;
+#pragma unroll
+        for (int e = 0; e < kPer; e += 2)
+            *reinterpret_cast<__nv_bfloat162 *>(dst + e) =
+                __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+        if (lane == 0 && p.lse)
+            p.lse[row_out] = W > 0.f ? (M + log2f(W)) * kLn2 : kNegInf;
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p)
@@ -473,42 +538,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 *last_flag = (atomicAdd(&p.counters[s], 1) == np - 1) ? 1 : 0;
             consumer_sync();
             if (*last_flag && !*abort_flag) {
-                // every piece of this sequence is written: merge them
+                // every piece of this sequence is written: merge them, one warp
+                // per head (warp-shuffle max/sum of the parts' log2-sum-exp,
+                // then the weighted sum of their rows, lanes along head_size)
                 __threadfence();
-                const int nparts = np * R;
-                for (int idx = threadIdx.x; idx < H * D; idx += kConsumerWarps * 32) {
-                    const int h = idx / D;
-                    const int d = idx - h * D;
-                    const int64_t row_out = int64_t(t) * H + h;
-                    float M = p.cascade ? __ldcg(p.lse_pre + row_out) : kNegInf;
-                    for (int q = 0; q < nparts; ++q) {
-                        const int64_t row = (int64_t(bf + q / R + s) * R + q % R) * H + h;
-                        M = fmaxf(M, __ldcg(p.lse_part + row));
-                    }
-                    float W = 0.f, acc = 0.f;
-                    if (M != kNegInf) {
-                        for (int q = 0; q < nparts; ++q) {
-                            const int64_t row = (int64_t(bf + q / R + s) * R + q % R) * H + h;
-                            const float lq = __ldcg(p.lse_part + row);
-                            if (lq == kNegInf)
-                                continue;  // an empty part adds nothing, whatever it holds
-                            const float w = exp2f(lq - M);
-                            W += w;
-                            acc += w * __ldcg(p.o_part + row * D + d);
-                        }
-                        if (p.cascade) {
-                            const float lq = __ldcg(p.lse_pre + row_out);
-                            if (lq != kNegInf) {
-                                const float w = exp2f(lq - M);
-                                W += w;
-                                acc += w * __ldcg(p.o_pre + row_out * D + d);
-                            }
-                        }
-                    }
-                    p.out[row_out * D + d] = __float2bfloat16_rn(W > 0.f ? acc / W : 0.f);
-                    if (d == 0 && p.lse)
-                        p.lse[row_out] = W > 0.f ? (M + log2f(W)) * kLn2 : kNegInf;
-                }
+                merge_pieces<D>(p, t, s, bf, np * R, R, warp, lane);
             }
         }
         if (x + 1 < hi) {
