@@ -269,50 +269,57 @@ __device__ __forceinline__ void pf_softmax(const PrefillParams &p, const int32_t
             tmem_wait_ld();
             const int lim = hi_row - (p.kv_lo + jt * kBN);  // columns c < lim admitted
             const bool full_tile = __all_sync(0xffffffffu, lim >= kBN);
-            // row max of the raw logits (four chains); the scale is positive so
-            // max and scaling commute
+            // row max of the raw logits: three-input max, four chains; the scale
+            // is positive so max and scaling commute
             float mx4[4] = {kPfNegInf, kPfNegInf, kPfNegInf, kPfNegInf};
-            if (full_tile) {
+            if (!full_tile) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(x[c][i]));
-            } else {
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float v = c * 32 + i < lim ? __uint_as_float(x[c][i]) : kPfNegInf;
-                        x[c][i] = __float_as_uint(v);
-                        mx4[i & 3] = fmaxf(mx4[i & 3], v);
-                    }
+                        if (c * 32 + i >= lim)
+                            x[c][i] = __float_as_uint(kPfNegInf);
             }
-            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; i += 2)
+                    mx4[(i >> 1) & 3] = fmax3(mx4[(i >> 1) & 3], __uint_as_float(x[c][i]),
+                                              __uint_as_float(x[c][i + 1]));
+            const float mx = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]) * p.scale_log2;
             // The reference max m moves only when the row max passes it by more
             // than the threshold: every p stays <= 2^8 and the O rescale in TMEM
             // is rare.  Exact either way: lse and 1/l use the same reference.
             const float m_new = mx > m + kRescaleThreshold ? mx : m;
             const float base = m_new == kPfNegInf ? 0.f : m_new;
-            float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+            // p = 2^(x*scale - base): the argument two elements at a time
+            // (fma.f32x2), the row sum likewise (add.f32x2), P packed to bf16
+            const uint64_t sl2 = pack_f32x2(p.scale_log2, p.scale_log2);
+            const uint64_t nb2 = pack_f32x2(-base, -base);
+            uint64_t sum2[2] = {pack_f32x2(0.f, 0.f), pack_f32x2(0.f, 0.f)};
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float p0 =
-                        fast_exp2(fmaf(__uint_as_float(x[c][2 * i]), p.scale_log2, -base));
-                    const float p1 =
-                        fast_exp2(fmaf(__uint_as_float(x[c][2 * i + 1]), p.scale_log2, -base));
-                    sum4[(2 * i) & 3] += p0;
-                    sum4[(2 * i + 1) & 3] += p1;
+                    const uint64_t arg = fma_f32x2(
+                        pack_f32x2(__uint_as_float(x[c][2 * i]), __uint_as_float(x[c][2 * i + 1])),
+                        sl2, nb2);
+                    float a0, a1;
+                    unpack_f32x2(arg, a0, a1);
+                    const float p0 = fast_exp2(a0);
+                    const float p1 = fast_exp2(a1);
+                    sum2[i & 1] = add_f32x2(sum2[i & 1], pack_f32x2(p0, p1));
                     pk[i] = pack_bf16x2(p0, p1);
                 }
                 tmem_st16(ts + c * 16, pk);
             }
             tmem_wait_st();
+            float s0, s1, s2, s3;
+            unpack_f32x2(sum2[0], s0, s1);
+            unpack_f32x2(sum2[1], s2, s3);
             const float alpha = fast_exp2(m - base);  // exactly 1 when m did not move
-            l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+            l = l * alpha + ((s0 + s1) + (s2 + s3));
             const bool moved = m_new != m;
             m = m_new;
             if (jt > 0) {
