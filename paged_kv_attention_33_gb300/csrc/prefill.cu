@@ -30,7 +30,7 @@
 //               as bf16, rescales its O row in TMEM when its reference max
 //               moved by more than 8, and at the end writes out = O / l and lse.
 // Registers: the producer warpgroup gives registers back (setmaxnreg) to the
-// two softmax warpgroups: 128 x 88 + 256 x 208 = 64512 = 384 x 168 at launch.
+// two softmax warpgroups: 128 x 104 + 256 x 200 = 64512 = 384 x 168 at launch.
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256, 256+D), O_B [256+D, 256+2D).
 #include <math.h>
 
@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t tbase = *tmem_holder;
 
     if (warp < 4) {
-        reg_dealloc<88>();
+        reg_dealloc<104>();
         if (warp == 0) {
             // ============================================================ producer
             if (lane == 0) {
@@ -587,7 +587,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             }
         } else if (warp == 1) {
             // ============================================================ MMA issuer
-            const uint32_t sQ = smem_addr(smem + Cfg::kQOff);
+            // Operand descriptors are built once; a k-step or a stage only moves
+            // the start-address field (16-byte units, no carry out of 14 bits as
+            // every tile lies below 256 KB), so each MMA costs one 64-bit add.
+            const uint64_t dQ0 = smem_desc_sw128(smem_addr(smem + Cfg::kQOff), 16, 1024);
+            const uint64_t dK0 = smem_desc_sw128(smem_addr(smem + Cfg::kKOff), 16, 1024);
+            const uint64_t dV0 =
+                smem_desc_sw128(smem_addr(smem + Cfg::kVOff), Cfg::kHalfBytes, 1024);
+            constexpr uint64_t kTileStep = Cfg::kTileBytes >> 4;
             uint32_t li = 0, kv_it = 0;
             uint32_t p_cnt[2] = {0, 0}, item_cnt[2] = {0, 0};
             PfItem it;
@@ -646,13 +653,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                                 break;
                             }
                             tc_fence_after();
-                            const uint32_t sV = smem_addr(smem + Cfg::kVOff + pst * Cfg::kTileBytes);
+                            const uint64_t dV = dV0 + pst * kTileStep;
                             if (lane == 0) {
+                                const uint32_t tO_ = tbase + 256 + tl * D;
+                                const uint32_t tP_ = tbase + tl * 128;
+                                mma_ts(tO_, tP_, dV, Cfg::kIdescPV, jp > 0 ? 1u : 0u);
 #pragma unroll
-                                for (int k = 0; k < kBN / 16; ++k)
-                                    mma_ts(tbase + 256 + tl * D, tbase + tl * 128 + k * 8,
-                                           smem_desc_sw128(sV + k * 2048, Cfg::kHalfBytes, 1024),
-                                           Cfg::kIdescPV, (jp > 0 || k > 0) ? 1u : 0u);
+                                for (int k = 1; k < kBN / 16; ++k)
+                                    mma_ts(tO_, tP_ + k * 8, dV + uint64_t(k * 2048 >> 4),
+                                           Cfg::kIdescPV, 1u);
                                 mma_commit(&bars.o_done[tl]);
                                 if (tl == (jp < it.n_kv[1] ? 1 : 0))
                                     mma_commit(&bars.v_empty[pst]);  // last reader of V(jp)
@@ -661,15 +670,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                         }
                         // ---- S_tl = Q_tl K^T of this K/V tile
                         if (jt < nk) {
-                            const uint32_t sK = smem_addr(smem + Cfg::kKOff + st * Cfg::kTileBytes);
-                            const uint32_t sQt = sQ + tl * Cfg::kTileBytes;
+                            const uint64_t dK = dK0 + st * kTileStep;
+                            const uint64_t dQ = dQ0 + tl * kTileStep;
                             if (lane == 0) {
+                                const uint32_t tS_ = tbase + tl * 128;
 #pragma unroll
                                 for (int k = 0; k < D / 16; ++k) {
-                                    const uint32_t off = (k >> 2) * Cfg::kHalfBytes + (k & 3) * 32;
-                                    mma_ss(tbase + tl * 128, smem_desc_sw128(sQt + off, 16, 1024),
-                                           smem_desc_sw128(sK + off, 16, 1024), Cfg::kIdescS,
-                                           k > 0);
+                                    const uint64_t off = ((k >> 2) * Cfg::kHalfBytes + (k & 3) * 32) >> 4;
+                                    mma_ss(tS_, dQ + off, dK + off, Cfg::kIdescS, k > 0 ? 1u : 0u);
                                 }
                                 mma_commit(&bars.s_full[tl]);
                                 if (tl == (jt < it.n_kv[1] ? 1 : 0))
@@ -699,7 +707,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             __syncwarp();
         }
     } else {
-        reg_alloc<208>();
+        reg_alloc<200>();
         const int tl = (warp - 4) / 4;  // warps 4-7: tile A, warps 8-11: tile B
         pf_softmax<D>(p, prefix, nseq, bars, tl, tbase + tl * 128, tbase + 256 + tl * D,
                       abort_flag);
