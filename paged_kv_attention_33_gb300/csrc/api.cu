@@ -154,6 +154,9 @@ Workspace plan_workspace(const DecodePlan &dp, int32_t num_tokens, int32_t num_d
     off = round256(off + rows_pf * head_size * 4);
     w.lse_suf = off;
     off = round256(off + rows_pf * 4);
+    w.pf_counters = off;
+    if (cascade || num_tokens > num_decodes)
+        off = round256(off + 2 * sizeof(int32_t));
     w.total = off;
     return w;
 }
@@ -346,7 +349,8 @@ pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const
         // prefix once for every query (tensor cores, no mask), each sequence's
         // own suffix [P, L_s), then a log-sum-exp merge of the parts.
         PrefillPass pre{0, kv_begin, 0, true, reinterpret_cast<float *>(wsp + ws.o_pre),
-                        reinterpret_cast<float *>(wsp + ws.lse_pre), 0};
+                        reinterpret_cast<float *>(wsp + ws.lse_pre), 0,
+                        reinterpret_cast<int32_t *>(wsp + ws.pf_counters) + 1};
         record_start(PKA_KERNEL_PREFILL, f.stream);
         e = launch_prefill(f, pre);
         record_stop(PKA_KERNEL_PREFILL, f.stream);
@@ -362,7 +366,7 @@ pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const
         PrefillPass pf{kv_begin, INT32_MAX, causal ? 1 : 0, false,
                        cascade ? reinterpret_cast<float *>(wsp + ws.o_suf) : nullptr,
                        cascade ? reinterpret_cast<float *>(wsp + ws.lse_suf) : nullptr,
-                       meta->num_decodes};
+                       meta->num_decodes, reinterpret_cast<int32_t *>(wsp + ws.pf_counters)};
         if (!cascade)
             record_start(PKA_KERNEL_PREFILL, f.stream);
         e = launch_prefill(f, pf);

@@ -52,6 +52,7 @@ struct Workspace {
     size_t counters;           // pieces finished per decode (int32)
     size_t o_pre, lse_pre;     // cascade: shared-prefix partial of every token
     size_t o_suf, lse_suf;     // cascade: suffix partial of every prefill token
+    size_t pf_counters;        // prefill work-queue counters (int32 x 2)
     size_t total;
 };
 
@@ -103,6 +104,7 @@ struct PrefillPass {
     float *o_part;
     float *lse_part;
     int32_t token_base;
+    int32_t *item_counter;  // device int32 for the dynamic work queue (zeroed per launch)
 };
 cudaError_t launch_prefill(const Fwd &f, const PrefillPass &pass);
 uint32_t prefill_take_error();

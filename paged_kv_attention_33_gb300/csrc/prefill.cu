@@ -10,7 +10,8 @@
 //
 // Work item: (sequence s, 256-query super-tile, query head h) = two 128-row
 // tiles A and B that share every K/V tile, in a persistent grid (one CTA per
-// SM, items round-robin, the heaviest causal tiles of each sequence first).
+// SM).  Items are claimed dynamically from a global counter (the heaviest
+// causal tiles of each sequence first), so CTAs that draw light items take more.
 // Roles (384 threads, three warpgroups):
 //   warp 0      TMA producer: Q tiles once per item, K and V tiles of 128 keys
 //               into two-stage rings (K one tile ahead of V, each freed by its
@@ -79,6 +80,7 @@ struct PrefillParams {
     float *lse;
     float *o_part;
     float *lse_part;
+    int32_t *item_counter;  // work items claimed so far (zeroed before each launch)
 };
 
 template <int D>
@@ -218,7 +220,26 @@ struct PfBars {
     uint64_t *q_full, *q_empty, *k_full, *v_full, *k_empty, *v_empty;
     uint64_t *s_full, *p_full, *o_done, *o_free;  // [2] each: tile A, tile B
     uint64_t *drain;
+    uint64_t *item_full, *item_empty;  // [2] each: the work-item hand-off ring
+    volatile int32_t *item_slot;       // [2]
 };
+
+// Number of consumer warps of the item ring: the MMA warp and 8 softmax warps.
+constexpr uint32_t kItemReaders = 9;
+
+// The n-th work item the producer handed to this CTA (-1: no more work).
+__device__ __forceinline__ int pf_next_item(const PfBars &bars, uint32_t n,
+                                            volatile int *abort_flag)
+{
+    const int slot = n & 1;
+    if (!pf_wait(&bars.item_full[slot], (n >> 1) & 1, abort_flag))
+        return -1;
+    const int item = bars.item_slot[slot];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0)
+        mbar_arrive(&bars.item_empty[slot]);
+    return item;
+}
 
 // ---------------------------------------------------------------- softmax role
 template <int D>
@@ -232,9 +253,12 @@ __device__ __forceinline__ void pf_softmax(const PrefillParams &p, const int32_t
     const int r = wq * 32 + lane;
     const uint32_t lane_off = uint32_t(wq * 32) << 16;
     const uint32_t ts = tS + lane_off;
-    uint32_t s_n = 0, pv_n = 0;
+    uint32_t s_n = 0, pv_n = 0, n_got = 0;
     PfItem it;
-    for (int item = blockIdx.x; pf_item(p, prefix, nseq, item, it); item += gridDim.x) {
+    for (;;) {
+        const int item = pf_next_item(bars, n_got++, abort_flag);
+        if (item < 0 || !pf_item(p, prefix, nseq, item, it))
+            break;
         const int rows = it.rows[tl];
         const int nkv = it.n_kv[tl];
         const bool valid = r < rows;
@@ -423,6 +447,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     bars.o_done = b + 12;    // [2]
     bars.o_free = b + 14;    // [2]
     bars.drain = b + 16;
+    bars.item_full = b + 20;   // [2]
+    bars.item_empty = b + 22;  // [2]
+    bars.item_slot = reinterpret_cast<volatile int32_t *>(smem + Cfg::kMiscOff + 8);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + Cfg::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::kMiscOff + 4);
     int32_t *prefix = reinterpret_cast<int32_t *>(smem + Cfg::kPrefixOff);
@@ -480,6 +507,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             mbar_init(&bars.o_free[i], 4);
         }
         mbar_init(bars.drain, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars.item_full[i], 1);
+            mbar_init(&bars.item_empty[i], kItemReaders);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -502,9 +533,28 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             }
             const uint64_t pol_kv = l2_policy_evict_last();
             const uint64_t pol_q = l2_policy_evict_first();
-            uint32_t li = 0, kv_it = 0;
+            uint32_t li = 0, kv_it = 0, n_pub = 0;
             PfItem it;
-            for (int item = blockIdx.x; pf_item(p, prefix, nseq, item, it); item += gridDim.x) {
+            for (;;) {
+                // claim the next work item (dynamic: a CTA that finishes early
+                // takes more) and hand its index to the MMA and softmax warps
+                int item = 0;
+                if (lane == 0)
+                    item = atomicAdd(p.item_counter, 1);
+                item = __shfl_sync(0xffffffffu, item, 0);
+                const bool have = pf_item(p, prefix, nseq, item, it);
+                const int slot = n_pub & 1;
+                if (n_pub >= 2 &&
+                    !pf_wait(&bars.item_empty[slot], ((n_pub >> 1) - 1) & 1, abort_flag))
+                    break;
+                if (lane == 0) {
+                    bars.item_slot[slot] = have ? item : -1;
+                    mbar_arrive(&bars.item_full[slot]);
+                }
+                __syncwarp();
+                ++n_pub;
+                if (!have)
+                    break;
                 if (it.n_kv_all == 0)
                     continue;
                 const int kvh = it.h / p.group;
@@ -599,8 +649,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             uint32_t p_cnt[2] = {0, 0}, item_cnt[2] = {0, 0};
             PfItem it;
             bool ok = true;
-            for (int item = blockIdx.x; ok && pf_item(p, prefix, nseq, item, it);
-                 item += gridDim.x) {
+            uint32_t n_got = 0;
+            while (ok) {
+                const int item = pf_next_item(bars, n_got++, abort_flag);
+                if (item < 0 || !pf_item(p, prefix, nseq, item, it))
+                    break;
                 if (it.n_kv_all == 0)
                     continue;
                 if (!pf_wait(bars.q_full, li & 1, abort_flag))
@@ -780,6 +833,9 @@ cudaError_t launch_prefill(const Fwd &f, const PrefillPass &pass)
     p.lse = f.lse;
     p.o_part = pass.o_part;
     p.lse_part = pass.lse_part;
+    p.item_counter = pass.item_counter;
+    if (cudaError_t e = cudaMemsetAsync(p.item_counter, 0, sizeof(int32_t), f.stream))
+        return e;
     int64_t items;
     if (pass.shared_prefix)
         items = int64_t((f.num_tokens + kSuper - 1) / kSuper) * f.num_heads;
