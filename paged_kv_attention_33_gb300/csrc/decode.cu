@@ -153,68 +153,120 @@ __device__ __forceinline__ int cta_of_stage(int64_t x, int64_t total, int grid)
     return static_cast<int>(((x + 1) * grid + total - 1) / total - 1);
 }
 
+__device__ __forceinline__ float warp_max32(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum32(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
 // Merge the nparts partials of decode s (token t): part q lives in slot
 // (bf + q / R + s), sub-row q % R; in a cascade the shared-prefix partial of
-// the token is one more part.  Warp w takes heads w, w+8, ...; every load of
-// a part is independent of the others, so they overlap.
+// the token is one more part.  Warp w takes heads w, w+8, ..., kHB of them at
+// a time: lane q holds part q's log2-sum-exp, so the maximum and the weights
+// come from shuffles, and the rows of all kHB heads are loaded together (lanes
+// along head_size), so a merge costs a few L2 round trips, not one per head.
 template <int D>
 __device__ __forceinline__ void merge_pieces(const DecodeParams &p, int t, int s, int bf,
                                              int nparts, int R, int warp, int lane)
 {
     constexpr int kPer = D / 32;  // dims per lane
+    constexpr int kHB = 4;        // heads per batch
     const int H = p.num_heads;
-    for (int h = warp; h < H; h += kConsumerWarps) {
-        const int64_t row_out = int64_t(t) * H + h;
-        const float l_pre = p.cascade ? __ldcg(p.lse_pre + row_out) : kNegInf;
-        float M = l_pre;
-        for (int q = lane; q < nparts; q += 32)
-            M = fmaxf(M, __ldcg(p.lse_part + (int64_t(bf + q / R + s) * R + q % R) * H + h));
+    auto part_row = [&](int q, int h) {
+        return (int64_t(bf + q / R + s) * R + q % R) * H + h;
+    };
+    for (int h0 = warp; h0 < H; h0 += kHB * kConsumerWarps) {
+        float lpre[kHB], wl[kHB], M[kHB], W[kHB];
+        float acc[kHB][kPer];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float acc[kPer];
+        for (int j = 0; j < kHB; ++j) {
+            const int h = h0 + j * kConsumerWarps;
+            const bool hv = h < H;
+            lpre[j] = hv && p.cascade ? __ldcg(p.lse_pre + int64_t(t) * H + h) : kNegInf;
+            wl[j] = hv && lane < nparts ? __ldcg(p.lse_part + part_row(lane, h)) : kNegInf;
+        }
 #pragma unroll
-        for (int e = 0; e < kPer; ++e)
-            acc[e] = 0.f;
-        float W = 0.f;
-        if (M != kNegInf) {
-#pragma unroll 4
-            for (int q = 0; q < nparts; ++q) {
-                const int64_t row = (int64_t(bf + q / R + s) * R + q % R) * H + h;
-                const float lq = __ldcg(p.lse_part + row);
-                // an empty part adds nothing, whatever its row holds
-                const float w = lq == kNegInf ? 0.f : exp2f(lq - M);
-                W += w;
-                const float *src = p.o_part + row * D + lane * kPer;
-                if constexpr (kPer == 4) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
-                    acc[0] += w * v.x;
-                    acc[1] += w * v.y;
-                    acc[2] += w * v.z;
-                    acc[3] += w * v.w;
-                } else {
-                    const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
-                    acc[0] += w * v.x;
-                    acc[1] += w * v.y;
+        for (int j = 0; j < kHB; ++j) {
+            const int h = h0 + j * kConsumerWarps;
+            float m = wl[j];
+            for (int q = lane + 32; q < nparts && h < H; q += 32)  // more than 32 parts
+                m = fmaxf(m, __ldcg(p.lse_part + part_row(q, h)));
+            M[j] = fmaxf(lpre[j], warp_max32(m));
+            // an empty part adds nothing
+            wl[j] = wl[j] == kNegInf ? 0.f : exp2f(wl[j] - M[j]);
+            W[j] = warp_sum32(wl[j]);
+#pragma unroll
+            for (int e = 0; e < kPer; ++e)
+                acc[j][e] = 0.f;
+        }
+#pragma unroll 2
+        for (int q = 0; q < nparts; ++q) {
+#pragma unroll
+            for (int j = 0; j < kHB; ++j) {
+                const int h = h0 + j * kConsumerWarps;
+                float w = __shfl_sync(0xffffffffu, wl[j], q & 31);
+                if (q >= 32) {  // warp-uniform
+                    const float lq = h < H ? __ldcg(p.lse_part + part_row(q, h)) : kNegInf;
+                    w = lq == kNegInf ? 0.f : exp2f(lq - M[j]);
+                    W[j] += w;
+                }
+                if (h < H) {
+                    const float *src = p.o_part + part_row(q, h) * D + lane * kPer;
+                    if constexpr (kPer == 4) {
+                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
+                        acc[j][0] += w * v.x;
+                        acc[j][1] += w * v.y;
+                        acc[j][2] += w * v.z;
+                        acc[j][3] += w * v.w;
+                    } else {
+                        const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
+                        acc[j][0] += w * v.x;
+                        acc[j][1] += w * v.y;
+                    }
                 }
             }
-            if (l_pre != kNegInf) {
-                const float w = exp2f(l_pre - M);
-                W += w;
-                const float *src = p.o_pre + row_out * D + lane * kPer;
-#pragma unroll
-                for (int e = 0; e < kPer; ++e)
-                    acc[e] += w * __ldcg(src + e);
-            }
         }
-        const float inv = W > 0.f ? 1.f / W : 0.f;
-        __nv_bfloat16 *dst = p.out + row_out * D + lane * kPer;
 #pragma unroll
-        for (int e = 0; e < kPer; e += 2)
-            *reinterpret_cast<__nv_bfloat162 *>(dst + e) =
-                __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
-        if (lane == 0 && p.lse)
-            p.lse[row_out] = W > 0.f ? (M + log2f(W)) * kLn2 : kNegInf;
+        for (int j = 0; j < kHB; ++j) {
+            const int h = h0 + j * kConsumerWarps;
+            if (h >= H)
+                continue;
+            const int64_t row_out = int64_t(t) * H + h;
+            if (lpre[j] != kNegInf) {
+                const float w = exp2f(lpre[j] - M[j]);
+                W[j] += w;
+                const float *src = p.o_pre + row_out * D + lane * kPer;
+                if constexpr (kPer == 4) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
+                    acc[j][0] += w * v.x;
+                    acc[j][1] += w * v.y;
+                    acc[j][2] += w * v.z;
+                    acc[j][3] += w * v.w;
+                } else {
+                    const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
+                    acc[j][0] += w * v.x;
+                    acc[j][1] += w * v.y;
+                }
+            }
+            const float inv = W[j] > 0.f ? 1.f / W[j] : 0.f;
+            __nv_bfloat16 *dst = p.out + row_out * D + lane * kPer;
+#pragma unroll
+            for (int e = 0; e < kPer; e += 2)
+                *reinterpret_cast<__nv_bfloat162 *>(dst + e) =
+                    __floats2bfloat162_rn(acc[j][e] * inv, acc[j][e + 1] * inv);
+            if (lane == 0 && p.lse)
+                p.lse[row_out] = W[j] > 0.f ? (M[j] + log2f(W[j])) * kLn2 : kNegInf;
+        }
     }
 }
 
