@@ -130,8 +130,24 @@ CUresult encode_kv_map(CUtensorMap *map, const void *cache, int32_t head_size,
 }
 
 // ------------------------------------------------------------ planning
+int32_t plan_prefix_splits(int32_t num_tokens, int32_t num_heads, int32_t prefix_len,
+                           int num_sms)
+{
+    if (prefix_len <= 0 || num_tokens <= 0)
+        return 1;
+    const int64_t items = (int64_t(num_tokens) + 255) / 256 * num_heads;
+    const int64_t tiles = (int64_t(prefix_len) + 127) / 128;
+    if (items >= num_sms)
+        return 1;
+    int64_t s = std::min<int64_t>(num_sms / items, std::max<int64_t>(1, tiles / 4));
+    const int64_t per = (tiles + s - 1) / s;  // tiles per chunk; no chunk is empty
+    s = (tiles + per - 1) / per;
+    return static_cast<int32_t>(std::max<int64_t>(1, s));
+}
+
 Workspace plan_workspace(const DecodePlan &dp, int32_t num_tokens, int32_t num_decodes,
-                         int32_t num_heads, int32_t head_size, bool cascade)
+                         int32_t num_heads, int32_t head_size, bool cascade,
+                         int32_t pre_splits)
 {
     Workspace w;
     size_t off = 0;
@@ -144,7 +160,8 @@ Workspace plan_workspace(const DecodePlan &dp, int32_t num_tokens, int32_t num_d
     off = round256(off + rows_part * 4);
     w.counters = off;
     off = round256(off + size_t(dp.chunk) * 4);
-    const size_t rows_all = cascade ? size_t(num_tokens) * num_heads : 0;
+    w.pre_splits = cascade ? pre_splits : 0;
+    const size_t rows_all = cascade ? size_t(pre_splits) * num_tokens * num_heads : 0;
     w.o_pre = off;
     off = round256(off + rows_all * head_size * 4);
     w.lse_pre = off;
@@ -267,9 +284,12 @@ size_t pka_workspace_size(const pka_meta *meta, int32_t num_tokens, int32_t num_
         return 0;
     const bool cascade = meta->common_prefix_len > 0;
     const int32_t kv_begin = meta->common_prefix_len;
-    DecodePlan dp = plan_decode(meta->split_kv_tokens, meta->num_decodes, num_kv_heads,
-                                sm_count());
-    return plan_workspace(dp, num_tokens, meta->num_decodes, num_heads, head_size, cascade).total;
+    const int sms = sm_count();
+    DecodePlan dp = plan_decode(meta->split_kv_tokens, meta->num_decodes, num_kv_heads, sms);
+    const int32_t pre_splits = plan_prefix_splits(num_tokens, num_heads, kv_begin, sms);
+    return plan_workspace(dp, num_tokens, meta->num_decodes, num_heads, head_size, cascade,
+                          pre_splits)
+        .total;
 }
 
 pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const pka_meta *meta,
@@ -332,7 +352,9 @@ pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const
 
     DecodePlan dp = plan_decode(meta->split_kv_tokens, meta->num_decodes, num_kv_heads,
                                 f.num_sms);
-    Workspace ws = plan_workspace(dp, num_tokens, meta->num_decodes, num_heads, head_size, cascade);
+    const int32_t pre_splits = plan_prefix_splits(num_tokens, num_heads, kv_begin, f.num_sms);
+    Workspace ws = plan_workspace(dp, num_tokens, meta->num_decodes, num_heads, head_size, cascade,
+                                  pre_splits);
     if (ws.total > 0 && (!workspace || workspace_bytes < ws.total || !aligned(workspace, 256)))
         return fail(PKA_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)",
                     ws.total, workspace_bytes);
@@ -350,7 +372,7 @@ pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const
         // own suffix [P, L_s), then a log-sum-exp merge of the parts.
         PrefillPass pre{0, kv_begin, 0, true, reinterpret_cast<float *>(wsp + ws.o_pre),
                         reinterpret_cast<float *>(wsp + ws.lse_pre), 0,
-                        reinterpret_cast<int32_t *>(wsp + ws.pf_counters) + 1};
+                        reinterpret_cast<int32_t *>(wsp + ws.pf_counters) + 1, pre_splits};
         record_start(PKA_KERNEL_PREFILL, f.stream);
         e = launch_prefill(f, pre);
         record_stop(PKA_KERNEL_PREFILL, f.stream);

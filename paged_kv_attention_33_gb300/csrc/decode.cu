@@ -74,8 +74,9 @@ struct DecodeParams {
     float *o_part;        // [slots, R, H, D] normalised partials
     float *lse_part;      // [slots, R, H], log2 units
     int32_t *counters;    // [nseq] pieces finished per sequence (zeroed per launch)
-    const float *o_pre;   // cascade: shared-prefix partial [T, H, D]
-    const float *lse_pre; // [T, H], log2 units
+    const float *o_pre;   // cascade: shared-prefix partials [pre_splits][T, H, D]
+    const float *lse_pre; // [pre_splits][T, H], log2 units
+    int32_t pre_splits;   // cascade: shared-prefix partials per row
 };
 
 constexpr int kConsumerWarps = 8;
@@ -169,12 +170,13 @@ __device__ __forceinline__ float warp_sum32(float v)
     return v;
 }
 
-// Merge the nparts partials of decode s (token t): part q lives in slot
-// (bf + q / R + s), sub-row q % R; in a cascade the shared-prefix partial of
-// the token is one more part.  Warp w takes heads w, w+8, ..., kHB of them at
-// a time: lane q holds part q's log2-sum-exp, so the maximum and the weights
-// come from shuffles, and the rows of all kHB heads are loaded together (lanes
-// along head_size), so a merge costs a few L2 round trips, not one per head.
+// Merge the partials of decode s (token t): its nparts pieces -- part q lives
+// in slot (bf + q / R + s), sub-row q % R -- and, in a cascade, the
+// pre_splits partials of the shared prefix (key chunk c at rows c*T*H + t*H +
+// h).  Warp w takes heads w, w+8, ..., kHB of them at a time: lane q holds part
+// q's log2-sum-exp, so the maximum and the weights come from shuffles, and the
+// rows of all kHB heads are loaded together (lanes along head_size), so a
+// merge costs a few L2 round trips, not one per head.
 template <int D>
 __device__ __forceinline__ void merge_pieces(const DecodeParams &p, int t, int s, int bf,
                                              int nparts, int R, int warp, int lane)
@@ -182,26 +184,29 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, int t, int s
     constexpr int kPer = D / 32;  // dims per lane
     constexpr int kHB = 4;        // heads per batch
     const int H = p.num_heads;
-    auto part_row = [&](int q, int h) {
-        return (int64_t(bf + q / R + s) * R + q % R) * H + h;
+    const int ntot = nparts + (p.cascade ? p.pre_splits : 0);
+    auto row_of = [&](int q, int h) -> int64_t {  // row of part q, head h
+        return q < nparts ? (int64_t(bf + q / R + s) * R + q % R) * H + h
+                          : (int64_t(q - nparts) * p.num_tokens + t) * H + h;
+    };
+    auto lse_of = [&](int q, int h) {
+        return __ldcg((q < nparts ? p.lse_part : p.lse_pre) + row_of(q, h));
     };
     for (int h0 = warp; h0 < H; h0 += kHB * kConsumerWarps) {
-        float lpre[kHB], wl[kHB], M[kHB], W[kHB];
+        float wl[kHB], M[kHB], W[kHB];
         float acc[kHB][kPer];
 #pragma unroll
         for (int j = 0; j < kHB; ++j) {
             const int h = h0 + j * kConsumerWarps;
-            const bool hv = h < H;
-            lpre[j] = hv && p.cascade ? __ldcg(p.lse_pre + int64_t(t) * H + h) : kNegInf;
-            wl[j] = hv && lane < nparts ? __ldcg(p.lse_part + part_row(lane, h)) : kNegInf;
+            wl[j] = h < H && lane < ntot ? lse_of(lane, h) : kNegInf;
         }
 #pragma unroll
         for (int j = 0; j < kHB; ++j) {
             const int h = h0 + j * kConsumerWarps;
             float m = wl[j];
-            for (int q = lane + 32; q < nparts && h < H; q += 32)  // more than 32 parts
-                m = fmaxf(m, __ldcg(p.lse_part + part_row(q, h)));
-            M[j] = fmaxf(lpre[j], warp_max32(m));
+            for (int q = lane + 32; q < ntot && h < H; q += 32)  // more than 32 parts
+                m = fmaxf(m, lse_of(q, h));
+            M[j] = warp_max32(m);
             // an empty part adds nothing
             wl[j] = wl[j] == kNegInf ? 0.f : exp2f(wl[j] - M[j]);
             W[j] = warp_sum32(wl[j]);
@@ -210,18 +215,19 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, int t, int s
                 acc[j][e] = 0.f;
         }
 #pragma unroll 2
-        for (int q = 0; q < nparts; ++q) {
+        for (int q = 0; q < ntot; ++q) {
+            const float *obase = q < nparts ? p.o_part : p.o_pre;
 #pragma unroll
             for (int j = 0; j < kHB; ++j) {
                 const int h = h0 + j * kConsumerWarps;
                 float w = __shfl_sync(0xffffffffu, wl[j], q & 31);
                 if (q >= 32) {  // warp-uniform
-                    const float lq = h < H ? __ldcg(p.lse_part + part_row(q, h)) : kNegInf;
+                    const float lq = h < H ? lse_of(q, h) : kNegInf;
                     w = lq == kNegInf ? 0.f : exp2f(lq - M[j]);
                     W[j] += w;
                 }
                 if (h < H) {
-                    const float *src = p.o_part + part_row(q, h) * D + lane * kPer;
+                    const float *src = obase + row_of(q, h) * D + lane * kPer;
                     if constexpr (kPer == 4) {
                         const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
                         acc[j][0] += w * v.x;
@@ -242,22 +248,6 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, int t, int s
             if (h >= H)
                 continue;
             const int64_t row_out = int64_t(t) * H + h;
-            if (lpre[j] != kNegInf) {
-                const float w = exp2f(lpre[j] - M[j]);
-                W[j] += w;
-                const float *src = p.o_pre + row_out * D + lane * kPer;
-                if constexpr (kPer == 4) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
-                    acc[j][0] += w * v.x;
-                    acc[j][1] += w * v.y;
-                    acc[j][2] += w * v.z;
-                    acc[j][3] += w * v.w;
-                } else {
-                    const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
-                    acc[j][0] += w * v.x;
-                    acc[j][1] += w * v.y;
-                }
-            }
             const float inv = W[j] > 0.f ? 1.f / W[j] : 0.f;
             __nv_bfloat16 *dst = p.out + row_out * D + lane * kPer;
 #pragma unroll
@@ -606,13 +596,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
 // --------------------------------------------------------------------- combine
 // Cascade only: every prefill token's suffix partial (from the prefill kernel)
-// merged with its shared-prefix partial -- the log-sum-exp merge of two parts.
+// merged with its pre_splits shared-prefix partials -- the log-sum-exp merge.
 // One warp per (token, head) row, lanes along head_size.
 struct CombineParams {
     int32_t num_tokens;
     int32_t num_decodes;
     int32_t num_heads;
-    const float *o_pre;  // [T, H, D]
+    int32_t pre_splits;
+    const float *o_pre;  // [pre_splits][T, H, D]
     const float *lse_pre;
     const float *o_suf;  // [T - num_decodes, H, D]
     const float *lse_suf;
@@ -629,26 +620,43 @@ __global__ void __launch_bounds__(256) cascade_prefill_combine_kernel(const Comb
     const int64_t nrows = int64_t(p.num_tokens - p.num_decodes) * p.num_heads;
     if (gw >= nrows)
         return;
-    const int64_t srow = gw;
     const int64_t row = int64_t(p.num_decodes) * p.num_heads + gw;
-    const float la = p.lse_suf[srow], lb = p.lse_pre[row];
-    const float mx = fmaxf(la, lb);
-    float wa = 0.f, wb = 0.f;
+    const int64_t split_rows = int64_t(p.num_tokens) * p.num_heads;
+    const int nparts = 1 + p.pre_splits;  // part 0: the suffix, part 1 + c: prefix chunk c
+    auto lse_of = [&](int q) {
+        return q == 0 ? p.lse_suf[gw] : p.lse_pre[(q - 1) * split_rows + row];
+    };
+    auto o_of = [&](int q) {
+        return (q == 0 ? p.o_suf + gw * D : p.o_pre + ((q - 1) * split_rows + row) * D) +
+               lane * kPer;
+    };
+    float mx = kNegInf;
+    for (int q = 0; q < nparts; ++q)
+        mx = fmaxf(mx, lse_of(q));
+    float acc[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e)
+        acc[e] = 0.f;
+    float ws = 0.f;
     if (mx != kNegInf) {
-        wa = la == kNegInf ? 0.f : exp2f(la - mx);
-        wb = lb == kNegInf ? 0.f : exp2f(lb - mx);
+        for (int q = 0; q < nparts; ++q) {
+            const float lq = lse_of(q);
+            if (lq == kNegInf)
+                continue;  // an empty part adds nothing (warp-uniform)
+            const float w = exp2f(lq - mx);
+            ws += w;
+            const float *src = o_of(q);
+#pragma unroll
+            for (int e = 0; e < kPer; ++e)
+                acc[e] += w * src[e];
+        }
     }
-    const float ws = wa + wb;
     const float inv = ws > 0.f ? 1.f / ws : 0.f;
-    const float *a = p.o_suf + srow * D + lane * kPer;
-    const float *bb = p.o_pre + row * D + lane * kPer;
     __nv_bfloat16 *dst = p.out + row * D + lane * kPer;
 #pragma unroll
-    for (int e = 0; e < kPer; e += 2) {
-        const float x0 = (wa > 0.f ? wa * a[e] : 0.f) + (wb > 0.f ? wb * bb[e] : 0.f);
-        const float x1 = (wa > 0.f ? wa * a[e + 1] : 0.f) + (wb > 0.f ? wb * bb[e + 1] : 0.f);
-        *reinterpret_cast<__nv_bfloat162 *>(dst + e) = __floats2bfloat162_rn(x0 * inv, x1 * inv);
-    }
+    for (int e = 0; e < kPer; e += 2)
+        *reinterpret_cast<__nv_bfloat162 *>(dst + e) =
+            __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
     if (lane == 0 && p.lse)
         p.lse[row] = ws > 0.f ? (mx + log2f(ws)) * kLn2 : kNegInf;
 }
@@ -706,6 +714,7 @@ static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Wor
     p.counters = reinterpret_cast<int32_t *>(wsp + ws.counters);
     p.o_pre = reinterpret_cast<const float *>(wsp + ws.o_pre);
     p.lse_pre = reinterpret_cast<const float *>(wsp + ws.lse_pre);
+    p.pre_splits = ws.pre_splits;
     // one launch per chunk of at most kMaxDecodeChunk decodes (stream ordered,
     // so chunks reuse the same partial slots and counters)
     for (int32_t seq0 = 0; seq0 < f.num_decodes; seq0 += dp.chunk) {
@@ -742,6 +751,7 @@ cudaError_t launch_cascade_prefill_combine(const Fwd &f, const Workspace &ws, ch
     p.num_tokens = f.num_tokens;
     p.num_decodes = f.num_decodes;
     p.num_heads = f.num_heads;
+    p.pre_splits = ws.pre_splits;
     p.o_pre = reinterpret_cast<const float *>(wsp + ws.o_pre);
     p.lse_pre = reinterpret_cast<const float *>(wsp + ws.lse_pre);
     p.o_suf = reinterpret_cast<const float *>(wsp + ws.o_suf);

@@ -50,7 +50,9 @@ struct DecodePlan {
 struct Workspace {
     size_t o_part, lse_part;   // decode piece partials
     size_t counters;           // pieces finished per decode (int32)
-    size_t o_pre, lse_pre;     // cascade: shared-prefix partial of every token
+    size_t o_pre, lse_pre;     // cascade: shared-prefix partials of every token, one per
+                               // key chunk of the prefix ([pre_splits][T, H, D])
+    int32_t pre_splits;        // cascade: key chunks of the shared-prefix pass
     size_t o_suf, lse_suf;     // cascade: suffix partial of every prefill token
     size_t pf_counters;        // prefill work-queue counters (int32 x 2)
     size_t total;
@@ -58,8 +60,14 @@ struct Workspace {
 
 DecodePlan plan_decode(int32_t split_kv_tokens, int32_t num_decodes, int32_t num_kv_heads,
                        int num_sms);
+// Cascade: the shared-prefix pass has ceil(T/256)*H work items; when they
+// fill less than one wave of the persistent grid, the prefix keys are cut into
+// chunks (at least 4 key tiles each) so that items x chunks fill about one wave.
+int32_t plan_prefix_splits(int32_t num_tokens, int32_t num_heads, int32_t prefix_len,
+                           int num_sms);
 Workspace plan_workspace(const DecodePlan &dp, int32_t num_tokens, int32_t num_decodes,
-                         int32_t num_heads, int32_t head_size, bool cascade);
+                         int32_t num_heads, int32_t head_size, bool cascade,
+                         int32_t pre_splits);
 
 // kv_write.cu
 cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *cache,
@@ -93,7 +101,8 @@ void count_launch();
 //  shared_prefix = false: the prefill sequences [num_decodes, num_seqs), keys
 //    [kv_lo, min(kv_cap, L_s)), causal or not;
 //  shared_prefix = true: every token of the batch against keys [0, kv_cap) of
-//    the prefix all sequences share (block-table row 0), no mask.
+//    the prefix all sequences share (block-table row 0), no mask; the keys are
+//    cut into kv_splits chunks, chunk c's partial at rows c*T*H + t*H + h.
 //  o_part == nullptr: write bf16 out / ln lse; else fp32 partials (normalised)
 //    and log2 lse at rows (t - token_base) * num_heads + h.
 struct PrefillPass {
@@ -105,6 +114,7 @@ struct PrefillPass {
     float *lse_part;
     int32_t token_base;
     int32_t *item_counter;  // device int32 for the dynamic work queue (zeroed per launch)
+    int32_t kv_splits = 1;  // shared_prefix: key chunks
 };
 cudaError_t launch_prefill(const Fwd &f, const PrefillPass &pass);
 uint32_t prefill_take_error();

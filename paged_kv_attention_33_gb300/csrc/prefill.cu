@@ -81,6 +81,8 @@ struct PrefillParams {
     float *o_part;
     float *lse_part;
     int32_t *item_counter;  // work items claimed so far (zeroed before each launch)
+    int32_t kv_splits;      // shared_prefix: key chunks, split_tiles key tiles each
+    int32_t split_tiles;
 };
 
 template <int D>
@@ -108,7 +110,9 @@ struct PfItem {
     int rows[2];   // valid query rows of tile A / B (0: tile absent)
     int n_kv[2];   // K/V tiles tile A / B attends
     int n_kv_all;  // K/V tiles the item loads (max of the two)
+    int kv_lo;     // first key of the item (a multiple of the key tile)
     int kv_hi;     // keys [kv_lo, kv_hi) are loaded
+    int split;     // shared_prefix: key chunk of the item (its partial's slice)
 };
 
 __device__ __forceinline__ int pf_tiles_of(int kv_lo, int hi)
@@ -123,17 +127,22 @@ __device__ __forceinline__ bool pf_item(const PrefillParams &p, const int32_t *p
     if (p.shared_prefix) {
         // one pseudo-sequence: all tokens of the batch, keys [0, kv_cap) of the
         // prefix every sequence shares, no mask (the prefix precedes every query)
+        // (keys of chunk `split` only; the chunks' partials are merged later)
         const int tiles = (p.num_tokens + kSuper - 1) / kSuper;
-        if (item >= tiles * p.num_heads)
+        const int per_split = tiles * p.num_heads;
+        if (item >= per_split * p.kv_splits)
             return false;
-        it.h = item % p.num_heads;
-        const int st_idx = tiles - 1 - item / p.num_heads;
+        it.split = item / per_split;
+        const int rem = item - it.split * per_split;
+        it.h = rem % p.num_heads;
+        const int st_idx = tiles - 1 - rem / p.num_heads;
         it.s = 0;
         qlen = p.num_tokens;
         it.t0 = st_idx * kSuper;
         it.qidx0 = it.t0;
-        it.L = p.kv_cap;
-        it.ctx = p.kv_cap;
+        it.kv_lo = p.kv_lo + it.split * p.split_tiles * kBN;
+        it.L = min(p.kv_cap, it.kv_lo + p.split_tiles * kBN);
+        it.ctx = it.L;
     } else {
         const int tiles = prefix[nseq];
         if (item >= tiles * p.num_heads)
@@ -157,6 +166,8 @@ __device__ __forceinline__ bool pf_item(const PrefillParams &p, const int32_t *p
         it.ctx = it.L - qlen;
         it.qidx0 = st_idx * kSuper;
         it.t0 = q0 + it.qidx0;
+        it.kv_lo = p.kv_lo;
+        it.split = 0;
     }
     it.rows[0] = max(0, min(kBM, qlen - it.qidx0));
     it.rows[1] = max(0, min(kBM, qlen - it.qidx0 - kBM));
@@ -170,7 +181,7 @@ __device__ __forceinline__ bool pf_item(const PrefillParams &p, const int32_t *p
                 hi = min(it.L, it.ctx + it.qidx0 + tl * kBM + it.rows[tl]);
             hi = min(hi, p.kv_cap);
         }
-        it.n_kv[tl] = it.rows[tl] > 0 ? pf_tiles_of(p.kv_lo, hi) : 0;
+        it.n_kv[tl] = it.rows[tl] > 0 ? pf_tiles_of(it.kv_lo, hi) : 0;
         all_hi = max(all_hi, hi);
     }
     it.kv_hi = all_hi;
@@ -268,7 +279,8 @@ __device__ __forceinline__ void pf_softmax(const PrefillParams &p, const int32_t
         if (nkv == 0) {
             // no admitted key at all: an empty part (cascade partial mode only)
             if (valid && p.partial) {
-                const int64_t row = int64_t(t - p.token_base) * p.num_heads + it.h;
+                const int64_t row =
+                    (int64_t(it.split) * p.num_tokens + t - p.token_base) * p.num_heads + it.h;
                 for (int d = 0; d < D; ++d)
                     p.o_part[row * D + d] = 0.f;
                 p.lse_part[row] = kPfNegInf;
@@ -291,7 +303,7 @@ __device__ __forceinline__ void pf_softmax(const PrefillParams &p, const int32_t
             for (int c = 0; c < 4; ++c)
                 tmem_ld32(ts + c * 32, x[c]);
             tmem_wait_ld();
-            const int lim = hi_row - (p.kv_lo + jt * kBN);  // columns c < lim admitted
+            const int lim = hi_row - (it.kv_lo + jt * kBN);  // columns c < lim admitted
             const bool full_tile = __all_sync(0xffffffffu, lim >= kBN);
             // row max of the raw logits: three-input max, four chains; the scale
             // is positive so max and scaling commute
@@ -381,7 +393,8 @@ __device__ __forceinline__ void pf_softmax(const PrefillParams &p, const int32_t
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const float lse2 = m + log2f(l);
             const int64_t orow = int64_t(t) * p.num_heads + it.h;
-            const int64_t prow = int64_t(t - p.token_base) * p.num_heads + it.h;
+            const int64_t prow =
+                (int64_t(it.split) * p.num_tokens + t - p.token_base) * p.num_heads + it.h;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
@@ -563,7 +576,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 // lane b owns TMA box b of every K/V tile; its block id is looked
                 // up for the next tile before waiting for a free stage
                 auto lane_block = [&](int jt) -> int {
-                    const int key0 = p.kv_lo + jt * kBN;
+                    const int key0 = it.kv_lo + jt * kBN;
                     const int nbox = (min(kBN, kv_hi - key0) + p.box_rows - 1) / p.box_rows;
                     if (lane >= nbox)
                         return -1;
@@ -599,7 +612,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     uint64_t *emp = which ? &bars.v_empty[st] : &bars.k_empty[st];
                     if (rnd > 0 && !pf_wait(emp, (rnd - 1) & 1, abort_flag))
                         return false;
-                    const int key0 = p.kv_lo + jt * kBN;
+                    const int key0 = it.kv_lo + jt * kBN;
                     const int nbox = (min(kBN, kv_hi - key0) + p.box_rows - 1) / p.box_rows;
                     const uint32_t bytes = nbox * p.box_rows * 128 * Cfg::kHalves;
                     uint64_t *bar = which ? &bars.v_full[st] : &bars.k_full[st];
@@ -683,7 +696,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                                 break;
                             }
                             ++p_cnt[tl];
-                            const int nvalid = it.kv_hi - (p.kv_lo + jp * kBN);
+                            const int nvalid = it.kv_hi - (it.kv_lo + jp * kBN);
                             const bool first_reader = tl == 0 || jp >= it.n_kv[0];
                             if (jp == n - 1 && nvalid < kBN && first_reader) {
                                 // rows past the last key may hold anything (or nothing
@@ -834,11 +847,18 @@ cudaError_t launch_prefill(const Fwd &f, const PrefillPass &pass)
     p.o_part = pass.o_part;
     p.lse_part = pass.lse_part;
     p.item_counter = pass.item_counter;
+    p.kv_splits = 1;
+    p.split_tiles = 0;
+    if (pass.shared_prefix) {
+        const int tiles = (pass.kv_cap - pass.kv_lo + kBN - 1) / kBN;
+        p.kv_splits = std::max(1, pass.kv_splits);
+        p.split_tiles = (tiles + p.kv_splits - 1) / p.kv_splits;
+    }
     if (cudaError_t e = cudaMemsetAsync(p.item_counter, 0, sizeof(int32_t), f.stream))
         return e;
     int64_t items;
     if (pass.shared_prefix)
-        items = int64_t((f.num_tokens + kSuper - 1) / kSuper) * f.num_heads;
+        items = int64_t((f.num_tokens + kSuper - 1) / kSuper) * f.num_heads * p.kv_splits;
     else
         items = (int64_t(f.num_tokens - f.num_decodes) + int64_t(nseq) * (kSuper - 1)) /
                 kSuper * f.num_heads;

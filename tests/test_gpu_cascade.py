@@ -23,6 +23,22 @@ def test_cascade_with_prefill_chunks(oracle, bs, P):
     G.check_batch(oracle, W.make_batch(sp, seed=4100 + bs), label=f"cascade bs={bs}")
 
 
+@pytest.mark.parametrize("H,Hkv,D,bs,P", [
+    (16, 2, 64, 16, 1008),    # 8 key tiles, the last one ragged: 2 chunks
+    (32, 8, 128, 64, 2048),   # 16 key tiles: 4 chunks
+    (64, 8, 128, 128, 4096),  # the cascade workload's shape: 2 chunks
+])
+def test_cascade_split_prefix(oracle, H, Hkv, D, bs, P):
+    """Prefixes long enough that the shared-prefix pass cuts its keys into
+    chunks (few work items, so the chunks fill the grid): one partial per
+    chunk, merged with the decode pieces and with the prefill suffixes."""
+    sp = W.BatchSpec("c5", H, Hkv, D, bs, decode_ctx=[P + 1, P + 17, P + 300, P + 129],
+                     prefill=[(33, P), (200, P + 40)], common_prefix_len=P)
+    b = W.make_batch(sp, seed=4300 + P)
+    G.check_batch(oracle, b, label=f"cascade split P={P}")
+    G.check_batch(oracle, b, split_kv_tokens=64, label=f"cascade split P={P}, 64 keys/CTA")
+
+
 def test_cascade_equals_plain(oracle):
     """The same batch with and without the cascade gives the same rows (both
     within tolerance of the oracle's plain attention)."""
