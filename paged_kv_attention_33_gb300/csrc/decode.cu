@@ -260,6 +260,60 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, int t, int s
     }
 }
 
+// Cascade, a sequence finished inside one warp: fold the pre_splits prefix
+// partials of its two heads (rows h0, h1 of token t) into this thread's slice
+// of the transposed accumulator o (dims 16*mt + gq and +8; o[mt][0|2] head h0,
+// o[mt][1|3] head h1), whose rows still need the scales sc0 / sc1 and whose
+// log2-sum-exps are ls0 / ls1.  On return o * sc is the merged row and ls its
+// log2-sum-exp.
+template <int D>
+__device__ __forceinline__ void merge_prefix_direct(const DecodeParams &p, int t, int h0, int h1,
+                                                    int gq, float (&o)[D / 16][4], float &sc0,
+                                                    float &sc1, float &ls0, float &ls1)
+{
+    const int64_t split_rows = int64_t(p.num_tokens) * p.num_heads;
+    const int64_t r0 = int64_t(t) * p.num_heads + h0;
+    const int64_t r1 = int64_t(t) * p.num_heads + h1;
+    float M0 = ls0, M1 = ls1;
+    for (int c = 0; c < p.pre_splits; ++c) {
+        M0 = fmaxf(M0, __ldg(p.lse_pre + c * split_rows + r0));
+        M1 = fmaxf(M1, __ldg(p.lse_pre + c * split_rows + r1));
+    }
+    // an empty part adds nothing
+    const float a0 = ls0 == kNegInf ? 0.f : exp2f(ls0 - M0);
+    const float a1 = ls1 == kNegInf ? 0.f : exp2f(ls1 - M1);
+    float W0 = a0, W1 = a1;
+    const float f0 = sc0 * a0, f1 = sc1 * a1;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+        o[mt][0] *= f0;
+        o[mt][2] *= f0;
+        o[mt][1] *= f1;
+        o[mt][3] *= f1;
+    }
+    for (int c = 0; c < p.pre_splits; ++c) {
+        const float l0 = __ldg(p.lse_pre + c * split_rows + r0);
+        const float l1 = __ldg(p.lse_pre + c * split_rows + r1);
+        const float w0 = l0 == kNegInf ? 0.f : exp2f(l0 - M0);
+        const float w1 = l1 == kNegInf ? 0.f : exp2f(l1 - M1);
+        W0 += w0;
+        W1 += w1;
+        const float *b0 = p.o_pre + (c * split_rows + r0) * D + gq;
+        const float *b1 = p.o_pre + (c * split_rows + r1) * D + gq;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            o[mt][0] += w0 * __ldg(b0 + 16 * mt);
+            o[mt][2] += w0 * __ldg(b0 + 16 * mt + 8);
+            o[mt][1] += w1 * __ldg(b1 + 16 * mt);
+            o[mt][3] += w1 * __ldg(b1 + 16 * mt + 8);
+        }
+    }
+    sc0 = W0 > 0.f ? 1.f / W0 : 0.f;
+    sc1 = W1 > 0.f ? 1.f / W1 : 0.f;
+    ls0 = W0 > 0.f ? M0 + log2f(W0) : kNegInf;
+    ls1 = W1 > 0.f ? M1 + log2f(W1) : kNegInf;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p)
@@ -431,9 +485,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     int s = s_first;
     int t = 0, L = 0;
     bool ok = true;
+    // the next piece's token and length are loaded one piece ahead
+    int t_nx = p.qsl[p.seq0 + s], L_nx = p.seq_lens[p.seq0 + s];
     auto begin_piece = [&]() {
-        t = p.qsl[p.seq0 + s];
-        L = p.seq_lens[p.seq0 + s];
+        t = t_nx;
+        L = L_nx;
+        if (s + 1 < nseq) {
+            t_nx = p.qsl[p.seq0 + s + 1];
+            L_nx = p.seq_lens[p.seq0 + s + 1];
+        }
         if (t < 0 || t >= p.num_tokens) {
             flag_error(kErrBadMetadata);
             t = 0;
@@ -522,31 +582,38 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const int bf = cta_of_stage(prefix[s], total, grid);
         const int bl = cta_of_stage(prefix[s + 1] - 1, total, grid);
         const int np = bl - bf + 1;
-        const bool direct = np == 1 && R == 1 && !p.cascade;
+        // a sequence inside one CTA (and one warp per kv head) is finished from
+        // registers; in a cascade its prefix partials are merged in right here
+        const bool direct = np == 1 && R == 1;
         const int n0 = 2 * tq, n1 = 2 * tq + 1;  // the two heads of this thread
         const float i0 = lr0 > 0.f ? 1.f / lr0 : 0.f;
         const float i1 = lr1 > 0.f ? 1.f / lr1 : 0.f;
         if (direct) {
             if (ok) {
+                float sc0 = i0, sc1 = i1;  // row scales of the output
+                float ls0 = m0 + log2f(lr0), ls1 = m1 + log2f(lr1);  // log2-sum-exp
+                if (p.cascade)
+                    merge_prefix_direct<D>(p, t, k * g + min(n0, g - 1), k * g + min(n1, g - 1), gq,
+                                           o, sc0, sc1, ls0, ls1);
 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt) {
                     const int d = 16 * mt + gq;
                     if (n0 < g) {
                         __nv_bfloat16 *dst = p.out + (int64_t(t) * H + k * g + n0) * D;
-                        dst[d] = __float2bfloat16_rn(o[mt][0] * i0);
-                        dst[d + 8] = __float2bfloat16_rn(o[mt][2] * i0);
+                        dst[d] = __float2bfloat16_rn(o[mt][0] * sc0);
+                        dst[d + 8] = __float2bfloat16_rn(o[mt][2] * sc0);
                     }
                     if (n1 < g) {
                         __nv_bfloat16 *dst = p.out + (int64_t(t) * H + k * g + n1) * D;
-                        dst[d] = __float2bfloat16_rn(o[mt][1] * i1);
-                        dst[d + 8] = __float2bfloat16_rn(o[mt][3] * i1);
+                        dst[d] = __float2bfloat16_rn(o[mt][1] * sc1);
+                        dst[d + 8] = __float2bfloat16_rn(o[mt][3] * sc1);
                     }
                 }
                 if (gq == 0 && p.lse) {
                     if (n0 < g)
-                        p.lse[int64_t(t) * H + k * g + n0] = (m0 + log2f(lr0)) * kLn2;
+                        p.lse[int64_t(t) * H + k * g + n0] = ls0 * kLn2;
                     if (n1 < g)
-                        p.lse[int64_t(t) * H + k * g + n1] = (m1 + log2f(lr1)) * kLn2;
+                        p.lse[int64_t(t) * H + k * g + n1] = ls1 * kLn2;
                 }
             }
         } else {
