@@ -236,4 +236,32 @@ __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t chunk)
     return row * 128u + ((chunk ^ (row & 7u)) << 4);
 }
 
+// Exclusive prefix sum of one int per thread over a block of kThreads (a
+// multiple of 32) threads; the block total goes to *total.  Warp-level
+// inclusive scans by shuffle, then each warp adds the totals of the warps
+// before it.  Contains __syncthreads(): every thread of the block must call it.
+template <int kThreads>
+__device__ __forceinline__ int block_exclusive_scan(int v, int32_t *total)
+{
+    static_assert(kThreads % 32 == 0 && kThreads <= 1024, "block size");
+    __shared__ int32_t warp_tot[kThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o)
+            inc += y;
+    }
+    if (lane == 31)
+        warp_tot[warp] = inc;
+    __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w)
+        base += warp_tot[w];
+    if (threadIdx.x == kThreads - 1)
+        *total = base + inc;
+    return base + inc - v;
+}
+
 }  // namespace pka

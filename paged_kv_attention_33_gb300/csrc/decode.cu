@@ -45,6 +45,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -173,73 +174,82 @@ __device__ __forceinline__ float warp_sum32(float v)
 // Merge the partials of decode s (token t): its nparts pieces -- part q lives
 // in slot (bf + q / R + s), sub-row q % R -- and, in a cascade, the
 // pre_splits partials of the shared prefix (key chunk c at rows c*T*H + t*H +
-// h).  Warp w takes heads w, w+8, ..., kHB of them at a time: lane q holds part
-// q's log2-sum-exp, so the maximum and the weights come from shuffles, and the
-// rows of all kHB heads are loaded together (lanes along head_size), so a
-// merge costs a few L2 round trips, not one per head.
+// h).  Warp w takes heads w, w+8, ..., kHB of them at a time, lanes along
+// head_size.  The parts are folded in rounds of kQB: every load of a round
+// (kQB x kHB log2-sum-exps and rows) is issued before any is used, so a merge
+// costs about one L2 round trip per round -- it runs at the end of a CTA's
+// range, while the other SMs still stream, where each round trip is long.
 template <int D>
 __device__ __forceinline__ void merge_pieces(const DecodeParams &p, int t, int s, int bf,
                                              int nparts, int R, int warp, int lane)
 {
     constexpr int kPer = D / 32;  // dims per lane
     constexpr int kHB = 4;        // heads per batch
+    constexpr int kQB = 2;        // parts per round
+    using Vec = typename std::conditional<kPer == 4, float4, float2>::type;
     const int H = p.num_heads;
     const int ntot = nparts + (p.cascade ? p.pre_splits : 0);
     auto row_of = [&](int q, int h) -> int64_t {  // row of part q, head h
         return q < nparts ? (int64_t(bf + q / R + s) * R + q % R) * H + h
                           : (int64_t(q - nparts) * p.num_tokens + t) * H + h;
     };
-    auto lse_of = [&](int q, int h) {
-        return __ldcg((q < nparts ? p.lse_part : p.lse_pre) + row_of(q, h));
-    };
     for (int h0 = warp; h0 < H; h0 += kHB * kConsumerWarps) {
-        float wl[kHB], M[kHB], W[kHB];
-        float acc[kHB][kPer];
+        float M[kHB], W[kHB], acc[kHB][kPer];
 #pragma unroll
         for (int j = 0; j < kHB; ++j) {
-            const int h = h0 + j * kConsumerWarps;
-            wl[j] = h < H && lane < ntot ? lse_of(lane, h) : kNegInf;
-        }
-#pragma unroll
-        for (int j = 0; j < kHB; ++j) {
-            const int h = h0 + j * kConsumerWarps;
-            float m = wl[j];
-            for (int q = lane + 32; q < ntot && h < H; q += 32)  // more than 32 parts
-                m = fmaxf(m, lse_of(q, h));
-            M[j] = warp_max32(m);
-            // an empty part adds nothing
-            wl[j] = wl[j] == kNegInf ? 0.f : exp2f(wl[j] - M[j]);
-            W[j] = warp_sum32(wl[j]);
+            M[j] = kNegInf;
+            W[j] = 0.f;
 #pragma unroll
             for (int e = 0; e < kPer; ++e)
                 acc[j][e] = 0.f;
         }
-#pragma unroll 2
-        for (int q = 0; q < ntot; ++q) {
-            const float *obase = q < nparts ? p.o_part : p.o_pre;
+        for (int q0 = 0; q0 < ntot; q0 += kQB) {
+            float lq[kQB][kHB];
+            Vec v[kQB][kHB];
 #pragma unroll
-            for (int j = 0; j < kHB; ++j) {
-                const int h = h0 + j * kConsumerWarps;
-                float w = __shfl_sync(0xffffffffu, wl[j], q & 31);
-                if (q >= 32) {  // warp-uniform
-                    const float lq = h < H ? lse_of(q, h) : kNegInf;
-                    w = lq == kNegInf ? 0.f : exp2f(lq - M[j]);
-                    W[j] += w;
-                }
-                if (h < H) {
-                    const float *src = obase + row_of(q, h) * D + lane * kPer;
-                    if constexpr (kPer == 4) {
-                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
-                        acc[j][0] += w * v.x;
-                        acc[j][1] += w * v.y;
-                        acc[j][2] += w * v.z;
-                        acc[j][3] += w * v.w;
+            for (int i = 0; i < kQB; ++i) {
+                const int q = q0 + i;
+                // the kHB heads of part q are rows row0 + 8j: one base address
+                const int64_t row0 = row_of(q < ntot ? q : 0, h0);
+                const float *lq_p = (q < nparts ? p.lse_part : p.lse_pre) + row0;
+                const Vec *v_p =
+                    reinterpret_cast<const Vec *>((q < nparts ? p.o_part : p.o_pre) + row0 * D) +
+                    lane;
+#pragma unroll
+                for (int j = 0; j < kHB; ++j) {
+                    if (q < ntot && h0 + j * kConsumerWarps < H) {
+                        lq[i][j] = __ldcg(lq_p + j * kConsumerWarps);
+                        v[i][j] = __ldcg(v_p + j * kConsumerWarps * (D / kPer));
                     } else {
-                        const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
-                        acc[j][0] += w * v.x;
-                        acc[j][1] += w * v.y;
+                        lq[i][j] = kNegInf;
+                        v[i][j] = Vec{};
                     }
                 }
+            }
+#pragma unroll
+            for (int j = 0; j < kHB; ++j) {
+                float mr = M[j];
+#pragma unroll
+                for (int i = 0; i < kQB; ++i)
+                    mr = fmaxf(mr, lq[i][j]);
+                if (mr == kNegInf)
+                    continue;  // every part so far is empty
+                const float a = exp2f(M[j] - mr);
+                W[j] *= a;
+#pragma unroll
+                for (int e = 0; e < kPer; ++e)
+                    acc[j][e] *= a;
+#pragma unroll
+                for (int i = 0; i < kQB; ++i) {
+                    // an empty part adds nothing, whatever its row holds
+                    const float w = lq[i][j] == kNegInf ? 0.f : exp2f(lq[i][j] - mr);
+                    W[j] += w;
+                    const float *x = reinterpret_cast<const float *>(&v[i][j]);
+#pragma unroll
+                    for (int e = 0; e < kPer; ++e)
+                        acc[j][e] += w * x[e];
+                }
+                M[j] = mr;
             }
         }
 #pragma unroll
@@ -335,28 +345,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const int lane = threadIdx.x & 31;
     const int nseq = p.nseq;
 
-    // ---- stage prefix sums over the decodes of this launch (block-wide scan)
+    // ---- stage prefix sums over the decodes of this launch: each thread sums a
+    // run of decodes, then a block-wide exclusive scan of the run sums
     {
-        __shared__ int32_t part[kDecodeThreads];
         const int per = (nseq + kDecodeThreads - 1) / kDecodeThreads;
         const int a = min(nseq, int(threadIdx.x) * per);
         const int e = min(nseq, a + per);
         int sum = 0;
         for (int k = a; k < e; ++k)
             sum += dec_stages(p, k, stage_keys);
-        part[threadIdx.x] = sum;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            int run = 0;
-            for (int i = 0; i < kDecodeThreads; ++i) {
-                const int v = part[i];
-                part[i] = run;
-                run += v;
-            }
-            prefix[nseq] = run;
-        }
-        __syncthreads();
-        int run = part[threadIdx.x];
+        int run = block_exclusive_scan<kDecodeThreads>(sum, prefix + nseq);
         for (int k = a; k < e; ++k) {
             prefix[k] = run;
             run += dec_stages(p, k, stage_keys);

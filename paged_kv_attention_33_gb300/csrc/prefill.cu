@@ -473,7 +473,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
     // ---- prefix sums of 256-query super-tiles per prefill sequence
     {
-        __shared__ int32_t part[kPfThreads];
         const int per = (nseq + kPfThreads - 1) / kPfThreads;
         const int a = min(nseq, int(threadIdx.x) * per);
         const int e = min(nseq, a + per);
@@ -483,19 +482,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const int ql = p.qsl[s + 1] - p.qsl[s];
             sum += ql > 0 ? (ql + kSuper - 1) / kSuper : 0;
         }
-        part[threadIdx.x] = sum;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            int run = 0;
-            for (int i = 0; i < kPfThreads; ++i) {
-                const int v = part[i];
-                part[i] = run;
-                run += v;
-            }
-            prefix[nseq] = run;
-        }
-        __syncthreads();
-        int run = part[threadIdx.x];
+        int run = block_exclusive_scan<kPfThreads>(sum, prefix + nseq);
         for (int k = a; k < e; ++k) {
             prefix[k] = run;
             const int s = p.first_seq + k;
