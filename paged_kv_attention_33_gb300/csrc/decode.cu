@@ -419,15 +419,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const int k = u % Hkv;
         int s = s_first;
         auto lookup = [&](int64_t x, int seq, int &row, int &slices) {
-            const int L = p.seq_lens[p.seq0 + seq];
+            // the table entry is read before the length is known (the row of
+            // the table is in bounds), so that both loads are in flight at once
             const int k0 = p.kv_begin + int(x - prefix[seq]) * stage_keys;
+            const int ks = k0 + 16 * r;
+            const int col = ks / p.block_size;
+            const int32_t *bt = p.block_table + int64_t(p.seq0 + seq) * p.bt_stride;
+            const int blk_raw = lane < kOps && col < p.bt_stride ? bt[col] : -1;
+            const int L = p.seq_lens[p.seq0 + seq];
             slices = max(0, min(R, (L - k0 + 15) / 16));
             row = -1;
             if (lane < kOps && r < slices) {
-                const int ks = k0 + 16 * r;
-                const int col = ks / p.block_size;
-                const int32_t *bt = p.block_table + int64_t(p.seq0 + seq) * p.bt_stride;
-                int blk = col < p.bt_stride ? bt[col] : -1;
+                int blk = blk_raw;
                 if (blk < 0 || blk >= p.num_blocks) {
                     flag_error(kErrBlockOutOfPool);
                     blk = 0;  // keep the transaction count whole; result is flagged
@@ -440,11 +443,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         for (int64_t x = lo; x < hi; ++x) {
             const int i = int(x - lo);
             const int row = row_next, slices = slices_next;
-            if (x + 1 < hi) {
-                while (prefix[s + 1] <= x + 1)
-                    ++s;
-                lookup(x + 1, s, row_next, slices_next);
-            }
             const int slot = i % Cfg::kStages;
             const int round = i / Cfg::kStages;
             if (round > 0 && !dec_wait(&empty[slot], (round - 1) & 1, abort_flag))
@@ -457,6 +455,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 uint8_t *dst = smem + slot * Cfg::kStageBytes + kv * Cfg::kKvBytes +
                                u * Cfg::kUnitBytes + half * 2048;
                 tma_load_3d(dst, &kv_map, &full[slot], half * 64, k, row, policy);
+            }
+            // the next stage's blocks are looked up after this one is issued
+            if (x + 1 < hi) {
+                while (prefix[s + 1] <= x + 1)
+                    ++s;
+                lookup(x + 1, s, row_next, slices_next);
             }
         }
         return;
