@@ -81,7 +81,23 @@ typedef enum {
  *                   CTA per SM); else a target number of keys per CTA, which
  *                   uses fewer CTAs when the batch is small (a tuning and
  *                   test knob; results are the same either way).
+ *  kv_layout        physical order of the pool (pka_kv_layout): PKA_LAYOUT_NHD
+ *                   (0, the default of a zero-initialised struct) or
+ *                   PKA_LAYOUT_HND.
  */
+
+/*
+ * Physical layouts of the pool ([FA/FI] "Resumen en una frase": the two
+ * layouts NHD / HND, chosen by get_kv_cache_stride_order).  The logical shape
+ * is always [num_blocks, 2, block_size, num_kv_heads, head_size]; the layout
+ * says which of block_size and num_kv_heads varies faster in memory:
+ *  NHD  [num_blocks, 2, block_size, num_kv_heads, head_size] -- the K (or V)
+ *       rows of one slot, all heads, are contiguous;
+ *  HND  [num_blocks, 2, num_kv_heads, block_size, head_size] -- the page of
+ *       one head (block_size rows) is contiguous.
+ */
+typedef enum { PKA_LAYOUT_NHD = 0, PKA_LAYOUT_HND = 1 } pka_kv_layout;
+
 typedef struct {
     const int32_t *query_start_loc;
     const int32_t *seq_lens;
@@ -93,6 +109,7 @@ typedef struct {
     int32_t max_seq_len;
     int32_t common_prefix_len;
     int32_t split_kv_tokens;
+    int32_t kv_layout;
 } pka_meta;
 
 /*
@@ -118,6 +135,17 @@ pka_status pka_reshape_and_cache(const void *key, const void *value, void *kv_ca
                                  const int64_t *slot_mapping, int32_t num_tokens,
                                  int32_t num_kv_heads, int32_t head_size, int32_t block_size,
                                  int64_t num_blocks, void *stream);
+
+/*
+ * pka_reshape_and_cache for a pool in the physical layout `kv_layout`
+ * (pka_kv_layout); PKA_LAYOUT_NHD is exactly pka_reshape_and_cache.  In HND
+ * the row of head k of slot (b, o) is at [b][kv][k][o].  Errors as
+ * pka_reshape_and_cache, plus PKA_ERR_INVALID_ARG for an unknown layout.
+ */
+pka_status pka_reshape_and_cache_ex(const void *key, const void *value, void *kv_cache,
+                                    const int64_t *slot_mapping, int32_t num_tokens,
+                                    int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                    int64_t num_blocks, int32_t kv_layout, void *stream);
 
 /*
  * Bytes of device workspace pka_paged_attn_forward needs for this batch

@@ -22,7 +22,7 @@ import threading
 
 from . import build as _build
 
-__all__ = ["Meta", "PkaError", "reshape_and_cache", "paged_attn_forward", "cascade_merge",
+__all__ = ["Meta", "PkaError", "LAYOUT_NHD", "LAYOUT_HND", "reshape_and_cache", "paged_attn_forward", "cascade_merge",
            "paged_attn_forward_noalloc", "workspace_size", "check_status", "set_kernel_events", "kernel_launches",
            "load_library",
            "library_path", "KERNEL_DECODE", "KERNEL_PREFILL"]
@@ -47,7 +47,25 @@ class _CMeta(ctypes.Structure):
     _fields_ = [("query_start_loc", _P), ("seq_lens", _P), ("block_table", _P),
                 ("block_table_stride", _I32), ("num_seqs", _I32), ("num_decodes", _I32),
                 ("max_query_len", _I32), ("max_seq_len", _I32), ("common_prefix_len", _I32),
-                ("split_kv_tokens", _I32)]
+                ("split_kv_tokens", _I32), ("kv_layout", _I32)]
+
+# Physical pool layouts (pka_kv_layout): the logical shape is always
+# [num_blocks, 2, block_size, num_kv_heads, head_size]; HND stores it as
+# [num_blocks, 2, num_kv_heads, block_size, head_size].
+LAYOUT_NHD = 0
+LAYOUT_HND = 1
+
+
+def _layout(kv_layout) -> int:
+    if isinstance(kv_layout, str):
+        return {"NHD": LAYOUT_NHD, "HND": LAYOUT_HND}[kv_layout.upper()]
+    return int(kv_layout)
+
+
+def _pool_dims(kv_cache, kv_layout):
+    """(num_blocks, block_size, num_kv_heads, head_size) of a pool tensor."""
+    nb, _, a, b, d = kv_cache.shape
+    return (nb, b, a, d) if _layout(kv_layout) == LAYOUT_HND else (nb, a, b, d)
 
 
 def library_path() -> str:
@@ -69,6 +87,9 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib = ctypes.CDLL(path)
         lib.pka_reshape_and_cache.argtypes = [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I64, _P]
         lib.pka_reshape_and_cache.restype = ctypes.c_int
+        lib.pka_reshape_and_cache_ex.argtypes = [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I64,
+                                                 _I32, _P]
+        lib.pka_reshape_and_cache_ex.restype = ctypes.c_int
         lib.pka_workspace_size.argtypes = [ctypes.POINTER(_CMeta), _I32, _I32, _I32, _I32, _I32]
         lib.pka_workspace_size.restype = ctypes.c_size_t
         lib.pka_paged_attn_forward.argtypes = [_P, _P, ctypes.POINTER(_CMeta), _P, _P, _I32,
@@ -116,11 +137,12 @@ class Meta:
 
     query_start_loc int32 [S+1], seq_lens int32 [S], block_table int32
     [S, stride] live on the device; num_decodes, max_query_len, max_seq_len,
-    common_prefix_len and split_kv_tokens are host integers.
+    common_prefix_len, split_kv_tokens and kv_layout (LAYOUT_NHD / LAYOUT_HND,
+    or "NHD" / "HND") are host values.
     """
 
     def __init__(self, query_start_loc, seq_lens, block_table, num_decodes, max_query_len,
-                 max_seq_len, common_prefix_len=0, split_kv_tokens=0):
+                 max_seq_len, common_prefix_len=0, split_kv_tokens=0, kv_layout=LAYOUT_NHD):
         self.query_start_loc = query_start_loc
         self.seq_lens = seq_lens
         self.block_table = block_table
@@ -129,10 +151,11 @@ class Meta:
         self.max_seq_len = int(max_seq_len)
         self.common_prefix_len = int(common_prefix_len)
         self.split_kv_tokens = int(split_kv_tokens)
+        self.kv_layout = _layout(kv_layout)
 
     @classmethod
     def from_host(cls, query_start_loc, seq_lens, block_table, num_decodes, device,
-                  common_prefix_len=0, split_kv_tokens=0):
+                  common_prefix_len=0, split_kv_tokens=0, kv_layout=LAYOUT_NHD):
         """Build from host (numpy) arrays, copying them to `device`."""
         import numpy as np
         import torch
@@ -146,21 +169,25 @@ class Meta:
         max_s = int(sl.max()) if len(sl) else 1
         return cls(torch.from_numpy(qsl).to(device), torch.from_numpy(sl).to(device),
                    torch.from_numpy(bt).to(device), nd, max_q, max_s, common_prefix_len,
-                   split_kv_tokens)
+                   split_kv_tokens, kv_layout)
 
     def _c(self) -> _CMeta:
         return _CMeta(self.query_start_loc.data_ptr(), self.seq_lens.data_ptr(),
                       self.block_table.data_ptr(), self.block_table.shape[1],
                       self.seq_lens.shape[0], self.num_decodes, self.max_query_len,
-                      self.max_seq_len, self.common_prefix_len, self.split_kv_tokens)
+                      self.max_seq_len, self.common_prefix_len, self.split_kv_tokens,
+                      self.kv_layout)
 
 
-def reshape_and_cache(key, value, kv_cache, slot_mapping, stream=None) -> None:
-    """Scatter key/value [T, Hkv, D] rows into kv_cache [NB, 2, bs, Hkv, D] at slot_mapping."""
+def reshape_and_cache(key, value, kv_cache, slot_mapping, stream=None,
+                      kv_layout=LAYOUT_NHD) -> None:
+    """Scatter key/value [T, Hkv, D] rows into kv_cache at slot_mapping; the pool
+    is [NB, 2, bs, Hkv, D] (NHD) or [NB, 2, Hkv, bs, D] (HND)."""
     lib = load_library()
-    nb, two, bs, hkv, d = kv_cache.shape
-    _check(lib.pka_reshape_and_cache(_ptr(key), _ptr(value), _ptr(kv_cache), _ptr(slot_mapping),
-                                     key.shape[0], hkv, d, bs, nb, _stream(stream)))
+    nb, bs, hkv, d = _pool_dims(kv_cache, kv_layout)
+    _check(lib.pka_reshape_and_cache_ex(_ptr(key), _ptr(value), _ptr(kv_cache),
+                                        _ptr(slot_mapping), key.shape[0], hkv, d, bs, nb,
+                                        _layout(kv_layout), _stream(stream)))
 
 
 def workspace_size(meta: Meta, num_tokens, num_heads, num_kv_heads, head_size, block_size) -> int:
@@ -177,7 +204,7 @@ def paged_attn_forward(query, kv_cache, meta: Meta, out, lse=None, scale=None, c
 
     lib = load_library()
     T, H, D = query.shape
-    nb, _, bs, hkv, _ = kv_cache.shape
+    nb, bs, hkv, _ = _pool_dims(kv_cache, meta.kv_layout)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     cm = meta._c()
@@ -199,7 +226,7 @@ def paged_attn_forward_noalloc(query, kv_cache, meta: Meta, out, lse=None, scale
     Calls that overlap on the GPU share that scratch and must be serialised."""
     lib = load_library()
     T, H, D = query.shape
-    nb, _, bs, hkv, _ = kv_cache.shape
+    nb, bs, hkv, _ = _pool_dims(kv_cache, meta.kv_layout)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     cm = meta._c()

@@ -117,16 +117,17 @@ CUresult encode_3d_bf16(CUtensorMap *map, const void *base, uint64_t d0, uint64_
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-// The pool [num_blocks, 2, block_size, num_kv_heads, head_size] seen as the
-// 3-D tensor (head_size, num_kv_heads, num_blocks*2*block_size); one box is
-// {64 dims, 1 head, 16 rows}, 128-byte swizzled.
 CUresult encode_kv_map(CUtensorMap *map, const void *cache, int32_t head_size,
-                       int32_t num_kv_heads, int32_t block_size, int64_t num_blocks)
+                       int32_t num_kv_heads, int32_t block_size, int64_t num_blocks, int32_t hnd,
+                       uint32_t box_rows)
 {
-    return encode_3d_bf16(map, cache, uint64_t(head_size), uint64_t(num_kv_heads),
-                          uint64_t(num_blocks) * 2 * uint64_t(block_size),
-                          uint64_t(head_size) * 2, uint64_t(num_kv_heads) * head_size * 2, 64, 1,
-                          16);
+    const uint64_t D = uint64_t(head_size), Hkv = uint64_t(num_kv_heads),
+                   bs = uint64_t(block_size), pages = uint64_t(num_blocks) * 2;
+    const uint64_t row = D * 2;  // bytes of one (slot, head) row
+    if (hnd)  // (dim, offset, page*Hkv + head): a head's page is bs contiguous rows
+        return encode_3d_bf16(map, cache, D, bs, pages * Hkv, row, row * bs, 64, box_rows, 1);
+    // (dim, head, page*bs + offset): a slot's heads are Hkv contiguous rows
+    return encode_3d_bf16(map, cache, D, Hkv, pages * bs, row, row * Hkv, 64, 1, box_rows);
 }
 
 // ------------------------------------------------------------ planning
@@ -184,6 +185,8 @@ static pka_status check_shape(const pka_meta *m, int32_t num_tokens, int32_t num
 {
     if (!m)
         return fail(PKA_ERR_INVALID_ARG, "meta is NULL");
+    if (m->kv_layout != PKA_LAYOUT_NHD && m->kv_layout != PKA_LAYOUT_HND)
+        return fail(PKA_ERR_INVALID_ARG, "unknown kv_layout %d", m->kv_layout);
     if (block_size <= 0 || block_size % 16 != 0)
         return fail(PKA_ERR_INVALID_ARG, "Block size must be a multiple of 16 (got %d).",
                     block_size);
@@ -253,6 +256,17 @@ pka_status pka_reshape_and_cache(const void *key, const void *value, void *kv_ca
                                  int32_t num_kv_heads, int32_t head_size, int32_t block_size,
                                  int64_t num_blocks, void *stream)
 {
+    return pka_reshape_and_cache_ex(key, value, kv_cache, slot_mapping, num_tokens, num_kv_heads,
+                                    head_size, block_size, num_blocks, PKA_LAYOUT_NHD, stream);
+}
+
+pka_status pka_reshape_and_cache_ex(const void *key, const void *value, void *kv_cache,
+                                    const int64_t *slot_mapping, int32_t num_tokens,
+                                    int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                    int64_t num_blocks, int32_t kv_layout, void *stream)
+{
+    if (kv_layout != PKA_LAYOUT_NHD && kv_layout != PKA_LAYOUT_HND)
+        return fail(PKA_ERR_INVALID_ARG, "unknown kv_layout %d", kv_layout);
     if (num_tokens < 0)
         return fail(PKA_ERR_INVALID_ARG, "num_tokens < 0");
     if (block_size <= 0 || block_size % 16 != 0)
@@ -271,6 +285,7 @@ pka_status pka_reshape_and_cache(const void *key, const void *value, void *kv_ca
         return fail(PKA_ERR_INVALID_ARG, "misaligned pointer (16 bytes required)");
     cudaError_t e = launch_reshape_and_cache(key, value, kv_cache, slot_mapping, num_tokens,
                                              num_kv_heads, head_size, block_size, num_blocks,
+                                             kv_layout == PKA_LAYOUT_HND ? 1 : 0,
                                              static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "reshape_and_cache launch");
@@ -313,8 +328,11 @@ pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const
         return fail(PKA_ERR_INVALID_ARG, "out must not alias query");
     if (num_blocks <= 0)
         return fail(PKA_ERR_INVALID_ARG, "num_blocks must be positive");
-    if (num_blocks * 2 * int64_t(block_size) >= (int64_t(1) << 31))
-        return fail(PKA_ERR_UNSUPPORTED, "pool has more than 2^31 token rows");
+    // the TMA row coordinate (page*block_size + offset, or page*num_kv_heads
+    // + head in HND) is a 32-bit integer
+    if (num_blocks * 2 * int64_t(meta->kv_layout == PKA_LAYOUT_HND ? num_kv_heads : block_size) >=
+        (int64_t(1) << 31))
+        return fail(PKA_ERR_UNSUPPORTED, "pool has more than 2^31 rows");
     if (!(scale > 0.f) || scale != scale || scale > 1e30f)
         return fail(PKA_ERR_INVALID_ARG, "scale must be a positive finite number");
 
@@ -345,6 +363,7 @@ pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const
     f.head_size = head_size;
     f.block_size = block_size;
     f.num_blocks = num_blocks;
+    f.kv_hnd = meta->kv_layout == PKA_LAYOUT_HND ? 1 : 0;
     f.scale = scale;
     f.causal = causal;
     f.stream = static_cast<cudaStream_t>(stream);
@@ -361,7 +380,8 @@ pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const
     char *wsp = static_cast<char *>(workspace);
 
     CUtensorMap kv_map;
-    CUresult cr = encode_kv_map(&kv_map, kv_cache, head_size, num_kv_heads, block_size, num_blocks);
+    CUresult cr = encode_kv_map(&kv_map, kv_cache, head_size, num_kv_heads, block_size, num_blocks,
+                                f.kv_hnd, 16);
     if (cr != CUDA_SUCCESS)
         return fail(PKA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(cr));
 

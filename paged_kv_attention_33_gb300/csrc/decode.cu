@@ -324,7 +324,7 @@ __device__ __forceinline__ void merge_prefix_direct(const DecodeParams &p, int t
     ls1 = W1 > 0.f ? M1 + log2f(W1) : kNegInf;
 }
 
-template <int D>
+template <int D, bool kHnd>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p)
 {
@@ -418,7 +418,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const int r = u / Hkv;
         const int k = u % Hkv;
         int s = s_first;
-        auto lookup = [&](int64_t x, int seq, int &row, int &slices) {
+        // TMA coordinates of the unit's 16 keys in the pool map: NHD (head,
+        // page*bs + offset), HND (offset, page*Hkv + head), page = block*2 + (K|V);
+        // row = -1: no keys
+        auto lookup = [&](int64_t x, int seq, int &row, int &c1, int &slices) {
             // the table entry is read before the length is known (the row of
             // the table is in bounds), so that both loads are in flight at once
             const int k0 = p.kv_begin + int(x - prefix[seq]) * stage_keys;
@@ -429,20 +432,22 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             const int L = p.seq_lens[p.seq0 + seq];
             slices = max(0, min(R, (L - k0 + 15) / 16));
             row = -1;
+            c1 = kHnd ? ks % p.block_size : k;
             if (lane < kOps && r < slices) {
                 int blk = blk_raw;
                 if (blk < 0 || blk >= p.num_blocks) {
                     flag_error(kErrBlockOutOfPool);
                     blk = 0;  // keep the transaction count whole; result is flagged
                 }
-                row = (blk * 2 + kv) * p.block_size + (ks % p.block_size);
+                row = kHnd ? (blk * 2 + kv) * Hkv + k
+                           : (blk * 2 + kv) * p.block_size + (ks % p.block_size);
             }
         };
-        int row_next, slices_next;
-        lookup(lo, s, row_next, slices_next);
+        int row_next, c1_next, slices_next;
+        lookup(lo, s, row_next, c1_next, slices_next);
         for (int64_t x = lo; x < hi; ++x) {
             const int i = int(x - lo);
-            const int row = row_next, slices = slices_next;
+            const int row = row_next, c1 = c1_next, slices = slices_next;
             const int slot = i % Cfg::kStages;
             const int round = i / Cfg::kStages;
             if (round > 0 && !dec_wait(&empty[slot], (round - 1) & 1, abort_flag))
@@ -454,13 +459,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             if (row >= 0) {
                 uint8_t *dst = smem + slot * Cfg::kStageBytes + kv * Cfg::kKvBytes +
                                u * Cfg::kUnitBytes + half * 2048;
-                tma_load_3d(dst, &kv_map, &full[slot], half * 64, k, row, policy);
+                tma_load_3d(dst, &kv_map, &full[slot], half * 64, c1, row, policy);
             }
             // the next stage's blocks are looked up after this one is issued
             if (x + 1 < hi) {
                 while (prefix[s + 1] <= x + 1)
                     ++s;
-                lookup(x + 1, s, row_next, slices_next);
+                lookup(x + 1, s, row_next, c1_next, slices_next);
             }
         }
         return;
@@ -743,7 +748,7 @@ DecodePlan plan_decode(int32_t split_kv_tokens, int32_t num_decodes, int32_t num
     return dp;
 }
 
-template <int D>
+template <int D, bool kHnd>
 static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Workspace &ws,
                                    char *wsp, const CUtensorMap &kv_map, int32_t kv_begin,
                                    bool cascade)
@@ -753,7 +758,7 @@ static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Wor
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D>,
+        cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D, kHnd>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(Cfg::kSmemBytes));
         if (e != cudaSuccess)
@@ -793,7 +798,8 @@ static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Wor
         if (e != cudaSuccess)
             return e;
         count_launch();
-        paged_decode_kernel<D><<<dp.grid, kDecodeThreads, Cfg::kSmemBytes, f.stream>>>(kv_map, p);
+        paged_decode_kernel<D, kHnd>
+            <<<dp.grid, kDecodeThreads, Cfg::kSmemBytes, f.stream>>>(kv_map, p);
         e = cudaGetLastError();
         if (e != cudaSuccess)
             return e;
@@ -807,8 +813,10 @@ cudaError_t launch_decode(const Fwd &f, const DecodePlan &dp, const Workspace &w
     if (f.num_decodes == 0)
         return cudaSuccess;
     if (f.head_size == 128)
-        return launch_decode_d<128>(f, dp, ws, wsp, kv_map, kv_begin, cascade);
-    return launch_decode_d<64>(f, dp, ws, wsp, kv_map, kv_begin, cascade);
+        return f.kv_hnd ? launch_decode_d<128, true>(f, dp, ws, wsp, kv_map, kv_begin, cascade)
+                        : launch_decode_d<128, false>(f, dp, ws, wsp, kv_map, kv_begin, cascade);
+    return f.kv_hnd ? launch_decode_d<64, true>(f, dp, ws, wsp, kv_map, kv_begin, cascade)
+                    : launch_decode_d<64, false>(f, dp, ws, wsp, kv_map, kv_begin, cascade);
 }
 
 cudaError_t launch_cascade_prefill_combine(const Fwd &f, const Workspace &ws, char *wsp)

@@ -31,6 +31,7 @@ struct Fwd {
     int32_t head_size;
     int32_t block_size;
     int64_t num_blocks;
+    int32_t kv_hnd;  // 1: pool in HND order, 0: NHD
     float scale;
     int32_t causal;
     cudaStream_t stream;
@@ -73,7 +74,8 @@ Workspace plan_workspace(const DecodePlan &dp, int32_t num_tokens, int32_t num_d
 cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *cache,
                                      const int64_t *slots, int32_t num_tokens,
                                      int32_t num_kv_heads, int32_t head_size,
-                                     int32_t block_size, int64_t num_blocks, cudaStream_t st);
+                                     int32_t block_size, int64_t num_blocks, int32_t hnd,
+                                     cudaStream_t st);
 uint32_t kv_write_take_error();
 
 // decode.cu: paged decode of sequences [0, num_decodes) over keys
@@ -124,7 +126,15 @@ constexpr int kMaxPrefillSeqsPerCall = 4096;
 CUresult encode_3d_bf16(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1,
                         uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes,
                         uint32_t box0, uint32_t box1, uint32_t box2);
+// The pool as a 3-D tensor whose box {64 dims, 1, rows} (NHD) / {64, rows, 1}
+// (HND) reads `rows` consecutive keys of one head of one page (page = block*2
+// + kv), 128-byte swizzled, in the same shared-memory layout either way:
+//   NHD  (head_size, num_kv_heads, pages*block_size), coordinates
+//        (dim, head, page*block_size + offset);
+//   HND  (head_size, block_size, pages*num_kv_heads), coordinates
+//        (dim, offset, page*num_kv_heads + head).
 CUresult encode_kv_map(CUtensorMap *map, const void *cache, int32_t head_size,
-                       int32_t num_kv_heads, int32_t block_size, int64_t num_blocks);
+                       int32_t num_kv_heads, int32_t block_size, int64_t num_blocks, int32_t hnd,
+                       uint32_t box_rows);
 
 }  // namespace pka

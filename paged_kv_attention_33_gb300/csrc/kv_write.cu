@@ -3,11 +3,14 @@
 //
 // Pool layout [num_blocks, 2, block_size, num_kv_heads, head_size] (the
 // "FlashAttention y FlashInfer" page, "Flujo de datos", get_kv_cache_shape):
-// the K row of slot (b, o) for all kv heads is one contiguous run of
-// num_kv_heads*head_size bf16 at ((b*2 + 0)*block_size + o), the V row the
-// same run at kv index 1.  One warp moves one token: it loads the K and V rows
-// with 16-byte non-coherent loads and stores them with 16-byte stores.  The
-// work is a pure copy (bit exact); HBM traffic is 2 x (read + write) of a row.
+// in NHD order the K row of slot (b, o) for all kv heads is one contiguous run
+// of num_kv_heads*head_size bf16 at ((b*2 + 0)*block_size + o), the V row the
+// same run at kv index 1; in HND order (the same page, "Resumen en una
+// frase": the two layouts) head k's row is at ((b*2 + kv)*num_kv_heads + k) *
+// block_size + o.  One warp moves one token: it loads the K and V rows with
+// 16-byte non-coherent loads and stores them with 16-byte stores, one head's
+// head_size*2 bytes at a time in HND.  The work is a pure copy (bit exact);
+// HBM traffic is 2 x (read + write) of a row.
 #include "common.cuh"
 #include "internal.h"
 
@@ -19,8 +22,9 @@ constexpr int kKvwUnroll = 4;
 __global__ void __launch_bounds__(kKvwThreads)
     reshape_and_cache_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
                              uint4 *__restrict__ cache, const int64_t *__restrict__ slots,
-                             int32_t num_tokens, int32_t row_vecs, int32_t block_size,
-                             int64_t num_blocks)
+                             int32_t num_tokens, int32_t row_vecs, int32_t head_vecs,
+                             int32_t num_kv_heads, int32_t block_size, int64_t num_blocks,
+                             int32_t hnd)
 {
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kKvwThreads + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -36,8 +40,14 @@ __global__ void __launch_bounds__(kKvwThreads)
     }
     const int64_t blk = slot / block_size;
     const int64_t off = slot - blk * block_size;
-    uint4 *kd = cache + ((blk * 2 + 0) * block_size + off) * row_vecs;
-    uint4 *vd = cache + ((blk * 2 + 1) * block_size + off) * row_vecs;
+    // 16-byte chunk i of the token's row (head i / head_vecs) in the pool
+    auto dst = [&](int kv, int i) -> uint4 * {
+        if (!hnd)
+            return cache + ((blk * 2 + kv) * block_size + off) * row_vecs + i;
+        const int h = i / head_vecs;
+        return cache + (((blk * 2 + kv) * num_kv_heads + h) * block_size + off) * head_vecs +
+               (i - h * head_vecs);
+    };
     const uint4 *ks = key + warp * row_vecs;
     const uint4 *vs = value + warp * row_vecs;
     for (int base = 0; base < row_vecs; base += 32 * kKvwUnroll) {
@@ -54,8 +64,8 @@ __global__ void __launch_bounds__(kKvwThreads)
         for (int u = 0; u < kKvwUnroll; ++u) {
             const int i = base + u * 32 + lane;
             if (i < row_vecs) {
-                kd[i] = kr[u];
-                vd[i] = vr[u];
+                *dst(0, i) = kr[u];
+                *dst(1, i) = vr[u];
             }
         }
     }
@@ -64,17 +74,20 @@ __global__ void __launch_bounds__(kKvwThreads)
 cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *cache,
                                      const int64_t *slots, int32_t num_tokens,
                                      int32_t num_kv_heads, int32_t head_size,
-                                     int32_t block_size, int64_t num_blocks, cudaStream_t st)
+                                     int32_t block_size, int64_t num_blocks, int32_t hnd,
+                                     cudaStream_t st)
 {
     if (num_tokens == 0)
         return cudaSuccess;
-    const int32_t row_vecs = num_kv_heads * head_size * 2 / 16;
+    const int32_t head_vecs = head_size * 2 / 16;
+    const int32_t row_vecs = num_kv_heads * head_vecs;
     const int64_t threads = static_cast<int64_t>(num_tokens) * 32;
     const unsigned grid = static_cast<unsigned>((threads + kKvwThreads - 1) / kKvwThreads);
     count_launch();
     reshape_and_cache_kernel<<<grid, kKvwThreads, 0, st>>>(
         static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
-        static_cast<uint4 *>(cache), slots, num_tokens, row_vecs, block_size, num_blocks);
+        static_cast<uint4 *>(cache), slots, num_tokens, row_vecs, head_vecs, num_kv_heads,
+        block_size, num_blocks, hnd);
     return cudaGetLastError();
 }
 

@@ -68,6 +68,7 @@ struct PrefillParams {
     int32_t block_size;
     int32_t box_rows;  // rows per K/V TMA box: gcd(block_size, 128)
     int32_t num_blocks;
+    int32_t num_kv_heads;
     int32_t kv_lo;     // first key attended
     int32_t kv_cap;    // keys >= kv_cap are not attended
     int32_t causal;
@@ -438,7 +439,7 @@ __device__ __forceinline__ void pf_softmax(const PrefillParams &p, const int32_t
     }
 }
 
-template <int D>
+template <int D, bool kHnd>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                       const __grid_constant__ CUtensorMap kv_map, const PrefillParams p)
@@ -607,12 +608,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                         mbar_arrive_expect_tx(bar, bytes);
                     __syncwarp();
                     if (lane < nbox) {
+                        // coordinates in the pool map: NHD (head, page*bs + offset),
+                        // HND (offset, page*Hkv + head), page = block*2 + (K|V)
                         const int key = key0 + lane * p.box_rows;
-                        const int row = (blk * 2 + which) * p.block_size + key % p.block_size;
+                        const int c1 = kHnd ? key % p.block_size : kvh;
+                        const int row = kHnd ? (blk * 2 + which) * p.num_kv_heads + kvh
+                                             : (blk * 2 + which) * p.block_size + key % p.block_size;
                         uint8_t *dst = smem + (which ? Cfg::kVOff : Cfg::kKOff) +
                                        st * Cfg::kTileBytes + lane * p.box_rows * 128;
                         for (int hf = 0; hf < Cfg::kHalves; ++hf)
-                            tma_load_3d(dst + hf * Cfg::kHalfBytes, &kv_map, bar, hf * 64, kvh,
+                            tma_load_3d(dst + hf * Cfg::kHalfBytes, &kv_map, bar, hf * 64, c1,
                                         row, pol_kv);
                     }
                     return true;
@@ -774,7 +779,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 }
 
 // --------------------------------------------------------------------- host
-template <int D>
+template <int D, bool kHnd>
 static cudaError_t launch_prefill_d(const Fwd &f, const PrefillParams &p, int grid)
 {
     using Cfg = PfCfg<D>;
@@ -782,7 +787,7 @@ static cudaError_t launch_prefill_d(const Fwd &f, const PrefillParams &p, int gr
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>,
+        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, kHnd>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(Cfg::kSmemBytes));
         if (e != cudaSuccess)
@@ -793,12 +798,11 @@ static cudaError_t launch_prefill_d(const Fwd &f, const PrefillParams &p, int gr
     if (encode_3d_bf16(&q_map, f.query, D, f.num_heads, f.num_tokens, uint64_t(D) * 2,
                        uint64_t(f.num_heads) * D * 2, 64, 1, kBM) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    if (encode_3d_bf16(&kv_map, f.kv_cache, D, f.num_kv_heads,
-                       uint64_t(f.num_blocks) * 2 * f.block_size, uint64_t(D) * 2,
-                       uint64_t(f.num_kv_heads) * D * 2, 64, 1, p.box_rows) != CUDA_SUCCESS)
+    if (encode_kv_map(&kv_map, f.kv_cache, D, f.num_kv_heads, f.block_size, f.num_blocks,
+                      f.kv_hnd, uint32_t(p.box_rows)) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     count_launch();
-    prefill_tc_kernel<D><<<grid, kPfThreads, Cfg::kSmemBytes, f.stream>>>(q_map, kv_map, p);
+    prefill_tc_kernel<D, kHnd><<<grid, kPfThreads, Cfg::kSmemBytes, f.stream>>>(q_map, kv_map, p);
     return cudaGetLastError();
 }
 
@@ -822,6 +826,7 @@ cudaError_t launch_prefill(const Fwd &f, const PrefillPass &pass)
     // block_size (prefix length) and 128 (tile), so use their gcd
     p.box_rows = std::gcd(f.block_size, 128);
     p.num_blocks = static_cast<int32_t>(f.num_blocks);
+    p.num_kv_heads = f.num_kv_heads;
     p.kv_lo = pass.kv_lo;
     p.kv_cap = pass.kv_cap;
     p.causal = pass.causal;
@@ -852,8 +857,9 @@ cudaError_t launch_prefill(const Fwd &f, const PrefillPass &pass)
     // persistent grid: one CTA per SM, but no more CTAs than work items
     const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(f.num_sms, items)));
     if (f.head_size == 128)
-        return launch_prefill_d<128>(f, p, grid);
-    return launch_prefill_d<64>(f, p, grid);
+        return f.kv_hnd ? launch_prefill_d<128, true>(f, p, grid)
+                        : launch_prefill_d<128, false>(f, p, grid);
+    return f.kv_hnd ? launch_prefill_d<64, true>(f, p, grid) : launch_prefill_d<64, false>(f, p, grid);
 }
 
 uint32_t prefill_take_error() { return take_device_error(); }

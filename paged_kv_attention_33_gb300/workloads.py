@@ -61,6 +61,7 @@ class BatchSpec:
     scale: float | None = None                       # None: 1/sqrt(head_size)
     causal: bool = True
     table_pad: int = 0                               # extra -1 columns in block_table
+    kv_layout: str = "NHD"                           # physical pool order: "NHD" or "HND"
 
     @property
     def num_decodes(self) -> int:
@@ -228,6 +229,22 @@ def make_batch(spec: BatchSpec, seed: int, device: str = "cpu") -> Batch:
             cache[blk[a:b], 0, off[a:b]] = normal(b - a, Hkv, D)
             cache[blk[a:b], 1, off[a:b]] = normal(b - a, Hkv, D)
     return Batch(spec, query, key, value, cache, slots, qsl, lens, table, nb)
+
+
+def to_layout(cache, kv_layout: str):
+    """The pool in physical order `kv_layout`: NHD is the logical
+    [NB, 2, bs, Hkv, D] itself, HND swaps the slot and head axes to
+    [NB, 2, Hkv, bs, D] (numpy array or torch tensor, contiguous)."""
+    if kv_layout.upper() == "NHD":
+        return cache
+    if isinstance(cache, np.ndarray):
+        return np.ascontiguousarray(np.swapaxes(cache, 2, 3))
+    return cache.transpose(2, 3).contiguous()
+
+
+def from_layout(pool, kv_layout: str):
+    """Inverse of to_layout: the logical [NB, 2, bs, Hkv, D] pool."""
+    return to_layout(pool, kv_layout)  # swapping the two axes again undoes it
 
 
 def to_host_bits(x) -> np.ndarray:

@@ -50,11 +50,12 @@ def run_library(batch: W.Batch, split_kv_tokens: int = 0, causal: bool | None = 
     cache = to_dev(batch.cache, dev)
     if not isinstance(batch.cache, np.ndarray):
         cache = cache.clone()  # keep the generated pool untouched
+    cache = W.to_layout(cache, sp.kv_layout)  # the pool in the batch's physical order
     slots = torch.from_numpy(batch.slot_mapping).to(dev)
-    pka.reshape_and_cache(k, v, cache, slots)
+    pka.reshape_and_cache(k, v, cache, slots, kv_layout=sp.kv_layout)
     meta = pka.Meta.from_host(batch.query_start_loc, batch.seq_lens, batch.block_table,
                               sp.num_decodes, dev, common_prefix_len=sp.common_prefix_len,
-                              split_kv_tokens=split_kv_tokens)
+                              split_kv_tokens=split_kv_tokens, kv_layout=sp.kv_layout)
     T = batch.num_tokens
     out = torch.full((T, sp.num_heads, sp.head_size), float("nan"), dtype=torch.bfloat16,
                      device=dev)
@@ -63,7 +64,7 @@ def run_library(batch: W.Batch, split_kv_tokens: int = 0, causal: bool | None = 
     pka.paged_attn_forward(q, cache, meta, out, lse, scale=sp.softmax_scale,
                            causal=sp.causal if causal is None else causal)
     pka.check_status()
-    return (W.to_host_bits(cache), W.to_host_bits(out),
+    return (W.to_host_bits(W.from_layout(cache, sp.kv_layout)), W.to_host_bits(out),
             None if lse is None else lse.cpu().numpy())
 
 

@@ -121,3 +121,38 @@ def test_cascade_merge_arguments(lib):
     assert lib.pka_cascade_merge(16, 16, 16, 16, 16, None, 4, 8, 60, None) == -1
     assert lib.pka_cascade_merge(None, 16, 16, 16, 16, None, 4, 8, 64, None) == -1
     assert lib.pka_cascade_merge(16, 16, 16, 16, 16, None, 0, 8, 64, None) == 0
+
+
+def test_unknown_kv_layout_is_rejected(lib):
+    """The pool layout is one of the two the pages name (NHD, HND)."""
+    assert _fwd(lib, _meta(kv_layout=2)) == -1
+    assert lib.pka_workspace_size(ctypes.byref(_meta(kv_layout=-1)), 2, 8, 2, 64, 16) == 0
+    assert lib.pka_reshape_and_cache_ex(16, 16, 16, 16, 1, 2, 64, 16, 4, 3, None) == -1
+    # a zero-initialised meta is NHD
+    assert pka._CMeta().kv_layout == pka.LAYOUT_NHD
+
+
+def test_hnd_pool_is_the_slot_head_transpose():
+    """The HND pool holds row (block b, kv, slot o, head k) at [b][kv][k][o]:
+    the logical [NB, 2, bs, Hkv, D] pool with the slot and head axes swapped
+    (checked element by element on a pool of distinct values), and the
+    conversion back is exact."""
+    import numpy as np
+
+    from paged_kv_attention_33_gb300 import workloads as W
+
+    nb, bs, hkv, d = 3, 4, 5, 6
+    logical = np.arange(nb * 2 * bs * hkv * d, dtype=np.uint16).reshape(nb, 2, bs, hkv, d)
+    hnd = W.to_layout(logical, "HND")
+    assert hnd.shape == (nb, 2, hkv, bs, d) and hnd.flags["C_CONTIGUOUS"]
+    for b in range(nb):
+        for kv in range(2):
+            for o in range(bs):
+                for k in range(hkv):
+                    assert np.array_equal(hnd[b, kv, k, o], logical[b, kv, o, k])
+    # head k's page is one contiguous run of bs*d elements
+    flat = hnd.reshape(-1)
+    start = ((1 * 2 + 1) * hkv + 2) * bs * d
+    assert np.array_equal(flat[start:start + bs * d].reshape(bs, d), logical[1, 1, :, 2])
+    assert np.array_equal(W.from_layout(hnd, "HND"), logical)
+    assert W.to_layout(logical, "NHD") is logical
