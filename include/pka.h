@@ -6,7 +6,9 @@
  *   pka_paged_attn_forward  attention of a mixed, decode-first batch over
  *                           the pool (split-KV decode, causal / chunked
  *                           prefill, optional shared-prefix cascade),
- *   pka_cascade_merge       log-sum-exp merge of two partial attentions.
+ *   pka_cascade_merge       log-sum-exp merge of two partial attentions,
+ *   pka_merge_partials      the N-way merge with an explicit lse base (the
+ *                           combine of a decode context-parallel step).
  *
  * Sources, cited by page title and section:
  *  [FA/FI]   "FlashAttention y FlashInfer: los dos grandes backends de atencion
@@ -65,6 +67,9 @@ typedef enum {
  *  seq_lens         int32 [num_seqs]; L_s >= 1, the whole KV length of s
  *                   including this step's tokens (already written by
  *                   pka_reshape_and_cache).  Prior context c_s = L_s - q_s.
+ *                   A decode may have L_s = 0 (no keys, e.g. a context-
+ *                   parallel rank's empty shard): its rows get out = 0 and
+ *                   lse = -inf.
  *  block_table      int32 [num_seqs, block_table_stride]; entry n of row s
  *                   is the physical block holding keys [n*bs, (n+1)*bs) of
  *                   s.  Entries past ceil(L_s/bs) are never read.
@@ -245,6 +250,33 @@ pka_status pka_paged_attn_forward_noalloc(const void *query, const void *kv_cach
 pka_status pka_cascade_merge(const void *out_a, const float *lse_a, const void *out_b,
                              const float *lse_b, void *out, float *lse_out, int32_t num_tokens,
                              int32_t num_heads, int32_t head_size, void *stream);
+
+/* Units of a log-sum-exp: natural log or log base 2. */
+typedef enum { PKA_LSE_BASE_E = 0, PKA_LSE_BASE_2 = 1 } pka_lse_base;
+
+/*
+ * Log-sum-exp merge of num_parts partial attentions of the same queries over
+ * disjoint key sets: the combine step of decode context parallelism, where
+ * each rank attends over its shard of every sequence's keys ([FA/FI] "Limites
+ * y fallos": the DCP combine branch; [backend] "Limites y fallos": the lse
+ * base, ln or log2, has to be the one the partials carry -- a wrong base
+ * silently breaks the softmax denominator across shards).  Per row
+ * r = t*num_heads + h, with b = e (PKA_LSE_BASE_E) or 2 (PKA_LSE_BASE_2):
+ *     lse = log_b(sum_p b^lse_p),   out = sum_p b^(lse_p - lse) * out_p
+ * A part with lse = -inf holds no keys and adds nothing; a row with no keys in
+ * any part gets out = 0, lse = -inf.
+ *
+ *  outs      device bf16 [num_parts, num_tokens, num_heads, head_size]
+ *  lses      device fp32 [num_parts, num_tokens, num_heads], base lse_base
+ *  out       device bf16 [num_tokens, num_heads, head_size]; must not alias outs
+ *  lse_out   device fp32 [num_tokens, num_heads] in base lse_base, or NULL
+ * Errors: PKA_ERR_INVALID_ARG for num_parts < 1, bad shapes (head_size a
+ * multiple of 8), an unknown base, null or misaligned pointers, out aliasing
+ * outs.  Asynchronous on `stream`.
+ */
+pka_status pka_merge_partials(const void *outs, const float *lses, int32_t num_parts, void *out,
+                              float *lse_out, int32_t num_tokens, int32_t num_heads,
+                              int32_t head_size, int32_t lse_base, void *stream);
 
 /*
  * Synchronise `stream`, then read and clear the sticky device error word.

@@ -23,7 +23,8 @@ import threading
 from . import build as _build
 
 __all__ = ["Meta", "PkaError", "LAYOUT_NHD", "LAYOUT_HND", "reshape_and_cache", "paged_attn_forward", "cascade_merge",
-           "paged_attn_forward_noalloc", "workspace_size", "check_status", "set_kernel_events", "kernel_launches",
+           "paged_attn_forward_noalloc", "workspace_size", "merge_partials", "LSE_BASE_E",
+           "LSE_BASE_2", "check_status", "set_kernel_events", "kernel_launches",
            "load_library",
            "library_path", "KERNEL_DECODE", "KERNEL_PREFILL"]
 
@@ -101,6 +102,8 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
                                                        ctypes.c_float, _I32, _P]
         lib.pka_paged_attn_forward_noalloc.restype = ctypes.c_int
         lib.pka_cascade_merge.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P]
+        lib.pka_merge_partials.argtypes = [_P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _P]
+        lib.pka_merge_partials.restype = ctypes.c_int
         lib.pka_cascade_merge.restype = ctypes.c_int
         lib.pka_set_kernel_events.argtypes = [_I32, _P, _P]
         lib.pka_set_kernel_events.restype = ctypes.c_int
@@ -241,6 +244,22 @@ def cascade_merge(out_a, lse_a, out_b, lse_b, out, lse_out=None, stream=None) ->
     T, H, D = out_a.shape
     _check(lib.pka_cascade_merge(_ptr(out_a), _ptr(lse_a), _ptr(out_b), _ptr(lse_b), _ptr(out),
                                  _ptr(lse_out), T, H, D, _stream(stream)))
+
+
+# Units of a log-sum-exp (pka_lse_base)
+LSE_BASE_E = 0
+LSE_BASE_2 = 1
+
+
+def merge_partials(outs, lses, out, lse_out=None, lse_base=LSE_BASE_E, stream=None) -> None:
+    """Log-sum-exp merge of P partial attentions over disjoint key sets:
+    outs [P, T, H, D] bf16, lses [P, T, H] fp32 in base lse_base (LSE_BASE_E:
+    natural log, LSE_BASE_2: log2) -> out [T, H, D] bf16, lse_out [T, H] in the
+    same base."""
+    lib = load_library()
+    P, T, H, D = outs.shape
+    _check(lib.pka_merge_partials(_ptr(outs), _ptr(lses), P, _ptr(out), _ptr(lse_out), T, H, D,
+                                  int(lse_base), _stream(stream)))
 
 
 KERNEL_DECODE = 0

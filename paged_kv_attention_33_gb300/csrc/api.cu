@@ -425,6 +425,37 @@ pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const
     return PKA_OK;
 }
 
+pka_status pka_merge_partials(const void *outs, const float *lses, int32_t num_parts, void *out,
+                              float *lse_out, int32_t num_tokens, int32_t num_heads,
+                              int32_t head_size, int32_t lse_base, void *stream)
+{
+    if (num_parts < 1 || num_tokens < 0 || num_heads <= 0 || head_size <= 0 ||
+        head_size % 8 != 0)
+        return fail(PKA_ERR_INVALID_ARG, "bad shape: parts %d tokens %d heads %d head_size %d",
+                    num_parts, num_tokens, num_heads, head_size);
+    if (lse_base != PKA_LSE_BASE_E && lse_base != PKA_LSE_BASE_2)
+        return fail(PKA_ERR_INVALID_ARG, "unknown lse base %d", lse_base);
+    if (num_tokens == 0)
+        return PKA_OK;
+    if (!outs || !lses || !out)
+        return fail(PKA_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(outs, 16) || !aligned(out, 16) || !aligned(lses, 4) ||
+        (lse_out && !aligned(lse_out, 4)))
+        return fail(PKA_ERR_INVALID_ARG, "misaligned pointer (16 bytes required)");
+    const size_t part_bytes = size_t(num_tokens) * num_heads * head_size * 2;
+    const char *o0 = static_cast<const char *>(outs);
+    const char *o1 = o0 + part_bytes * size_t(num_parts);
+    const char *d0 = static_cast<const char *>(out);
+    if (d0 < o1 && o0 < d0 + part_bytes)
+        return fail(PKA_ERR_INVALID_ARG, "out must not alias outs");
+    cudaError_t e = launch_merge_partials(outs, lses, num_parts, out, lse_out, num_tokens,
+                                          num_heads, head_size, lse_base == PKA_LSE_BASE_2 ? 1 : 0,
+                                          static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "merge_partials launch");
+    return PKA_OK;
+}
+
 pka_status pka_cascade_merge(const void *out_a, const float *lse_a, const void *out_b,
                              const float *lse_b, void *out, float *lse_out, int32_t num_tokens,
                              int32_t num_heads, int32_t head_size, void *stream)

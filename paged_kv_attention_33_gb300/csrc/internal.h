@@ -93,6 +93,11 @@ cudaError_t launch_cascade_merge(const void *out_a, const float *lse_a, const vo
                                  int32_t num_tokens, int32_t num_heads, int32_t head_size,
                                  cudaStream_t st);
 
+cudaError_t launch_merge_partials(const void *outs, const float *lses, int32_t num_parts,
+                                  void *out, float *lse_out, int32_t num_tokens,
+                                  int32_t num_heads, int32_t head_size, int32_t base2,
+                                  cudaStream_t st);
+
 // Set the thread-local message pka_last_error() returns (api.cu).
 void set_last_error(const char *fmt, ...);
 

@@ -156,3 +156,12 @@ def test_hnd_pool_is_the_slot_head_transpose():
     assert np.array_equal(flat[start:start + bs * d].reshape(bs, d), logical[1, 1, :, 2])
     assert np.array_equal(W.from_layout(hnd, "HND"), logical)
     assert W.to_layout(logical, "NHD") is logical
+
+
+def test_merge_partials_arguments(lib):
+    assert lib.pka_merge_partials(16, 16, 0, 4096, None, 4, 8, 64, 0, None) == -1    # no parts
+    assert lib.pka_merge_partials(16, 16, 2, 4096, None, 4, 8, 60, 0, None) == -1    # head_size
+    assert lib.pka_merge_partials(16, 16, 2, 65536, None, 4, 8, 64, 7, None) == -1   # base
+    assert lib.pka_merge_partials(None, 16, 2, 65536, None, 4, 8, 64, 0, None) == -1
+    assert lib.pka_merge_partials(16, 16, 2, 16 + 4 * 8 * 64 * 2, None, 4, 8, 64, 0, None) == -1  # alias
+    assert lib.pka_merge_partials(16, 16, 2, 16, None, 0, 8, 64, 0, None) == 0       # empty
