@@ -203,6 +203,36 @@ pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const
                                   void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * pka_reshape_and_cache followed by pka_paged_attn_forward, with the cache
+ * write folded into the forward's launches ([FA/FI] "Responsabilidades": the
+ * FlashAttention kernel writes the KV cache itself,
+ * forward_includes_kv_cache_update).  Same results, bit for bit in the pool,
+ * as the two calls.  When the batch has decodes, the decode kernel writes
+ * every new row: each decode's new K/V row is copied from `key`/`value` into
+ * the tile its attention reads (the pool need not hold it yet) and stored at
+ * its slot, and the prefill tokens' rows are stored before the prefill pass
+ * reads them -- no separate write launch.  A batch without decodes writes
+ * first and then attends (two launches).
+ *
+ *  key, value     device bf16 [num_tokens, num_kv_heads, head_size], as in
+ *                 pka_reshape_and_cache
+ *  slot_mapping   device int64 [num_tokens]; for a decode token the slot of
+ *                 its sequence's last key (key L_s - 1 through block_table),
+ *                 which is what makes the fused and the two-call results agree
+ *  kv_cache       device pool, written in place (layout meta->kv_layout)
+ *  other arguments as pka_paged_attn_forward.
+ * Errors: those of the two calls.
+ */
+pka_status pka_paged_attn_forward_fused(const void *query, const void *key, const void *value,
+                                        const int64_t *slot_mapping, void *kv_cache,
+                                        const pka_meta *meta, void *out, float *lse,
+                                        int32_t num_tokens, int32_t num_heads,
+                                        int32_t num_kv_heads, int32_t head_size,
+                                        int32_t block_size, int64_t num_blocks, float scale,
+                                        int32_t causal, void *workspace, size_t workspace_bytes,
+                                        void *stream);
+
+/*
  * pka_paged_attn_forward for callers that cannot allocate device memory.
  * The pages have no counterpart of this entry point.
  *

@@ -23,7 +23,8 @@ import threading
 from . import build as _build
 
 __all__ = ["Meta", "PkaError", "LAYOUT_NHD", "LAYOUT_HND", "reshape_and_cache", "paged_attn_forward", "cascade_merge",
-           "paged_attn_forward_noalloc", "workspace_size", "merge_partials", "LSE_BASE_E",
+           "paged_attn_forward_noalloc", "paged_attn_forward_fused", "workspace_size",
+           "merge_partials", "LSE_BASE_E",
            "LSE_BASE_2", "check_status", "set_kernel_events", "kernel_launches",
            "load_library",
            "library_path", "KERNEL_DECODE", "KERNEL_PREFILL"]
@@ -103,6 +104,11 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pka_paged_attn_forward_noalloc.restype = ctypes.c_int
         lib.pka_cascade_merge.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P]
         lib.pka_merge_partials.argtypes = [_P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _P]
+        lib.pka_paged_attn_forward_fused.argtypes = [_P, _P, _P, _P, _P, ctypes.POINTER(_CMeta),
+                                                     _P, _P, _I32, _I32, _I32, _I32, _I32,
+                                                     _I64, ctypes.c_float, _I32, _P,
+                                                     ctypes.c_size_t, _P]
+        lib.pka_paged_attn_forward_fused.restype = ctypes.c_int
         lib.pka_merge_partials.restype = ctypes.c_int
         lib.pka_cascade_merge.restype = ctypes.c_int
         lib.pka_set_kernel_events.argtypes = [_I32, _P, _P]
@@ -219,6 +225,30 @@ def paged_attn_forward(query, kv_cache, meta: Meta, out, lse=None, scale=None, c
                                       _ptr(lse), T, H, hkv, D, bs, nb, float(scale),
                                       1 if causal else 0, _ptr(workspace), ws_bytes,
                                       _stream(stream)))
+
+
+def paged_attn_forward_fused(query, key, value, slot_mapping, kv_cache, meta: Meta, out,
+                             lse=None, scale=None, causal=True, workspace=None,
+                             stream=None) -> None:
+    """reshape_and_cache(key, value, kv_cache, slot_mapping) then paged_attn_forward,
+    with the cache write folded into the forward's decode launch."""
+    import torch
+
+    lib = load_library()
+    T, H, D = query.shape
+    nb, bs, hkv, _ = _pool_dims(kv_cache, meta.kv_layout)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    cm = meta._c()
+    need = int(lib.pka_workspace_size(ctypes.byref(cm), T, H, hkv, D, bs))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.pka_paged_attn_forward_fused(_ptr(query), _ptr(key), _ptr(value),
+                                            _ptr(slot_mapping), _ptr(kv_cache), ctypes.byref(cm),
+                                            _ptr(out), _ptr(lse), T, H, hkv, D, bs, nb,
+                                            float(scale), 1 if causal else 0, _ptr(workspace),
+                                            ws_bytes, _stream(stream)))
 
 
 def paged_attn_forward_noalloc(query, kv_cache, meta: Meta, out, lse=None, scale=None,

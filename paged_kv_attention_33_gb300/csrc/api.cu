@@ -307,11 +307,19 @@ size_t pka_workspace_size(const pka_meta *meta, int32_t num_tokens, int32_t num_
         .total;
 }
 
-pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const pka_meta *meta,
-                                  void *out, float *lse, int32_t num_tokens, int32_t num_heads,
-                                  int32_t num_kv_heads, int32_t head_size, int32_t block_size,
-                                  int64_t num_blocks, float scale, int32_t causal,
-                                  void *workspace, size_t workspace_bytes, void *stream)
+// This step's new K/V rows for pka_paged_attn_forward_fused.
+struct FuseArgs {
+    const void *key;
+    const void *value;
+    const int64_t *slots;
+    void *kv_cache;
+};
+
+static pka_status forward_impl(const void *query, const void *kv_cache, const pka_meta *meta,
+                               void *out, float *lse, int32_t num_tokens, int32_t num_heads,
+                               int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                               int64_t num_blocks, float scale, int32_t causal, void *workspace,
+                               size_t workspace_bytes, void *stream, const FuseArgs *fuse)
 {
     pka_status st = check_shape(meta, num_tokens, num_heads, num_kv_heads, head_size, block_size);
     if (st != PKA_OK)
@@ -368,6 +376,13 @@ pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const
     f.causal = causal;
     f.stream = static_cast<cudaStream_t>(stream);
     f.num_sms = sm_count();
+    if (fuse) {
+        f.fuse_write = 1;
+        f.new_key = fuse->key;
+        f.new_value = fuse->value;
+        f.slots = fuse->slots;
+        f.kv_cache_w = fuse->kv_cache;
+    }
 
     DecodePlan dp = plan_decode(meta->split_kv_tokens, meta->num_decodes, num_kv_heads,
                                 f.num_sms);
@@ -423,6 +438,51 @@ pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const
             return cuda_fail(e, "cascade combine launch");
     }
     return PKA_OK;
+}
+
+pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const pka_meta *meta,
+                                  void *out, float *lse, int32_t num_tokens, int32_t num_heads,
+                                  int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                  int64_t num_blocks, float scale, int32_t causal,
+                                  void *workspace, size_t workspace_bytes, void *stream)
+{
+    return forward_impl(query, kv_cache, meta, out, lse, num_tokens, num_heads, num_kv_heads,
+                        head_size, block_size, num_blocks, scale, causal, workspace,
+                        workspace_bytes, stream, nullptr);
+}
+
+pka_status pka_paged_attn_forward_fused(const void *query, const void *key, const void *value,
+                                        const int64_t *slot_mapping, void *kv_cache,
+                                        const pka_meta *meta, void *out, float *lse,
+                                        int32_t num_tokens, int32_t num_heads,
+                                        int32_t num_kv_heads, int32_t head_size,
+                                        int32_t block_size, int64_t num_blocks, float scale,
+                                        int32_t causal, void *workspace, size_t workspace_bytes,
+                                        void *stream)
+{
+    pka_status st = check_shape(meta, num_tokens, num_heads, num_kv_heads, head_size, block_size);
+    if (st != PKA_OK)
+        return st;
+    if (num_tokens == 0 || meta->num_seqs == 0)
+        return PKA_OK;
+    if (!key || !value || !slot_mapping)
+        return fail(PKA_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(key, 16) || !aligned(value, 16) || !aligned(slot_mapping, 8))
+        return fail(PKA_ERR_INVALID_ARG, "misaligned pointer (16 bytes required)");
+    if (meta->num_decodes == 0) {
+        // no decode launch to carry the write: write first, then attend
+        st = pka_reshape_and_cache_ex(key, value, kv_cache, slot_mapping, num_tokens, num_kv_heads,
+                                      head_size, block_size, num_blocks, meta->kv_layout, stream);
+        if (st != PKA_OK)
+            return st;
+        return forward_impl(query, kv_cache, meta, out, lse, num_tokens, num_heads, num_kv_heads,
+                            head_size, block_size, num_blocks, scale, causal, workspace,
+                            workspace_bytes, stream, nullptr);
+    }
+    const FuseArgs fa{key, value, slot_mapping, kv_cache};
+    return forward_impl(query, kv_cache, meta, out, lse, num_tokens, num_heads, num_kv_heads,
+                        head_size, block_size, num_blocks, scale, causal, workspace,
+                        workspace_bytes, stream, &fa);
 }
 
 pka_status pka_merge_partials(const void *outs, const float *lses, int32_t num_parts, void *out,

@@ -78,6 +78,14 @@ struct DecodeParams {
     const float *o_pre;   // cascade: shared-prefix partials [pre_splits][T, H, D]
     const float *lse_pre; // [pre_splits][T, H], log2 units
     int32_t pre_splits;   // cascade: shared-prefix partials per row
+    // fused cache write (pka_paged_attn_forward_fused): this step's K/V rows
+    // [T, Hkv, D] and their slots; the pool is written through `pool`
+    int32_t fuse_write;
+    const uint4 *new_key;
+    const uint4 *new_value;
+    const int64_t *slots;
+    uint4 *pool;
+    int32_t num_decodes_all;  // tokens [num_decodes_all, T) are prefill tokens
 };
 
 constexpr int kConsumerWarps = 8;
@@ -324,6 +332,36 @@ __device__ __forceinline__ void merge_prefix_direct(const DecodeParams &p, int t
     ls1 = W1 > 0.f ? M1 + log2f(W1) : kNegInf;
 }
 
+// Heads [h0, h1) of token tk's new K and V rows into the pool at slot sl
+// (block sl / bs, offset sl % bs), 16 bytes per lane, NHD or HND order -- the
+// cache write of the "FlashAttention y FlashInfer" page ("Responsabilidades":
+// the cache-update op), done inside the forward.  A negative slot is padding;
+// a slot past the pool is skipped and flagged.
+template <int D, bool kHnd>
+__device__ __forceinline__ void write_pool_row(const DecodeParams &p, int64_t tk, int64_t sl,
+                                               int lane, int h0, int h1)
+{
+    if (sl < 0)
+        return;
+    if (sl >= int64_t(p.num_blocks) * p.block_size) {
+        if (lane == 0)
+            flag_error(kErrSlotOutOfPool);
+        return;
+    }
+    constexpr int kChunks = D / 8;
+    const int64_t blk = sl / p.block_size, off = sl % p.block_size;
+    const int Hkv = p.num_kv_heads;
+    for (int i = lane; i < (h1 - h0) * kChunks; i += 32) {
+        const int h = h0 + i / kChunks, c = i % kChunks;
+        const int64_t src = (tk * Hkv + h) * kChunks + c;
+        for (int kv = 0; kv < 2; ++kv) {
+            const int64_t row = kHnd ? ((blk * 2 + kv) * Hkv + h) * p.block_size + off
+                                     : ((blk * 2 + kv) * p.block_size + off) * Hkv + h;
+            p.pool[row * kChunks + c] = __ldg((kv ? p.new_value : p.new_key) + src);
+        }
+    }
+}
+
 template <int D, bool kHnd>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p)
@@ -344,6 +382,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int nseq = p.nseq;
+
+    if (p.fuse_write && p.seq0 == 0) {
+        // the prefill tokens' new rows, one token per warp over the grid (the
+        // prefill kernel reads them after this launch; nothing here does)
+        const int64_t nw = int64_t(gridDim.x) * (kDecodeThreads / 32);
+        for (int64_t tk = p.num_decodes_all + int64_t(blockIdx.x) * (kDecodeThreads / 32) + warp;
+             tk < p.num_tokens; tk += nw)
+            write_pool_row<D, kHnd>(p, tk, p.slots[tk], lane, 0, Hkv);
+    }
 
     // ---- stage prefix sums over the decodes of this launch: each thread sums a
     // run of decodes, then a block-wide exclusive scan of the run sums
@@ -535,6 +582,30 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             const uint32_t kbase =
                 smem_addr(smem + slot * Cfg::kStageBytes + u * Cfg::kUnitBytes);
             const uint32_t vbase = kbase + Cfg::kKvBytes;
+            if (p.fuse_write && L - 1 < ks + 16) {
+                // this stage holds the decode's new key (key L-1): the pool may
+                // not have it yet, so it is taken from the step's K/V rows into
+                // the staged tile, and written to the pool at the token's slot
+                const int64_t sl = p.slots[t];
+                if (sl >= 0 && sl < int64_t(p.num_blocks) * p.block_size) {
+                    constexpr int kChunks = D / 8;  // 16-byte chunks of one head's row
+                    if (lane < kChunks) {
+                        const int64_t src = (int64_t(t) * Hkv + k) * kChunks + lane;
+                        const uint4 nk = __ldg(p.new_key + src), nv = __ldg(p.new_value + src);
+                        const uint32_t o = (lane >> 3) * 2048 + swz128(L - 1 - ks, lane & 7);
+                        uint8_t *tile = smem + slot * Cfg::kStageBytes + u * Cfg::kUnitBytes;
+                        *reinterpret_cast<uint4 *>(tile + o) = nk;
+                        *reinterpret_cast<uint4 *>(tile + Cfg::kKvBytes + o) = nv;
+                        // the stage is refilled by TMA later: order these
+                        // generic writes before the async proxy's
+                        fence_proxy_async_smem();
+                    }
+                    write_pool_row<D, kHnd>(p, t, sl, lane, k, k + 1);
+                    __syncwarp();
+                } else if (sl >= 0 && lane == 0) {
+                    flag_error(kErrSlotOutOfPool);
+                }
+            }
             // S^T = K Q^T
             float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -789,6 +860,12 @@ static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Wor
     p.o_pre = reinterpret_cast<const float *>(wsp + ws.o_pre);
     p.lse_pre = reinterpret_cast<const float *>(wsp + ws.lse_pre);
     p.pre_splits = ws.pre_splits;
+    p.fuse_write = f.fuse_write;
+    p.new_key = static_cast<const uint4 *>(f.new_key);
+    p.new_value = static_cast<const uint4 *>(f.new_value);
+    p.slots = f.slots;
+    p.pool = static_cast<uint4 *>(f.kv_cache_w);
+    p.num_decodes_all = f.num_decodes;
     // one launch per chunk of at most kMaxDecodeChunk decodes (stream ordered,
     // so chunks reuse the same partial slots and counters)
     for (int32_t seq0 = 0; seq0 < f.num_decodes; seq0 += dp.chunk) {

@@ -32,6 +32,12 @@ struct Fwd {
     int32_t block_size;
     int64_t num_blocks;
     int32_t kv_hnd;  // 1: pool in HND order, 0: NHD
+    // fused cache write: the decode launch also writes this step's K/V rows
+    int32_t fuse_write = 0;
+    const void *new_key = nullptr;
+    const void *new_value = nullptr;
+    const int64_t *slots = nullptr;
+    void *kv_cache_w = nullptr;
     float scale;
     int32_t causal;
     cudaStream_t stream;

@@ -73,12 +73,6 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Generic-proxy writes to shared memory made visible to the async proxy
-// (tensor core / TMA) before they read it.
-__device__ __forceinline__ void fence_proxy_async_smem()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 // ------------------------------------------------------------ MMA
 // D[tmem] (+)= A[smem desc] * B[smem desc]

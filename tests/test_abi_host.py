@@ -165,3 +165,16 @@ def test_merge_partials_arguments(lib):
     assert lib.pka_merge_partials(None, 16, 2, 65536, None, 4, 8, 64, 0, None) == -1
     assert lib.pka_merge_partials(16, 16, 2, 16 + 4 * 8 * 64 * 2, None, 4, 8, 64, 0, None) == -1  # alias
     assert lib.pka_merge_partials(16, 16, 2, 16, None, 0, 8, 64, 0, None) == 0       # empty
+
+
+def test_fused_forward_arguments(lib):
+    m = _meta()
+    fused = lib.pka_paged_attn_forward_fused
+    # null / misaligned new rows or slots
+    assert fused(256, None, 256, 256, 512, ctypes.byref(m), 1024, None, 2, 8, 2, 64, 16, 64,
+                 0.125, 1, None, 0, None) == -1
+    assert fused(256, 256, 256, 4, 512, ctypes.byref(m), 1024, None, 2, 8, 2, 64, 16, 64,
+                 0.125, 1, None, 0, None) == -1
+    # the forward's own checks still apply (block size)
+    assert fused(256, 256, 256, 256, 512, ctypes.byref(m), 1024, None, 2, 8, 2, 64, 24, 64,
+                 0.125, 1, None, 0, None) == -1
