@@ -1,9 +1,11 @@
 """Benchmark of one paged-KV attention step on GB300.
 
 A step is one pass of the hot path over one synthetic batch: the cache write
-of this step's new K/V rows (reshape_and_cache) followed by the attention
-forward (paged_attn_forward: split-KV decode + combine, prefill, cascade as
-the batch needs).  The headline workload is the decode-heavy batch: 128
+of this step's new K/V rows and the attention forward (split-KV decode +
+combine, prefill, cascade as the batch needs), made through
+paged_attn_forward_fused, which folds the cache write into the forward's
+decode launch (the same bytes and results as reshape_and_cache followed by
+paged_attn_forward; --two-call times that pair instead).  The headline workload is the decode-heavy batch: 128
 decode requests, prior context ~ U[512, 8192], 32 query heads over 8 kv heads,
 head_size 128, block_size 16, pages shuffled across the pool.  Its value is
 KV bytes read per second (GB/s); its KV (about 2.3 GB) is far larger than L2,
@@ -14,6 +16,7 @@ Prints ONE JSON line (rank 0).  Flags:
   --impl reference                the fp64 CPU oracle on a bounded sample, on the host cores
   --workload NAME                 another named workload (for profiling runs)
   --no-cpu-baseline               skip the oracle timing (profiling runs)
+  --two-call                      write the cache with its own launch (reshape_and_cache)
 """
 from __future__ import annotations
 
@@ -169,12 +172,22 @@ class Step:
                                   self.spec.head_size, self.spec.block_size)
         self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
 
+    fused = True  # the cache write inside the forward (paged_attn_forward_fused)
+
     def run(self, q=None, k=None, v=None, slots=None, meta=None):
         b = self.batch
-        self.pka.reshape_and_cache(b.key if k is None else k, b.value if v is None else v,
-                                   b.cache, self.slots if slots is None else slots)
-        self.pka.paged_attn_forward(b.query if q is None else q, b.cache,
-                                    self.meta if meta is None else meta, self.out, self.lse,
+        q = b.query if q is None else q
+        k = b.key if k is None else k
+        v = b.value if v is None else v
+        slots = self.slots if slots is None else slots
+        meta = self.meta if meta is None else meta
+        if self.fused:
+            self.pka.paged_attn_forward_fused(q, k, v, slots, b.cache, meta, self.out, self.lse,
+                                              scale=self.spec.softmax_scale,
+                                              causal=self.spec.causal, workspace=self.ws)
+            return
+        self.pka.reshape_and_cache(k, v, b.cache, slots)
+        self.pka.paged_attn_forward(q, b.cache, meta, self.out, self.lse,
                                     scale=self.spec.softmax_scale, causal=self.spec.causal,
                                     workspace=self.ws)
 
@@ -409,6 +422,8 @@ def run_ours(args):
                    "num_kv_heads": spec.num_kv_heads, "head_size": spec.head_size,
                    "block_size": spec.block_size, "kv_bytes_per_step": kv_bytes,
                    "l2": "inputs larger than L2 (KV per step >> 129 MB), no flush",
+                   "step_calls": "paged_attn_forward_fused" if Step.fused
+                   else "reshape_and_cache + paged_attn_forward",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "roofline": roofline,
         "e2e": {"value": world * kv_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
@@ -524,7 +539,11 @@ def main():
                     help="short run for a profiler: W + K steps only")
     ap.add_argument("--max-decodes", type=int, default=None,
                     help="keep only the first N decode requests (small profiling case)")
+    ap.add_argument("--two-call", action="store_true",
+                    help="reshape_and_cache and paged_attn_forward as two calls")
     args = ap.parse_args()
+    if args.two_call:
+        Step.fused = False
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
