@@ -54,6 +54,17 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_cascade_attention.restype = ctypes.c_int
     lib.oracle_lse_merge.argtypes = [_P, _P, _P, _P, _I64, _I64, _P, _P]
     lib.oracle_lse_merge.restype = None
+    lib.oracle_quantize_e4m3.argtypes = [_P, _I64, ctypes.c_float, _P]
+    lib.oracle_quantize_e4m3.restype = None
+    lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_value.restype = ctypes.c_double
+    lib.oracle_reshape_and_cache_fp8.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64,
+                                                 ctypes.c_float, ctypes.c_float]
+    lib.oracle_reshape_and_cache_fp8.restype = ctypes.c_int
+    lib.oracle_paged_attention_fp8.argtypes = [_P, _P, ctypes.c_double, ctypes.c_double, _P,
+                                               _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _I64,
+                                               ctypes.c_double, ctypes.c_int, _P, _I64, _P, _P]
+    lib.oracle_paged_attention_fp8.restype = ctypes.c_int
     return lib
 
 
@@ -171,6 +182,64 @@ class Oracle:
         for rc in rcs:
             if rc != 0:
                 raise ValueError(f"oracle attention failed ({rc})")
+
+    # -- fp8 (e4m3) pool -----------------------------------------------------
+    def quantize_e4m3(self, x_bits, scale):
+        """uint8 e4m3 codes of the bf16 values `x_bits` divided by `scale` (fp32)."""
+        x = _c(x_bits, np.uint16)
+        out = np.empty(x.shape, dtype=np.uint8)
+        self.lib.oracle_quantize_e4m3(_ptr(x), x.size, float(np.float32(scale)), _ptr(out))
+        return out
+
+    def e4m3_value(self, codes):
+        """Exact value (float64) of each e4m3 code."""
+        codes = np.asarray(codes, dtype=np.uint8)
+        return np.array([self.lib.oracle_e4m3_value(int(c)) for c in codes.ravel()],
+                        dtype=np.float64).reshape(codes.shape)
+
+    def reshape_and_cache_fp8(self, key, value, cache8, slot_mapping, k_scale, v_scale):
+        """Quantise key/value rows into the uint8 e4m3 pool `cache8` in place."""
+        key = _c(key, np.uint16)
+        value = _c(value, np.uint16)
+        assert cache8.dtype == np.uint8 and cache8.flags.c_contiguous
+        slots = _c(slot_mapping, np.int64)
+        nb, two, bs, hkv, d = cache8.shape
+        rc = self.lib.oracle_reshape_and_cache_fp8(
+            _ptr(key), _ptr(value), _ptr(cache8), _ptr(slots), slots.shape[0], hkv, d, bs, nb,
+            float(np.float32(k_scale)), float(np.float32(v_scale)))
+        if rc != 0:
+            raise ValueError(f"oracle reshape_and_cache_fp8 failed ({rc})")
+
+    def paged_attention_fp8(self, query, cache8, k_scale, v_scale, qsl, seq_lens, block_table,
+                            scale, causal=True, rows=None, threads=1):
+        """paged_attention over an e4m3 pool (K = code*k_scale, V = code*v_scale)."""
+        query = _c(query, np.uint16)
+        cache8 = _c(cache8, np.uint8)
+        qsl = _c(qsl, np.int32)
+        seq_lens = _c(seq_lens, np.int32)
+        block_table = _c(block_table, np.int32)
+        T, H, D = query.shape
+        nb, _, bs, hkv, _ = cache8.shape
+        if rows is None:
+            rows = np.arange(T * H, dtype=np.int64)
+        rows = _c(rows, np.int64)
+        n = rows.shape[0]
+        out = np.zeros((n, D), dtype=np.float64)
+        lse = np.zeros((n,), dtype=np.float64)
+        S = seq_lens.shape[0]
+
+        def run(lo, hi):
+            if hi <= lo:
+                return 0
+            return self.lib.oracle_paged_attention_fp8(
+                _ptr(query), _ptr(cache8), float(np.float32(k_scale)), float(np.float32(v_scale)),
+                _ptr(qsl), _ptr(seq_lens), _ptr(block_table), block_table.shape[1], S, H, hkv, D,
+                bs, nb, float(scale), int(bool(causal)), _ptr(rows[lo:hi]), hi - lo,
+                out[lo:hi].ctypes.data_as(ctypes.c_void_p),
+                lse[lo:hi].ctypes.data_as(ctypes.c_void_p))
+
+        self._parallel(run, n, threads)
+        return out, lse
 
     # -- merge ---------------------------------------------------------------
     def lse_merge(self, o_a, lse_a, o_b, lse_b):

@@ -60,6 +60,85 @@ static const uint16_t *pool_row(const uint16_t *cache, int64_t block, int64_t kv
 }
 
 /*
+ * FP8 E4M3 (the OCP 8-bit floating-point format: 1 sign bit, 4 exponent bits
+ * with bias 7, 3 mantissa bits; no infinities; S.1111.111 is NaN; largest
+ * finite 448 = 1.75 * 2^8; subnormals m/8 * 2^-6).  The pages name an fp8
+ * e4m3 KV cache ([FA/FI] "Resumen en una frase" and "Limites y fallos":
+ * fp8 / fp8_e4m3 KV cache) without a quantisation rule; the reading taken:
+ * one fp32 scale per tensor (k_scale for K, v_scale for V), code =
+ * e4m3(x / scale) with x / scale computed in fp32, rounded to nearest
+ * (ties to the even code) and saturated to +-448; value = code * scale.
+ */
+static double e4m3_value(uint8_t c)
+{
+    int sign = c >> 7, ex = (c >> 3) & 15, man = c & 7;
+    double v;
+    if (ex == 15 && man == 7)
+        return NAN;
+    if (ex == 0)
+        v = ldexp((double)man, -9); /* subnormal: man/8 * 2^-6 */
+    else
+        v = ldexp(8.0 + man, ex - 10); /* (1 + man/8) * 2^(ex-7) */
+    return sign ? -v : v;
+}
+
+/* Nearest e4m3 code to the float y: the 127 non-negative finite codes in
+ * increasing order are scanned for the closest value; a tie goes to the code
+ * whose last mantissa bit is 0; |y| above 448 saturates to 448; the sign is
+ * kept (also for zero); NaN gives 0x7f. */
+static uint8_t e4m3_encode(float y)
+{
+    if (y != y)
+        return 0x7f;
+    int neg = signbit(y) != 0;
+    double a = fabs((double)y);
+    uint8_t best = 0;
+    if (a >= 448.0) {
+        best = 0x7e;
+    } else {
+        double best_d = a; /* distance to code 0 */
+        for (int c = 1; c <= 0x7e; ++c) {
+            double d = fabs(e4m3_value((uint8_t)c) - a);
+            if (d < best_d || (d == best_d && (c & 1) == 0)) {
+                best = (uint8_t)c;
+                best_d = d;
+            }
+        }
+    }
+    return (uint8_t)(best | (neg ? 0x80 : 0));
+}
+
+/* Codes of x[i] / scale (fp32 division) for n values (bf16 bit patterns). */
+void oracle_quantize_e4m3(const uint16_t *x, int64_t n, float scale, uint8_t *out)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        float xf = (float)bf16_value(x[i]);
+        volatile float y = xf / scale; /* fp32 division, as stored */
+        out[i] = e4m3_encode(y);
+    }
+}
+
+double oracle_e4m3_value(uint8_t c) { return e4m3_value(c); }
+
+/* Element e of row (block, kv, offset, head) of a pool in bf16 (codes8 ==
+ * NULL) or e4m3 with per-tensor scales. */
+typedef struct {
+    const uint16_t *bf16;
+    const uint8_t *codes8;
+    double k_scale, v_scale;
+    int64_t block_size, num_kv_heads, head_size;
+} pool_view;
+
+static double pool_elem(const pool_view *pv, int64_t block, int64_t kv, int64_t offset,
+                        int64_t head, int64_t e)
+{
+    int64_t row = ((block * 2 + kv) * pv->block_size + offset) * pv->num_kv_heads + head;
+    if (pv->codes8)
+        return e4m3_value(pv->codes8[row * pv->head_size + e]) * (kv ? pv->v_scale : pv->k_scale);
+    return bf16_value(pv->bf16[row * pv->head_size + e]);
+}
+
+/*
  * reshape_and_cache: for every new token t with slot = slot_mapping[t] >= 0,
  * copy key[t] into the K slot (slot / block_size, slot % block_size) of the
  * pool and value[t] into the V slot, byte for byte.  slot < 0 is padding and
@@ -109,10 +188,10 @@ int oracle_reshape_and_cache(const uint16_t *key, const uint16_t *value, uint16_
  * x is scratch of at least hi-lo doubles.
  * Returns 0, or -1 when a block-table entry it needs is outside the pool.
  */
-static int attend_row(const uint16_t *q, const uint16_t *cache, const int32_t *bt_row,
-                      int64_t lo, int64_t hi, int64_t kv_head, int64_t num_kv_heads,
-                      int64_t head_size, int64_t block_size, int64_t num_blocks,
-                      double scale, double *x, double *out, double *lse)
+static int attend_row(const uint16_t *q, const pool_view *pv, const int32_t *bt_row,
+                      int64_t lo, int64_t hi, int64_t kv_head, int64_t head_size,
+                      int64_t block_size, int64_t num_blocks, double scale, double *x,
+                      double *out, double *lse)
 {
     for (int64_t e = 0; e < head_size; ++e)
         out[e] = 0.0;
@@ -126,18 +205,15 @@ static int attend_row(const uint16_t *q, const uint16_t *cache, const int32_t *b
         if (block < 0 || block >= num_blocks)
             return -1;
 #if ORACLE_MUTANT == 5
-        const uint16_t *k = pool_row(cache, block, 1, j % block_size, kv_head, block_size,
-                                     num_kv_heads, head_size); /* planted: V used as K */
+        int64_t k_kv = 1, k_off = j % block_size; /* planted: V used as K */
 #elif ORACLE_MUTANT == 6
-        const uint16_t *k = pool_row(cache, block, 0, (j + 1) % block_size, kv_head, block_size,
-                                     num_kv_heads, head_size); /* planted: wrong in-page offset */
+        int64_t k_kv = 0, k_off = (j + 1) % block_size; /* planted: wrong in-page offset */
 #else
-        const uint16_t *k = pool_row(cache, block, 0, j % block_size, kv_head, block_size,
-                                     num_kv_heads, head_size);
+        int64_t k_kv = 0, k_off = j % block_size;
 #endif
         double dot = 0.0;
         for (int64_t e = 0; e < head_size; ++e)
-            dot += bf16_value(q[e]) * bf16_value(k[e]);
+            dot += bf16_value(q[e]) * pool_elem(pv, block, k_kv, k_off, kv_head, e);
 #if ORACLE_MUTANT == 1
         x[j - lo] = dot; /* planted: scale dropped */
 #else
@@ -160,11 +236,9 @@ static int attend_row(const uint16_t *q, const uint16_t *cache, const int32_t *b
 #endif
     for (int64_t j = lo; j < hi; ++j) {
         int64_t block = bt_row[j / block_size];
-        const uint16_t *v = pool_row(cache, block, 1, j % block_size, kv_head, block_size,
-                                     num_kv_heads, head_size);
         double p = exp(x[j - lo] - l);
         for (int64_t e = 0; e < head_size; ++e)
-            out[e] += p * bf16_value(v[e]);
+            out[e] += p * pool_elem(pv, block, 1, j % block_size, kv_head, e);
     }
     *lse = l;
     return 0;
@@ -197,13 +271,13 @@ static int64_t owner_seq(const int32_t *qsl, int64_t num_seqs, int64_t t)
  * Returns 0, -1 for a block id outside the pool, -2 for bad metadata,
  * -3 for an allocation failure.
  */
-int oracle_paged_attention(const uint16_t *query, const uint16_t *cache, const int32_t *qsl,
-                           const int32_t *seq_lens, const int32_t *block_table,
-                           int64_t block_table_stride, int64_t num_seqs, int64_t num_heads,
-                           int64_t num_kv_heads, int64_t head_size, int64_t block_size,
-                           int64_t num_blocks, double scale, int causal, int64_t key_lo,
-                           int64_t key_hi, const int64_t *rows, int64_t num_rows, double *out,
-                           double *lse)
+static int paged_attention_view(const uint16_t *query, const pool_view *pv,
+                                const int32_t *qsl, const int32_t *seq_lens,
+                                const int32_t *block_table, int64_t block_table_stride,
+                                int64_t num_seqs, int64_t num_heads, int64_t num_kv_heads,
+                                int64_t head_size, int64_t block_size, int64_t num_blocks,
+                                double scale, int causal, int64_t key_lo, int64_t key_hi,
+                                const int64_t *rows, int64_t num_rows, double *out, double *lse)
 {
     if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0)
         return -2;
@@ -250,13 +324,72 @@ int oracle_paged_attention(const uint16_t *query, const uint16_t *cache, const i
 #else
         int64_t kv_head = h / group;
 #endif
-        rc = attend_row(query + (t * num_heads + h) * head_size, cache,
-                        block_table + s * block_table_stride, lo, hi, kv_head, num_kv_heads,
-                        head_size, block_size, num_blocks, scale, x, out + k * head_size,
-                        lse + k);
+        rc = attend_row(query + (t * num_heads + h) * head_size, pv,
+                        block_table + s * block_table_stride, lo, hi, kv_head, head_size,
+                        block_size, num_blocks, scale, x, out + k * head_size, lse + k);
     }
     free(x);
     return rc;
+}
+
+int oracle_paged_attention(const uint16_t *query, const uint16_t *cache, const int32_t *qsl,
+                           const int32_t *seq_lens, const int32_t *block_table,
+                           int64_t block_table_stride, int64_t num_seqs, int64_t num_heads,
+                           int64_t num_kv_heads, int64_t head_size, int64_t block_size,
+                           int64_t num_blocks, double scale, int causal, int64_t key_lo,
+                           int64_t key_hi, const int64_t *rows, int64_t num_rows, double *out,
+                           double *lse)
+{
+    pool_view pv = {cache, NULL, 1.0, 1.0, block_size, num_kv_heads, head_size};
+    return paged_attention_view(query, &pv, qsl, seq_lens, block_table, block_table_stride,
+                                num_seqs, num_heads, num_kv_heads, head_size, block_size,
+                                num_blocks, scale, causal, key_lo, key_hi, rows, num_rows, out,
+                                lse);
+}
+
+/*
+ * oracle_paged_attention over an e4m3 pool (one byte per element, same
+ * [num_blocks, 2, block_size, num_kv_heads, head_size] shape): K element
+ * value = e4m3 code * k_scale, V element value = code * v_scale.
+ */
+int oracle_paged_attention_fp8(const uint16_t *query, const uint8_t *cache8, double k_scale,
+                               double v_scale, const int32_t *qsl, const int32_t *seq_lens,
+                               const int32_t *block_table, int64_t block_table_stride,
+                               int64_t num_seqs, int64_t num_heads, int64_t num_kv_heads,
+                               int64_t head_size, int64_t block_size, int64_t num_blocks,
+                               double scale, int causal, const int64_t *rows, int64_t num_rows,
+                               double *out, double *lse)
+{
+    pool_view pv = {NULL, cache8, k_scale, v_scale, block_size, num_kv_heads, head_size};
+    return paged_attention_view(query, &pv, qsl, seq_lens, block_table, block_table_stride,
+                                num_seqs, num_heads, num_kv_heads, head_size, block_size,
+                                num_blocks, scale, causal, 0, -1, rows, num_rows, out, lse);
+}
+
+/*
+ * reshape_and_cache into an e4m3 pool: K rows quantised with k_scale, V rows
+ * with v_scale (oracle_quantize_e4m3), stored at the slot as in
+ * oracle_reshape_and_cache.  Returns 0, or -1 for a slot outside the pool.
+ */
+int oracle_reshape_and_cache_fp8(const uint16_t *key, const uint16_t *value, uint8_t *cache8,
+                                 const int64_t *slot_mapping, int64_t num_tokens,
+                                 int64_t num_kv_heads, int64_t head_size, int64_t block_size,
+                                 int64_t num_blocks, float k_scale, float v_scale)
+{
+    int64_t row_elems = num_kv_heads * head_size;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        if (slot >= num_blocks * block_size)
+            return -1;
+        int64_t block = slot / block_size, off = slot % block_size;
+        oracle_quantize_e4m3(key + t * row_elems, row_elems, k_scale,
+                             cache8 + ((block * 2 + 0) * block_size + off) * row_elems);
+        oracle_quantize_e4m3(value + t * row_elems, row_elems, v_scale,
+                             cache8 + ((block * 2 + 1) * block_size + off) * row_elems);
+    }
+    return 0;
 }
 
 /*
