@@ -89,6 +89,11 @@ typedef enum {
  *  kv_layout        physical order of the pool (pka_kv_layout): PKA_LAYOUT_NHD
  *                   (0, the default of a zero-initialised struct) or
  *                   PKA_LAYOUT_HND.
+ *  kv_dtype         element type of the pool (pka_kv_dtype): PKA_KV_BF16 (0,
+ *                   the default) or PKA_KV_FP8_E4M3.
+ *  k_scale, v_scale fp8 pools only: the per-tensor dequantisation scales of
+ *                   K and V (element value = e4m3 code value x scale);
+ *                   positive and finite.  Ignored for bf16.
  */
 
 /*
@@ -103,6 +108,18 @@ typedef enum {
  */
 typedef enum { PKA_LAYOUT_NHD = 0, PKA_LAYOUT_HND = 1 } pka_kv_layout;
 
+/*
+ * Element type of the pool ([FA/FI] "Resumen en una frase" and "Limites y
+ * fallos": an fp8 e4m3 KV cache).  The pages fix no quantisation rule; this
+ * library uses one fp32 scale per tensor for K and one for V:
+ *     code  = e4m3(x / scale)   (x/scale in binary32, rounded to the nearest
+ *                                e4m3 value, ties to the even code, clamped
+ *                                to +-448: the OCP E4M3 format, no infinity)
+ *     value = e4m3_value(code) * scale
+ * An fp8 pool has the bf16 pool's logical shape with one byte per element.
+ */
+typedef enum { PKA_KV_BF16 = 0, PKA_KV_FP8_E4M3 = 1 } pka_kv_dtype;
+
 typedef struct {
     const int32_t *query_start_loc;
     const int32_t *seq_lens;
@@ -115,6 +132,9 @@ typedef struct {
     int32_t common_prefix_len;
     int32_t split_kv_tokens;
     int32_t kv_layout;
+    int32_t kv_dtype;
+    float k_scale;
+    float v_scale;
 } pka_meta;
 
 /*
@@ -153,6 +173,25 @@ pka_status pka_reshape_and_cache_ex(const void *key, const void *value, void *kv
                                     int64_t num_blocks, int32_t kv_layout, void *stream);
 
 /*
+ * pka_reshape_and_cache_ex into an fp8 e4m3 pool (pka_kv_dtype): every element
+ * of the token's K row is stored as e4m3(k / k_scale), of its V row as
+ * e4m3(v / v_scale), by the rule stated at pka_kv_dtype.
+ *
+ *  kv_cache       device uint8 pool, the bf16 pool's shape in the layout
+ *                 kv_layout, one byte per element, written in place
+ *  k_scale, v_scale  positive finite fp32 scales (host values)
+ *
+ * Errors as pka_reshape_and_cache_ex, plus PKA_ERR_INVALID_ARG for a scale
+ * that is not positive and finite and PKA_ERR_UNSUPPORTED for head_size not
+ * a multiple of 16.
+ */
+pka_status pka_reshape_and_cache_fp8(const void *key, const void *value, void *kv_cache,
+                                     const int64_t *slot_mapping, int32_t num_tokens,
+                                     int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                     int64_t num_blocks, int32_t kv_layout, float k_scale,
+                                     float v_scale, void *stream);
+
+/*
  * Bytes of device workspace pka_paged_attn_forward needs for this batch
  * (split-KV and cascade partial results, fp32).  Same shape arguments as the
  * forward; depends only on host-side fields of `meta`.  Returns 0 when the
@@ -180,6 +219,8 @@ size_t pka_workspace_size(const pka_meta *meta, int32_t num_tokens, int32_t num_
  *
  *  query      device bf16 [num_tokens, num_heads, head_size]
  *  kv_cache   device bf16 [num_blocks, 2, block_size, num_kv_heads, head_size]
+ *             (uint8 codes of that shape for an fp8 pool; the order of the
+ *             middle axes is meta->kv_layout)
  *  meta       host pointer to the batch metadata above
  *  out        device bf16 [num_tokens, num_heads, head_size]; must not alias
  *             query; every row of every query token is written
@@ -195,6 +236,10 @@ size_t pka_workspace_size(const pka_meta *meta, int32_t num_tokens, int32_t num_
  * num_heads/num_kv_heads <= 8 for decodes; block_size a multiple of 16
  * (PKA_ERR_INVALID_ARG otherwise, as [FA/FI] "Limites y fallos" and
  * [backend] "Limites y fallos" require); other shapes PKA_ERR_UNSUPPORTED.
+ * An fp8 pool (meta->kv_dtype = PKA_KV_FP8_E4M3) is served for decode-only
+ * batches (num_decodes = num_seqs, common_prefix_len 0) at head_size 128: K_j
+ * and V_j above are then the dequantised values code x k_scale and
+ * code x v_scale; other fp8 batches return PKA_ERR_UNSUPPORTED.
  */
 pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const pka_meta *meta,
                                   void *out, float *lse, int32_t num_tokens, int32_t num_heads,
@@ -219,9 +264,13 @@ pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const
  *  slot_mapping   device int64 [num_tokens]; for a decode token the slot of
  *                 its sequence's last key (key L_s - 1 through block_table),
  *                 which is what makes the fused and the two-call results agree
- *  kv_cache       device pool, written in place (layout meta->kv_layout)
+ *  kv_cache       device pool, written in place (layout meta->kv_layout);
+ *                 for an fp8 pool the rows are stored as pka_reshape_and_cache_fp8
+ *                 stores them, with meta->k_scale and meta->v_scale, and the
+ *                 attention reads the stored codes
  *  other arguments as pka_paged_attn_forward.
- * Errors: those of the two calls.
+ * Errors: those of the two calls; a batch the forward does not serve returns
+ * before anything is written.
  */
 pka_status pka_paged_attn_forward_fused(const void *query, const void *key, const void *value,
                                         const int64_t *slot_mapping, void *kv_cache,

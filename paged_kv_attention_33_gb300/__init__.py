@@ -22,7 +22,8 @@ import threading
 
 from . import build as _build
 
-__all__ = ["Meta", "PkaError", "LAYOUT_NHD", "LAYOUT_HND", "reshape_and_cache", "paged_attn_forward", "cascade_merge",
+__all__ = ["Meta", "PkaError", "LAYOUT_NHD", "LAYOUT_HND", "KV_BF16", "KV_FP8_E4M3",
+           "reshape_and_cache", "reshape_and_cache_fp8", "paged_attn_forward", "cascade_merge",
            "paged_attn_forward_noalloc", "paged_attn_forward_fused", "workspace_size",
            "merge_partials", "LSE_BASE_E",
            "LSE_BASE_2", "check_status", "set_kernel_events", "kernel_launches",
@@ -49,13 +50,27 @@ class _CMeta(ctypes.Structure):
     _fields_ = [("query_start_loc", _P), ("seq_lens", _P), ("block_table", _P),
                 ("block_table_stride", _I32), ("num_seqs", _I32), ("num_decodes", _I32),
                 ("max_query_len", _I32), ("max_seq_len", _I32), ("common_prefix_len", _I32),
-                ("split_kv_tokens", _I32), ("kv_layout", _I32)]
+                ("split_kv_tokens", _I32), ("kv_layout", _I32), ("kv_dtype", _I32),
+                ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
 # Physical pool layouts (pka_kv_layout): the logical shape is always
 # [num_blocks, 2, block_size, num_kv_heads, head_size]; HND stores it as
 # [num_blocks, 2, num_kv_heads, block_size, head_size].
 LAYOUT_NHD = 0
 LAYOUT_HND = 1
+
+
+# Element types of the pool (pka_kv_dtype): bf16, or fp8 e4m3 codes with one
+# fp32 dequantisation scale per tensor for K and for V.
+KV_BF16 = 0
+KV_FP8_E4M3 = 1
+
+
+def _kv_dtype(kv_dtype) -> int:
+    if isinstance(kv_dtype, str):
+        return {"BF16": KV_BF16, "FP8": KV_FP8_E4M3, "FP8_E4M3": KV_FP8_E4M3,
+                "E4M3": KV_FP8_E4M3}[kv_dtype.upper()]
+    return int(kv_dtype)
 
 
 def _layout(kv_layout) -> int:
@@ -92,6 +107,9 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pka_reshape_and_cache_ex.argtypes = [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I64,
                                                  _I32, _P]
         lib.pka_reshape_and_cache_ex.restype = ctypes.c_int
+        lib.pka_reshape_and_cache_fp8.argtypes = [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I64,
+                                                  _I32, ctypes.c_float, ctypes.c_float, _P]
+        lib.pka_reshape_and_cache_fp8.restype = ctypes.c_int
         lib.pka_workspace_size.argtypes = [ctypes.POINTER(_CMeta), _I32, _I32, _I32, _I32, _I32]
         lib.pka_workspace_size.restype = ctypes.c_size_t
         lib.pka_paged_attn_forward.argtypes = [_P, _P, ctypes.POINTER(_CMeta), _P, _P, _I32,
@@ -147,11 +165,14 @@ class Meta:
     query_start_loc int32 [S+1], seq_lens int32 [S], block_table int32
     [S, stride] live on the device; num_decodes, max_query_len, max_seq_len,
     common_prefix_len, split_kv_tokens and kv_layout (LAYOUT_NHD / LAYOUT_HND,
-    or "NHD" / "HND") are host values.
+    or "NHD" / "HND") are host values, and so are kv_dtype (KV_BF16, or
+    KV_FP8_E4M3 / "fp8" for a pool of e4m3 codes) with its scales k_scale and
+    v_scale.
     """
 
     def __init__(self, query_start_loc, seq_lens, block_table, num_decodes, max_query_len,
-                 max_seq_len, common_prefix_len=0, split_kv_tokens=0, kv_layout=LAYOUT_NHD):
+                 max_seq_len, common_prefix_len=0, split_kv_tokens=0, kv_layout=LAYOUT_NHD,
+                 kv_dtype=KV_BF16, k_scale=1.0, v_scale=1.0):
         self.query_start_loc = query_start_loc
         self.seq_lens = seq_lens
         self.block_table = block_table
@@ -161,10 +182,14 @@ class Meta:
         self.common_prefix_len = int(common_prefix_len)
         self.split_kv_tokens = int(split_kv_tokens)
         self.kv_layout = _layout(kv_layout)
+        self.kv_dtype = _kv_dtype(kv_dtype)
+        self.k_scale = float(k_scale)
+        self.v_scale = float(v_scale)
 
     @classmethod
     def from_host(cls, query_start_loc, seq_lens, block_table, num_decodes, device,
-                  common_prefix_len=0, split_kv_tokens=0, kv_layout=LAYOUT_NHD):
+                  common_prefix_len=0, split_kv_tokens=0, kv_layout=LAYOUT_NHD,
+                  kv_dtype=KV_BF16, k_scale=1.0, v_scale=1.0):
         """Build from host (numpy) arrays, copying them to `device`."""
         import numpy as np
         import torch
@@ -178,14 +203,14 @@ class Meta:
         max_s = int(sl.max()) if len(sl) else 1
         return cls(torch.from_numpy(qsl).to(device), torch.from_numpy(sl).to(device),
                    torch.from_numpy(bt).to(device), nd, max_q, max_s, common_prefix_len,
-                   split_kv_tokens, kv_layout)
+                   split_kv_tokens, kv_layout, kv_dtype, k_scale, v_scale)
 
     def _c(self) -> _CMeta:
         return _CMeta(self.query_start_loc.data_ptr(), self.seq_lens.data_ptr(),
                       self.block_table.data_ptr(), self.block_table.shape[1],
                       self.seq_lens.shape[0], self.num_decodes, self.max_query_len,
                       self.max_seq_len, self.common_prefix_len, self.split_kv_tokens,
-                      self.kv_layout)
+                      self.kv_layout, self.kv_dtype, self.k_scale, self.v_scale)
 
 
 def reshape_and_cache(key, value, kv_cache, slot_mapping, stream=None,
@@ -197,6 +222,21 @@ def reshape_and_cache(key, value, kv_cache, slot_mapping, stream=None,
     _check(lib.pka_reshape_and_cache_ex(_ptr(key), _ptr(value), _ptr(kv_cache),
                                         _ptr(slot_mapping), key.shape[0], hkv, d, bs, nb,
                                         _layout(kv_layout), _stream(stream)))
+
+
+def reshape_and_cache_fp8(key, value, kv_cache, slot_mapping, k_scale, v_scale, stream=None,
+                          kv_layout=LAYOUT_NHD) -> None:
+    """Quantise key/value [T, Hkv, D] (bf16) rows into an e4m3 pool (uint8 or
+    float8_e4m3fn, [NB, 2, bs, Hkv, D] NHD or [NB, 2, Hkv, bs, D] HND):
+    code = e4m3(x / scale), ties to even, clamped to +-448."""
+    lib = load_library()
+    if kv_cache.element_size() != 1:
+        raise ValueError("an fp8 pool has one byte per element")
+    nb, bs, hkv, d = _pool_dims(kv_cache, kv_layout)
+    _check(lib.pka_reshape_and_cache_fp8(_ptr(key), _ptr(value), _ptr(kv_cache),
+                                         _ptr(slot_mapping), key.shape[0], hkv, d, bs, nb,
+                                         _layout(kv_layout), float(k_scale), float(v_scale),
+                                         _stream(stream)))
 
 
 def workspace_size(meta: Meta, num_tokens, num_heads, num_kv_heads, head_size, block_size) -> int:

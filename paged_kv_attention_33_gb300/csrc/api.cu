@@ -101,9 +101,9 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-CUresult encode_3d_bf16(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1,
-                        uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes,
-                        uint32_t box0, uint32_t box1, uint32_t box2)
+static CUresult encode_3d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base,
+                          uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1_bytes,
+                          uint64_t stride2_bytes, uint32_t box0, uint32_t box1, uint32_t box2)
 {
     auto fn = encode_fn();
     if (!fn)
@@ -112,22 +112,33 @@ CUresult encode_3d_bf16(CUtensorMap *map, const void *base, uint64_t d0, uint64_
     cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
     cuuint32_t box[3] = {box0, box1, box2};
     cuuint32_t estr[3] = {1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+    return fn(map, dtype, 3, const_cast<void *>(base), dims, strides,
               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+CUresult encode_3d_bf16(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1,
+                        uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes,
+                        uint32_t box0, uint32_t box1, uint32_t box2)
+{
+    return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, d0, d1, d2, stride1_bytes,
+                     stride2_bytes, box0, box1, box2);
+}
+
 CUresult encode_kv_map(CUtensorMap *map, const void *cache, int32_t head_size,
                        int32_t num_kv_heads, int32_t block_size, int64_t num_blocks, int32_t hnd,
-                       uint32_t box_rows)
+                       uint32_t box_rows, int32_t elem_bytes)
 {
     const uint64_t D = uint64_t(head_size), Hkv = uint64_t(num_kv_heads),
                    bs = uint64_t(block_size), pages = uint64_t(num_blocks) * 2;
-    const uint64_t row = D * 2;  // bytes of one (slot, head) row
+    const uint64_t row = D * uint64_t(elem_bytes);  // bytes of one (slot, head) row
+    const CUtensorMapDataType dt =
+        elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint32_t box0 = 128u / uint32_t(elem_bytes);  // one 128-byte swizzle row
     if (hnd)  // (dim, offset, page*Hkv + head): a head's page is bs contiguous rows
-        return encode_3d_bf16(map, cache, D, bs, pages * Hkv, row, row * bs, 64, box_rows, 1);
+        return encode_3d(map, dt, cache, D, bs, pages * Hkv, row, row * bs, box0, box_rows, 1);
     // (dim, head, page*bs + offset): a slot's heads are Hkv contiguous rows
-    return encode_3d_bf16(map, cache, D, Hkv, pages * bs, row, row * Hkv, 64, 1, box_rows);
+    return encode_3d(map, dt, cache, D, Hkv, pages * bs, row, row * Hkv, box0, 1, box_rows);
 }
 
 // ------------------------------------------------------------ planning
@@ -179,6 +190,8 @@ Workspace plan_workspace(const DecodePlan &dp, int32_t num_tokens, int32_t num_d
     return w;
 }
 
+static bool scale_ok(float s) { return s > 0.f && s <= 3.4e38f; }
+
 // Checks shared by pka_workspace_size and pka_paged_attn_forward.
 static pka_status check_shape(const pka_meta *m, int32_t num_tokens, int32_t num_heads,
                               int32_t num_kv_heads, int32_t head_size, int32_t block_size)
@@ -187,6 +200,10 @@ static pka_status check_shape(const pka_meta *m, int32_t num_tokens, int32_t num
         return fail(PKA_ERR_INVALID_ARG, "meta is NULL");
     if (m->kv_layout != PKA_LAYOUT_NHD && m->kv_layout != PKA_LAYOUT_HND)
         return fail(PKA_ERR_INVALID_ARG, "unknown kv_layout %d", m->kv_layout);
+    if (m->kv_dtype != PKA_KV_BF16 && m->kv_dtype != PKA_KV_FP8_E4M3)
+        return fail(PKA_ERR_INVALID_ARG, "unknown kv_dtype %d", m->kv_dtype);
+    if (m->kv_dtype == PKA_KV_FP8_E4M3 && !(scale_ok(m->k_scale) && scale_ok(m->v_scale)))
+        return fail(PKA_ERR_INVALID_ARG, "k_scale / v_scale must be positive and finite");
     if (block_size <= 0 || block_size % 16 != 0)
         return fail(PKA_ERR_INVALID_ARG, "Block size must be a multiple of 16 (got %d).",
                     block_size);
@@ -229,6 +246,14 @@ static pka_status check_shape(const pka_meta *m, int32_t num_tokens, int32_t num
                     num_heads / num_kv_heads);
     if (m->num_decodes > 65535)
         return fail(PKA_ERR_UNSUPPORTED, "more than 65535 decodes in one call");
+    if (m->kv_dtype == PKA_KV_FP8_E4M3) {
+        if (head_size != 128)
+            return fail(PKA_ERR_UNSUPPORTED, "fp8 pool: head_size %d is not built (128)",
+                        head_size);
+        if (m->num_decodes != m->num_seqs || m->common_prefix_len > 0)
+            return fail(PKA_ERR_UNSUPPORTED,
+                        "fp8 pool: only decode batches without a shared prefix are served");
+    }
     return PKA_OK;
 }
 
@@ -289,6 +314,44 @@ pka_status pka_reshape_and_cache_ex(const void *key, const void *value, void *kv
                                              static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "reshape_and_cache launch");
+    return PKA_OK;
+}
+
+pka_status pka_reshape_and_cache_fp8(const void *key, const void *value, void *kv_cache,
+                                     const int64_t *slot_mapping, int32_t num_tokens,
+                                     int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                     int64_t num_blocks, int32_t kv_layout, float k_scale,
+                                     float v_scale, void *stream)
+{
+    if (kv_layout != PKA_LAYOUT_NHD && kv_layout != PKA_LAYOUT_HND)
+        return fail(PKA_ERR_INVALID_ARG, "unknown kv_layout %d", kv_layout);
+    if (num_tokens < 0)
+        return fail(PKA_ERR_INVALID_ARG, "num_tokens < 0");
+    if (block_size <= 0 || block_size % 16 != 0)
+        return fail(PKA_ERR_INVALID_ARG, "Block size must be a multiple of 16 (got %d).",
+                    block_size);
+    if (head_size <= 0 || head_size % 8 != 0 || num_kv_heads <= 0 || num_blocks <= 0)
+        return fail(PKA_ERR_INVALID_ARG,
+                    "bad shape: head_size %d (multiple of 8), num_kv_heads %d, num_blocks %lld",
+                    head_size, num_kv_heads, static_cast<long long>(num_blocks));
+    if (!scale_ok(k_scale) || !scale_ok(v_scale))
+        return fail(PKA_ERR_INVALID_ARG, "k_scale / v_scale must be positive and finite");
+    if (head_size % 16 != 0)
+        return fail(PKA_ERR_UNSUPPORTED, "fp8 pool: head_size %d not a multiple of 16",
+                    head_size);
+    if (num_tokens == 0)
+        return PKA_OK;
+    if (!key || !value || !kv_cache || !slot_mapping)
+        return fail(PKA_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(key, 16) || !aligned(value, 16) || !aligned(kv_cache, 16) ||
+        !aligned(slot_mapping, 8))
+        return fail(PKA_ERR_INVALID_ARG, "misaligned pointer (16 bytes required)");
+    cudaError_t e = launch_reshape_and_cache_fp8(
+        key, value, kv_cache, slot_mapping, num_tokens, num_kv_heads, head_size, block_size,
+        num_blocks, kv_layout == PKA_LAYOUT_HND ? 1 : 0, k_scale, v_scale,
+        static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "reshape_and_cache_fp8 launch");
     return PKA_OK;
 }
 
@@ -372,6 +435,9 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
     f.block_size = block_size;
     f.num_blocks = num_blocks;
     f.kv_hnd = meta->kv_layout == PKA_LAYOUT_HND ? 1 : 0;
+    f.kv_fp8 = meta->kv_dtype == PKA_KV_FP8_E4M3 ? 1 : 0;
+    f.k_scale = meta->k_scale;
+    f.v_scale = meta->v_scale;
     f.scale = scale;
     f.causal = causal;
     f.stream = static_cast<cudaStream_t>(stream);
@@ -396,7 +462,7 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
 
     CUtensorMap kv_map;
     CUresult cr = encode_kv_map(&kv_map, kv_cache, head_size, num_kv_heads, block_size, num_blocks,
-                                f.kv_hnd, 16);
+                                f.kv_hnd, 16, f.kv_fp8 ? 1 : 2);
     if (cr != CUDA_SUCCESS)
         return fail(PKA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(cr));
 
@@ -471,8 +537,13 @@ pka_status pka_paged_attn_forward_fused(const void *query, const void *key, cons
         return fail(PKA_ERR_INVALID_ARG, "misaligned pointer (16 bytes required)");
     if (meta->num_decodes == 0) {
         // no decode launch to carry the write: write first, then attend
-        st = pka_reshape_and_cache_ex(key, value, kv_cache, slot_mapping, num_tokens, num_kv_heads,
-                                      head_size, block_size, num_blocks, meta->kv_layout, stream);
+        st = meta->kv_dtype == PKA_KV_FP8_E4M3
+                 ? pka_reshape_and_cache_fp8(key, value, kv_cache, slot_mapping, num_tokens,
+                                             num_kv_heads, head_size, block_size, num_blocks,
+                                             meta->kv_layout, meta->k_scale, meta->v_scale, stream)
+                 : pka_reshape_and_cache_ex(key, value, kv_cache, slot_mapping, num_tokens,
+                                            num_kv_heads, head_size, block_size, num_blocks,
+                                            meta->kv_layout, stream);
         if (st != PKA_OK)
             return st;
         return forward_impl(query, kv_cache, meta, out, lse, num_tokens, num_heads, num_kv_heads,

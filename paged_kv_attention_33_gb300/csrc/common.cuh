@@ -1,10 +1,13 @@
 // common.cuh -- small sm_103a building blocks shared by the kernels of the
 // paged-KV attention library: mbarriers with bounded waits, TMA tensor loads,
-// warp-level bf16 tensor-core fragments and the device error word.
+// warp-level bf16/f16 tensor-core fragments, fp8 e4m3 conversions and the
+// device error word.
 #pragma once
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -166,6 +169,22 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &r0, uint3
                  : "r"(addr));
 }
 
+// 16 bytes from shared memory (a 16-byte aligned shared-window address).
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+// Word i of a 16-byte vector (i a compile-time constant after unrolling).
+__device__ __forceinline__ uint32_t u4_word(const uint4 &v, int i)
+{
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
 // D (16x8 fp32) += A (16x16 bf16, row) * B (16x8 bf16, col)
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
                                                uint32_t a2, uint32_t a3, uint32_t b0,
@@ -173,6 +192,18 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// D (16x8 fp32) += A (16x16 f16, row) * B (16x8 f16, col)
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
         "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -190,6 +221,48 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (low half), .y = hi
     return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    __half2 v = __floats2half2_rn(lo, hi);  // .x = lo (low half), .y = hi
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// ---------------------------------------------------------------- fp8 e4m3
+// Bytes of (a, b) picked by the selector's four nibbles (byte i of the result
+// = byte nibble_i of the 8-byte value b:a).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// Two e4m3 codes (low byte -> low half) as two f16: exact, every e4m3 value
+// is an f16 normal number.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
+{
+    const __half2_raw h =
+        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes), __NV_E4M3);
+    return uint32_t(h.x) | (uint32_t(h.y) << 16);
+}
+
+// Eight bf16 (one 16-byte vector, element 0 in the low half of .x) divided by
+// `scale` in binary32 and rounded to e4m3 codes, ties to even, clamped to
+// +-448: the pool's quantisation rule.  Codes come out in element order.
+__device__ __forceinline__ uint2 quantize8_e4m3(uint4 x, float scale)
+{
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 f;
+        f.x = __fdiv_rn(__uint_as_float(w[i] << 16), scale);
+        f.y = __fdiv_rn(__uint_as_float(w[i] & 0xffff0000u), scale);
+        c[i] = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);  // .x -> low byte
+    }
+    return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
 
 // 2^x on the special-function unit (the hardware instruction itself).

@@ -86,6 +86,9 @@ struct DecodeParams {
     const int64_t *slots;
     uint4 *pool;
     int32_t num_decodes_all;  // tokens [num_decodes_all, T) are prefill tokens
+    // fp8 pool: element value = code value x scale (K, V)
+    float k_scale;
+    float v_scale;
 };
 
 constexpr int kConsumerWarps = 8;
@@ -94,13 +97,16 @@ constexpr int kMaxDecodeChunk = 4096;
 constexpr float kNegInf = -INFINITY;
 constexpr float kLn2 = 0.69314718055994530942f;
 
-template <int D>
+// kFp8: the pool holds e4m3 codes (one byte per element); the ring then
+// keeps twice the stages so that as many bytes are in flight.
+template <int D, bool kFp8 = false>
 struct DecodeCfg {
-    static constexpr int kHalves = D / 64;
-    static constexpr int kUnitBytes = 16 * D * 2;                  // 16 rows x D bf16
+    static constexpr int kRowBytes = D * (kFp8 ? 1 : 2);           // one key of one head
+    static constexpr int kHalves = kRowBytes / 128;                // 128-byte TMA boxes per row
+    static constexpr int kUnitBytes = 16 * kRowBytes;              // 16 keys
     static constexpr int kKvBytes = kConsumerWarps * kUnitBytes;   // all units of K (or V)
     static constexpr int kStageBytes = 2 * kKvBytes;
-    static constexpr int kStages = (D == 128) ? 3 : 6;
+    static constexpr int kStages = kStageBytes >= 65536 ? 3 : 6;
     static constexpr int kBarOff = kStages * kStageBytes;
     static constexpr int kMiscOff = kBarOff + 2 * kStages * 8;    // last-piece flag, abort flag
     static constexpr int kPrefixOff = kMiscOff + 16;
@@ -332,12 +338,37 @@ __device__ __forceinline__ void merge_prefix_direct(const DecodeParams &p, int t
     ls1 = W1 > 0.f ? M1 + log2f(W1) : kNegInf;
 }
 
+// 16 e4m3 codes of chunk c (elements 16c..16c+15) of token tk's row of kv
+// head h: the fp8 pool's quantisation of two 16-byte bf16 vectors.
+template <int D>
+__device__ __noinline__ uint4 quantized_chunk(const DecodeParams &p, int64_t tk, int h, int c,
+                                                 int kv)
+{
+    const uint4 *src = (kv ? p.new_value : p.new_key) + (tk * p.num_kv_heads + h) * (D / 8) + 2 * c;
+    const float sc = kv ? p.v_scale : p.k_scale;
+    const uint2 lo = quantize8_e4m3(__ldg(src), sc), hi = quantize8_e4m3(__ldg(src + 1), sc);
+    return make_uint4(lo.x, lo.y, hi.x, hi.y);
+}
+
+// 16-byte chunk c of kv head h's K (kv 0) or V (kv 1) row of slot sl (block
+// sl / bs, offset sl % bs) in a pool of kChunks chunks per row, NHD or HND.
+template <bool kHnd>
+__device__ __forceinline__ int64_t pool_chunk(const DecodeParams &p, int64_t sl, int kv, int h,
+                                              int c, int kChunks)
+{
+    const int64_t blk = sl / p.block_size, off = sl % p.block_size;
+    const int Hkv = p.num_kv_heads;
+    const int64_t row = kHnd ? ((blk * 2 + kv) * Hkv + h) * p.block_size + off
+                             : ((blk * 2 + kv) * p.block_size + off) * Hkv + h;
+    return row * kChunks + c;
+}
+
 // Heads [h0, h1) of token tk's new K and V rows into the pool at slot sl
 // (block sl / bs, offset sl % bs), 16 bytes per lane, NHD or HND order -- the
 // cache write of the "FlashAttention y FlashInfer" page ("Responsabilidades":
-// the cache-update op), done inside the forward.  A negative slot is padding;
-// a slot past the pool is skipped and flagged.
-template <int D, bool kHnd>
+// the cache-update op), done inside the forward; an fp8 pool gets the codes.
+// A negative slot is padding; a slot past the pool is skipped and flagged.
+template <int D, bool kHnd, bool kFp8>
 __device__ __forceinline__ void write_pool_row(const DecodeParams &p, int64_t tk, int64_t sl,
                                                int lane, int h0, int h1)
 {
@@ -348,25 +379,26 @@ __device__ __forceinline__ void write_pool_row(const DecodeParams &p, int64_t tk
             flag_error(kErrSlotOutOfPool);
         return;
     }
-    constexpr int kChunks = D / 8;
-    const int64_t blk = sl / p.block_size, off = sl % p.block_size;
-    const int Hkv = p.num_kv_heads;
+    constexpr int kChunks = D / (kFp8 ? 16 : 8);  // 16-byte chunks of one head's row
     for (int i = lane; i < (h1 - h0) * kChunks; i += 32) {
         const int h = h0 + i / kChunks, c = i % kChunks;
-        const int64_t src = (tk * Hkv + h) * kChunks + c;
         for (int kv = 0; kv < 2; ++kv) {
-            const int64_t row = kHnd ? ((blk * 2 + kv) * Hkv + h) * p.block_size + off
-                                     : ((blk * 2 + kv) * p.block_size + off) * Hkv + h;
-            p.pool[row * kChunks + c] = __ldg((kv ? p.new_value : p.new_key) + src);
+            uint4 v;
+            if constexpr (kFp8)
+                v = quantized_chunk<D>(p, tk, h, c, kv);
+            else
+                v = __ldg((kv ? p.new_value : p.new_key) + (tk * p.num_kv_heads + h) * kChunks + c);
+            p.pool[pool_chunk<kHnd>(p, sl, kv, h, c, kChunks)] = v;
         }
     }
 }
 
-template <int D, bool kHnd>
+template <int D, bool kHnd, bool kFp8>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p)
 {
-    using Cfg = DecodeCfg<D>;
+    static_assert(!kFp8 || D == 128, "the fp8 tile addressing assumes 128-byte rows");
+    using Cfg = DecodeCfg<D, kFp8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -389,7 +421,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const int64_t nw = int64_t(gridDim.x) * (kDecodeThreads / 32);
         for (int64_t tk = p.num_decodes_all + int64_t(blockIdx.x) * (kDecodeThreads / 32) + warp;
              tk < p.num_tokens; tk += nw)
-            write_pool_row<D, kHnd>(p, tk, p.slots[tk], lane, 0, Hkv);
+            write_pool_row<D, kHnd, kFp8>(p, tk, p.slots[tk], lane, 0, Hkv);
     }
 
     // ---- stage prefix sums over the decodes of this launch: each thread sums a
@@ -453,7 +485,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
-        // lane = one (unit, K|V, 64-dim half) box of every stage; its block id is
+        // lane = one (unit, K|V, 128-byte half) box of every stage; its block id is
         // looked up for the next stage before waiting for a free slot
         if (lane == 0)
             tma_prefetch_desc(&kv_map);
@@ -506,7 +538,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             if (row >= 0) {
                 uint8_t *dst = smem + slot * Cfg::kStageBytes + kv * Cfg::kKvBytes +
                                u * Cfg::kUnitBytes + half * 2048;
-                tma_load_3d(dst, &kv_map, &full[slot], half * 64, c1, row, policy);
+                tma_load_3d(dst, &kv_map, &full[slot], half * (128 / (kFp8 ? 1 : 2)), c1, row,
+                            policy);
             }
             // the next stage's blocks are looked up after this one is issued
             if (x + 1 < hi) {
@@ -536,6 +569,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     uint32_t qf[D / 16][2];
     float o[D / 16][4];
     float m0, m1, l0, l1;
+    // log2-domain multipliers of the raw scores of heads n0 = 2tq and n1 = 2tq+1
+    float mul0 = p.scale_log2, mul1 = p.scale_log2;
     int s = s_first;
     int t = 0, L = 0;
     bool ok = true;
@@ -558,10 +593,55 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const bool live = gq < g;
         const uint32_t *qrow =
             p.query + ((static_cast<int64_t>(t) * H + k * g + (live ? gq : 0)) * D) / 2;
+        if constexpr (kFp8) {
+            // f16 fragments (the K tile is dequantised to f16), each head
+            // prescaled by the power of two 2^(14-e) that puts its largest |q|
+            // (in [2^e, 2^(e+1))) into [2^14, 2^15): bf16 has a wider range
+            // than f16, and normal bf16 values are exact in f16.  Step
+            // kk = 4*hh + m takes rows (2tq, 2tq+1 | 2tq+8, 2tq+9) from dims
+            // 64*hh + 16*tq + 4*m + (0, 1 | 2, 3): the dims one 16-byte read
+            // of a K row gives this thread (below).
+            const uint4 *qv = reinterpret_cast<const uint4 *>(qrow);
+            uint4 raw[D / 64][2];
+            float amax = 0.f;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            qf[kk][0] = live ? __ldg(qrow + (16 * kk + 2 * tq) / 2) : 0u;
-            qf[kk][1] = live ? __ldg(qrow + (16 * kk + 8 + 2 * tq) / 2) : 0u;
+            for (int hh = 0; hh < D / 64; ++hh)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    raw[hh][j] = live ? __ldg(qv + (64 * hh + 16 * tq) / 8 + j) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const uint32_t x = u4_word(raw[hh][j], w);
+                        amax = fmax3(amax, fabsf(__uint_as_float(x << 16)),
+                                     fabsf(__uint_as_float(x & 0xffff0000u)));
+                    }
+                }
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            const int e =
+                amax > 0.f ? max(int((__float_as_uint(amax) >> 23) & 0xffu) - 127, -112) : 0;
+            const float pre = __uint_as_float(uint32_t(127 + 14 - e) << 23);
+            const float mul = p.scale_log2 * p.k_scale * __uint_as_float(uint32_t(127 - 14 + e) << 23);
+#pragma unroll
+            for (int hh = 0; hh < D / 64; ++hh)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const uint32_t w0 = u4_word(raw[hh][m >> 1], 2 * (m & 1));
+                    const uint32_t w1 = u4_word(raw[hh][m >> 1], 2 * (m & 1) + 1);
+                    qf[4 * hh + m][0] = pack_f16x2(__uint_as_float(w0 << 16) * pre,
+                                                   __uint_as_float(w0 & 0xffff0000u) * pre);
+                    qf[4 * hh + m][1] = pack_f16x2(__uint_as_float(w1 << 16) * pre,
+                                                   __uint_as_float(w1 & 0xffff0000u) * pre);
+                }
+            // head n is prescaled in the lanes with gq = n (lane 4n)
+            mul0 = __shfl_sync(0xffffffffu, mul, 8 * tq);
+            mul1 = __shfl_sync(0xffffffffu, mul, 8 * tq + 4);
+        } else {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                qf[kk][0] = live ? __ldg(qrow + (16 * kk + 2 * tq) / 2) : 0u;
+                qf[kk][1] = live ? __ldg(qrow + (16 * kk + 8 + 2 * tq) / 2) : 0u;
+            }
         }
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt)
@@ -586,40 +666,72 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 // this stage holds the decode's new key (key L-1): the pool may
                 // not have it yet, so it is taken from the step's K/V rows into
                 // the staged tile, and written to the pool at the token's slot
+                // (the same registers both times: lanes [0, kChunks) cover head
+                // k's row)
                 const int64_t sl = p.slots[t];
                 if (sl >= 0 && sl < int64_t(p.num_blocks) * p.block_size) {
-                    constexpr int kChunks = D / 8;  // 16-byte chunks of one head's row
-                    if (lane < kChunks) {
-                        const int64_t src = (int64_t(t) * Hkv + k) * kChunks + lane;
-                        const uint4 nk = __ldg(p.new_key + src), nv = __ldg(p.new_value + src);
-                        const uint32_t o = (lane >> 3) * 2048 + swz128(L - 1 - ks, lane & 7);
-                        uint8_t *tile = smem + slot * Cfg::kStageBytes + u * Cfg::kUnitBytes;
-                        *reinterpret_cast<uint4 *>(tile + o) = nk;
-                        *reinterpret_cast<uint4 *>(tile + Cfg::kKvBytes + o) = nv;
-                        // the stage is refilled by TMA later: order these
-                        // generic writes before the async proxy's
+                    constexpr int kChunks = Cfg::kRowBytes / 16;  // 16-byte chunks of a row
+                    // lanes [0, kChunks) take the K row, the next kChunks the V row
+                    // (an fp8 pool: 8 + 8 lanes; bf16 D=128: 16 + 16)
+                    static_assert(2 * kChunks <= 32, "one chunk per lane");
+                    if (lane < 2 * kChunks) {
+                        const int kv = lane / kChunks, c = lane % kChunks;
+                        uint4 nr;
+                        if constexpr (kFp8)
+                            nr = quantized_chunk<D>(p, t, k, c, kv);
+                        else
+                            nr = __ldg((kv ? p.new_value : p.new_key) +
+                                       (int64_t(t) * Hkv + k) * kChunks + c);
+                        const uint32_t o = (c >> 3) * 2048 + swz128(L - 1 - ks, c & 7);
+                        uint8_t *tile = smem + slot * Cfg::kStageBytes + kv * Cfg::kKvBytes +
+                                        u * Cfg::kUnitBytes;
+                        *reinterpret_cast<uint4 *>(tile + o) = nr;
+                        // the stage is refilled by TMA later: order this generic
+                        // write before the async proxy's
                         fence_proxy_async_smem();
+                        p.pool[pool_chunk<kHnd>(p, sl, kv, k, c, kChunks)] = nr;
                     }
-                    write_pool_row<D, kHnd>(p, t, sl, lane, k, k + 1);
                     __syncwarp();
                 } else if (sl >= 0 && lane == 0) {
                     flag_error(kErrSlotOutOfPool);
                 }
             }
-            // S^T = K Q^T
+            // S^T = K Q^T; row gq of S^T is key kp of the tile, row gq+8 key kp+8
             float c[4] = {0.f, 0.f, 0.f, 0.f};
+            int kp;
+            if constexpr (kFp8) {
+                // rows gq (and gq+8) read key (gq>>1) + 4*(gq&1): the two rows of
+                // a quarter-warp then differ in swizzle bit 2 and their 16-byte
+                // reads fall in different banks.  One read = 16 dims of a key:
+                // dims 64*hh + 16*tq + 4*m + (0, 1 | 2, 3) for step 4*hh + m.
+                kp = (gq >> 1) + 4 * (gq & 1);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t ch = 2 * kk + k_chunk;
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(kbase + (ch >> 3) * 2048 + swz128(k_row, ch & 7), a0, a1, a2, a3);
-                mma_bf16_16816(c, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+                for (int hh = 0; hh < D / 64; ++hh) {
+                    const uint4 kr0 = lds128(kbase + swz128(kp, 4 * hh + tq));
+                    const uint4 kr1 = lds128(kbase + swz128(kp + 8, 4 * hh + tq));
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const uint32_t w0 = u4_word(kr0, m), w1 = u4_word(kr1, m);
+                        mma_f16_16816(c, e4m3x2_to_f16x2(w0 & 0xffffu), e4m3x2_to_f16x2(w1 & 0xffffu),
+                                      e4m3x2_to_f16x2(w0 >> 16), e4m3x2_to_f16x2(w1 >> 16),
+                                      qf[4 * hh + m][0], qf[4 * hh + m][1]);
+                    }
+                }
+            } else {
+                kp = gq;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t ch = 2 * kk + k_chunk;
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(kbase + (ch >> 3) * 2048 + swz128(k_row, ch & 7), a0, a1, a2, a3);
+                    mma_bf16_16816(c, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+                }
             }
-            const bool va = gq < valid, vb = gq + 8 < valid;
-            const float s0 = va ? c[0] * p.scale_log2 : kNegInf;
-            const float s1 = va ? c[1] * p.scale_log2 : kNegInf;
-            const float s2 = vb ? c[2] * p.scale_log2 : kNegInf;
-            const float s3 = vb ? c[3] * p.scale_log2 : kNegInf;
+            const bool va = kp < valid, vb = kp + 8 < valid;
+            const float s0 = va ? c[0] * mul0 : kNegInf;
+            const float s1 = va ? c[1] * mul1 : kNegInf;
+            const float s2 = vb ? c[2] * mul0 : kNegInf;
+            const float s3 = vb ? c[3] * mul1 : kNegInf;
             const float mn0 = fmaxf(m0, warp_max_heads(fmaxf(s0, s2)));
             const float mn1 = fmaxf(m1, warp_max_heads(fmaxf(s1, s3)));
             const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
@@ -629,23 +741,66 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             l1 = l1 * al1 + (p1 + p3);
             m0 = mn0;
             m1 = mn1;
-            const uint32_t b0 = movmatrix_trans(pack_bf16x2(p0, p1));  // keys 0-7
-            const uint32_t b1 = movmatrix_trans(pack_bf16x2(p2, p3));  // keys 8-15
-            // rows of V past the end of the sequence may hold anything: zero them
-            const uint32_t mlo = (2 * tq < valid ? 0x0000ffffu : 0u) |
-                                 (2 * tq + 1 < valid ? 0xffff0000u : 0u);
-            const uint32_t mhi = (2 * tq + 8 < valid ? 0x0000ffffu : 0u) |
-                                 (2 * tq + 9 < valid ? 0xffff0000u : 0u);
+            // P^T as B fragments: rows 0-7 and 8-15 of S^T
+            const uint32_t b0 = movmatrix_trans(kFp8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1));
+            const uint32_t b1 = movmatrix_trans(kFp8 ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3));
+            if constexpr (kFp8) {
+                // V^T fragments: columns 2tq, 2tq+1, 2tq+8, 2tq+9 are S^T rows,
+                // i.e. keys tq, tq+4, tq+8, tq+12; row gq of step mt is dim
+                // 16*gq + 2*mt and row gq+8 dim 16*gq + 2*mt + 1, so one 16-byte
+                // read per key covers all steps.  Odd-gq lanes read their two
+                // keys in the other order (conflict-free quarter-warps) and the
+                // byte permute undoes it.  Keys past the end of the sequence
+                // may hold anything (an e4m3 NaN too): zero them.
+                const bool odd = gq & 1;
+                const uint32_t r0 = odd ? tq + 4 : tq, r1 = odd ? tq : tq + 4;
+                const uint4 x0 = lds128(vbase + swz128(r0, gq)), y0 = lds128(vbase + swz128(r1, gq));
+                const uint4 x1 = lds128(vbase + swz128(r0 + 8, gq));
+                const uint4 y1 = lds128(vbase + swz128(r1 + 8, gq));
+                // bytes (key tq, key tq+4) of dims 4w, 4w+1 | 4w+2, 4w+3
+                const uint32_t sel_a = odd ? 0x1504u : 0x5140u, sel_b = odd ? 0x3726u : 0x7362u;
+                const uint32_t mlo = (tq < valid ? 0x0000ffffu : 0u) |
+                                     (tq + 4 < valid ? 0xffff0000u : 0u);
+                const uint32_t mhi = (tq + 8 < valid ? 0x0000ffffu : 0u) |
+                                     (tq + 12 < valid ? 0xffff0000u : 0u);
 #pragma unroll
-            for (int mt = 0; mt < D / 16; ++mt) {
-                const uint32_t ch = 2 * mt + v_chunk;
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4_trans(vbase + (ch >> 3) * 2048 + swz128(v_row, ch & 7), a0, a1, a2, a3);
-                o[mt][0] *= al0;
-                o[mt][1] *= al1;
-                o[mt][2] *= al0;
-                o[mt][3] *= al1;
-                mma_bf16_16816(o[mt], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, b0, b1);
+                for (int w = 0; w < 4; ++w) {
+                    const uint32_t lo0 = prmt(u4_word(x0, w), u4_word(y0, w), sel_a);
+                    const uint32_t hi0 = prmt(u4_word(x0, w), u4_word(y0, w), sel_b);
+                    const uint32_t lo1 = prmt(u4_word(x1, w), u4_word(y1, w), sel_a);
+                    const uint32_t hi1 = prmt(u4_word(x1, w), u4_word(y1, w), sel_b);
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int mt = 2 * w + j;
+                        const uint32_t q0 = j ? hi0 : lo0, q1 = j ? hi1 : lo1;
+                        o[mt][0] *= al0;
+                        o[mt][1] *= al1;
+                        o[mt][2] *= al0;
+                        o[mt][3] *= al1;
+                        mma_f16_16816(o[mt], e4m3x2_to_f16x2(q0 & 0xffffu) & mlo,
+                                      e4m3x2_to_f16x2(q0 >> 16) & mlo,
+                                      e4m3x2_to_f16x2(q1 & 0xffffu) & mhi,
+                                      e4m3x2_to_f16x2(q1 >> 16) & mhi, b0, b1);
+                    }
+                }
+            } else {
+                // rows of V past the end of the sequence may hold anything: zero them
+                const uint32_t mlo = (2 * tq < valid ? 0x0000ffffu : 0u) |
+                                     (2 * tq + 1 < valid ? 0xffff0000u : 0u);
+                const uint32_t mhi = (2 * tq + 8 < valid ? 0x0000ffffu : 0u) |
+                                     (2 * tq + 9 < valid ? 0xffff0000u : 0u);
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    const uint32_t ch = 2 * mt + v_chunk;
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_trans(vbase + (ch >> 3) * 2048 + swz128(v_row, ch & 7), a0, a1, a2,
+                                  a3);
+                    o[mt][0] *= al0;
+                    o[mt][1] *= al1;
+                    o[mt][2] *= al0;
+                    o[mt][3] *= al1;
+                    mma_bf16_16816(o[mt], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, b0, b1);
+                }
             }
         }
         __syncwarp();
@@ -664,27 +819,41 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         // registers; in a cascade its prefix partials are merged in right here
         const bool direct = np == 1 && R == 1;
         const int n0 = 2 * tq, n1 = 2 * tq + 1;  // the two heads of this thread
-        const float i0 = lr0 > 0.f ? 1.f / lr0 : 0.f;
-        const float i1 = lr1 > 0.f ? 1.f / lr1 : 0.f;
+        // row scales of the output (an fp8 pool's V dequantisation folded in)
+        const float vsc = kFp8 ? p.v_scale : 1.f;
+        const float i0 = lr0 > 0.f ? vsc / lr0 : 0.f;
+        const float i1 = lr1 > 0.f ? vsc / lr1 : 0.f;
         if (direct) {
             if (ok) {
                 float sc0 = i0, sc1 = i1;  // row scales of the output
                 float ls0 = m0 + log2f(lr0), ls1 = m1 + log2f(lr1);  // log2-sum-exp
-                if (p.cascade)
-                    merge_prefix_direct<D>(p, t, k * g + min(n0, g - 1), k * g + min(n1, g - 1), gq,
-                                           o, sc0, sc1, ls0, ls1);
+                if constexpr (!kFp8) {  // no cascade over an fp8 pool
+                    if (p.cascade)
+                        merge_prefix_direct<D>(p, t, k * g + min(n0, g - 1),
+                                               k * g + min(n1, g - 1), gq, o, sc0, sc1, ls0, ls1);
+                }
 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt) {
-                    const int d = 16 * mt + gq;
-                    if (n0 < g) {
-                        __nv_bfloat16 *dst = p.out + (int64_t(t) * H + k * g + n0) * D;
-                        dst[d] = __float2bfloat16_rn(o[mt][0] * sc0);
-                        dst[d + 8] = __float2bfloat16_rn(o[mt][2] * sc0);
-                    }
-                    if (n1 < g) {
-                        __nv_bfloat16 *dst = p.out + (int64_t(t) * H + k * g + n1) * D;
-                        dst[d] = __float2bfloat16_rn(o[mt][1] * sc1);
-                        dst[d + 8] = __float2bfloat16_rn(o[mt][3] * sc1);
+                    __nv_bfloat16 *d0 = p.out + (int64_t(t) * H + k * g + n0) * D;
+                    __nv_bfloat16 *d1 = p.out + (int64_t(t) * H + k * g + n1) * D;
+                    if constexpr (kFp8) {  // dims 16*gq + 2*mt and +1: one pair
+                        const int d = 16 * gq + 2 * mt;
+                        if (n0 < g)
+                            *reinterpret_cast<__nv_bfloat162 *>(d0 + d) =
+                                __floats2bfloat162_rn(o[mt][0] * sc0, o[mt][2] * sc0);
+                        if (n1 < g)
+                            *reinterpret_cast<__nv_bfloat162 *>(d1 + d) =
+                                __floats2bfloat162_rn(o[mt][1] * sc1, o[mt][3] * sc1);
+                    } else {  // dims 16*mt + gq and +8
+                        const int d = 16 * mt + gq;
+                        if (n0 < g) {
+                            d0[d] = __float2bfloat16_rn(o[mt][0] * sc0);
+                            d0[d + 8] = __float2bfloat16_rn(o[mt][2] * sc0);
+                        }
+                        if (n1 < g) {
+                            d1[d] = __float2bfloat16_rn(o[mt][1] * sc1);
+                            d1[d + 8] = __float2bfloat16_rn(o[mt][3] * sc1);
+                        }
                     }
                 }
                 if (gq == 0 && p.lse) {
@@ -700,16 +869,26 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             if (ok) {
 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt) {
-                    const int d = 16 * mt + gq;
-                    if (n0 < g) {
-                        float *dst = p.o_part + (prow + n0) * D;
-                        dst[d] = o[mt][0] * i0;
-                        dst[d + 8] = o[mt][2] * i0;
-                    }
-                    if (n1 < g) {
-                        float *dst = p.o_part + (prow + n1) * D;
-                        dst[d] = o[mt][1] * i1;
-                        dst[d + 8] = o[mt][3] * i1;
+                    float *d0 = p.o_part + (prow + n0) * D;
+                    float *d1 = p.o_part + (prow + n1) * D;
+                    if constexpr (kFp8) {
+                        const int d = 16 * gq + 2 * mt;
+                        if (n0 < g)
+                            *reinterpret_cast<float2 *>(d0 + d) =
+                                make_float2(o[mt][0] * i0, o[mt][2] * i0);
+                        if (n1 < g)
+                            *reinterpret_cast<float2 *>(d1 + d) =
+                                make_float2(o[mt][1] * i1, o[mt][3] * i1);
+                    } else {
+                        const int d = 16 * mt + gq;
+                        if (n0 < g) {
+                            d0[d] = o[mt][0] * i0;
+                            d0[d + 8] = o[mt][2] * i0;
+                        }
+                        if (n1 < g) {
+                            d1[d] = o[mt][1] * i1;
+                            d1[d + 8] = o[mt][3] * i1;
+                        }
                     }
                 }
                 if (gq == 0) {
@@ -819,17 +998,17 @@ DecodePlan plan_decode(int32_t split_kv_tokens, int32_t num_decodes, int32_t num
     return dp;
 }
 
-template <int D, bool kHnd>
+template <int D, bool kHnd, bool kFp8>
 static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Workspace &ws,
                                    char *wsp, const CUtensorMap &kv_map, int32_t kv_begin,
                                    bool cascade)
 {
-    using Cfg = DecodeCfg<D>;
+    using Cfg = DecodeCfg<D, kFp8>;
     static int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D, kHnd>,
+        cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D, kHnd, kFp8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(Cfg::kSmemBytes));
         if (e != cudaSuccess)
@@ -866,6 +1045,8 @@ static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Wor
     p.slots = f.slots;
     p.pool = static_cast<uint4 *>(f.kv_cache_w);
     p.num_decodes_all = f.num_decodes;
+    p.k_scale = f.k_scale;
+    p.v_scale = f.v_scale;
     // one launch per chunk of at most kMaxDecodeChunk decodes (stream ordered,
     // so chunks reuse the same partial slots and counters)
     for (int32_t seq0 = 0; seq0 < f.num_decodes; seq0 += dp.chunk) {
@@ -875,7 +1056,7 @@ static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Wor
         if (e != cudaSuccess)
             return e;
         count_launch();
-        paged_decode_kernel<D, kHnd>
+        paged_decode_kernel<D, kHnd, kFp8>
             <<<dp.grid, kDecodeThreads, Cfg::kSmemBytes, f.stream>>>(kv_map, p);
         e = cudaGetLastError();
         if (e != cudaSuccess)
@@ -889,11 +1070,19 @@ cudaError_t launch_decode(const Fwd &f, const DecodePlan &dp, const Workspace &w
 {
     if (f.num_decodes == 0)
         return cudaSuccess;
+    if (f.kv_fp8) {  // head_size 128 only (checked by the caller)
+        if (f.head_size != 128 || cascade)
+            return cudaErrorInvalidValue;
+        return f.kv_hnd
+                   ? launch_decode_d<128, true, true>(f, dp, ws, wsp, kv_map, kv_begin, cascade)
+                   : launch_decode_d<128, false, true>(f, dp, ws, wsp, kv_map, kv_begin, cascade);
+    }
     if (f.head_size == 128)
-        return f.kv_hnd ? launch_decode_d<128, true>(f, dp, ws, wsp, kv_map, kv_begin, cascade)
-                        : launch_decode_d<128, false>(f, dp, ws, wsp, kv_map, kv_begin, cascade);
-    return f.kv_hnd ? launch_decode_d<64, true>(f, dp, ws, wsp, kv_map, kv_begin, cascade)
-                    : launch_decode_d<64, false>(f, dp, ws, wsp, kv_map, kv_begin, cascade);
+        return f.kv_hnd
+                   ? launch_decode_d<128, true, false>(f, dp, ws, wsp, kv_map, kv_begin, cascade)
+                   : launch_decode_d<128, false, false>(f, dp, ws, wsp, kv_map, kv_begin, cascade);
+    return f.kv_hnd ? launch_decode_d<64, true, false>(f, dp, ws, wsp, kv_map, kv_begin, cascade)
+                    : launch_decode_d<64, false, false>(f, dp, ws, wsp, kv_map, kv_begin, cascade);
 }
 
 cudaError_t launch_cascade_prefill_combine(const Fwd &f, const Workspace &ws, char *wsp)

@@ -32,6 +32,9 @@ struct Fwd {
     int32_t block_size;
     int64_t num_blocks;
     int32_t kv_hnd;  // 1: pool in HND order, 0: NHD
+    int32_t kv_fp8 = 0;  // 1: pool of e4m3 codes (decode only), 0: bf16
+    float k_scale = 1.f;
+    float v_scale = 1.f;
     // fused cache write: the decode launch also writes this step's K/V rows
     int32_t fuse_write = 0;
     const void *new_key = nullptr;
@@ -82,6 +85,11 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *c
                                      int32_t num_kv_heads, int32_t head_size,
                                      int32_t block_size, int64_t num_blocks, int32_t hnd,
                                      cudaStream_t st);
+cudaError_t launch_reshape_and_cache_fp8(const void *key, const void *value, void *cache,
+                                         const int64_t *slots, int32_t num_tokens,
+                                         int32_t num_kv_heads, int32_t head_size,
+                                         int32_t block_size, int64_t num_blocks, int32_t hnd,
+                                         float k_scale, float v_scale, cudaStream_t st);
 uint32_t kv_write_take_error();
 
 // decode.cu: paged decode of sequences [0, num_decodes) over keys
@@ -137,15 +145,17 @@ constexpr int kMaxPrefillSeqsPerCall = 4096;
 CUresult encode_3d_bf16(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1,
                         uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes,
                         uint32_t box0, uint32_t box1, uint32_t box2);
-// The pool as a 3-D tensor whose box {64 dims, 1, rows} (NHD) / {64, rows, 1}
-// (HND) reads `rows` consecutive keys of one head of one page (page = block*2
-// + kv), 128-byte swizzled, in the same shared-memory layout either way:
+// The pool as a 3-D tensor whose box {128 bytes, 1, rows} (NHD) / {128 bytes,
+// rows, 1} (HND) -- 64 bf16 dims, or 128 e4m3 dims of an fp8 pool
+// (elem_bytes 1) -- reads `rows` consecutive keys of one head of one page
+// (page = block*2 + kv), 128-byte swizzled, in the same shared-memory layout
+// either way:
 //   NHD  (head_size, num_kv_heads, pages*block_size), coordinates
 //        (dim, head, page*block_size + offset);
 //   HND  (head_size, block_size, pages*num_kv_heads), coordinates
 //        (dim, offset, page*num_kv_heads + head).
 CUresult encode_kv_map(CUtensorMap *map, const void *cache, int32_t head_size,
                        int32_t num_kv_heads, int32_t block_size, int64_t num_blocks, int32_t hnd,
-                       uint32_t box_rows);
+                       uint32_t box_rows, int32_t elem_bytes = 2);
 
 }  // namespace pka

@@ -71,6 +71,71 @@ __global__ void __launch_bounds__(kKvwThreads)
     }
 }
 
+// The same scatter into an fp8 e4m3 pool: every element is stored as
+// e4m3(x / scale) (k_scale for K, v_scale for V; the quantisation of the
+// "FlashAttention y FlashInfer" page's fp8 KV cache, per-tensor scale).  A
+// lane moves one 16-element chunk: two 16-byte bf16 loads in, one 16-byte
+// store of codes out.  HBM traffic is 2 x (2 + 1) bytes per element.
+__global__ void __launch_bounds__(kKvwThreads)
+    reshape_and_cache_fp8_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
+                                 uint4 *__restrict__ cache, const int64_t *__restrict__ slots,
+                                 int32_t num_tokens, int32_t row_chunks, int32_t head_chunks,
+                                 int32_t num_kv_heads, int32_t block_size, int64_t num_blocks,
+                                 int32_t hnd, float k_scale, float v_scale)
+{
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kKvwThreads + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp >= num_tokens)
+        return;
+    const int64_t slot = slots[warp];
+    if (slot < 0)
+        return;
+    if (slot >= num_blocks * block_size) {
+        if (lane == 0)
+            flag_error(kErrSlotOutOfPool);
+        return;
+    }
+    const int64_t blk = slot / block_size;
+    const int64_t off = slot - blk * block_size;
+    auto dst = [&](int kv, int i) -> uint4 * {
+        if (!hnd)
+            return cache + ((blk * 2 + kv) * block_size + off) * row_chunks + i;
+        const int h = i / head_chunks;
+        return cache + (((blk * 2 + kv) * num_kv_heads + h) * block_size + off) * head_chunks +
+               (i - h * head_chunks);
+    };
+    const uint4 *ks = key + warp * row_chunks * 2;
+    const uint4 *vs = value + warp * row_chunks * 2;
+    for (int i = lane; i < row_chunks; i += 32) {
+        const uint4 k0 = __ldg(ks + 2 * i), k1 = __ldg(ks + 2 * i + 1);
+        const uint4 v0 = __ldg(vs + 2 * i), v1 = __ldg(vs + 2 * i + 1);
+        const uint2 kl = quantize8_e4m3(k0, k_scale), kh = quantize8_e4m3(k1, k_scale);
+        const uint2 vl = quantize8_e4m3(v0, v_scale), vh = quantize8_e4m3(v1, v_scale);
+        *dst(0, i) = make_uint4(kl.x, kl.y, kh.x, kh.y);
+        *dst(1, i) = make_uint4(vl.x, vl.y, vh.x, vh.y);
+    }
+}
+
+cudaError_t launch_reshape_and_cache_fp8(const void *key, const void *value, void *cache,
+                                         const int64_t *slots, int32_t num_tokens,
+                                         int32_t num_kv_heads, int32_t head_size,
+                                         int32_t block_size, int64_t num_blocks, int32_t hnd,
+                                         float k_scale, float v_scale, cudaStream_t st)
+{
+    if (num_tokens == 0)
+        return cudaSuccess;
+    const int32_t head_chunks = head_size / 16;
+    const int32_t row_chunks = num_kv_heads * head_chunks;
+    const int64_t threads = static_cast<int64_t>(num_tokens) * 32;
+    const unsigned grid = static_cast<unsigned>((threads + kKvwThreads - 1) / kKvwThreads);
+    count_launch();
+    reshape_and_cache_fp8_kernel<<<grid, kKvwThreads, 0, st>>>(
+        static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
+        static_cast<uint4 *>(cache), slots, num_tokens, row_chunks, head_chunks, num_kv_heads,
+        block_size, num_blocks, hnd, k_scale, v_scale);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *cache,
                                      const int64_t *slots, int32_t num_tokens,
                                      int32_t num_kv_heads, int32_t head_size,

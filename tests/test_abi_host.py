@@ -178,3 +178,37 @@ def test_fused_forward_arguments(lib):
     # the forward's own checks still apply (block size)
     assert fused(256, 256, 256, 256, 512, ctypes.byref(m), 1024, None, 2, 8, 2, 64, 24, 64,
                  0.125, 1, None, 0, None) == -1
+
+
+def test_fp8_pool_arguments(lib):
+    """kv_dtype is one of the two pool element types; an fp8 pool needs
+    positive finite scales and is served for decode-only batches without a
+    shared prefix at head_size 128 (UNSUPPORTED otherwise, before any work)."""
+    fp8 = dict(kv_dtype=pka.KV_FP8_E4M3, k_scale=0.5, v_scale=2.0)
+    assert pka._CMeta().kv_dtype == pka.KV_BF16  # a zero-initialised meta is bf16
+    assert _fwd(lib, _meta(kv_dtype=2)) == -1
+    assert lib.pka_workspace_size(ctypes.byref(_meta(kv_dtype=-1)), 2, 8, 2, 128, 16) == 0
+    for bad in (0.0, -1.0, float("inf"), float("nan")):
+        assert _fwd(lib, _meta(**{**fp8, "k_scale": bad}), D=128) == -1
+        assert _fwd(lib, _meta(**{**fp8, "v_scale": bad}), D=128) == -1
+    assert _fwd(lib, _meta(**fp8), D=64) == -2                        # head_size 64
+    assert _fwd(lib, _meta(num_decodes=1, max_query_len=4, **fp8), T=5, D=128) == -2  # prefill
+    assert _fwd(lib, _meta(common_prefix_len=16, **fp8), D=128) == -2  # cascade
+    assert lib.pka_workspace_size(ctypes.byref(_meta(**fp8)), 2, 8, 2, 64, 16) == 0
+    # a bf16 meta ignores the scales
+    assert lib.pka_workspace_size(ctypes.byref(_meta(k_scale=-1.0)), 2, 8, 2, 64, 16) > 0
+    # the fused entry refuses an unserved fp8 batch before writing anything
+    m = _meta(num_decodes=0, max_query_len=4, **fp8)
+    assert lib.pka_paged_attn_forward_fused(256, 256, 256, 256, 512, ctypes.byref(m), 1024, None,
+                                            5, 8, 2, 128, 16, 64, 0.125, 1, None, 0, None) == -2
+
+
+def test_fp8_cache_write_arguments(lib):
+    w = lib.pka_reshape_and_cache_fp8
+    assert w(16, 16, 16, 16, 1, 2, 128, 16, 4, 0, 0.0, 1.0, None) == -1   # scale
+    assert w(16, 16, 16, 16, 1, 2, 128, 16, 4, 0, 1.0, float("nan"), None) == -1
+    assert w(16, 16, 16, 16, 1, 2, 128, 16, 4, 5, 1.0, 1.0, None) == -1   # layout
+    assert w(16, 16, 16, 16, 1, 2, 128, 24, 4, 0, 1.0, 1.0, None) == -1   # block size
+    assert w(16, 16, 16, 16, 1, 2, 72, 16, 4, 0, 1.0, 1.0, None) == -2    # head_size % 16
+    assert w(None, 16, 16, 16, 1, 2, 128, 16, 4, 0, 1.0, 1.0, None) == -1  # null
+    assert w(16, 16, 16, 16, 0, 2, 128, 16, 4, 0, 1.0, 1.0, None) == 0     # nothing to do

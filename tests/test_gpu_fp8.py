@@ -1,0 +1,166 @@
+"""GPU parity of the fp8 (e4m3) KV pool (the "FlashAttention y FlashInfer"
+page, "Resumen en una frase" and "Limites y fallos": an fp8 e4m3 KV cache;
+one fp32 scale per tensor for K and for V).
+
+The starting pool is the generated bf16 pool quantised by the oracle (the
+prior context as earlier steps' writes would have left it; unused slots hold
+bf16 NaN, i.e. the e4m3 NaN code, which no admitted key may touch).  The cache
+write must match the oracle's codes byte for byte; attention rows are compared
+with the oracle's fp64 attention over the dequantised pool at the bf16 path's
+tolerances (the kernel computes on the exact code values, so quantisation
+adds no error between the two sides).
+"""
+import numpy as np
+import pytest
+
+from paged_kv_attention_33_gb300 import workloads as W
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+
+def fp8_pool(oracle, batch, k_scale, v_scale):
+    c = G.host_bits(batch.cache)
+    p8 = np.empty(c.shape, dtype=np.uint8)
+    p8[:, 0] = oracle.quantize_e4m3(np.ascontiguousarray(c[:, 0]), k_scale)
+    p8[:, 1] = oracle.quantize_e4m3(np.ascontiguousarray(c[:, 1]), v_scale)
+    return p8
+
+
+def run_fp8(batch, pool8, k_scale, v_scale, split_kv_tokens=0, fused=False, query=None):
+    """The fp8 write and forward through the C ABI; host copies of the logical
+    pool codes, the output bits and the lse."""
+    import torch
+
+    import paged_kv_attention_33_gb300 as pka
+
+    dev = G.device()
+    sp = batch.spec
+    q = G.to_dev(batch.query if query is None else query, dev)
+    k = G.to_dev(batch.key, dev)
+    v = G.to_dev(batch.value, dev)
+    cache = W.to_layout(torch.from_numpy(pool8).to(dev), sp.kv_layout)
+    slots = torch.from_numpy(batch.slot_mapping).to(dev)
+    meta = pka.Meta.from_host(batch.query_start_loc, batch.seq_lens, batch.block_table,
+                              sp.num_decodes, dev, split_kv_tokens=split_kv_tokens,
+                              kv_layout=sp.kv_layout, kv_dtype="fp8", k_scale=k_scale,
+                              v_scale=v_scale)
+    T = batch.num_tokens
+    out = torch.full((T, sp.num_heads, sp.head_size), float("nan"), dtype=torch.bfloat16,
+                     device=dev)
+    lse = torch.full((T, sp.num_heads), float("nan"), dtype=torch.float32, device=dev)
+    if fused:
+        pka.paged_attn_forward_fused(q, k, v, slots, cache, meta, out, lse,
+                                     scale=sp.softmax_scale)
+    else:
+        pka.reshape_and_cache_fp8(k, v, cache, slots, k_scale, v_scale, kv_layout=sp.kv_layout)
+        pka.paged_attn_forward(q, cache, meta, out, lse, scale=sp.softmax_scale)
+    pka.check_status()
+    return (W.from_layout(cache, sp.kv_layout).cpu().numpy(), W.to_host_bits(out),
+            lse.cpu().numpy())
+
+
+def check_fp8(oracle, batch, k_scale, v_scale, split_kv_tokens=0, fused=False, label="",
+              query=None, lse_rel=0.0):
+    pool = fp8_pool(oracle, batch, k_scale, v_scale)
+    want = pool.copy()
+    oracle.reshape_and_cache_fp8(batch.key, batch.value, want, batch.slot_mapping, k_scale,
+                                 v_scale)
+    got_pool, out, lse = run_fp8(batch, pool, k_scale, v_scale, split_kv_tokens, fused, query)
+    assert np.array_equal(want, got_pool), f"{label}: fp8 cache write differs"
+    sp = batch.spec
+    qh = batch.query if query is None else query
+    o_ref, l_ref = oracle.paged_attention_fp8(qh, want, k_scale, v_scale, batch.query_start_loc,
+                                              batch.seq_lens, batch.block_table,
+                                              sp.softmax_scale, threads=8)
+    rows = np.arange(batch.num_tokens * sp.num_heads, dtype=np.int64)
+    res = G.compare(out, None, o_ref, l_ref, rows, sp.num_heads)
+    G.assert_close(res, label)
+    t, h = rows // sp.num_heads, rows % sp.num_heads
+    le = np.abs(lse[t, h].astype(np.float64) - l_ref)
+    tol = G.LSE_ABS + lse_rel * np.abs(l_ref)
+    assert np.all(np.isfinite(lse[t, h])) and np.all(le <= tol), \
+        f"{label}: lse error {le.max()}"
+    return out, lse, got_pool
+
+
+def _decode_spec(name, H, Hkv, bs, ctx, layout="NHD"):
+    return W.BatchSpec(name, H, Hkv, 128, bs, decode_ctx=ctx, kv_layout=layout)
+
+
+@pytest.mark.parametrize("Hkv,g", [(8, 1), (8, 4), (4, 8), (2, 8), (1, 8), (1, 5)])
+def test_fp8_decode_heads(oracle, Hkv, g):
+    ctx = [0, 1, 14, 15, 16, 17, 100, 255, 256, 1000, 2047, 3001]
+    sp = _decode_spec(f"fp8_{Hkv}_{g}", Hkv * g, Hkv, 16, ctx)
+    b = W.make_batch(sp, seed=8000 + 10 * Hkv + g)
+    check_fp8(oracle, b, 0.0625, 0.03125, label=f"Hkv={Hkv} g={g}")
+    check_fp8(oracle, b, 0.0371, 0.0173, split_kv_tokens=48,
+              label=f"Hkv={Hkv} g={g} split 48, non-power-of-two scales")
+
+
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+@pytest.mark.parametrize("bs", [16, 64, 256, 1024])
+def test_fp8_decode_layouts_and_pages(oracle, layout, bs):
+    ctx = [3, 200, 511, 1023, 1500, 4000]
+    sp = _decode_spec(f"fp8_{layout}_{bs}", 32, 8, bs, ctx, layout)
+    b = W.make_batch(sp, seed=8100 + bs)
+    check_fp8(oracle, b, 0.05, 0.02, label=f"{layout} bs={bs}")
+    check_fp8(oracle, b, 0.05, 0.02, split_kv_tokens=64, label=f"{layout} bs={bs} split 64")
+
+
+def test_fp8_saturating_scale(oracle):
+    """A scale small enough that many |x|/scale exceed 448: those codes clamp
+    to +-448 in both the write and the oracle."""
+    sp = _decode_spec("fp8_sat", 16, 4, 16, [40, 300])
+    b = W.make_batch(sp, seed=8200)
+    check_fp8(oracle, b, 1.0 / 256, 1.0 / 300, label="saturating")
+
+
+@pytest.mark.parametrize("shift", [-24, -12, 12, 18])
+def test_fp8_query_far_from_f16_range(oracle, shift):
+    """The kernel takes Q to f16 with a power-of-two prescale per head; queries
+    scaled by 2^shift (past f16's largest value at +18, into its subnormals at
+    -24) must give the oracle's rows.  At large scores the lse is compared
+    relative to its magnitude (fp32 resolves ~1e-7 of it)."""
+    sp = _decode_spec(f"fp8_q{shift}", 32, 8, 16, [5, 77, 1000])
+    b = W.make_batch(sp, seed=8300 + shift)
+    q = W.f32_to_bf16_bits(W.bf16_bits_to_f32(b.query) * np.float32(2.0 ** shift))
+    check_fp8(oracle, b, 0.0625, 0.0625, query=q, label=f"q x 2^{shift}", lse_rel=1e-6)
+
+
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+def test_fp8_fused_write_matches_two_calls(oracle, layout):
+    """pka_paged_attn_forward_fused on an fp8 pool: the decode launch quantises
+    each new row into its staged tile and its slot; pool bytes equal to the
+    oracle's, rows equal to the oracle's, and bit-identical to the two calls."""
+    sp = _decode_spec(f"fp8_fused_{layout}", 32, 8, 16, [0, 15, 16, 31, 500, 2000], layout)
+    b = W.make_batch(sp, seed=8400)
+    o1, l1, p1 = check_fp8(oracle, b, 0.04, 0.03, fused=True, label=f"fused {layout}")
+    o2, l2, p2 = check_fp8(oracle, b, 0.04, 0.03, fused=False, label=f"two-call {layout}")
+    assert np.array_equal(p1, p2)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_fp8_unserved_batches_are_refused(oracle):
+    import torch
+
+    import paged_kv_attention_33_gb300 as pka
+
+    sp = W.BatchSpec("fp8_mixed", 16, 4, 128, 16, decode_ctx=[10], prefill=[(20, 5)])
+    b = W.make_batch(sp, seed=8500)
+    dev = G.device()
+    pool = torch.from_numpy(fp8_pool(oracle, b, 0.1, 0.1)).to(dev)
+    meta = pka.Meta.from_host(b.query_start_loc, b.seq_lens, b.block_table, sp.num_decodes,
+                              dev, kv_dtype="fp8", k_scale=0.1, v_scale=0.1)
+    q = G.to_dev(b.query, dev)
+    with pytest.raises(pka.PkaError) as e:
+        pka.paged_attn_forward(q, pool, meta, torch.empty_like(q))
+    assert e.value.status == -2
+    before = pool.clone()
+    with pytest.raises(pka.PkaError) as e:
+        pka.paged_attn_forward_fused(q, G.to_dev(b.key, dev), G.to_dev(b.value, dev),
+                                     torch.from_numpy(b.slot_mapping).to(dev), pool, meta,
+                                     torch.empty_like(q))
+    assert e.value.status == -2
+    torch.cuda.synchronize()
+    assert torch.equal(before, pool)  # nothing was written
