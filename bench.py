@@ -17,6 +17,8 @@ Prints ONE JSON line (rank 0).  Flags:
   --workload NAME                 another named workload (for profiling runs)
   --no-cpu-baseline               skip the oracle timing (profiling runs)
   --two-call                      write the cache with its own launch (reshape_and_cache)
+  --no-fp8                        skip the fp8 e4m3 pool decode sub-measurement
+  --profile [--kv-dtype fp8]      short run for a profiler (optionally over an fp8 pool)
 """
 from __future__ import annotations
 
@@ -303,6 +305,8 @@ def run_ours(args):
     st = Step(args.workload, dev, args.max_decodes)
     spec = st.spec
     if args.profile:
+        if args.kv_dtype == "fp8":
+            to_fp8_pool(st)
         return run_profile(args, st)
     kv_bytes, pf_flops = units(spec)
     stream = torch.cuda.current_stream()
@@ -435,6 +439,12 @@ def run_ours(args):
     }
     if pf_flops:
         line["prefill_tflops"] = pf_flops / (ms * 1e-3) / 1e12
+    if args.workload == "decode_heavy" and not args.no_fp8:
+        # the fp8 e4m3 pool: half the bytes of the same batch
+        del st
+        torch.cuda.empty_cache()
+        line["fp8_decode"] = measure_fp8_decode(args, dev, peaks, peaks_kind)
+        st = None
     if args.workload != "prefill" and not args.no_prefill:
         # the metric's second half: prefill TFLOP/s on the varlen prefill workload
         # (8 prompts, 1024..8192 tokens), timed in the same run
@@ -456,6 +466,75 @@ def run_ours(args):
 
         dist.destroy_process_group()
     return 0
+
+
+def to_fp8_pool(st):
+    """Replace the step's bf16 pool by its e4m3 quantisation (every slot written
+    by the library's reshape_and_cache_fp8; per-tensor scales 4/448, i.e. |x| up
+    to 4 sigma of the N(0, 1) rows is representable) and switch its metadata to
+    the fp8 pool."""
+    import torch
+
+    pka, sp, b = st.pka, st.spec, st.batch
+    k_scale = v_scale = 4.0 / 448
+    pool8 = torch.zeros((b.cache.shape[0], 2, sp.block_size, sp.num_kv_heads, sp.head_size),
+                        dtype=torch.uint8, device=b.cache.device)
+    rows_k = b.cache[:, 0].reshape(-1, sp.num_kv_heads, sp.head_size).contiguous()
+    rows_v = b.cache[:, 1].reshape(-1, sp.num_kv_heads, sp.head_size).contiguous()
+    every_slot = torch.arange(rows_k.shape[0], dtype=torch.int64, device=b.cache.device)
+    pka.reshape_and_cache_fp8(rows_k, rows_v, pool8, every_slot, k_scale, v_scale)
+    del rows_k, rows_v, every_slot
+    b.cache = pool8
+    st.meta.kv_dtype, st.meta.k_scale, st.meta.v_scale = pka.KV_FP8_E4M3, k_scale, v_scale
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def measure_fp8_decode(args, dev, peaks, peaks_kind):
+    """The headline decode batch over an fp8 e4m3 pool (one byte per element,
+    per-tensor scales): the same fused step (the new rows quantised into the
+    pool inside the decode launch), its step and kernel time and the fp8 KV
+    bytes per second against the copy roofline.  The pool is the bf16 pool's
+    context quantised by the library's own reshape_and_cache_fp8 (setup, not
+    timed)."""
+    import torch
+
+    import paged_kv_attention_33_gb300 as pka
+
+    st = Step("decode_heavy", dev, args.max_decodes)
+    to_fp8_pool(st)
+    kv_bytes = A.decode_kv_bytes(st.spec, 0, elem_bytes=1)
+    for _ in range(max(3, args.warmup)):
+        st.run()
+    torch.cuda.synchronize()
+    steps = max(5, min(args.steps, 200))
+    k0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    k1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for e in k0 + k1:
+        e.record()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        pka.set_kernel_events(pka.KERNEL_DECODE, k0[i], k1[i])
+        st.run()
+    pka.set_kernel_events(pka.KERNEL_DECODE, None, None)
+    e1.record()
+    torch.cuda.synchronize()
+    pka.check_status()
+    ms, k_ms = max_over_ranks([e0.elapsed_time(e1) / steps,
+                               sum(a.elapsed_time(c) for a, c in zip(k0, k1)) / steps], dev)
+    peak = float(peaks["hbm_gbs"])
+    achieved = kv_bytes / (k_ms * 1e-3) / 1e9
+    return {"workload": "decode_heavy", "kv_dtype": "fp8_e4m3", "steps": steps,
+            "kv_bytes_per_step": kv_bytes, "ms_per_step": ms,
+            "GBps": kv_bytes / (ms * 1e-3) / 1e9,
+            "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel (fp8)",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "kernel_ms": k_ms,
+                         "peak_source": f"{peaks_kind} copy bandwidth (hbm_gbs)",
+                         "traffic": None}}
 
 
 def measure_prefill(args, dev, peaks, peaks_kind):
@@ -517,7 +596,9 @@ def run_profile(args, st):
     st.pka.check_status()
     ms = e0.elapsed_time(e1) / args.steps
     kv_bytes, flops = units(st.spec)
-    print(json.dumps({"profile_run": True, "workload": args.workload,
+    if args.kv_dtype == "fp8":
+        kv_bytes //= 2
+    print(json.dumps({"profile_run": True, "workload": args.workload, "kv_dtype": args.kv_dtype,
                       "num_decodes": st.spec.num_decodes, "ms_per_step": ms,
                       "kv_bytes_per_step": kv_bytes, "prefill_flops_per_step": flops,
                       "GBps_step": kv_bytes / (ms * 1e-3) / 1e9,
@@ -535,6 +616,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the prefill sub-measurement")
+    ap.add_argument("--no-fp8", action="store_true",
+                    help="skip the fp8-pool decode sub-measurement")
+    ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
+                    help="pool element type of --profile runs (fp8: decode workloads)")
     ap.add_argument("--profile", action="store_true",
                     help="short run for a profiler: W + K steps only")
     ap.add_argument("--max-decodes", type=int, default=None,

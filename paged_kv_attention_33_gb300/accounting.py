@@ -18,8 +18,9 @@ from .workloads import BatchSpec
 BF16 = 2
 
 
-def decode_kv_bytes(spec: BatchSpec, kv_begin: int = 0) -> int:
-    row = spec.num_kv_heads * spec.head_size * 2 * BF16
+def decode_kv_bytes(spec: BatchSpec, kv_begin: int = 0, elem_bytes: int = BF16) -> int:
+    """K and V bytes the decodes read (elem_bytes 1 for an fp8 e4m3 pool)."""
+    row = spec.num_kv_heads * spec.head_size * 2 * elem_bytes
     return sum(max(0, L - kv_begin) for L in spec.seq_lens[: spec.num_decodes]) * row
 
 

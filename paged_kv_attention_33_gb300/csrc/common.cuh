@@ -209,6 +209,33 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D (16x8 fp32) += A (16x32 e4m3, row) * B (32x8 e4m3, col).  A register i
+// holds 4 consecutive k of row (lane>>2) (+8 for registers 1, 3), k offset
+// 4*(lane&3) (+16 for registers 2, 3); B registers 0 / 1 hold k 4*(lane&3)+0..3
+// (+16) of column lane>>2; the lowest byte is the lowest k.
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two 16x16 byte matrices, transposed: lanes 0-15 give the 16-byte rows of
+// matrix 0, lanes 16-31 those of matrix 1; lane l receives, of matrix m,
+// rows 4*(l&3)..+3 of column l>>2 (register 2m) and of column 8 + (l>>2)
+// (register 2m+1), the lowest byte from the lowest row.
+__device__ __forceinline__ void ldsm_x2_trans_b8(uint32_t addr, uint32_t &r0, uint32_t &r1,
+                                                 uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m16n16.x2.trans.shared.b8 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
 // Transpose of an 8x8 b16 matrix held one packed pair per thread.
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x)
 {
@@ -246,6 +273,24 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
     const __half2_raw h =
         __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes), __NV_E4M3);
     return uint32_t(h.x) | (uint32_t(h.y) << 16);
+}
+
+// e4m3 codes of (lo, hi), rounded to nearest even and clamped to +-448, lo in
+// the low byte of the 16-bit result.
+__device__ __forceinline__ uint32_t e4m3x2_rn(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// The two values of a pair of e4m3 codes (low byte -> lo), as floats.
+__device__ __forceinline__ void e4m3x2_values(uint32_t two_codes, float &lo, float &hi)
+{
+    const uint32_t h = e4m3x2_to_f16x2(two_codes);
+    const __half2 v = *reinterpret_cast<const __half2 *>(&h);
+    lo = __low2float(v);
+    hi = __high2float(v);
 }
 
 // Eight bf16 (one 16-byte vector, element 0 in the low half of .x) divided by

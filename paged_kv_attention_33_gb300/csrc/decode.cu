@@ -97,13 +97,16 @@ constexpr int kMaxDecodeChunk = 4096;
 constexpr float kNegInf = -INFINITY;
 constexpr float kLn2 = 0.69314718055994530942f;
 
-// kFp8: the pool holds e4m3 codes (one byte per element); the ring then
-// keeps twice the stages so that as many bytes are in flight.
+// kFp8: the pool holds e4m3 codes (one byte per element) and a unit is 32
+// keys (the k extent of an fp8 mma), loaded as two 16-row boxes, so that a
+// stage moves as many bytes as a bf16 one.
 template <int D, bool kFp8 = false>
 struct DecodeCfg {
+    static constexpr int kUnitKeys = kFp8 ? 32 : 16;               // keys of one unit
     static constexpr int kRowBytes = D * (kFp8 ? 1 : 2);           // one key of one head
     static constexpr int kHalves = kRowBytes / 128;                // 128-byte TMA boxes per row
-    static constexpr int kUnitBytes = 16 * kRowBytes;              // 16 keys
+    static constexpr int kBoxes = kHalves * kUnitKeys / 16;        // 2 KB boxes per unit
+    static constexpr int kUnitBytes = kUnitKeys * kRowBytes;
     static constexpr int kKvBytes = kConsumerWarps * kUnitBytes;   // all units of K (or V)
     static constexpr int kStageBytes = 2 * kKvBytes;
     static constexpr int kStages = kStageBytes >= 65536 ? 3 : 6;
@@ -193,13 +196,11 @@ __device__ __forceinline__ float warp_sum32(float v)
 // (kQB x kHB log2-sum-exps and rows) is issued before any is used, so a merge
 // costs about one L2 round trip per round -- it runs at the end of a CTA's
 // range, while the other SMs still stream, where each round trip is long.
-template <int D>
+template <int D, int kQB = 2, int kHB = 4>  // kQB: parts per round, kHB: heads per batch
 __device__ __forceinline__ void merge_pieces(const DecodeParams &p, int t, int s, int bf,
                                              int nparts, int R, int warp, int lane)
 {
     constexpr int kPer = D / 32;  // dims per lane
-    constexpr int kHB = 4;        // heads per batch
-    constexpr int kQB = 2;        // parts per round
     using Vec = typename std::conditional<kPer == 4, float4, float2>::type;
     const int H = p.num_heads;
     const int ntot = nparts + (p.cascade ? p.pre_splits : 0);
@@ -393,11 +394,20 @@ __device__ __forceinline__ void write_pool_row(const DecodeParams &p, int64_t tk
     }
 }
 
-template <int D, bool kHnd, bool kFp8>
+// kG (fp8 pool): the query-head group rounded up to 2, 4 or 8; each head
+// then owns 8/kG columns of the S mma, one Q term per column.
+template <int D, bool kHnd, bool kFp8, int kG = 8>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p)
 {
     static_assert(!kFp8 || D == 128, "the fp8 tile addressing assumes 128-byte rows");
+    static_assert(kG == 2 || kG == 4 || kG == 8, "padded group");
+    // e4m3 terms of the split Q: four (q to 2^-16) where a head has spare
+    // columns; three (q to 2^-12) at kG = 8, where a fourth would not fit in
+    // registers
+    constexpr int kTerms = kG == 8 ? 3 : 4;
+    constexpr int kTpm = 8 / kG;                       // terms per mma (columns per head)
+    constexpr int kNmma = (kTerms + kTpm - 1) / kTpm;  // S mmas per 32 dims: 1, 2 or 4
     using Cfg = DecodeCfg<D, kFp8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -410,7 +420,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
     const int Hkv = p.num_kv_heads;
     const int R = kConsumerWarps / Hkv;
-    const int stage_keys = 16 * R;
+    const int stage_keys = Cfg::kUnitKeys * R;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int nseq = p.nseq;
@@ -485,34 +495,41 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
-        // lane = one (unit, K|V, 128-byte half) box of every stage; its block id is
-        // looked up for the next stage before waiting for a free slot
+        // lane = one 2 KB box (16 keys x 128 bytes) of every stage: (unit, K|V,
+        // box), box = the 128-byte half of a bf16 row, or the 16-key half of an
+        // fp8 unit; its block id is looked up for the next stage before waiting
+        // for a free slot
         if (lane == 0)
             tma_prefetch_desc(&kv_map);
         const uint64_t policy = l2_policy_evict_first();
-        constexpr int kOps = kConsumerWarps * 2 * Cfg::kHalves;  // <= 32
+        constexpr int kOps = kConsumerWarps * 2 * Cfg::kBoxes;  // <= 32
+        static_assert(kOps <= 32, "one box per lane");
         const int u = lane % kConsumerWarps;
         const int kv = (lane / kConsumerWarps) & 1;
-        const int half = lane / (2 * kConsumerWarps);
+        const int box = lane / (2 * kConsumerWarps);
+        const int half = kFp8 ? 0 : box;          // 128-byte half of the row
+        const int key_off = kFp8 ? 16 * box : 0;  // first key of the box in the unit
         const int r = u / Hkv;
         const int k = u % Hkv;
         int s = s_first;
-        // TMA coordinates of the unit's 16 keys in the pool map: NHD (head,
+        // TMA coordinates of the box's 16 keys in the pool map: NHD (head,
         // page*bs + offset), HND (offset, page*Hkv + head), page = block*2 + (K|V);
-        // row = -1: no keys
-        auto lookup = [&](int64_t x, int seq, int &row, int &c1, int &slices) {
+        // row = -1: no keys (a box whose first key is past the end is not loaded,
+        // its block-table entry is not valid); live16 = loaded 16-key blocks of
+        // each kv head, the same for all lanes
+        auto lookup = [&](int64_t x, int seq, int &row, int &c1, int &live16) {
             // the table entry is read before the length is known (the row of
             // the table is in bounds), so that both loads are in flight at once
             const int k0 = p.kv_begin + int(x - prefix[seq]) * stage_keys;
-            const int ks = k0 + 16 * r;
+            const int ks = k0 + Cfg::kUnitKeys * r + key_off;
             const int col = ks / p.block_size;
             const int32_t *bt = p.block_table + int64_t(p.seq0 + seq) * p.bt_stride;
             const int blk_raw = lane < kOps && col < p.bt_stride ? bt[col] : -1;
             const int L = p.seq_lens[p.seq0 + seq];
-            slices = max(0, min(R, (L - k0 + 15) / 16));
+            live16 = max(0, min(R * Cfg::kUnitKeys / 16, (L - k0 + 15) / 16));
             row = -1;
             c1 = kHnd ? ks % p.block_size : k;
-            if (lane < kOps && r < slices) {
+            if (lane < kOps && ks < L) {
                 int blk = blk_raw;
                 if (blk < 0 || blk >= p.num_blocks) {
                     flag_error(kErrBlockOutOfPool);
@@ -522,22 +539,23 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                            : (blk * 2 + kv) * p.block_size + (ks % p.block_size);
             }
         };
-        int row_next, c1_next, slices_next;
-        lookup(lo, s, row_next, c1_next, slices_next);
+        int row_next, c1_next, live_next;
+        lookup(lo, s, row_next, c1_next, live_next);
         for (int64_t x = lo; x < hi; ++x) {
             const int i = int(x - lo);
-            const int row = row_next, c1 = c1_next, slices = slices_next;
+            const int row = row_next, c1 = c1_next, live16 = live_next;
             const int slot = i % Cfg::kStages;
             const int round = i / Cfg::kStages;
             if (round > 0 && !dec_wait(&empty[slot], (round - 1) & 1, abort_flag))
                 break;
-            if (lane == 0)
+            if (lane == 0)  // boxes of 2 KB: live 16-key blocks x heads x K|V (x halves)
                 mbar_arrive_expect_tx(&full[slot],
-                                      static_cast<uint32_t>(slices * Hkv * 2 * Cfg::kUnitBytes));
+                                      static_cast<uint32_t>(live16 * (kFp8 ? 1 : Cfg::kHalves) *
+                                                            Hkv * 2 * 2048));
             __syncwarp();
             if (row >= 0) {
                 uint8_t *dst = smem + slot * Cfg::kStageBytes + kv * Cfg::kKvBytes +
-                               u * Cfg::kUnitBytes + half * 2048;
+                               u * Cfg::kUnitBytes + box * 2048;
                 tma_load_3d(dst, &kv_map, &full[slot], half * (128 / (kFp8 ? 1 : 2)), c1, row,
                             policy);
             }
@@ -545,7 +563,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             if (x + 1 < hi) {
                 while (prefix[s + 1] <= x + 1)
                     ++s;
-                lookup(x + 1, s, row_next, c1_next, slices_next);
+                lookup(x + 1, s, row_next, c1_next, live_next);
             }
         }
         return;
@@ -566,7 +584,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const uint32_t v_row = (lane & 7) + (lane >> 4) * 8;  // V: transposed A
     const uint32_t v_chunk = (lane >> 3) & 1;
 
-    uint32_t qf[D / 16][2];
+    // Q^T as B fragments: bf16 pairs (bf16 pool), or (fp8 pool) this lane's
+    // column of each S mma (one e4m3 term of the split Q), 4 k-steps of 32
+    // dims (qf[mma*4 + step])
+    uint32_t qf[kFp8 ? 4 * kNmma : D / 16][2];
     float o[D / 16][4];
     float m0, m1, l0, l1;
     // log2-domain multipliers of the raw scores of heads n0 = 2tq and n1 = 2tq+1
@@ -594,21 +615,26 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const uint32_t *qrow =
             p.query + ((static_cast<int64_t>(t) * H + k * g + (live ? gq : 0)) * D) / 2;
         if constexpr (kFp8) {
-            // f16 fragments (the K tile is dequantised to f16), each head
-            // prescaled by the power of two 2^(14-e) that puts its largest |q|
-            // (in [2^e, 2^(e+1))) into [2^14, 2^15): bf16 has a wider range
-            // than f16, and normal bf16 values are exact in f16.  Step
-            // kk = 4*hh + m takes rows (2tq, 2tq+1 | 2tq+8, 2tq+9) from dims
-            // 64*hh + 16*tq + 4*m + (0, 1 | 2, 3): the dims one 16-byte read
-            // of a K row gives this thread (below).
-            const uint4 *qv = reinterpret_cast<const uint4 *>(qrow);
-            uint4 raw[D / 64][2];
+            // Q, prescaled per head by the power of two 2^(7-E) that puts its
+            // largest |q| (in [2^E, 2^(E+1))) into [128, 256), is split into
+            // kTerms e4m3 terms, q' = t1 + ... to 2^-(4 kTerms) of |q'| (each term
+            // rounds the remainder of the ones before, which fp32 holds
+            // exactly), so that K . q' runs as fp8 products on the unconverted
+            // codes.  Column n of an S mma is head n % kG, term slot n / kG:
+            // mma m carries term m*kTpm + slot.  Step 2*hh + j takes k =
+            // 4tq..4tq+3 from dims 64hh + 16tq + 8j + 0..3 and k = 16+4tq.. from
+            // dims +4..7: the bytes one 16-byte read of a K row gives a lane.
+            const int hq = gq % kG, slot = gq / kG;
+            const bool hlive = hq < g;
+            const uint4 *qv = reinterpret_cast<const uint4 *>(
+                p.query + ((static_cast<int64_t>(t) * H + k * g + (hlive ? hq : 0)) * D) / 2);
+            uint4 raw[2][2];
             float amax = 0.f;
 #pragma unroll
-            for (int hh = 0; hh < D / 64; ++hh)
+            for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
-                    raw[hh][j] = live ? __ldg(qv + (64 * hh + 16 * tq) / 8 + j) : make_uint4(0, 0, 0, 0);
+                    raw[hh][j] = hlive ? __ldg(qv + (64 * hh + 16 * tq) / 8 + j) : make_uint4(0, 0, 0, 0);
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
                         const uint32_t x = u4_word(raw[hh][j], w);
@@ -618,24 +644,46 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 }
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-            const int e =
-                amax > 0.f ? max(int((__float_as_uint(amax) >> 23) & 0xffu) - 127, -112) : 0;
-            const float pre = __uint_as_float(uint32_t(127 + 14 - e) << 23);
-            const float mul = p.scale_log2 * p.k_scale * __uint_as_float(uint32_t(127 - 14 + e) << 23);
+            const int e = amax > 0.f
+                              ? min(max(int((__float_as_uint(amax) >> 23) & 0xffu) - 127, -119), 127)
+                              : 0;
+            const float pre = __uint_as_float(uint32_t(127 + 7 - e) << 23);
+            const float mul = p.scale_log2 * p.k_scale * __uint_as_float(uint32_t(127 - 7 + e) << 23);
 #pragma unroll
-            for (int hh = 0; hh < D / 64; ++hh)
+            for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const uint32_t w0 = u4_word(raw[hh][m >> 1], 2 * (m & 1));
-                    const uint32_t w1 = u4_word(raw[hh][m >> 1], 2 * (m & 1) + 1);
-                    qf[4 * hh + m][0] = pack_f16x2(__uint_as_float(w0 << 16) * pre,
-                                                   __uint_as_float(w0 & 0xffff0000u) * pre);
-                    qf[4 * hh + m][1] = pack_f16x2(__uint_as_float(w1 << 16) * pre,
-                                                   __uint_as_float(w1 & 0xffff0000u) * pre);
-                }
-            // head n is prescaled in the lanes with gq = n (lane 4n)
-            mul0 = __shfl_sync(0xffffffffu, mul, 8 * tq);
-            mul1 = __shfl_sync(0xffffffffu, mul, 8 * tq + 4);
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int bi = 0; bi < 2; ++bi) {  // b0: dims +0..3, b1: dims +4..7
+                        uint32_t code[kTerms] = {};
+#pragma unroll
+                        for (int pr = 0; pr < 2; ++pr) {  // dim pairs (0, 1), (2, 3)
+                            const uint32_t x = u4_word(raw[hh][j], 2 * bi + pr);
+                            float r0 = __uint_as_float(x << 16) * pre;
+                            float r1 = __uint_as_float(x & 0xffff0000u) * pre;
+#pragma unroll
+                            for (int term = 0; term < kTerms; ++term) {
+                                const uint32_t c2 = e4m3x2_rn(r0, r1);
+                                code[term] |= c2 << (16 * pr);
+                                float v0, v1;
+                                e4m3x2_values(c2, v0, v1);
+                                r0 -= v0;  // exact: v0 is r0 rounded to 4 bits
+                                r1 -= v1;
+                            }
+                        }
+#pragma unroll
+                        for (int m = 0; m < kNmma; ++m) {
+                            uint32_t cm = code[0];
+#pragma unroll
+                            for (int term = 1; term < kTerms; ++term)
+                                cm = (m * kTpm + slot == term) ? code[term] : cm;
+                            qf[m * 4 + 2 * hh + j][bi] = m * kTpm + slot < kTerms ? cm : 0u;
+                        }
+                    }
+            // the heads of this lane's accumulator columns 2tq, 2tq+1 are
+            // prescaled in lanes 4 * head
+            mul0 = __shfl_sync(0xffffffffu, mul, 4 * ((2 * tq) % kG));
+            mul1 = __shfl_sync(0xffffffffu, mul, 4 * ((2 * tq + 1) % kG));
         } else {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
@@ -656,13 +704,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const int slot = i % Cfg::kStages;
         if (ok && !dec_wait(&full[slot], (i / Cfg::kStages) & 1, abort_flag))
             ok = false;
-        const int ks = p.kv_begin + int(x - prefix[s]) * stage_keys + 16 * r;
-        const int valid = min(16, L - ks);
+        const int ks = p.kv_begin + int(x - prefix[s]) * stage_keys + Cfg::kUnitKeys * r;
+        const int valid = min(Cfg::kUnitKeys, L - ks);
         if (ok && valid > 0) {
             const uint32_t kbase =
                 smem_addr(smem + slot * Cfg::kStageBytes + u * Cfg::kUnitBytes);
             const uint32_t vbase = kbase + Cfg::kKvBytes;
-            if (p.fuse_write && L - 1 < ks + 16) {
+            if (p.fuse_write && L - 1 < ks + Cfg::kUnitKeys) {
                 // this stage holds the decode's new key (key L-1): the pool may
                 // not have it yet, so it is taken from the step's K/V rows into
                 // the staged tile, and written to the pool at the token's slot
@@ -696,29 +744,129 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                     flag_error(kErrSlotOutOfPool);
                 }
             }
-            // S^T = K Q^T; row gq of S^T is key kp of the tile, row gq+8 key kp+8
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
-            int kp;
             if constexpr (kFp8) {
-                // rows gq (and gq+8) read key (gq>>1) + 4*(gq&1): the two rows of
-                // a quarter-warp then differ in swizzle bit 2 and their 16-byte
-                // reads fall in different banks.  One read = 16 dims of a key:
-                // dims 64*hh + 16*tq + 4*m + (0, 1 | 2, 3) for step 4*hh + m.
-                kp = (gq >> 1) + 4 * (gq & 1);
+                // ---- S^T = K Q^T over the unit's 32 keys, two 16-key row tiles,
+                // on the e4m3 codes: kNmma fp8 products per 32 dims, whose
+                // columns n and n + kG (and n + 2kG, ...) hold the same head's
+                // other Q terms and are summed across lanes (xor 2, xor 1).
+                // Row gq (gq+8) of tile t2 is key 16*t2 + ka (+2),
+                // ka = 8*(gq>>2) + 4*(gq&1) + ((gq>>1)&1): the two rows of a
+                // quarter-warp differ in swizzle bit 2 (conflict-free 16-byte
+                // reads) and the V rows gathered below are conflict free too.
+                const int ka = 8 * (gq >> 2) + 4 * (gq & 1) + ((gq >> 1) & 1);
+                float sc[2][4];
 #pragma unroll
-                for (int hh = 0; hh < D / 64; ++hh) {
-                    const uint4 kr0 = lds128(kbase + swz128(kp, 4 * hh + tq));
-                    const uint4 kr1 = lds128(kbase + swz128(kp + 8, 4 * hh + tq));
+                for (int t2 = 0; t2 < 2; ++t2) {
+                    float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const uint32_t w0 = u4_word(kr0, m), w1 = u4_word(kr1, m);
-                        mma_f16_16816(c, e4m3x2_to_f16x2(w0 & 0xffffu), e4m3x2_to_f16x2(w1 & 0xffffu),
-                                      e4m3x2_to_f16x2(w0 >> 16), e4m3x2_to_f16x2(w1 >> 16),
-                                      qf[4 * hh + m][0], qf[4 * hh + m][1]);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const uint4 kr0 = lds128(kbase + swz128(16 * t2 + ka, 4 * hh + tq));
+                        const uint4 kr1 = lds128(kbase + swz128(16 * t2 + ka + 2, 4 * hh + tq));
+#pragma unroll
+                        for (int j = 0; j < 2; ++j)
+#pragma unroll
+                            for (int m = 0; m < kNmma; ++m)
+                                mma_e4m3_16832(c, u4_word(kr0, 2 * j), u4_word(kr1, 2 * j),
+                                               u4_word(kr0, 2 * j + 1), u4_word(kr1, 2 * j + 1),
+                                               qf[m * 4 + 2 * hh + j][0], qf[m * 4 + 2 * hh + j][1]);
                     }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        if constexpr (kG <= 4)
+                            c[i] += __shfl_xor_sync(0xffffffffu, c[i], 2);
+                        if constexpr (kG <= 2)
+                            c[i] += __shfl_xor_sync(0xffffffffu, c[i], 1);
+                    }
+                    const bool va = 16 * t2 + ka < valid, vb = 16 * t2 + ka + 2 < valid;
+                    sc[t2][0] = va ? c[0] * mul0 : kNegInf;
+                    sc[t2][1] = va ? c[1] * mul1 : kNegInf;
+                    sc[t2][2] = vb ? c[2] * mul0 : kNegInf;
+                    sc[t2][3] = vb ? c[3] * mul1 : kNegInf;
                 }
+                const float mn0 = fmaxf(
+                    m0, warp_max_heads(fmax3(fmaxf(sc[0][0], sc[0][2]), sc[1][0], sc[1][2])));
+                const float mn1 = fmaxf(
+                    m1, warp_max_heads(fmax3(fmaxf(sc[0][1], sc[0][3]), sc[1][1], sc[1][3])));
+                const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+                float pv[2][4];
+#pragma unroll
+                for (int t2 = 0; t2 < 2; ++t2)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        pv[t2][i] = fast_exp2(sc[t2][i] - ((i & 1) ? mn1 : mn0));
+                l0 = l0 * al0 + ((pv[0][0] + pv[0][2]) + (pv[1][0] + pv[1][2]));
+                l1 = l1 * al1 + ((pv[0][1] + pv[0][3]) + (pv[1][1] + pv[1][3]));
+                m0 = mn0;
+                m1 = mn1;
+                // ---- P^T as e4m3 B fragments: 256*p (exact) split into hi = its
+                // value rounded to 4 significant bits (Veltkamp's split with the
+                // factor 2^20 + 1, exact in e4m3) and lo = the remainder rounded
+                // to e4m3, so hi + lo is p to ~2^-8, as a bf16 P would be.  One
+                // 16-bit element per (key, head) = (hi, lo) codes; movmatrix
+                // turns rows (keys) into columns: the lane then holds keys 2tq,
+                // 2tq+1 (and +8) of head gq, and byte permutes gather the hi and
+                // the lo bytes of keys (2tq, 2tq+1, 2tq+8, 2tq+9) of a tile: k =
+                // 4tq..4tq+3 of its 16.
+                uint32_t bh[2], bl[2];
+#pragma unroll
+                for (int t2 = 0; t2 < 2; ++t2) {
+                    uint32_t e[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float x = pv[t2][i] * 256.f;
+                        const float t = __fmul_rn(x, 1048577.f);
+                        const float h = __fsub_rn(t, __fsub_rn(t, x));
+                        e[i] = e4m3x2_rn(h, __fsub_rn(x, h));
+                    }
+                    const uint32_t X = movmatrix_trans(e[0] | (e[1] << 16));  // rows gq
+                    const uint32_t Y = movmatrix_trans(e[2] | (e[3] << 16));  // rows gq + 8
+                    bh[t2] = prmt(X, Y, 0x6420u);
+                    bl[t2] = prmt(X, Y, 0x7531u);
+                }
+                // ---- O^T += V^T P^T, 16 dims per step: ldmatrix row j (k index
+                // j of the B fragment) is key vkey(j) of the tile, the key whose
+                // P sits at k = j above; lanes 16-31 give the rows of keys 16-31.
+                const int jl = lane & 15, tj = jl >> 2, ij = jl & 3;
+                const int vrow = 16 * (lane >> 4) + 8 * (tj >> 1) + 4 * (ij & 1) +
+                                 2 * (ij >> 1) + (tj & 1);
+                auto pv_pass = [&](auto masked) {
+                    // keys past the end may hold anything (e4m3 NaN codes too):
+                    // zero their bytes; this lane's k = 4tq..4tq+3 (+16)
+                    uint32_t mk01 = 0xffffffffu, mk23 = 0xffffffffu;
+                    if constexpr (decltype(masked)::value) {
+                        mk01 = mk23 = 0u;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int kk = 8 * (tq >> 1) + 4 * (i & 1) + 2 * (i >> 1) + (tq & 1);
+                            mk01 |= kk < valid ? 0xffu << (8 * i) : 0u;
+                            mk23 |= kk + 16 < valid ? 0xffu << (8 * i) : 0u;
+                        }
+                    }
+#pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x2_trans_b8(vbase + swz128(vrow, mt), a0, a1, a2, a3);
+                        if constexpr (decltype(masked)::value) {
+                            a0 &= mk01;
+                            a1 &= mk01;
+                            a2 &= mk23;
+                            a3 &= mk23;
+                        }
+                        o[mt][0] *= al0;
+                        o[mt][1] *= al1;
+                        o[mt][2] *= al0;
+                        o[mt][3] *= al1;
+                        mma_e4m3_16832(o[mt], a0, a1, a2, a3, bh[0], bh[1]);
+                        mma_e4m3_16832(o[mt], a0, a1, a2, a3, bl[0], bl[1]);
+                    }
+                };
+                if (valid < 32)
+                    pv_pass(std::true_type{});
+                else
+                    pv_pass(std::false_type{});
             } else {
-                kp = gq;
+                // S^T = K Q^T
+                float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t ch = 2 * kk + k_chunk;
@@ -726,64 +874,23 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                     ldsm_x4(kbase + (ch >> 3) * 2048 + swz128(k_row, ch & 7), a0, a1, a2, a3);
                     mma_bf16_16816(c, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
                 }
-            }
-            const bool va = kp < valid, vb = kp + 8 < valid;
-            const float s0 = va ? c[0] * mul0 : kNegInf;
-            const float s1 = va ? c[1] * mul1 : kNegInf;
-            const float s2 = vb ? c[2] * mul0 : kNegInf;
-            const float s3 = vb ? c[3] * mul1 : kNegInf;
-            const float mn0 = fmaxf(m0, warp_max_heads(fmaxf(s0, s2)));
-            const float mn1 = fmaxf(m1, warp_max_heads(fmaxf(s1, s3)));
-            const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
-            const float p0 = fast_exp2(s0 - mn0), p1 = fast_exp2(s1 - mn1);
-            const float p2 = fast_exp2(s2 - mn0), p3 = fast_exp2(s3 - mn1);
-            l0 = l0 * al0 + (p0 + p2);
-            l1 = l1 * al1 + (p1 + p3);
-            m0 = mn0;
-            m1 = mn1;
-            // P^T as B fragments: rows 0-7 and 8-15 of S^T
-            const uint32_t b0 = movmatrix_trans(kFp8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1));
-            const uint32_t b1 = movmatrix_trans(kFp8 ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3));
-            if constexpr (kFp8) {
-                // V^T fragments: columns 2tq, 2tq+1, 2tq+8, 2tq+9 are S^T rows,
-                // i.e. keys tq, tq+4, tq+8, tq+12; row gq of step mt is dim
-                // 16*gq + 2*mt and row gq+8 dim 16*gq + 2*mt + 1, so one 16-byte
-                // read per key covers all steps.  Odd-gq lanes read their two
-                // keys in the other order (conflict-free quarter-warps) and the
-                // byte permute undoes it.  Keys past the end of the sequence
-                // may hold anything (an e4m3 NaN too): zero them.
-                const bool odd = gq & 1;
-                const uint32_t r0 = odd ? tq + 4 : tq, r1 = odd ? tq : tq + 4;
-                const uint4 x0 = lds128(vbase + swz128(r0, gq)), y0 = lds128(vbase + swz128(r1, gq));
-                const uint4 x1 = lds128(vbase + swz128(r0 + 8, gq));
-                const uint4 y1 = lds128(vbase + swz128(r1 + 8, gq));
-                // bytes (key tq, key tq+4) of dims 4w, 4w+1 | 4w+2, 4w+3
-                const uint32_t sel_a = odd ? 0x1504u : 0x5140u, sel_b = odd ? 0x3726u : 0x7362u;
-                const uint32_t mlo = (tq < valid ? 0x0000ffffu : 0u) |
-                                     (tq + 4 < valid ? 0xffff0000u : 0u);
-                const uint32_t mhi = (tq + 8 < valid ? 0x0000ffffu : 0u) |
-                                     (tq + 12 < valid ? 0xffff0000u : 0u);
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const uint32_t lo0 = prmt(u4_word(x0, w), u4_word(y0, w), sel_a);
-                    const uint32_t hi0 = prmt(u4_word(x0, w), u4_word(y0, w), sel_b);
-                    const uint32_t lo1 = prmt(u4_word(x1, w), u4_word(y1, w), sel_a);
-                    const uint32_t hi1 = prmt(u4_word(x1, w), u4_word(y1, w), sel_b);
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const int mt = 2 * w + j;
-                        const uint32_t q0 = j ? hi0 : lo0, q1 = j ? hi1 : lo1;
-                        o[mt][0] *= al0;
-                        o[mt][1] *= al1;
-                        o[mt][2] *= al0;
-                        o[mt][3] *= al1;
-                        mma_f16_16816(o[mt], e4m3x2_to_f16x2(q0 & 0xffffu) & mlo,
-                                      e4m3x2_to_f16x2(q0 >> 16) & mlo,
-                                      e4m3x2_to_f16x2(q1 & 0xffffu) & mhi,
-                                      e4m3x2_to_f16x2(q1 >> 16) & mhi, b0, b1);
-                    }
-                }
-            } else {
+                const bool va = gq < valid, vb = gq + 8 < valid;
+                const float s0 = va ? c[0] * mul0 : kNegInf;
+                const float s1 = va ? c[1] * mul1 : kNegInf;
+                const float s2 = vb ? c[2] * mul0 : kNegInf;
+                const float s3 = vb ? c[3] * mul1 : kNegInf;
+                const float mn0 = fmaxf(m0, warp_max_heads(fmaxf(s0, s2)));
+                const float mn1 = fmaxf(m1, warp_max_heads(fmaxf(s1, s3)));
+                const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+                const float p0 = fast_exp2(s0 - mn0), p1 = fast_exp2(s1 - mn1);
+                const float p2 = fast_exp2(s2 - mn0), p3 = fast_exp2(s3 - mn1);
+                l0 = l0 * al0 + (p0 + p2);
+                l1 = l1 * al1 + (p1 + p3);
+                m0 = mn0;
+                m1 = mn1;
+                // P^T as B fragments: rows 0-7 and 8-15 of S^T
+                const uint32_t b0 = movmatrix_trans(pack_bf16x2(p0, p1));
+                const uint32_t b1 = movmatrix_trans(pack_bf16x2(p2, p3));
                 // rows of V past the end of the sequence may hold anything: zero them
                 const uint32_t mlo = (2 * tq < valid ? 0x0000ffffu : 0u) |
                                      (2 * tq + 1 < valid ? 0xffff0000u : 0u);
@@ -820,7 +927,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const bool direct = np == 1 && R == 1;
         const int n0 = 2 * tq, n1 = 2 * tq + 1;  // the two heads of this thread
         // row scales of the output (an fp8 pool's V dequantisation folded in)
-        const float vsc = kFp8 ? p.v_scale : 1.f;
+        const float vsc = kFp8 ? p.v_scale * (1.f / 256.f) : 1.f;  // P was scaled by 256
         const float i0 = lr0 > 0.f ? vsc / lr0 : 0.f;
         const float i1 = lr1 > 0.f ? vsc / lr1 : 0.f;
         if (direct) {
@@ -833,27 +940,17 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                                                k * g + min(n1, g - 1), gq, o, sc0, sc1, ls0, ls1);
                 }
 #pragma unroll
-                for (int mt = 0; mt < D / 16; ++mt) {
-                    __nv_bfloat16 *d0 = p.out + (int64_t(t) * H + k * g + n0) * D;
-                    __nv_bfloat16 *d1 = p.out + (int64_t(t) * H + k * g + n1) * D;
-                    if constexpr (kFp8) {  // dims 16*gq + 2*mt and +1: one pair
-                        const int d = 16 * gq + 2 * mt;
-                        if (n0 < g)
-                            *reinterpret_cast<__nv_bfloat162 *>(d0 + d) =
-                                __floats2bfloat162_rn(o[mt][0] * sc0, o[mt][2] * sc0);
-                        if (n1 < g)
-                            *reinterpret_cast<__nv_bfloat162 *>(d1 + d) =
-                                __floats2bfloat162_rn(o[mt][1] * sc1, o[mt][3] * sc1);
-                    } else {  // dims 16*mt + gq and +8
-                        const int d = 16 * mt + gq;
-                        if (n0 < g) {
-                            d0[d] = __float2bfloat16_rn(o[mt][0] * sc0);
-                            d0[d + 8] = __float2bfloat16_rn(o[mt][2] * sc0);
-                        }
-                        if (n1 < g) {
-                            d1[d] = __float2bfloat16_rn(o[mt][1] * sc1);
-                            d1[d + 8] = __float2bfloat16_rn(o[mt][3] * sc1);
-                        }
+                for (int mt = 0; mt < D / 16; ++mt) {  // dims 16*mt + gq and +8
+                    const int d = 16 * mt + gq;
+                    if (n0 < g) {
+                        __nv_bfloat16 *dst = p.out + (int64_t(t) * H + k * g + n0) * D;
+                        dst[d] = __float2bfloat16_rn(o[mt][0] * sc0);
+                        dst[d + 8] = __float2bfloat16_rn(o[mt][2] * sc0);
+                    }
+                    if (n1 < g) {
+                        __nv_bfloat16 *dst = p.out + (int64_t(t) * H + k * g + n1) * D;
+                        dst[d] = __float2bfloat16_rn(o[mt][1] * sc1);
+                        dst[d + 8] = __float2bfloat16_rn(o[mt][3] * sc1);
                     }
                 }
                 if (gq == 0 && p.lse) {
@@ -869,26 +966,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             if (ok) {
 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt) {
-                    float *d0 = p.o_part + (prow + n0) * D;
-                    float *d1 = p.o_part + (prow + n1) * D;
-                    if constexpr (kFp8) {
-                        const int d = 16 * gq + 2 * mt;
-                        if (n0 < g)
-                            *reinterpret_cast<float2 *>(d0 + d) =
-                                make_float2(o[mt][0] * i0, o[mt][2] * i0);
-                        if (n1 < g)
-                            *reinterpret_cast<float2 *>(d1 + d) =
-                                make_float2(o[mt][1] * i1, o[mt][3] * i1);
-                    } else {
-                        const int d = 16 * mt + gq;
-                        if (n0 < g) {
-                            d0[d] = o[mt][0] * i0;
-                            d0[d + 8] = o[mt][2] * i0;
-                        }
-                        if (n1 < g) {
-                            d1[d] = o[mt][1] * i1;
-                            d1[d + 8] = o[mt][3] * i1;
-                        }
+                    const int d = 16 * mt + gq;
+                    if (n0 < g) {
+                        float *dst = p.o_part + (prow + n0) * D;
+                        dst[d] = o[mt][0] * i0;
+                        dst[d + 8] = o[mt][2] * i0;
+                    }
+                    if (n1 < g) {
+                        float *dst = p.o_part + (prow + n1) * D;
+                        dst[d] = o[mt][1] * i1;
+                        dst[d + 8] = o[mt][3] * i1;
                     }
                 }
                 if (gq == 0) {
@@ -908,7 +995,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 // per head (warp-shuffle max/sum of the parts' log2-sum-exp,
                 // then the weighted sum of their rows, lanes along head_size)
                 __threadfence();
-                merge_pieces<D>(p, t, s, bf, np * R, R, warp, lane);
+                // (the fp8 stage loop leaves fewer registers: one part per
+                // round, two heads per batch)
+                merge_pieces<D, kFp8 ? 1 : 2, kFp8 ? 2 : 4>(p, t, s, bf, np * R, R, warp, lane);
             }
         }
         if (x + 1 < hi) {
@@ -998,7 +1087,7 @@ DecodePlan plan_decode(int32_t split_kv_tokens, int32_t num_decodes, int32_t num
     return dp;
 }
 
-template <int D, bool kHnd, bool kFp8>
+template <int D, bool kHnd, bool kFp8, int kG = 8>
 static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Workspace &ws,
                                    char *wsp, const CUtensorMap &kv_map, int32_t kv_begin,
                                    bool cascade)
@@ -1008,7 +1097,7 @@ static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Wor
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D, kHnd, kFp8>,
+        cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D, kHnd, kFp8, kG>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(Cfg::kSmemBytes));
         if (e != cudaSuccess)
@@ -1056,7 +1145,7 @@ static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Wor
         if (e != cudaSuccess)
             return e;
         count_launch();
-        paged_decode_kernel<D, kHnd, kFp8>
+        paged_decode_kernel<D, kHnd, kFp8, kG>
             <<<dp.grid, kDecodeThreads, Cfg::kSmemBytes, f.stream>>>(kv_map, p);
         e = cudaGetLastError();
         if (e != cudaSuccess)
@@ -1073,9 +1162,15 @@ cudaError_t launch_decode(const Fwd &f, const DecodePlan &dp, const Workspace &w
     if (f.kv_fp8) {  // head_size 128 only (checked by the caller)
         if (f.head_size != 128 || cascade)
             return cudaErrorInvalidValue;
-        return f.kv_hnd
-                   ? launch_decode_d<128, true, true>(f, dp, ws, wsp, kv_map, kv_begin, cascade)
-                   : launch_decode_d<128, false, true>(f, dp, ws, wsp, kv_map, kv_begin, cascade);
+        const int g = f.num_heads / f.num_kv_heads;
+        if (g <= 2)
+            return f.kv_hnd ? launch_decode_d<128, true, true, 2>(f, dp, ws, wsp, kv_map, kv_begin, cascade)
+                            : launch_decode_d<128, false, true, 2>(f, dp, ws, wsp, kv_map, kv_begin, cascade);
+        if (g <= 4)
+            return f.kv_hnd ? launch_decode_d<128, true, true, 4>(f, dp, ws, wsp, kv_map, kv_begin, cascade)
+                            : launch_decode_d<128, false, true, 4>(f, dp, ws, wsp, kv_map, kv_begin, cascade);
+        return f.kv_hnd ? launch_decode_d<128, true, true, 8>(f, dp, ws, wsp, kv_map, kv_begin, cascade)
+                        : launch_decode_d<128, false, true, 8>(f, dp, ws, wsp, kv_map, kv_begin, cascade);
     }
     if (f.head_size == 128)
         return f.kv_hnd
