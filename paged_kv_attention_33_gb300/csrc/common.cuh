@@ -209,21 +209,6 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// D (16x8 fp32) += A (16x32 e4m3, row) * B (32x8 e4m3, col).  A register i
-// holds 4 consecutive k of row (lane>>2) (+8 for registers 1, 3), k offset
-// 4*(lane&3) (+16 for registers 2, 3); B registers 0 / 1 hold k 4*(lane&3)+0..3
-// (+16) of column lane>>2; the lowest byte is the lowest k.
-__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1,
-                                               uint32_t a2, uint32_t a3, uint32_t b0,
-                                               uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, "
-        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 // Two 16x16 byte matrices, transposed: lanes 0-15 give the 16-byte rows of
 // matrix 0, lanes 16-31 those of matrix 1; lane l receives, of matrix m,
 // rows 4*(l&3)..+3 of column l>>2 (register 2m) and of column 8 + (l>>2)
@@ -257,40 +242,16 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
 }
 
 // ---------------------------------------------------------------- fp8 e4m3
-// Bytes of (a, b) picked by the selector's four nibbles (byte i of the result
-// = byte nibble_i of the 8-byte value b:a).
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+// Four e4m3 codes (bytes 0..3 of w) as two f16 pairs: lo = (byte 0, byte 1),
+// hi = (byte 2, byte 3), the lower byte in the lower half; exact.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint32_t &hi)
 {
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
-}
-
-// Two e4m3 codes (low byte -> low half) as two f16: exact, every e4m3 value
-// is an f16 normal number.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
-{
-    const __half2_raw h =
-        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes), __NV_E4M3);
-    return uint32_t(h.x) | (uint32_t(h.y) << 16);
-}
-
-// e4m3 codes of (lo, hi), rounded to nearest even and clamped to +-448, lo in
-// the low byte of the 16-bit result.
-__device__ __forceinline__ uint32_t e4m3x2_rn(float lo, float hi)
-{
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-// The two values of a pair of e4m3 codes (low byte -> lo), as floats.
-__device__ __forceinline__ void e4m3x2_values(uint32_t two_codes, float &lo, float &hi)
-{
-    const uint32_t h = e4m3x2_to_f16x2(two_codes);
-    const __half2 v = *reinterpret_cast<const __half2 *>(&h);
-    lo = __low2float(v);
-    hi = __high2float(v);
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
 }
 
 // Eight bf16 (one 16-byte vector, element 0 in the low half of .x) divided by

@@ -394,20 +394,11 @@ __device__ __forceinline__ void write_pool_row(const DecodeParams &p, int64_t tk
     }
 }
 
-// kG (fp8 pool): the query-head group rounded up to 2, 4 or 8; each head
-// then owns 8/kG columns of the S mma, one Q term per column.
-template <int D, bool kHnd, bool kFp8, int kG = 8>
+template <int D, bool kHnd, bool kFp8>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p)
 {
     static_assert(!kFp8 || D == 128, "the fp8 tile addressing assumes 128-byte rows");
-    static_assert(kG == 2 || kG == 4 || kG == 8, "padded group");
-    // e4m3 terms of the split Q: four (q to 2^-16) where a head has spare
-    // columns; three (q to 2^-12) at kG = 8, where a fourth would not fit in
-    // registers
-    constexpr int kTerms = kG == 8 ? 3 : 4;
-    constexpr int kTpm = 8 / kG;                       // terms per mma (columns per head)
-    constexpr int kNmma = (kTerms + kTpm - 1) / kTpm;  // S mmas per 32 dims: 1, 2 or 4
     using Cfg = DecodeCfg<D, kFp8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -584,10 +575,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const uint32_t v_row = (lane & 7) + (lane >> 4) * 8;  // V: transposed A
     const uint32_t v_chunk = (lane >> 3) & 1;
 
-    // Q^T as B fragments: bf16 pairs (bf16 pool), or (fp8 pool) this lane's
-    // column of each S mma (one e4m3 term of the split Q), 4 k-steps of 32
-    // dims (qf[mma*4 + step])
-    uint32_t qf[kFp8 ? 4 * kNmma : D / 16][2];
+    // Q^T as B fragments: bf16 pairs, or (fp8 pool) prescaled f16 pairs
+    uint32_t qf[D / 16][2];
     float o[D / 16][4];
     float m0, m1, l0, l1;
     // log2-domain multipliers of the raw scores of heads n0 = 2tq and n1 = 2tq+1
@@ -615,26 +604,21 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const uint32_t *qrow =
             p.query + ((static_cast<int64_t>(t) * H + k * g + (live ? gq : 0)) * D) / 2;
         if constexpr (kFp8) {
-            // Q, prescaled per head by the power of two 2^(7-E) that puts its
-            // largest |q| (in [2^E, 2^(E+1))) into [128, 256), is split into
-            // kTerms e4m3 terms, q' = t1 + ... to 2^-(4 kTerms) of |q'| (each term
-            // rounds the remainder of the ones before, which fp32 holds
-            // exactly), so that K . q' runs as fp8 products on the unconverted
-            // codes.  Column n of an S mma is head n % kG, term slot n / kG:
-            // mma m carries term m*kTpm + slot.  Step 2*hh + j takes k =
-            // 4tq..4tq+3 from dims 64hh + 16tq + 8j + 0..3 and k = 16+4tq.. from
-            // dims +4..7: the bytes one 16-byte read of a K row gives a lane.
-            const int hq = gq % kG, slot = gq / kG;
-            const bool hlive = hq < g;
-            const uint4 *qv = reinterpret_cast<const uint4 *>(
-                p.query + ((static_cast<int64_t>(t) * H + k * g + (hlive ? hq : 0)) * D) / 2);
-            uint4 raw[2][2];
+            // f16 fragments (the K and V codes are converted to f16, exactly),
+            // each head prescaled by the power of two 2^(14-E) that puts its
+            // largest |q| (in [2^E, 2^(E+1))) into [2^14, 2^15): bf16 has a
+            // wider range than f16, and normal bf16 values are exact in f16.
+            // Step kk = 4*hh + m takes rows (2tq, 2tq+1 | 2tq+8, 2tq+9) from
+            // dims 64*hh + 16*tq + 4*m + (0, 1 | 2, 3): the dims one 16-byte
+            // read of a K row gives this lane (below).
+            const uint4 *qv = reinterpret_cast<const uint4 *>(qrow);
+            uint4 raw[D / 64][2];
             float amax = 0.f;
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
+            for (int hh = 0; hh < D / 64; ++hh)
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
-                    raw[hh][j] = hlive ? __ldg(qv + (64 * hh + 16 * tq) / 8 + j) : make_uint4(0, 0, 0, 0);
+                    raw[hh][j] = live ? __ldg(qv + (64 * hh + 16 * tq) / 8 + j) : make_uint4(0, 0, 0, 0);
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
                         const uint32_t x = u4_word(raw[hh][j], w);
@@ -644,46 +628,24 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 }
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-            const int e = amax > 0.f
-                              ? min(max(int((__float_as_uint(amax) >> 23) & 0xffu) - 127, -119), 127)
-                              : 0;
-            const float pre = __uint_as_float(uint32_t(127 + 7 - e) << 23);
-            const float mul = p.scale_log2 * p.k_scale * __uint_as_float(uint32_t(127 - 7 + e) << 23);
+            const int e =
+                amax > 0.f ? max(int((__float_as_uint(amax) >> 23) & 0xffu) - 127, -112) : 0;
+            const float pre = __uint_as_float(uint32_t(127 + 14 - e) << 23);
+            const float mul = p.scale_log2 * p.k_scale * __uint_as_float(uint32_t(127 - 14 + e) << 23);
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
+            for (int hh = 0; hh < D / 64; ++hh)
 #pragma unroll
-                for (int j = 0; j < 2; ++j)
-#pragma unroll
-                    for (int bi = 0; bi < 2; ++bi) {  // b0: dims +0..3, b1: dims +4..7
-                        uint32_t code[kTerms] = {};
-#pragma unroll
-                        for (int pr = 0; pr < 2; ++pr) {  // dim pairs (0, 1), (2, 3)
-                            const uint32_t x = u4_word(raw[hh][j], 2 * bi + pr);
-                            float r0 = __uint_as_float(x << 16) * pre;
-                            float r1 = __uint_as_float(x & 0xffff0000u) * pre;
-#pragma unroll
-                            for (int term = 0; term < kTerms; ++term) {
-                                const uint32_t c2 = e4m3x2_rn(r0, r1);
-                                code[term] |= c2 << (16 * pr);
-                                float v0, v1;
-                                e4m3x2_values(c2, v0, v1);
-                                r0 -= v0;  // exact: v0 is r0 rounded to 4 bits
-                                r1 -= v1;
-                            }
-                        }
-#pragma unroll
-                        for (int m = 0; m < kNmma; ++m) {
-                            uint32_t cm = code[0];
-#pragma unroll
-                            for (int term = 1; term < kTerms; ++term)
-                                cm = (m * kTpm + slot == term) ? code[term] : cm;
-                            qf[m * 4 + 2 * hh + j][bi] = m * kTpm + slot < kTerms ? cm : 0u;
-                        }
-                    }
-            // the heads of this lane's accumulator columns 2tq, 2tq+1 are
-            // prescaled in lanes 4 * head
-            mul0 = __shfl_sync(0xffffffffu, mul, 4 * ((2 * tq) % kG));
-            mul1 = __shfl_sync(0xffffffffu, mul, 4 * ((2 * tq + 1) % kG));
+                for (int m = 0; m < 4; ++m) {
+                    const uint32_t w0 = u4_word(raw[hh][m >> 1], 2 * (m & 1));
+                    const uint32_t w1 = u4_word(raw[hh][m >> 1], 2 * (m & 1) + 1);
+                    qf[4 * hh + m][0] = pack_f16x2(__uint_as_float(w0 << 16) * pre,
+                                                   __uint_as_float(w0 & 0xffff0000u) * pre);
+                    qf[4 * hh + m][1] = pack_f16x2(__uint_as_float(w1 << 16) * pre,
+                                                   __uint_as_float(w1 & 0xffff0000u) * pre);
+                }
+            // head n is prescaled in the lanes with gq = n (lane 4n)
+            mul0 = __shfl_sync(0xffffffffu, mul, 8 * tq);
+            mul1 = __shfl_sync(0xffffffffu, mul, 8 * tq + 4);
         } else {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
@@ -745,13 +707,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 }
             }
             if constexpr (kFp8) {
-                // ---- S^T = K Q^T over the unit's 32 keys, two 16-key row tiles,
-                // on the e4m3 codes: kNmma fp8 products per 32 dims, whose
-                // columns n and n + kG (and n + 2kG, ...) hold the same head's
-                // other Q terms and are summed across lanes (xor 2, xor 1).
-                // Row gq (gq+8) of tile t2 is key 16*t2 + ka (+2),
-                // ka = 8*(gq>>2) + 4*(gq&1) + ((gq>>1)&1): the two rows of a
-                // quarter-warp differ in swizzle bit 2 (conflict-free 16-byte
+                // ---- S^T = K Q^T over the unit's 32 keys, two 16-key row tiles.
+                // Each K code is converted to f16 once (exact) and meets the f16
+                // Q in mma m16n8k16.  Row gq (gq+8) of tile t2 is key 16*t2 + ka
+                // (+2), ka = 8*(gq>>2) + 4*(gq&1) + ((gq>>1)&1): the two rows of
+                // a quarter-warp differ in swizzle bit 2 (conflict-free 16-byte
                 // reads) and the V rows gathered below are conflict free too.
                 const int ka = 8 * (gq >> 2) + 4 * (gq & 1) + ((gq >> 1) & 1);
                 float sc[2][4];
@@ -759,23 +719,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 for (int t2 = 0; t2 < 2; ++t2) {
                     float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
+                    for (int hh = 0; hh < D / 64; ++hh) {
                         const uint4 kr0 = lds128(kbase + swz128(16 * t2 + ka, 4 * hh + tq));
                         const uint4 kr1 = lds128(kbase + swz128(16 * t2 + ka + 2, 4 * hh + tq));
 #pragma unroll
-                        for (int j = 0; j < 2; ++j)
-#pragma unroll
-                            for (int m = 0; m < kNmma; ++m)
-                                mma_e4m3_16832(c, u4_word(kr0, 2 * j), u4_word(kr1, 2 * j),
-                                               u4_word(kr0, 2 * j + 1), u4_word(kr1, 2 * j + 1),
-                                               qf[m * 4 + 2 * hh + j][0], qf[m * 4 + 2 * hh + j][1]);
-                    }
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        if constexpr (kG <= 4)
-                            c[i] += __shfl_xor_sync(0xffffffffu, c[i], 2);
-                        if constexpr (kG <= 2)
-                            c[i] += __shfl_xor_sync(0xffffffffu, c[i], 1);
+                        for (int m = 0; m < 4; ++m) {
+                            uint32_t a0, a1, a2, a3;
+                            e4m3x4_to_f16x2x2(u4_word(kr0, m), a0, a2);
+                            e4m3x4_to_f16x2x2(u4_word(kr1, m), a1, a3);
+                            mma_f16_16816(c, a0, a1, a2, a3, qf[4 * hh + m][0], qf[4 * hh + m][1]);
+                        }
                     }
                     const bool va = 16 * t2 + ka < valid, vb = 16 * t2 + ka + 2 < valid;
                     sc[t2][0] = va ? c[0] * mul0 : kNegInf;
@@ -798,66 +751,58 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 l1 = l1 * al1 + ((pv[0][1] + pv[0][3]) + (pv[1][1] + pv[1][3]));
                 m0 = mn0;
                 m1 = mn1;
-                // ---- P^T as e4m3 B fragments: 256*p (exact) split into hi = its
-                // value rounded to 4 significant bits (Veltkamp's split with the
-                // factor 2^20 + 1, exact in e4m3) and lo = the remainder rounded
-                // to e4m3, so hi + lo is p to ~2^-8, as a bf16 P would be.  One
-                // 16-bit element per (key, head) = (hi, lo) codes; movmatrix
-                // turns rows (keys) into columns: the lane then holds keys 2tq,
-                // 2tq+1 (and +8) of head gq, and byte permutes gather the hi and
-                // the lo bytes of keys (2tq, 2tq+1, 2tq+8, 2tq+9) of a tile: k =
-                // 4tq..4tq+3 of its 16.
-                uint32_t bh[2], bl[2];
+                // ---- P^T as f16 B fragments: movmatrix turns S^T rows (keys)
+                // into columns, so the lane holds keys (2tq, 2tq+1) and (2tq+8,
+                // 2tq+9) of tile t2 for head gq: k = (2tq, 2tq+1 | 2tq+8, 2tq+9)
+                // of a 16-key mma, in the order the V rows are gathered below.
+                uint32_t b0[2], b1[2];
 #pragma unroll
                 for (int t2 = 0; t2 < 2; ++t2) {
-                    uint32_t e[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float x = pv[t2][i] * 256.f;
-                        const float t = __fmul_rn(x, 1048577.f);
-                        const float h = __fsub_rn(t, __fsub_rn(t, x));
-                        e[i] = e4m3x2_rn(h, __fsub_rn(x, h));
-                    }
-                    const uint32_t X = movmatrix_trans(e[0] | (e[1] << 16));  // rows gq
-                    const uint32_t Y = movmatrix_trans(e[2] | (e[3] << 16));  // rows gq + 8
-                    bh[t2] = prmt(X, Y, 0x6420u);
-                    bl[t2] = prmt(X, Y, 0x7531u);
+                    b0[t2] = movmatrix_trans(pack_f16x2(pv[t2][0], pv[t2][1]));
+                    b1[t2] = movmatrix_trans(pack_f16x2(pv[t2][2], pv[t2][3]));
                 }
-                // ---- O^T += V^T P^T, 16 dims per step: ldmatrix row j (k index
-                // j of the B fragment) is key vkey(j) of the tile, the key whose
-                // P sits at k = j above; lanes 16-31 give the rows of keys 16-31.
+                // ---- O^T += V^T P^T, 16 dims per step: ldmatrix row j is key
+                // vkey(j) of the tile (rows 4tq..4tq+3 of a register = S^T rows
+                // 2tq, 2tq+1, 2tq+8, 2tq+9); lanes 16-31 give the rows of keys
+                // 16-31.  Each register's four codes become the (2tq, 2tq+1)
+                // and (2tq+8, 2tq+9) f16 pairs of one dim.
                 const int jl = lane & 15, tj = jl >> 2, ij = jl & 3;
                 const int vrow = 16 * (lane >> 4) + 8 * (tj >> 1) + 4 * (ij & 1) +
                                  2 * (ij >> 1) + (tj & 1);
                 auto pv_pass = [&](auto masked) {
                     // keys past the end may hold anything (e4m3 NaN codes too):
-                    // zero their bytes; this lane's k = 4tq..4tq+3 (+16)
-                    uint32_t mk01 = 0xffffffffu, mk23 = 0xffffffffu;
+                    // zero their bytes; this lane's bytes are keys vkey(4tq + i)
+                    uint32_t mk0 = 0xffffffffu, mk1 = 0xffffffffu;
                     if constexpr (decltype(masked)::value) {
-                        mk01 = mk23 = 0u;
+                        mk0 = mk1 = 0u;
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const int kk = 8 * (tq >> 1) + 4 * (i & 1) + 2 * (i >> 1) + (tq & 1);
-                            mk01 |= kk < valid ? 0xffu << (8 * i) : 0u;
-                            mk23 |= kk + 16 < valid ? 0xffu << (8 * i) : 0u;
+                            mk0 |= kk < valid ? 0xffu << (8 * i) : 0u;
+                            mk1 |= kk + 16 < valid ? 0xffu << (8 * i) : 0u;
                         }
                     }
 #pragma unroll
                     for (int mt = 0; mt < D / 16; ++mt) {
-                        uint32_t a0, a1, a2, a3;
-                        ldsm_x2_trans_b8(vbase + swz128(vrow, mt), a0, a1, a2, a3);
+                        uint32_t v[4];  // [tile 0: dim gq, dim gq+8, tile 1: dim gq, dim gq+8]
+                        ldsm_x2_trans_b8(vbase + swz128(vrow, mt), v[0], v[1], v[2], v[3]);
                         if constexpr (decltype(masked)::value) {
-                            a0 &= mk01;
-                            a1 &= mk01;
-                            a2 &= mk23;
-                            a3 &= mk23;
+                            v[0] &= mk0;
+                            v[1] &= mk0;
+                            v[2] &= mk1;
+                            v[3] &= mk1;
                         }
                         o[mt][0] *= al0;
                         o[mt][1] *= al1;
                         o[mt][2] *= al0;
                         o[mt][3] *= al1;
-                        mma_e4m3_16832(o[mt], a0, a1, a2, a3, bh[0], bh[1]);
-                        mma_e4m3_16832(o[mt], a0, a1, a2, a3, bl[0], bl[1]);
+#pragma unroll
+                        for (int t2 = 0; t2 < 2; ++t2) {
+                            uint32_t a0, a1, a2, a3;
+                            e4m3x4_to_f16x2x2(v[2 * t2], a0, a2);
+                            e4m3x4_to_f16x2x2(v[2 * t2 + 1], a1, a3);
+                            mma_f16_16816(o[mt], a0, a1, a2, a3, b0[t2], b1[t2]);
+                        }
                     }
                 };
                 if (valid < 32)
@@ -927,7 +872,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const bool direct = np == 1 && R == 1;
         const int n0 = 2 * tq, n1 = 2 * tq + 1;  // the two heads of this thread
         // row scales of the output (an fp8 pool's V dequantisation folded in)
-        const float vsc = kFp8 ? p.v_scale * (1.f / 256.f) : 1.f;  // P was scaled by 256
+        const float vsc = kFp8 ? p.v_scale : 1.f;
         const float i0 = lr0 > 0.f ? vsc / lr0 : 0.f;
         const float i1 = lr1 > 0.f ? vsc / lr1 : 0.f;
         if (direct) {
@@ -1087,7 +1032,7 @@ DecodePlan plan_decode(int32_t split_kv_tokens, int32_t num_decodes, int32_t num
     return dp;
 }
 
-template <int D, bool kHnd, bool kFp8, int kG = 8>
+template <int D, bool kHnd, bool kFp8>
 static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Workspace &ws,
                                    char *wsp, const CUtensorMap &kv_map, int32_t kv_begin,
                                    bool cascade)
@@ -1097,7 +1042,7 @@ static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Wor
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D, kHnd, kFp8, kG>,
+        cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D, kHnd, kFp8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(Cfg::kSmemBytes));
         if (e != cudaSuccess)
@@ -1145,7 +1090,7 @@ static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Wor
         if (e != cudaSuccess)
             return e;
         count_launch();
-        paged_decode_kernel<D, kHnd, kFp8, kG>
+        paged_decode_kernel<D, kHnd, kFp8>
             <<<dp.grid, kDecodeThreads, Cfg::kSmemBytes, f.stream>>>(kv_map, p);
         e = cudaGetLastError();
         if (e != cudaSuccess)
@@ -1162,15 +1107,9 @@ cudaError_t launch_decode(const Fwd &f, const DecodePlan &dp, const Workspace &w
     if (f.kv_fp8) {  // head_size 128 only (checked by the caller)
         if (f.head_size != 128 || cascade)
             return cudaErrorInvalidValue;
-        const int g = f.num_heads / f.num_kv_heads;
-        if (g <= 2)
-            return f.kv_hnd ? launch_decode_d<128, true, true, 2>(f, dp, ws, wsp, kv_map, kv_begin, cascade)
-                            : launch_decode_d<128, false, true, 2>(f, dp, ws, wsp, kv_map, kv_begin, cascade);
-        if (g <= 4)
-            return f.kv_hnd ? launch_decode_d<128, true, true, 4>(f, dp, ws, wsp, kv_map, kv_begin, cascade)
-                            : launch_decode_d<128, false, true, 4>(f, dp, ws, wsp, kv_map, kv_begin, cascade);
-        return f.kv_hnd ? launch_decode_d<128, true, true, 8>(f, dp, ws, wsp, kv_map, kv_begin, cascade)
-                        : launch_decode_d<128, false, true, 8>(f, dp, ws, wsp, kv_map, kv_begin, cascade);
+        return f.kv_hnd
+                   ? launch_decode_d<128, true, true>(f, dp, ws, wsp, kv_map, kv_begin, cascade)
+                   : launch_decode_d<128, false, true>(f, dp, ws, wsp, kv_map, kv_begin, cascade);
     }
     if (f.head_size == 128)
         return f.kv_hnd
