@@ -36,6 +36,19 @@
 // The tensor work is g FLOP per byte of KV, far below the ridge point, so the
 // warp-level mma is ample; the kernel is bound by HBM.
 //
+// An fp8 e4m3 pool (the "FlashAttention y FlashInfer" page, "Resumen en una
+// frase" and "Limites y fallos": an fp8 KV cache; one scale per tensor for K
+// and V) halves the bytes, so the same stage carries 32 keys per unit, loaded
+// as two 16-row boxes of 128-byte code rows.  The codes are converted to f16
+// once each (exact: every e4m3 value is an f16 normal), K from 16-byte row
+// reads and V from ldmatrix.m16n16.trans.b8 (a byte transpose), and meet
+// f16 Q (each head prescaled by a power of two into f16 range, exact for bf16
+// values) and f16 P in mma m16n8k16; k_scale is folded into the score scale
+// and v_scale into the output scale.  The keys of a unit are taken in an
+// order that keeps both the K row reads and the V row gathers free of bank
+// conflicts.  (On this GPU an fp8 mma.sync converts both operands itself on
+// every call, which would convert each code once per Q or P term.)
+//
 // At the end of a piece every warp writes its rows straight from registers:
 // the final bf16 rows and lse, or (several pieces, or Hkv < 8 where several
 // warps share a kv head) a normalised fp32 partial and its log2-sum-exp.
