@@ -674,6 +674,29 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     };
     begin_piece();
 
+    // Running max of the two heads with a lazy rescale: it moves only when a
+    // unit's max (cand, log2 units) exceeds it by more than 8, so every p is
+    // at most 2^8 and the rescale of O and l (warp-uniform) is rare after a
+    // piece's first unit; the result is the same up to rounding.
+    auto update_max = [&](float cand0, float cand1) {
+        const bool up0 = cand0 > m0 + 8.f, up1 = cand1 > m1 + 8.f;
+        if (__any_sync(0xffffffffu, up0 || up1)) {
+            const float al0 = up0 ? fast_exp2(m0 - cand0) : 1.f;
+            const float al1 = up1 ? fast_exp2(m1 - cand1) : 1.f;
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                o[mt][0] *= al0;
+                o[mt][1] *= al1;
+                o[mt][2] *= al0;
+                o[mt][3] *= al1;
+            }
+            l0 *= al0;
+            l1 *= al1;
+            m0 = up0 ? cand0 : m0;
+            m1 = up1 ? cand1 : m1;
+        }
+    };
+
     for (int64_t x = lo; x < hi; ++x) {
         const int i = int(x - lo);
         const int slot = i % Cfg::kStages;
@@ -749,21 +772,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                     sc[t2][2] = vb ? c[2] * mul0 : kNegInf;
                     sc[t2][3] = vb ? c[3] * mul1 : kNegInf;
                 }
-                const float mn0 = fmaxf(
-                    m0, warp_max_heads(fmax3(fmaxf(sc[0][0], sc[0][2]), sc[1][0], sc[1][2])));
-                const float mn1 = fmaxf(
-                    m1, warp_max_heads(fmax3(fmaxf(sc[0][1], sc[0][3]), sc[1][1], sc[1][3])));
-                const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+                update_max(warp_max_heads(fmax3(fmaxf(sc[0][0], sc[0][2]), sc[1][0], sc[1][2])),
+                           warp_max_heads(fmax3(fmaxf(sc[0][1], sc[0][3]), sc[1][1], sc[1][3])));
                 float pv[2][4];
 #pragma unroll
                 for (int t2 = 0; t2 < 2; ++t2)
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        pv[t2][i] = fast_exp2(sc[t2][i] - ((i & 1) ? mn1 : mn0));
-                l0 = l0 * al0 + ((pv[0][0] + pv[0][2]) + (pv[1][0] + pv[1][2]));
-                l1 = l1 * al1 + ((pv[0][1] + pv[0][3]) + (pv[1][1] + pv[1][3]));
-                m0 = mn0;
-                m1 = mn1;
+                        pv[t2][i] = fast_exp2(sc[t2][i] - ((i & 1) ? m1 : m0));
+                l0 += (pv[0][0] + pv[0][2]) + (pv[1][0] + pv[1][2]);
+                l1 += (pv[0][1] + pv[0][3]) + (pv[1][1] + pv[1][3]);
                 // ---- P^T as f16 B fragments: movmatrix turns S^T rows (keys)
                 // into columns, so the lane holds keys (2tq, 2tq+1) and (2tq+8,
                 // 2tq+9) of tile t2 for head gq: k = (2tq, 2tq+1 | 2tq+8, 2tq+9)
@@ -805,10 +823,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                             v[2] &= mk1;
                             v[3] &= mk1;
                         }
-                        o[mt][0] *= al0;
-                        o[mt][1] *= al1;
-                        o[mt][2] *= al0;
-                        o[mt][3] *= al1;
 #pragma unroll
                         for (int t2 = 0; t2 < 2; ++t2) {
                             uint32_t a0, a1, a2, a3;
@@ -837,35 +851,43 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 const float s1 = va ? c[1] * mul1 : kNegInf;
                 const float s2 = vb ? c[2] * mul0 : kNegInf;
                 const float s3 = vb ? c[3] * mul1 : kNegInf;
-                const float mn0 = fmaxf(m0, warp_max_heads(fmaxf(s0, s2)));
-                const float mn1 = fmaxf(m1, warp_max_heads(fmaxf(s1, s3)));
-                const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
-                const float p0 = fast_exp2(s0 - mn0), p1 = fast_exp2(s1 - mn1);
-                const float p2 = fast_exp2(s2 - mn0), p3 = fast_exp2(s3 - mn1);
-                l0 = l0 * al0 + (p0 + p2);
-                l1 = l1 * al1 + (p1 + p3);
-                m0 = mn0;
-                m1 = mn1;
+                update_max(warp_max_heads(fmaxf(s0, s2)), warp_max_heads(fmaxf(s1, s3)));
+                const float p0 = fast_exp2(s0 - m0), p1 = fast_exp2(s1 - m1);
+                const float p2 = fast_exp2(s2 - m0), p3 = fast_exp2(s3 - m1);
+                l0 += p0 + p2;
+                l1 += p1 + p3;
                 // P^T as B fragments: rows 0-7 and 8-15 of S^T
                 const uint32_t b0 = movmatrix_trans(pack_bf16x2(p0, p1));
                 const uint32_t b1 = movmatrix_trans(pack_bf16x2(p2, p3));
-                // rows of V past the end of the sequence may hold anything: zero them
-                const uint32_t mlo = (2 * tq < valid ? 0x0000ffffu : 0u) |
-                                     (2 * tq + 1 < valid ? 0xffff0000u : 0u);
-                const uint32_t mhi = (2 * tq + 8 < valid ? 0x0000ffffu : 0u) |
-                                     (2 * tq + 9 < valid ? 0xffff0000u : 0u);
+                auto pv_pass = [&](auto masked) {
+                    // rows of V past the end of the sequence may hold anything:
+                    // zero them (only a sequence's last unit has such rows)
+                    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+                    if constexpr (decltype(masked)::value) {
+                        mlo = (2 * tq < valid ? 0x0000ffffu : 0u) |
+                              (2 * tq + 1 < valid ? 0xffff0000u : 0u);
+                        mhi = (2 * tq + 8 < valid ? 0x0000ffffu : 0u) |
+                              (2 * tq + 9 < valid ? 0xffff0000u : 0u);
+                    }
 #pragma unroll
-                for (int mt = 0; mt < D / 16; ++mt) {
-                    const uint32_t ch = 2 * mt + v_chunk;
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4_trans(vbase + (ch >> 3) * 2048 + swz128(v_row, ch & 7), a0, a1, a2,
-                                  a3);
-                    o[mt][0] *= al0;
-                    o[mt][1] *= al1;
-                    o[mt][2] *= al0;
-                    o[mt][3] *= al1;
-                    mma_bf16_16816(o[mt], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, b0, b1);
-                }
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        const uint32_t ch = 2 * mt + v_chunk;
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4_trans(vbase + (ch >> 3) * 2048 + swz128(v_row, ch & 7), a0, a1,
+                                      a2, a3);
+                        if constexpr (decltype(masked)::value) {
+                            a0 &= mlo;
+                            a1 &= mlo;
+                            a2 &= mhi;
+                            a3 &= mhi;
+                        }
+                        mma_bf16_16816(o[mt], a0, a1, a2, a3, b0, b1);
+                    }
+                };
+                if (valid < 16)
+                    pv_pass(std::true_type{});
+                else
+                    pv_pass(std::false_type{});
             }
         }
         __syncwarp();
