@@ -273,10 +273,11 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def committed_traffic(workload):
+def committed_traffic(workload, kv_dtype="bf16"):
     """Per-launch DRAM bytes of the decode kernel from the committed ncu summary,
     or None when the kernel source changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", f"decode_kernel_{workload}_traffic.json")
+    suffix = "" if kv_dtype == "bf16" else f"_{kv_dtype}"
+    path = os.path.join(ROOT, "profiles", f"decode_kernel_{workload}{suffix}_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
@@ -534,7 +535,8 @@ def measure_fp8_decode(args, dev, peaks, peaks_kind):
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "kernel_ms": k_ms,
                          "peak_source": f"{peaks_kind} copy bandwidth (hbm_gbs)",
-                         "traffic": None}}
+                         "algorithmic_bytes_per_launch": kv_bytes,
+                         "traffic": committed_traffic("decode_heavy", "fp8")}}
 
 
 def measure_prefill(args, dev, peaks, peaks_kind):
