@@ -231,6 +231,36 @@ def make_batch(spec: BatchSpec, seed: int, device: str = "cpu") -> Batch:
     return Batch(spec, query, key, value, cache, slots, qsl, lens, table, nb)
 
 
+E4M3_NAN = 0x7F
+
+
+def random_fp8_pool(batch: Batch, seed: int, max_code: int = 0x48):
+    """A seeded e4m3 pool shaped like batch.cache: every slot the bf16 pool fills
+    holds a random finite code of magnitude code <= max_code (0x48 = 4.0), every
+    slot it leaves NaN holds the e4m3 NaN code.  Codes are drawn directly (no
+    quantisation): numpy for a host batch, a seeded torch generator on the
+    batch's device otherwise.  Returns an array / tensor of uint8."""
+    if isinstance(batch.cache, np.ndarray):
+        rng = np.random.Generator(np.random.PCG64(seed))
+        mag = rng.integers(0, max_code + 1, size=batch.cache.shape, dtype=np.uint8)
+        sign = rng.integers(0, 2, size=batch.cache.shape, dtype=np.uint8) << 7
+        codes = mag | sign
+        codes[(batch.cache & 0x7FFF) > 0x7F80] = E4M3_NAN
+        return codes
+    import torch
+
+    dev = batch.cache.device
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    mag = torch.randint(0, max_code + 1, batch.cache.shape, generator=g, device=dev,
+                        dtype=torch.uint8)
+    sign = torch.randint(0, 2, batch.cache.shape, generator=g, device=dev,
+                         dtype=torch.uint8) * 128
+    codes = mag | sign
+    codes[torch.isnan(batch.cache)] = E4M3_NAN
+    return codes
+
+
 def to_layout(cache, kv_layout: str):
     """The pool in physical order `kv_layout`: NHD is the logical
     [NB, 2, bs, Hkv, D] itself, HND swaps the slot and head axes to
