@@ -176,22 +176,43 @@ class Step:
 
     fused = True  # the cache write inside the forward (paged_attn_forward_fused)
 
-    def run(self, q=None, k=None, v=None, slots=None, meta=None):
+    def run(self, q=None, k=None, v=None, slots=None, meta=None, out=None, lse=None):
         b = self.batch
         q = b.query if q is None else q
         k = b.key if k is None else k
         v = b.value if v is None else v
         slots = self.slots if slots is None else slots
         meta = self.meta if meta is None else meta
+        out = self.out if out is None else out
+        lse = self.lse if lse is None else lse
         if self.fused:
-            self.pka.paged_attn_forward_fused(q, k, v, slots, b.cache, meta, self.out, self.lse,
+            self.pka.paged_attn_forward_fused(q, k, v, slots, b.cache, meta, out, lse,
                                               scale=self.spec.softmax_scale,
                                               causal=self.spec.causal, workspace=self.ws)
             return
         self.pka.reshape_and_cache(k, v, b.cache, slots)
-        self.pka.paged_attn_forward(q, b.cache, meta, self.out, self.lse,
+        self.pka.paged_attn_forward(q, b.cache, meta, out, lse,
                                     scale=self.spec.softmax_scale, causal=self.spec.causal,
                                     workspace=self.ws)
+
+
+def pack_buffers(torch, tensors, dev):
+    """One pinned host byte buffer and one device byte buffer holding every
+    tensor of `tensors` in 256-byte aligned regions (host contents copied in);
+    returns (host, device, host views, device views) with the tensors' shapes."""
+    offs, total = {}, 0
+    for name, t in tensors.items():
+        offs[name] = total
+        total = (total + t.numel() * t.element_size() + 255) // 256 * 256
+    host = torch.empty(total, dtype=torch.uint8).pin_memory()
+    device = torch.empty(total, dtype=torch.uint8, device=dev)
+    hv, dv = {}, {}
+    for name, t in tensors.items():
+        n = t.numel() * t.element_size()
+        hv[name] = host[offs[name]:offs[name] + n].view(t.dtype).view(t.shape)
+        dv[name] = device[offs[name]:offs[name] + n].view(t.dtype).view(t.shape)
+        hv[name].copy_(t.detach().cpu())
+    return host, device, hv, dv
 
 
 def units(spec):
@@ -366,30 +387,30 @@ def run_ours(args):
     ms, k_ms = max_over_ranks([ms, k_ms], dev)
     value = world * kv_bytes / (ms * 1e-3) / 1e9
 
-    # end to end through the public API with host buffers
+    # end to end through the public API with host buffers: the step's inputs
+    # (q, k, v, slot mapping, metadata) staged in one pinned buffer and copied in
+    # one H2D copy, out and lse read back in one D2H copy; the library gets views
     b = st.batch
-    host = {
-        "q": b.query.cpu().pin_memory(), "k": b.key.cpu().pin_memory(),
-        "v": b.value.cpu().pin_memory(),
-        "slots": torch.from_numpy(b.slot_mapping).pin_memory(),
-        "qsl": torch.from_numpy(b.query_start_loc).pin_memory(),
-        "sl": torch.from_numpy(b.seq_lens).pin_memory(),
-        "bt": torch.from_numpy(np.ascontiguousarray(b.block_table)).pin_memory(),
+    parts = {
+        "q": b.query.cpu(), "k": b.key.cpu(), "v": b.value.cpu(),
+        "slots": torch.from_numpy(b.slot_mapping),
+        "qsl": torch.from_numpy(b.query_start_loc),
+        "sl": torch.from_numpy(b.seq_lens),
+        "bt": torch.from_numpy(np.ascontiguousarray(b.block_table)),
     }
-    dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
-    out_host = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
-    lse_host = torch.empty(st.lse.shape, dtype=st.lse.dtype).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = out_host.numel() * out_host.element_size() + lse_host.numel() * lse_host.element_size()
-    meta_e2e = pka.Meta(dbuf["qsl"], dbuf["sl"], dbuf["bt"], st.meta.num_decodes,
+    h_stage, d_stage, h_views, d_views = pack_buffers(torch, parts, dev)
+    outs = {"out": st.out, "lse": st.lse}
+    h_ret, d_ret, h_outs, d_outs = pack_buffers(torch, outs, dev)
+    h2d = h_stage.numel()
+    d2h = h_ret.numel()
+    meta_e2e = pka.Meta(d_views["qsl"], d_views["sl"], d_views["bt"], st.meta.num_decodes,
                         st.meta.max_query_len, st.meta.max_seq_len, st.meta.common_prefix_len)
 
     def e2e_step():
-        for k in host:
-            dbuf[k].copy_(host[k], non_blocking=True)
-        st.run(q=dbuf["q"], k=dbuf["k"], v=dbuf["v"], slots=dbuf["slots"], meta=meta_e2e)
-        out_host.copy_(st.out, non_blocking=True)
-        lse_host.copy_(st.lse, non_blocking=True)
+        d_stage.copy_(h_stage, non_blocking=True)
+        st.run(q=d_views["q"], k=d_views["k"], v=d_views["v"], slots=d_views["slots"],
+               meta=meta_e2e, out=d_outs["out"], lse=d_outs["lse"])
+        h_ret.copy_(d_ret, non_blocking=True)
 
     for _ in range(max(3, args.warmup)):
         e2e_step()
