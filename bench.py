@@ -215,6 +215,15 @@ def pack_buffers(torch, tensors, dev):
     return host, device, hv, dv
 
 
+def workload_config(name, spec):
+    """The `config` keys that name the workload (shared by both arms)."""
+    return {"workload": name, "num_decodes": spec.num_decodes,
+            "num_prefills": len(spec.prefill), "num_heads": spec.num_heads,
+            "num_kv_heads": spec.num_kv_heads, "head_size": spec.head_size,
+            "block_size": spec.block_size,
+            "kv_bytes_per_step": A.decode_kv_bytes(spec, spec.common_prefix_len)}
+
+
 def units(spec):
     """(KV bytes, prefill flops) of one step."""
     return A.decode_kv_bytes(spec, spec.common_prefix_len), A.prefill_flops(spec)
@@ -275,7 +284,9 @@ def run_reference(args):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": name, "sample_per_step": desc}, "impl": "reference",
+        "config": {**workload_config(name, spec), "sample_per_step": desc,
+                   "parallelism": f"fp64 oracle on {threads} host threads"},
+        "impl": "reference",
         "cpu_baseline": {"kind": "oracle", "cores": threads, "sample": desc, "value": value,
                          "unit": "GB/s"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -443,10 +454,7 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": args.workload, "num_decodes": spec.num_decodes,
-                   "num_prefills": len(spec.prefill), "num_heads": spec.num_heads,
-                   "num_kv_heads": spec.num_kv_heads, "head_size": spec.head_size,
-                   "block_size": spec.block_size, "kv_bytes_per_step": kv_bytes,
+        "config": {**workload_config(args.workload, spec),
                    "l2": "inputs larger than L2 (KV per step >> 129 MB), no flush",
                    "step_calls": "paged_attn_forward_fused" if Step.fused
                    else "reshape_and_cache + paged_attn_forward",
