@@ -18,6 +18,7 @@ Prints ONE JSON line (rank 0).  Flags:
   --no-cpu-baseline               skip the oracle timing (profiling runs)
   --two-call                      write the cache with its own launch (reshape_and_cache)
   --no-fp8                        skip the fp8 e4m3 pool decode sub-measurement
+  --no-workloads                  skip the other configurations' short timed runs
   --profile [--kv-dtype fp8]      short run for a profiler (optionally over an fp8 pool)
 """
 from __future__ import annotations
@@ -481,6 +482,8 @@ def run_ours(args):
         del st
         torch.cuda.empty_cache()
         line["prefill"] = measure_prefill(args, dev, peaks, peaks_kind)
+    if args.workload == "decode_heavy" and not args.no_workloads:
+        line["workloads"] = measure_workloads(args, dev, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
 
@@ -568,6 +571,99 @@ def measure_fp8_decode(args, dev, peaks, peaks_kind):
                          "traffic": committed_traffic("decode_heavy", "fp8")}}
 
 
+def timed_steps(torch, pka, st, steps, kernels=(0, 1), run=None):
+    """Mean step time and mean per-launch kernel times (CUDA events; the library
+    records the decode (0) and prefill (1) kernels' events on their stream)."""
+    run = st.run if run is None else run
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    ev = {k: ([torch.cuda.Event(enable_timing=True) for _ in range(steps)],
+              [torch.cuda.Event(enable_timing=True) for _ in range(steps)]) for k in kernels}
+    for a, b in ev.values():
+        for e in a + b:
+            e.record()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        for k, (a, b) in ev.items():
+            pka.set_kernel_events(k, a[i], b[i])
+        run()
+    for k in ev:
+        pka.set_kernel_events(k, None, None)
+    e1.record()
+    torch.cuda.synchronize()
+    pka.check_status()
+    ms = e0.elapsed_time(e1) / steps
+    kms = {k: sum(x.elapsed_time(y) for x, y in zip(a, b)) / steps for k, (a, b) in ev.items()}
+    return ms, kms
+
+
+def measure_workloads(args, dev, peaks):
+    """The other configurations of the method, one short timed run each (20 steps
+    after 3 warm-ups, CUDA events): tiny_decode (latency), mixed (decode GB/s and
+    prefill TFLOP/s against their peaks), cascade (suffix GB/s and the
+    naive-equivalent GB/s), and decode_heavy's cache write and attention timed
+    separately (two calls) beside the fused step."""
+    import torch
+
+    import paged_kv_attention_33_gb300 as pka
+
+    hbm = float(peaks["hbm_gbs"])
+    tf = float(peaks.get("bf16_tflops", PEAKS_FALLBACK["bf16_tflops"]))
+    res = {}
+    st = Step("tiny_decode", dev)
+    ms, kms = timed_steps(torch, pka, st, 20)
+    res["tiny_decode"] = {"ms_per_step": ms, "decode_kernel_ms": kms[0],
+                          "bound": "latency (0.2 MB of KV)"}
+    del st
+    st = Step("mixed", dev)
+    kv, fl = units(st.spec)
+    ms, kms = timed_steps(torch, pka, st, 20)
+    res["mixed"] = {"ms_per_step": ms, "decode_kernel_ms": kms[0], "prefill_kernel_ms": kms[1],
+                    "decode_GBps": kv / (kms[0] * 1e-3) / 1e9,
+                    "decode_frac_of_hbm": kv / (kms[0] * 1e-3) / 1e9 / hbm,
+                    "prefill_TFLOPs": fl / (kms[1] * 1e-3) / 1e12,
+                    "prefill_frac_of_bf16": fl / (kms[1] * 1e-3) / 1e12 / tf,
+                    "kv_bytes_per_step": kv, "prefill_flops_per_step": fl}
+    del st
+    torch.cuda.empty_cache()
+    st = Step("cascade", dev)
+    kv, _ = units(st.spec)
+    sp = st.spec
+    naive, casc = A.cascade_prefix_token_reads(
+        sp.num_decodes, sp.common_prefix_len,
+        [L - sp.common_prefix_len for L in sp.seq_lens[: sp.num_decodes]])
+    row = sp.num_kv_heads * sp.head_size * 2 * 2
+    ms, kms = timed_steps(torch, pka, st, 20)
+    res["cascade"] = {"ms_per_step": ms, "decode_kernel_ms": kms[0],
+                      "prefix_pass_ms": kms[1],
+                      "suffix_GBps": kv / (kms[0] * 1e-3) / 1e9,
+                      "cascade_GBps_step": casc * row / (ms * 1e-3) / 1e9,
+                      "naive_equivalent_GBps_step": naive * row / (ms * 1e-3) / 1e9,
+                      "bytes_read_cascade": casc * row, "bytes_read_naive": naive * row}
+    del st
+    torch.cuda.empty_cache()
+    st = Step("decode_heavy", dev)
+    kv, _ = units(st.spec)
+    b = st.batch
+    ms_w, _ = timed_steps(torch, pka, st, 20, kernels=(),
+                          run=lambda: pka.reshape_and_cache(b.key, b.value, b.cache, st.slots))
+    Step.fused = False
+    try:
+        ms2, kms2 = timed_steps(torch, pka, st, 20, kernels=(0,))
+    finally:
+        Step.fused = not args.two_call
+    res["decode_heavy_two_call"] = {"reshape_and_cache_ms": ms_w, "step_ms": ms2,
+                                    "decode_kernel_ms": kms2[0],
+                                    "decode_frac_of_hbm": kv / (kms2[0] * 1e-3) / 1e9 / hbm}
+    del st
+    torch.cuda.empty_cache()
+    return res
+
+
 def measure_prefill(args, dev, peaks, peaks_kind):
     """Prefill workload: step and kernel time (CUDA events on the launching
     stream, the kernel bracketed by the library), TFLOP/s and the fraction of
@@ -649,6 +745,8 @@ def main():
                     help="skip the prefill sub-measurement")
     ap.add_argument("--no-fp8", action="store_true",
                     help="skip the fp8-pool decode sub-measurement")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other configurations' short timed runs")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
                     help="pool element type of --profile runs (fp8: decode workloads)")
     ap.add_argument("--profile", action="store_true",
