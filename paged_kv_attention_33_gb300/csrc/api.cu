@@ -186,8 +186,29 @@ Workspace plan_workspace(const DecodePlan &dp, int32_t num_tokens, int32_t num_d
     w.pf_counters = off;
     if (cascade || num_tokens > num_decodes)
         off = round256(off + 2 * sizeof(int32_t));
+    w.fp8_table = w.fp8_scratch = off;
+    w.fp8_blocks_per_seq = 0;
     w.total = off;
     return w;
+}
+
+void plan_fp8_prefill(Workspace &w, bool kv_fp8, int32_t num_seqs, int32_t num_decodes,
+                      int32_t max_seq_len, int32_t block_size, int32_t num_kv_heads,
+                      int32_t head_size)
+{
+    const int32_t nprefill = num_seqs - num_decodes;
+    if (!kv_fp8 || nprefill <= 0)
+        return;
+    const int32_t mb = (max_seq_len + block_size - 1) / block_size;
+    size_t off = w.total;
+    // the table first: a read past its last row (a length above max_seq_len,
+    // flagged) stays inside the workspace
+    w.fp8_table = off;
+    off = round256(off + size_t(num_seqs) * mb * 4);
+    w.fp8_scratch = off;
+    off = round256(off + size_t(nprefill) * mb * 2 * block_size * num_kv_heads * head_size * 2);
+    w.fp8_blocks_per_seq = mb;
+    w.total = off;
 }
 
 static bool scale_ok(float s) { return s > 0.f && s <= 3.4e38f; }
@@ -250,9 +271,8 @@ static pka_status check_shape(const pka_meta *m, int32_t num_tokens, int32_t num
         if (head_size != 128)
             return fail(PKA_ERR_UNSUPPORTED, "fp8 pool: head_size %d is not built (128)",
                         head_size);
-        if (m->num_decodes != m->num_seqs || m->common_prefix_len > 0)
-            return fail(PKA_ERR_UNSUPPORTED,
-                        "fp8 pool: only decode batches without a shared prefix are served");
+        if (m->common_prefix_len > 0)
+            return fail(PKA_ERR_UNSUPPORTED, "fp8 pool: no shared-prefix cascade");
     }
     return PKA_OK;
 }
@@ -365,9 +385,11 @@ size_t pka_workspace_size(const pka_meta *meta, int32_t num_tokens, int32_t num_
     const int sms = sm_count();
     DecodePlan dp = plan_decode(meta->split_kv_tokens, meta->num_decodes, num_kv_heads, sms);
     const int32_t pre_splits = plan_prefix_splits(num_tokens, num_heads, kv_begin, sms);
-    return plan_workspace(dp, num_tokens, meta->num_decodes, num_heads, head_size, cascade,
-                          pre_splits)
-        .total;
+    Workspace w = plan_workspace(dp, num_tokens, meta->num_decodes, num_heads, head_size, cascade,
+                                 pre_splits);
+    plan_fp8_prefill(w, meta->kv_dtype == PKA_KV_FP8_E4M3, meta->num_seqs, meta->num_decodes,
+                     meta->max_seq_len, block_size, num_kv_heads, head_size);
+    return w.total;
 }
 
 // This step's new K/V rows for pka_paged_attn_forward_fused.
@@ -455,6 +477,11 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
     const int32_t pre_splits = plan_prefix_splits(num_tokens, num_heads, kv_begin, f.num_sms);
     Workspace ws = plan_workspace(dp, num_tokens, meta->num_decodes, num_heads, head_size, cascade,
                                   pre_splits);
+    plan_fp8_prefill(ws, f.kv_fp8 != 0, meta->num_seqs, meta->num_decodes, meta->max_seq_len,
+                     block_size, num_kv_heads, head_size);
+    if (ws.fp8_blocks_per_seq > 0 &&
+        int64_t(num_prefills) * ws.fp8_blocks_per_seq * 2 * block_size >= (int64_t(1) << 31))
+        return fail(PKA_ERR_UNSUPPORTED, "fp8 prefill copy has more than 2^31 rows");
     if (ws.total > 0 && (!workspace || workspace_bytes < ws.total || !aligned(workspace, 256)))
         return fail(PKA_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)",
                     ws.total, workspace_bytes);
@@ -490,9 +517,28 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
                        cascade ? reinterpret_cast<float *>(wsp + ws.o_suf) : nullptr,
                        cascade ? reinterpret_cast<float *>(wsp + ws.lse_suf) : nullptr,
                        meta->num_decodes, reinterpret_cast<int32_t *>(wsp + ws.pf_counters)};
+        // an fp8 pool: the prefill sequences' blocks are first copied out as bf16
+        // code values (exact) into the workspace, and the tensor-core prefill runs
+        // on that copy with k_scale in the score scale and v_scale on the output
+        Fwd fp = f;
+        if (f.kv_fp8) {
+            int32_t *table = reinterpret_cast<int32_t *>(wsp + ws.fp8_table);
+            void *scratch = wsp + ws.fp8_scratch;
+            e = launch_dequant_prefill_blocks(f, scratch, table, ws.fp8_blocks_per_seq);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "fp8 prefill copy launch");
+            fp.kv_cache = scratch;
+            fp.block_table = table;
+            fp.bt_stride = ws.fp8_blocks_per_seq;
+            fp.num_blocks = int64_t(num_prefills) * ws.fp8_blocks_per_seq;
+            fp.kv_hnd = 0;
+            fp.kv_fp8 = 0;
+            fp.scale = f.scale * f.k_scale;
+            fp.out_scale = f.v_scale;
+        }
         if (!cascade)
             record_start(PKA_KERNEL_PREFILL, f.stream);
-        e = launch_prefill(f, pf);
+        e = launch_prefill(fp, pf);
         if (!cascade)
             record_stop(PKA_KERNEL_PREFILL, f.stream);
         if (e != cudaSuccess)

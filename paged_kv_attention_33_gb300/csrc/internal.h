@@ -32,9 +32,10 @@ struct Fwd {
     int32_t block_size;
     int64_t num_blocks;
     int32_t kv_hnd;  // 1: pool in HND order, 0: NHD
-    int32_t kv_fp8 = 0;  // 1: pool of e4m3 codes (decode only), 0: bf16
+    int32_t kv_fp8 = 0;  // 1: pool of e4m3 codes, 0: bf16
     float k_scale = 1.f;
     float v_scale = 1.f;
+    float out_scale = 1.f;  // prefill: output multiplier (v_scale over a dequantised copy)
     // fused cache write: the decode launch also writes this step's K/V rows
     int32_t fuse_write = 0;
     const void *new_key = nullptr;
@@ -65,6 +66,11 @@ struct Workspace {
     int32_t pre_splits;        // cascade: key chunks of the shared-prefix pass
     size_t o_suf, lse_suf;     // cascade: suffix partial of every prefill token
     size_t pf_counters;        // prefill work-queue counters (int32 x 2)
+    // fp8 pool with prefills: the prefill sequences' blocks as bf16 code values
+    // (fp8_blocks_per_seq = ceil(max_seq_len / bs) blocks per prefill sequence)
+    // and their block table ([num_seqs, fp8_blocks_per_seq] int32)
+    size_t fp8_scratch, fp8_table;
+    int32_t fp8_blocks_per_seq;
     size_t total;
 };
 
@@ -78,6 +84,11 @@ int32_t plan_prefix_splits(int32_t num_tokens, int32_t num_heads, int32_t prefix
 Workspace plan_workspace(const DecodePlan &dp, int32_t num_tokens, int32_t num_decodes,
                          int32_t num_heads, int32_t head_size, bool cascade,
                          int32_t pre_splits);
+// The fp8 prefill copy: blocks per prefill sequence and bytes of the bf16 scratch pool
+// (0 when the pool is bf16 or there are no prefills); appended to a planned workspace.
+void plan_fp8_prefill(Workspace &w, bool kv_fp8, int32_t num_seqs, int32_t num_decodes,
+                      int32_t max_seq_len, int32_t block_size, int32_t num_kv_heads,
+                      int32_t head_size);
 
 // kv_write.cu
 cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *cache,
@@ -90,6 +101,10 @@ cudaError_t launch_reshape_and_cache_fp8(const void *key, const void *value, voi
                                          int32_t num_kv_heads, int32_t head_size,
                                          int32_t block_size, int64_t num_blocks, int32_t hnd,
                                          float k_scale, float v_scale, cudaStream_t st);
+// The prefill sequences' blocks of an fp8 pool (f.kv_cache, layout f.kv_hnd)
+// as bf16 code values in a dense NHD scratch pool, and its block table.
+cudaError_t launch_dequant_prefill_blocks(const Fwd &f, void *scratch, int32_t *table,
+                                          int32_t max_blocks);
 uint32_t kv_write_take_error();
 
 // decode.cu: paged decode of sequences [0, num_decodes) over keys

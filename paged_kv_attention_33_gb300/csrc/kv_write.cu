@@ -156,6 +156,78 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *c
     return cudaGetLastError();
 }
 
+// The blocks of the prefill sequences of an fp8 pool as bf16 code values (no
+// scale: every e4m3 value is exact in bf16; the attention applies k_scale and
+// v_scale) in a dense NHD scratch pool: CTA (p, n) takes block column n of
+// prefill sequence s = first_seq + p, copies pool block bt[s][n] to scratch
+// block p*max_blocks + n and writes that id into the scratch table at [s][n].
+// Columns past ceil(L_s / bs) are left alone (the attention never reads them).
+__global__ void __launch_bounds__(kKvwThreads)
+    dequant_prefill_blocks_kernel(const uint4 *__restrict__ pool, uint4 *__restrict__ scratch,
+                                  int32_t *__restrict__ table, const int32_t *__restrict__ bt,
+                                  int32_t bt_stride, const int32_t *__restrict__ seq_lens,
+                                  int32_t first_seq, int32_t max_blocks, int32_t block_size,
+                                  int32_t num_kv_heads, int32_t head_chunks, int64_t num_blocks,
+                                  int32_t hnd)
+{
+    const int32_t p = blockIdx.y, n = blockIdx.x;
+    const int32_t s = first_seq + p;
+    const int32_t L = seq_lens[s];
+    if (n == 0 && threadIdx.x == 0 && int64_t(L) > int64_t(max_blocks) * block_size)
+        flag_error(kErrBadMetadata);  // longer than max_seq_len: its tail was not copied
+    if (n * block_size >= L)
+        return;
+    const int64_t dst_blk = int64_t(p) * max_blocks + n;
+    if (threadIdx.x == 0)
+        table[int64_t(s) * max_blocks + n] = static_cast<int32_t>(dst_blk);
+    const int32_t src_blk = bt[int64_t(s) * bt_stride + n];
+    if (src_blk < 0 || src_blk >= num_blocks) {
+        if (threadIdx.x == 0)
+            flag_error(kErrBlockOutOfPool);
+        return;
+    }
+    // 16-code chunk i of the block in NHD order: (kv, offset, head, chunk)
+    const int32_t per_kv = block_size * num_kv_heads * head_chunks;
+    for (int32_t i = threadIdx.x; i < 2 * per_kv; i += kKvwThreads) {
+        const int32_t kv = i / per_kv, r = i % per_kv;
+        const int32_t off = r / (num_kv_heads * head_chunks);
+        const int32_t h = (r / head_chunks) % num_kv_heads, c = r % head_chunks;
+        const int64_t src = hnd ? (((int64_t(src_blk) * 2 + kv) * num_kv_heads + h) * block_size +
+                                   off) * head_chunks + c
+                                : (int64_t(src_blk) * 2 * per_kv + i);
+        const uint4 codes = pool[src];
+        const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t lo, hi;  // f16 pairs of bytes (0, 1) and (2, 3)
+            e4m3x4_to_f16x2x2(w[j], lo, hi);
+            const __half2 a = *reinterpret_cast<const __half2 *>(&lo);
+            const __half2 b = *reinterpret_cast<const __half2 *>(&hi);
+            o[2 * j] = pack_bf16x2(__low2float(a), __high2float(a));
+            o[2 * j + 1] = pack_bf16x2(__low2float(b), __high2float(b));
+        }
+        uint4 *d = scratch + (dst_blk * 2 * per_kv + i) * 2;
+        d[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+cudaError_t launch_dequant_prefill_blocks(const Fwd &f, void *scratch, int32_t *table,
+                                          int32_t max_blocks)
+{
+    const int32_t nprefill = f.num_seqs - f.num_decodes;
+    if (nprefill <= 0 || max_blocks <= 0)
+        return cudaSuccess;
+    count_launch();
+    dim3 grid(static_cast<unsigned>(max_blocks), static_cast<unsigned>(nprefill));
+    dequant_prefill_blocks_kernel<<<grid, kKvwThreads, 0, f.stream>>>(
+        static_cast<const uint4 *>(f.kv_cache), static_cast<uint4 *>(scratch), table,
+        f.block_table, f.bt_stride, f.seq_lens, f.num_decodes, max_blocks, f.block_size,
+        f.num_kv_heads, f.head_size / 16, f.num_blocks, f.kv_hnd);
+    return cudaGetLastError();
+}
+
 uint32_t kv_write_take_error() { return take_device_error(); }
 
 }  // namespace pka

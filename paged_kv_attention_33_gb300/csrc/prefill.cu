@@ -73,6 +73,7 @@ struct PrefillParams {
     int32_t kv_cap;    // keys >= kv_cap are not attended
     int32_t causal;
     float scale_log2;
+    float out_scale;     // output multiplier (the V scale of a dequantised fp8 copy)
     int32_t partial;     // 0: bf16 out + ln lse; 1: fp32 partial + log2 lse
     int32_t token_base;  // partial rows are (t - token_base) * H + h
     int32_t shared_prefix;  // 1: every token of the batch against keys [0, kv_cap) of
@@ -391,7 +392,7 @@ __device__ __forceinline__ void pf_softmax(const PrefillParams &p, const int32_t
         ++pv_n;
         tc_fence_after();
         {
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float inv = l > 0.f ? p.out_scale / l : 0.f;
             const float lse2 = m + log2f(l);
             const int64_t orow = int64_t(t) * p.num_heads + it.h;
             const int64_t prow =
@@ -831,6 +832,7 @@ cudaError_t launch_prefill(const Fwd &f, const PrefillPass &pass)
     p.kv_cap = pass.kv_cap;
     p.causal = pass.causal;
     p.scale_log2 = f.scale * 1.4426950408889634f;
+    p.out_scale = f.out_scale;
     p.partial = pass.o_part != nullptr ? 1 : 0;
     p.token_base = pass.token_base;
     p.shared_prefix = pass.shared_prefix ? 1 : 0;

@@ -106,3 +106,43 @@ def test_merge_partials_kernel_against_oracle(oracle):
     with pytest.raises(pka.PkaError):
         o = W.to_device(outs, dev)
         pka.merge_partials(o, torch.from_numpy(lses).to(dev), o[2], None)
+
+
+@pytest.mark.parametrize("world", [1, 2, 4])
+def test_dcp_over_an_fp8_pool(oracle, world):
+    """The same sharding over an fp8 e4m3 pool (per-tensor scales): every rank
+    runs the fp8 decode on its shard (some shards empty), the partials merge to
+    the oracle's unsharded fp8 attention."""
+    import torch
+
+    import paged_kv_attention_33_gb300 as pka
+
+    sp = W.BatchSpec(f"dcp8_{world}", 32, 8, 128, 16, decode_ctx=[0, 5, 15, 16, 35, 300, 2500])
+    b = W.make_batch(sp, seed=8200 + world)
+    ks, vs = 0.05, 0.04
+    c = G.host_bits(b.cache)
+    pool = np.empty(c.shape, dtype=np.uint8)
+    pool[:, 0] = oracle.quantize_e4m3(np.ascontiguousarray(c[:, 0]), ks)
+    pool[:, 1] = oracle.quantize_e4m3(np.ascontiguousarray(c[:, 1]), vs)
+    dev = "cuda"
+    cache = torch.from_numpy(pool).to(dev)
+    pka.reshape_and_cache_fp8(G.to_dev(b.key, dev), G.to_dev(b.value, dev), cache,
+                              torch.from_numpy(b.slot_mapping).to(dev), ks, vs)
+    q = G.to_dev(b.query, dev)
+    outs, lses = [], []
+    for r in range(world):
+        lens, table = dcp.shard_decode_metadata(b.seq_lens, b.block_table, sp.block_size, r,
+                                                world)
+        meta = pka.Meta.from_host(b.query_start_loc, lens, table, sp.num_decodes, dev,
+                                  kv_dtype="fp8", k_scale=ks, v_scale=vs)
+        o, l = dcp.gpu_local_partial(q, cache, meta, scale=sp.softmax_scale)
+        outs.append(o)
+        lses.append(l)
+    pka.check_status()
+    out, lse = dcp.gpu_merge(torch.stack(outs), torch.stack(lses))
+    oracle.reshape_and_cache_fp8(b.key, b.value, pool, b.slot_mapping, ks, vs)
+    o_ref, l_ref = oracle.paged_attention_fp8(b.query, pool, ks, vs, b.query_start_loc,
+                                              b.seq_lens, b.block_table, sp.softmax_scale)
+    rows = np.arange(b.num_tokens * sp.num_heads, dtype=np.int64)
+    res = G.compare(W.to_host_bits(out), lse.cpu().numpy(), o_ref, l_ref, rows, sp.num_heads)
+    G.assert_close(res, f"dcp fp8 world={world}")

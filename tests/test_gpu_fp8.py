@@ -27,7 +27,8 @@ def fp8_pool(oracle, batch, k_scale, v_scale):
     return p8
 
 
-def run_fp8(batch, pool8, k_scale, v_scale, split_kv_tokens=0, fused=False, query=None):
+def run_fp8(batch, pool8, k_scale, v_scale, split_kv_tokens=0, fused=False, query=None,
+            causal=True):
     """The fp8 write and forward through the C ABI; host copies of the logical
     pool codes, the output bits and the lse."""
     import torch
@@ -51,10 +52,10 @@ def run_fp8(batch, pool8, k_scale, v_scale, split_kv_tokens=0, fused=False, quer
     lse = torch.full((T, sp.num_heads), float("nan"), dtype=torch.float32, device=dev)
     if fused:
         pka.paged_attn_forward_fused(q, k, v, slots, cache, meta, out, lse,
-                                     scale=sp.softmax_scale)
+                                     scale=sp.softmax_scale, causal=causal)
     else:
         pka.reshape_and_cache_fp8(k, v, cache, slots, k_scale, v_scale, kv_layout=sp.kv_layout)
-        pka.paged_attn_forward(q, cache, meta, out, lse, scale=sp.softmax_scale)
+        pka.paged_attn_forward(q, cache, meta, out, lse, scale=sp.softmax_scale, causal=causal)
     pka.check_status()
     return (W.from_layout(cache, sp.kv_layout).cpu().numpy(), W.to_host_bits(out),
             lse.cpu().numpy())
@@ -85,18 +86,19 @@ def score_bound(oracle, batch, pool8, k_scale, query):
 
 
 def check_fp8(oracle, batch, k_scale, v_scale, split_kv_tokens=0, fused=False, label="",
-              query=None, lse_rel_bound=0.0):
+              query=None, lse_rel_bound=0.0, causal=True):
     pool = fp8_pool(oracle, batch, k_scale, v_scale)
     want = pool.copy()
     oracle.reshape_and_cache_fp8(batch.key, batch.value, want, batch.slot_mapping, k_scale,
                                  v_scale)
-    got_pool, out, lse = run_fp8(batch, pool, k_scale, v_scale, split_kv_tokens, fused, query)
+    got_pool, out, lse = run_fp8(batch, pool, k_scale, v_scale, split_kv_tokens, fused, query,
+                                 causal)
     assert np.array_equal(want, got_pool), f"{label}: fp8 cache write differs"
     sp = batch.spec
     qh = batch.query if query is None else query
     o_ref, l_ref = oracle.paged_attention_fp8(qh, want, k_scale, v_scale, batch.query_start_loc,
                                               batch.seq_lens, batch.block_table,
-                                              sp.softmax_scale, threads=8)
+                                              sp.softmax_scale, causal=causal, threads=8)
     rows = np.arange(batch.num_tokens * sp.num_heads, dtype=np.int64)
     res = G.compare(out, None, o_ref, l_ref, rows, sp.num_heads)
     G.assert_close(res, label)
@@ -184,17 +186,73 @@ def test_fp8_fused_write_matches_two_calls(oracle, layout):
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
+@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("layout,bs", [("NHD", 16), ("HND", 16), ("NHD", 64), ("HND", 256)])
+def test_fp8_mixed_decode_and_prefill(oracle, layout, bs, fused):
+    """Decodes and prefill chunks (with and without prior context, ragged 128-row
+    tiles) over one fp8 pool: the decodes read the codes, the prefills run on
+    the workspace's bf16 copy of their blocks; one call or two."""
+    sp = W.BatchSpec(f"fp8_mixed_{layout}_{bs}", 32, 8, 128, bs, decode_ctx=[0, 17, 600],
+                     prefill=[(1, 0), (130, 0), (257, 300), (64, 1100)], kv_layout=layout)
+    b = W.make_batch(sp, seed=8600 + bs + (1 if layout == "HND" else 0))
+    check_fp8(oracle, b, 0.04, 0.03, fused=fused, label=f"mixed {layout} bs={bs} fused={fused}")
+
+
+def test_fp8_prefill_only_and_non_causal(oracle):
+    """A batch of prefills alone over an fp8 pool (the fused call writes first,
+    then attends), causal and not."""
+    sp = W.BatchSpec("fp8_prefill", 16, 4, 128, 16, prefill=[(200, 0), (40, 70), (129, 512)])
+    b = W.make_batch(sp, seed=8700)
+    check_fp8(oracle, b, 0.06, 0.02, fused=True, label="prefill only, fused")
+    check_fp8(oracle, b, 0.06, 0.02, label="prefill only, non-causal", causal=False)
+
+
+def test_fp8_mixed_full_size_sampled(oracle):
+    """The mixed workload at full size (64 decodes over up to 16k keys, then 4
+    chunks of 2048 queries over up to 16k of context) over a seeded fp8 pool,
+    through the fused call, checked on sampled rows."""
+    import torch
+
+    import paged_kv_attention_33_gb300 as pka
+
+    spec = W.named_spec("mixed")
+    b = W.make_batch(spec, seed=1004, device="cuda")
+    pool = W.random_fp8_pool(b, seed=1014)
+    want = pool.cpu().numpy()
+    del b.cache
+    torch.cuda.empty_cache()
+    ks, vs = 4.0 / 448, 4.0 / 448
+    meta = pka.Meta.from_host(b.query_start_loc, b.seq_lens, b.block_table, spec.num_decodes,
+                              "cuda", kv_dtype="fp8", k_scale=ks, v_scale=vs)
+    out = torch.empty_like(b.query)
+    lse = torch.empty(b.query.shape[:2], dtype=torch.float32, device="cuda")
+    pka.paged_attn_forward_fused(b.query, b.key, b.value, torch.from_numpy(b.slot_mapping).cuda(),
+                                 pool, meta, out, lse, scale=spec.softmax_scale)
+    pka.check_status()
+    key, value, query = (W.to_host_bits(x) for x in (b.key, b.value, b.query))
+    oracle.reshape_and_cache_fp8(key, value, want, b.slot_mapping, ks, vs)
+    assert np.array_equal(want, pool.cpu().numpy()), "fp8 cache write differs"
+    rows = W.sample_rows(b, 512, seed=6)
+    o_ref, l_ref = oracle.paged_attention_fp8(query, want, ks, vs, b.query_start_loc,
+                                              b.seq_lens, b.block_table, spec.softmax_scale,
+                                              rows=rows, threads=16)
+    res = G.compare(W.to_host_bits(out), lse.cpu().numpy(), o_ref, l_ref, rows, spec.num_heads)
+    G.assert_close(res, "mixed fp8")
+
+
 def test_fp8_unserved_batches_are_refused(oracle):
     import torch
 
     import paged_kv_attention_33_gb300 as pka
 
-    sp = W.BatchSpec("fp8_mixed", 16, 4, 128, 16, decode_ctx=[10], prefill=[(20, 5)])
+    sp = W.BatchSpec("fp8_cascade", 16, 4, 128, 16, decode_ctx=[40, 50], prefill=[(20, 35)],
+                     common_prefix_len=32)
     b = W.make_batch(sp, seed=8500)
     dev = G.device()
     pool = torch.from_numpy(fp8_pool(oracle, b, 0.1, 0.1)).to(dev)
     meta = pka.Meta.from_host(b.query_start_loc, b.seq_lens, b.block_table, sp.num_decodes,
-                              dev, kv_dtype="fp8", k_scale=0.1, v_scale=0.1)
+                              dev, common_prefix_len=32, kv_dtype="fp8", k_scale=0.1,
+                              v_scale=0.1)
     q = G.to_dev(b.query, dev)
     with pytest.raises(pka.PkaError) as e:
         pka.paged_attn_forward(q, pool, meta, torch.empty_like(q))
