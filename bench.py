@@ -519,6 +519,11 @@ def to_fp8_pool(st):
     del rows_k, rows_v, every_slot
     b.cache = pool8
     st.meta.kv_dtype, st.meta.k_scale, st.meta.v_scale = pka.KV_FP8_E4M3, k_scale, v_scale
+    # prefills over an fp8 pool need the workspace for the bf16 copy of their blocks
+    need = pka.workspace_size(st.meta, b.num_tokens, sp.num_heads, sp.num_kv_heads,
+                              sp.head_size, sp.block_size)
+    if need > st.ws.numel():
+        st.ws = torch.empty(need, dtype=torch.uint8, device=b.cache.device)
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
 
@@ -628,6 +633,20 @@ def measure_workloads(args, dev, peaks):
                     "prefill_TFLOPs": fl / (kms[1] * 1e-3) / 1e12,
                     "prefill_frac_of_bf16": fl / (kms[1] * 1e-3) / 1e12 / tf,
                     "kv_bytes_per_step": kv, "prefill_flops_per_step": fl}
+    del st
+    torch.cuda.empty_cache()
+    # the same batch over an fp8 pool (the prefills run on a bf16 copy of their blocks)
+    st = Step("mixed", dev)
+    to_fp8_pool(st)
+    kv8 = A.decode_kv_bytes(st.spec, 0, elem_bytes=1)
+    ms, kms = timed_steps(torch, pka, st, 20)
+    res["mixed_fp8"] = {"ms_per_step": ms, "decode_kernel_ms": kms[0],
+                        "prefill_kernel_ms": kms[1],
+                        "decode_GBps": kv8 / (kms[0] * 1e-3) / 1e9,
+                        "decode_frac_of_hbm": kv8 / (kms[0] * 1e-3) / 1e9 / hbm,
+                        "prefill_TFLOPs": fl / (kms[1] * 1e-3) / 1e12,
+                        "kv_bytes_per_step": kv8,
+                        "note": "step includes the copy of the prefill blocks to bf16"}
     del st
     torch.cuda.empty_cache()
     st = Step("cascade", dev)
