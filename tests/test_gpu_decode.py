@@ -142,3 +142,39 @@ def test_cascade_merge_kernel(oracle):
     pka.cascade_merge(a, la_t, W.to_device(ob, dev), torch.from_numpy(lb).to(dev), a, la_t)
     pka.check_status()
     assert torch.equal(a.view(torch.int16), out.view(torch.int16))
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_decode_batch_above_one_launch(oracle, fused):
+    """More decodes than one decode launch takes (4096): the batch runs as two
+    launches that reuse the partial slots and counters, the fused write's
+    substitution happening in each; every row checked."""
+    import torch
+
+    import paged_kv_attention_33_gb300 as pka
+
+    rng = np.random.Generator(np.random.PCG64(2400))
+    ctx = [int(x) for x in rng.integers(0, 40, size=4500)]
+    sp = _spec(8, 2, 64, 16, ctx)
+    b = W.make_batch(sp, seed=2401)
+    if not fused:
+        G.check_batch(oracle, b, label="4500 decodes")
+        return
+    dev = "cuda"
+    cache = G.to_dev(b.cache, dev)
+    meta = pka.Meta.from_host(b.query_start_loc, b.seq_lens, b.block_table, sp.num_decodes, dev)
+    q = G.to_dev(b.query, dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+    pka.paged_attn_forward_fused(q, G.to_dev(b.key, dev), G.to_dev(b.value, dev),
+                                 torch.from_numpy(b.slot_mapping).to(dev), cache, meta, out, lse,
+                                 scale=sp.softmax_scale)
+    pka.check_status()
+    want = G.host_bits(b.cache).copy()
+    oracle.reshape_and_cache(b.key, b.value, want, b.slot_mapping)
+    assert np.array_equal(want, W.to_host_bits(cache))
+    o_ref, l_ref = oracle.paged_attention(b.query, want, b.query_start_loc, b.seq_lens,
+                                          b.block_table, sp.softmax_scale, threads=8)
+    rows = np.arange(b.num_tokens * sp.num_heads, dtype=np.int64)
+    G.assert_close(G.compare(W.to_host_bits(out), lse.cpu().numpy(), o_ref, l_ref, rows,
+                             sp.num_heads), "4500 decodes fused")

@@ -300,3 +300,12 @@ def test_fp8_decode_heavy_full_size_sampled(oracle):
                                               rows=rows, threads=16)
     res = G.compare(W.to_host_bits(out), lse.cpu().numpy(), o_ref, l_ref, rows, spec.num_heads)
     G.assert_close(res, "decode_heavy fp8")
+
+
+def test_fp8_decode_batch_above_one_launch(oracle):
+    """4500 fp8 decodes: two decode launches, the fused write in each."""
+    rng = np.random.Generator(np.random.PCG64(8800))
+    ctx = [int(x) for x in rng.integers(0, 40, size=4500)]
+    sp = _decode_spec("fp8_4500", 4, 1, 16, ctx)  # one kv head keeps the pool small
+    b = W.make_batch(sp, seed=8801)
+    check_fp8(oracle, b, 0.05, 0.05, fused=True, label="4500 fp8 decodes")
