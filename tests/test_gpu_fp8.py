@@ -118,7 +118,8 @@ def _decode_spec(name, H, Hkv, bs, ctx, layout="NHD"):
 
 @pytest.mark.parametrize("Hkv,g", [(8, 1), (8, 2), (8, 3), (8, 4), (4, 8), (2, 8), (1, 8), (1, 5)])
 def test_fp8_decode_heads(oracle, Hkv, g):
-    ctx = [0, 1, 14, 15, 16, 17, 100, 255, 256, 1000, 2047, 3001]
+    # lengths around the 16-key boxes and the 32-key units (L = ctx + 1)
+    ctx = [0, 1, 14, 15, 16, 17, 30, 31, 32, 62, 63, 64, 100, 255, 256, 1000, 2047, 3001]
     sp = _decode_spec(f"fp8_{Hkv}_{g}", Hkv * g, Hkv, 16, ctx)
     b = W.make_batch(sp, seed=8000 + 10 * Hkv + g)
     check_fp8(oracle, b, 0.0625, 0.03125, label=f"Hkv={Hkv} g={g}")
