@@ -2,10 +2,15 @@
  * pka.h -- C ABI of the paged-KV attention forward for GB300 (sm_103a).
  *
  * One serving-engine attention step over a paged KV pool:
- *   pka_reshape_and_cache   write this step's K/V rows into the pool,
+ *   pka_reshape_and_cache   write this step's K/V rows into the pool
+ *                           (_ex: NHD or HND pool; _fp8: an fp8 e4m3 pool),
  *   pka_paged_attn_forward  attention of a mixed, decode-first batch over
  *                           the pool (split-KV decode, causal / chunked
- *                           prefill, optional shared-prefix cascade),
+ *                           prefill, optional shared-prefix cascade; bf16
+ *                           or fp8 e4m3 pool, NHD or HND),
+ *   pka_paged_attn_forward_fused  the two above in one call, the write done
+ *                           inside the decode launch,
+ *   pka_paged_attn_forward_noalloc  the forward without a caller workspace,
  *   pka_cascade_merge       log-sum-exp merge of two partial attentions,
  *   pka_merge_partials      the N-way merge with an explicit lse base (the
  *                           combine of a decode context-parallel step).

@@ -310,3 +310,29 @@ def test_fp8_decode_batch_above_one_launch(oracle):
     sp = _decode_spec("fp8_4500", 4, 1, 16, ctx)  # one kv head keeps the pool small
     b = W.make_batch(sp, seed=8801)
     check_fp8(oracle, b, 0.05, 0.05, fused=True, label="4500 fp8 decodes")
+
+
+@pytest.mark.parametrize("which", ["decode", "prefill"])
+def test_fp8_out_of_pool_block_is_flagged(oracle, which):
+    """A block-table entry outside an fp8 pool is never read: the decode kernel
+    (or, for a prefill, the block copy) skips it and flags it, and
+    check_status reports PKA_ERR_DEVICE_CHECK once."""
+    import torch
+
+    import paged_kv_attention_33_gb300 as pka
+
+    sp = W.BatchSpec(f"fp8_oob_{which}", 8, 1, 128, 16, decode_ctx=[40], prefill=[(20, 30)])
+    b = W.make_batch(sp, seed=8900)
+    table = b.block_table.copy()
+    row = 0 if which == "decode" else 1
+    table[row, 1] = b.num_blocks + 5
+    dev = "cuda"
+    pool = torch.from_numpy(fp8_pool(oracle, b, 0.05, 0.05)).to(dev)
+    meta = pka.Meta.from_host(b.query_start_loc, b.seq_lens, table, sp.num_decodes, dev,
+                              kv_dtype="fp8", k_scale=0.05, v_scale=0.05)
+    q = G.to_dev(b.query, dev)
+    pka.paged_attn_forward(q, pool, meta, torch.empty_like(q), scale=sp.softmax_scale)
+    with pytest.raises(pka.PkaError) as e:
+        pka.check_status()
+    assert e.value.status == -5
+    pka.check_status()  # the error word was cleared
