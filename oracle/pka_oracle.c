@@ -85,8 +85,9 @@ static double e4m3_value(uint8_t c)
 /* Nearest e4m3 code to the float y: the 127 non-negative finite codes in
  * increasing order are scanned for the closest value; a tie goes to the code
  * whose last mantissa bit is 0; |y| above 448 saturates to 448; the sign is
- * kept (also for zero); NaN gives 0x7f. */
-static uint8_t e4m3_encode(float y)
+ * kept (also for zero); NaN gives 0x7f.  mag[c] = e4m3_value(c) for the
+ * codes 0..0x7e, filled once by the caller. */
+static uint8_t e4m3_encode(float y, const double *mag)
 {
     if (y != y)
         return 0x7f;
@@ -98,7 +99,7 @@ static uint8_t e4m3_encode(float y)
     } else {
         double best_d = a; /* distance to code 0 */
         for (int c = 1; c <= 0x7e; ++c) {
-            double d = fabs(e4m3_value((uint8_t)c) - a);
+            double d = fabs(mag[c] - a);
             if (d < best_d || (d == best_d && (c & 1) == 0)) {
                 best = (uint8_t)c;
                 best_d = d;
@@ -111,10 +112,13 @@ static uint8_t e4m3_encode(float y)
 /* Codes of x[i] / scale (fp32 division) for n values (bf16 bit patterns). */
 void oracle_quantize_e4m3(const uint16_t *x, int64_t n, float scale, uint8_t *out)
 {
+    double mag[0x7f];
+    for (int c = 0; c < 0x7f; ++c)
+        mag[c] = e4m3_value((uint8_t)c);
     for (int64_t i = 0; i < n; ++i) {
         float xf = (float)bf16_value(x[i]);
         volatile float y = xf / scale; /* fp32 division, as stored */
-        out[i] = e4m3_encode(y);
+        out[i] = e4m3_encode(y, mag);
     }
 }
 
