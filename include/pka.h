@@ -242,12 +242,13 @@ size_t pka_workspace_size(const pka_meta *meta, int32_t num_tokens, int32_t num_
  * (PKA_ERR_INVALID_ARG otherwise, as [FA/FI] "Limites y fallos" and
  * [backend] "Limites y fallos" require); other shapes PKA_ERR_UNSUPPORTED.
  * An fp8 pool (meta->kv_dtype = PKA_KV_FP8_E4M3) is served at head_size 128
- * without a shared prefix (common_prefix_len 0; otherwise PKA_ERR_UNSUPPORTED):
- * K_j and V_j above are then the dequantised values code x k_scale and
- * code x v_scale.  Decodes read the codes directly; for prefill sequences the
- * forward first copies their blocks (ceil(max_seq_len / block_size) per
- * prefill sequence) into the workspace as bf16 code values, which
- * pka_workspace_size counts.
+ * (other head sizes: PKA_ERR_UNSUPPORTED): K_j and V_j above are then the
+ * dequantised values code x k_scale and code x v_scale.  Decodes read the
+ * codes directly; the tensor-core passes (prefill sequences, a cascade's
+ * shared prefix) run on copies of the blocks they read, made in the workspace
+ * as bf16 code values (ceil(max_seq_len / block_size) blocks per prefill
+ * sequence, plus common_prefix_len / block_size when decodes share a prefix),
+ * which pka_workspace_size counts.
  */
 pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const pka_meta *meta,
                                   void *out, float *lse, int32_t num_tokens, int32_t num_heads,

@@ -187,27 +187,35 @@ Workspace plan_workspace(const DecodePlan &dp, int32_t num_tokens, int32_t num_d
     if (cascade || num_tokens > num_decodes)
         off = round256(off + 2 * sizeof(int32_t));
     w.fp8_table = w.fp8_scratch = off;
-    w.fp8_blocks_per_seq = 0;
+    w.fp8_blocks_per_seq = w.fp8_prefix_blocks = 0;
+    w.fp8_scratch_blocks = 0;
     w.total = off;
     return w;
 }
 
 void plan_fp8_prefill(Workspace &w, bool kv_fp8, int32_t num_seqs, int32_t num_decodes,
-                      int32_t max_seq_len, int32_t block_size, int32_t num_kv_heads,
-                      int32_t head_size)
+                      int32_t max_seq_len, int32_t common_prefix_len, int32_t block_size,
+                      int32_t num_kv_heads, int32_t head_size)
 {
     const int32_t nprefill = num_seqs - num_decodes;
-    if (!kv_fp8 || nprefill <= 0)
+    const bool cascade = common_prefix_len > 0;
+    if (!kv_fp8 || (nprefill <= 0 && !cascade))
         return;
     const int32_t mb = (max_seq_len + block_size - 1) / block_size;
+    // the shared prefix is read through row 0; a decode there has no copy of
+    // its own, so its first P/bs blocks get one
+    const int32_t pb = cascade && num_decodes > 0 ? common_prefix_len / block_size : 0;
     size_t off = w.total;
     // the table first: a read past its last row (a length above max_seq_len,
     // flagged) stays inside the workspace
     w.fp8_table = off;
     off = round256(off + size_t(num_seqs) * mb * 4);
     w.fp8_scratch = off;
-    off = round256(off + size_t(nprefill) * mb * 2 * block_size * num_kv_heads * head_size * 2);
+    w.fp8_scratch_blocks = int64_t(nprefill) * mb + pb;
+    off = round256(off + size_t(w.fp8_scratch_blocks) * 2 * block_size * num_kv_heads *
+                             head_size * 2);
     w.fp8_blocks_per_seq = mb;
+    w.fp8_prefix_blocks = pb;
     w.total = off;
 }
 
@@ -271,8 +279,6 @@ static pka_status check_shape(const pka_meta *m, int32_t num_tokens, int32_t num
         if (head_size != 128)
             return fail(PKA_ERR_UNSUPPORTED, "fp8 pool: head_size %d is not built (128)",
                         head_size);
-        if (m->common_prefix_len > 0)
-            return fail(PKA_ERR_UNSUPPORTED, "fp8 pool: no shared-prefix cascade");
     }
     return PKA_OK;
 }
@@ -388,7 +394,8 @@ size_t pka_workspace_size(const pka_meta *meta, int32_t num_tokens, int32_t num_
     Workspace w = plan_workspace(dp, num_tokens, meta->num_decodes, num_heads, head_size, cascade,
                                  pre_splits);
     plan_fp8_prefill(w, meta->kv_dtype == PKA_KV_FP8_E4M3, meta->num_seqs, meta->num_decodes,
-                     meta->max_seq_len, block_size, num_kv_heads, head_size);
+                     meta->max_seq_len, meta->common_prefix_len, block_size, num_kv_heads,
+                     head_size);
     return w.total;
 }
 
@@ -478,9 +485,8 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
     Workspace ws = plan_workspace(dp, num_tokens, meta->num_decodes, num_heads, head_size, cascade,
                                   pre_splits);
     plan_fp8_prefill(ws, f.kv_fp8 != 0, meta->num_seqs, meta->num_decodes, meta->max_seq_len,
-                     block_size, num_kv_heads, head_size);
-    if (ws.fp8_blocks_per_seq > 0 &&
-        int64_t(num_prefills) * ws.fp8_blocks_per_seq * 2 * block_size >= (int64_t(1) << 31))
+                     meta->common_prefix_len, block_size, num_kv_heads, head_size);
+    if (ws.fp8_scratch_blocks * 2 * block_size >= (int64_t(1) << 31))
         return fail(PKA_ERR_UNSUPPORTED, "fp8 prefill copy has more than 2^31 rows");
     if (ws.total > 0 && (!workspace || workspace_bytes < ws.total || !aligned(workspace, 256)))
         return fail(PKA_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)",
@@ -494,6 +500,34 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
         return fail(PKA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(cr));
 
     cudaError_t e;
+    // An fp8 pool: the tensor-core prefill (prefill sequences, the cascade's
+    // shared prefix) runs on bf16 copies of the blocks it reads, made in the
+    // workspace as exact code values, with k_scale in the score scale and
+    // v_scale on the output; the decodes read the codes themselves.
+    Fwd fp = f;
+    int32_t *fp8_table = reinterpret_cast<int32_t *>(wsp + ws.fp8_table);
+    void *fp8_scratch = wsp + ws.fp8_scratch;
+    const int32_t mb = ws.fp8_blocks_per_seq;
+    if (f.kv_fp8 && ws.fp8_scratch_blocks > 0) {
+        fp.kv_cache = fp8_scratch;
+        fp.block_table = fp8_table;
+        fp.bt_stride = mb;
+        fp.num_blocks = ws.fp8_scratch_blocks;
+        fp.kv_hnd = 0;
+        fp.kv_fp8 = 0;
+        fp.scale = f.scale * f.k_scale;
+        fp.out_scale = f.v_scale;
+        // before any pass: the prefill rows' copies when no decode launch writes
+        // new rows first (the prefix is then row 0's own copy), else the prefix
+        // blocks of row 0 (no new row lies in the prefix)
+        if (meta->num_decodes == 0)
+            e = launch_dequant_blocks(f, fp8_scratch, fp8_table, 0, num_prefills, mb, mb, 0, mb);
+        else
+            e = launch_dequant_blocks(f, fp8_scratch, fp8_table, 0, 1, 0, ws.fp8_prefix_blocks,
+                                      int64_t(num_prefills) * mb, mb);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "fp8 block copy launch");
+    }
     if (cascade) {
         // [blog] "Que aporta FlashInfer: JIT y cascade attention": the shared
         // prefix once for every query (tensor cores, no mask), each sequence's
@@ -502,7 +536,7 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
                         reinterpret_cast<float *>(wsp + ws.lse_pre), 0,
                         reinterpret_cast<int32_t *>(wsp + ws.pf_counters) + 1, pre_splits};
         record_start(PKA_KERNEL_PREFILL, f.stream);
-        e = launch_prefill(f, pre);
+        e = launch_prefill(fp, pre);
         record_stop(PKA_KERNEL_PREFILL, f.stream);
         if (e != cudaSuccess)
             return cuda_fail(e, "cascade prefix launch");
@@ -517,24 +551,13 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
                        cascade ? reinterpret_cast<float *>(wsp + ws.o_suf) : nullptr,
                        cascade ? reinterpret_cast<float *>(wsp + ws.lse_suf) : nullptr,
                        meta->num_decodes, reinterpret_cast<int32_t *>(wsp + ws.pf_counters)};
-        // an fp8 pool: the prefill sequences' blocks are first copied out as bf16
-        // code values (exact) into the workspace, and the tensor-core prefill runs
-        // on that copy with k_scale in the score scale and v_scale on the output
-        Fwd fp = f;
-        if (f.kv_fp8) {
-            int32_t *table = reinterpret_cast<int32_t *>(wsp + ws.fp8_table);
-            void *scratch = wsp + ws.fp8_scratch;
-            e = launch_dequant_prefill_blocks(f, scratch, table, ws.fp8_blocks_per_seq);
+        // fp8 after the decode launch (which wrote this step's rows): the
+        // prefill sequences' blocks
+        if (f.kv_fp8 && meta->num_decodes > 0) {
+            e = launch_dequant_blocks(f, fp8_scratch, fp8_table, meta->num_decodes, num_prefills,
+                                      mb, mb, 0, mb);
             if (e != cudaSuccess)
-                return cuda_fail(e, "fp8 prefill copy launch");
-            fp.kv_cache = scratch;
-            fp.block_table = table;
-            fp.bt_stride = ws.fp8_blocks_per_seq;
-            fp.num_blocks = int64_t(num_prefills) * ws.fp8_blocks_per_seq;
-            fp.kv_hnd = 0;
-            fp.kv_fp8 = 0;
-            fp.scale = f.scale * f.k_scale;
-            fp.out_scale = f.v_scale;
+                return cuda_fail(e, "fp8 block copy launch");
         }
         if (!cascade)
             record_start(PKA_KERNEL_PREFILL, f.stream);

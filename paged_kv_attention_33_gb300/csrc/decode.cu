@@ -914,11 +914,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             if (ok) {
                 float sc0 = i0, sc1 = i1;  // row scales of the output
                 float ls0 = m0 + log2f(lr0), ls1 = m1 + log2f(lr1);  // log2-sum-exp
-                if constexpr (!kFp8) {  // no cascade over an fp8 pool
-                    if (p.cascade)
-                        merge_prefix_direct<D>(p, t, k * g + min(n0, g - 1),
-                                               k * g + min(n1, g - 1), gq, o, sc0, sc1, ls0, ls1);
-                }
+                if (p.cascade)  // (both pools: o holds dims 16*mt + gq and +8)
+                    merge_prefix_direct<D>(p, t, k * g + min(n0, g - 1), k * g + min(n1, g - 1),
+                                           gq, o, sc0, sc1, ls0, ls1);
 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt) {  // dims 16*mt + gq and +8
                     const int d = 16 * mt + gq;
@@ -1140,7 +1138,7 @@ cudaError_t launch_decode(const Fwd &f, const DecodePlan &dp, const Workspace &w
     if (f.num_decodes == 0)
         return cudaSuccess;
     if (f.kv_fp8) {  // head_size 128 only (checked by the caller)
-        if (f.head_size != 128 || cascade)
+        if (f.head_size != 128)
             return cudaErrorInvalidValue;
         return f.kv_hnd
                    ? launch_decode_d<128, true, true>(f, dp, ws, wsp, kv_map, kv_begin, cascade)

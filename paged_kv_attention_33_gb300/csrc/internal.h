@@ -66,11 +66,15 @@ struct Workspace {
     int32_t pre_splits;        // cascade: key chunks of the shared-prefix pass
     size_t o_suf, lse_suf;     // cascade: suffix partial of every prefill token
     size_t pf_counters;        // prefill work-queue counters (int32 x 2)
-    // fp8 pool with prefills: the prefill sequences' blocks as bf16 code values
-    // (fp8_blocks_per_seq = ceil(max_seq_len / bs) blocks per prefill sequence)
-    // and their block table ([num_seqs, fp8_blocks_per_seq] int32)
+    // fp8 pool with prefills or a cascade: the prefill sequences' blocks as bf16
+    // code values (fp8_blocks_per_seq = ceil(max_seq_len / bs) blocks per prefill
+    // sequence), then (cascade with decodes) the shared prefix's fp8_prefix_blocks
+    // blocks of block-table row 0, and their block table ([num_seqs,
+    // fp8_blocks_per_seq] int32)
     size_t fp8_scratch, fp8_table;
     int32_t fp8_blocks_per_seq;
+    int32_t fp8_prefix_blocks;
+    int64_t fp8_scratch_blocks;
     size_t total;
 };
 
@@ -87,8 +91,8 @@ Workspace plan_workspace(const DecodePlan &dp, int32_t num_tokens, int32_t num_d
 // The fp8 prefill copy: blocks per prefill sequence and bytes of the bf16 scratch pool
 // (0 when the pool is bf16 or there are no prefills); appended to a planned workspace.
 void plan_fp8_prefill(Workspace &w, bool kv_fp8, int32_t num_seqs, int32_t num_decodes,
-                      int32_t max_seq_len, int32_t block_size, int32_t num_kv_heads,
-                      int32_t head_size);
+                      int32_t max_seq_len, int32_t common_prefix_len, int32_t block_size,
+                      int32_t num_kv_heads, int32_t head_size);
 
 // kv_write.cu
 cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *cache,
@@ -101,10 +105,13 @@ cudaError_t launch_reshape_and_cache_fp8(const void *key, const void *value, voi
                                          int32_t num_kv_heads, int32_t head_size,
                                          int32_t block_size, int64_t num_blocks, int32_t hnd,
                                          float k_scale, float v_scale, cudaStream_t st);
-// The prefill sequences' blocks of an fp8 pool (f.kv_cache, layout f.kv_hnd)
-// as bf16 code values in a dense NHD scratch pool, and its block table.
-cudaError_t launch_dequant_prefill_blocks(const Fwd &f, void *scratch, int32_t *table,
-                                          int32_t max_blocks);
+// Blocks of an fp8 pool (f.kv_cache, layout f.kv_hnd) as bf16 code values in a
+// dense NHD scratch pool and its block table: block-table rows [first_row,
+// first_row + num_rows), columns below min(ceil(L/bs), col_limit), row p at
+// scratch blocks dst_base + p*row_blocks + n, table rows of stride table_stride.
+cudaError_t launch_dequant_blocks(const Fwd &f, void *scratch, int32_t *table, int32_t first_row,
+                                  int32_t num_rows, int32_t row_blocks, int32_t col_limit,
+                                  int64_t dst_base, int32_t table_stride);
 uint32_t kv_write_take_error();
 
 // decode.cu: paged decode of sequences [0, num_decodes) over keys

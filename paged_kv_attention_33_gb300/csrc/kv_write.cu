@@ -156,30 +156,33 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *c
     return cudaGetLastError();
 }
 
-// The blocks of the prefill sequences of an fp8 pool as bf16 code values (no
-// scale: every e4m3 value is exact in bf16; the attention applies k_scale and
-// v_scale) in a dense NHD scratch pool: CTA (p, n) takes block column n of
-// prefill sequence s = first_seq + p, copies pool block bt[s][n] to scratch
-// block p*max_blocks + n and writes that id into the scratch table at [s][n].
-// Columns past ceil(L_s / bs) are left alone (the attention never reads them).
+// Blocks of an fp8 pool as bf16 code values (no scale: every e4m3 value is
+// exact in bf16; the attention applies k_scale and v_scale) in a dense NHD
+// scratch pool: CTA (p, n) takes block column n of block-table row s =
+// first_row + p, copies pool block bt[s][n] to scratch block dst_base +
+// p*row_blocks + n and writes that id into the scratch table at [s][n] (row
+// stride table_stride).  Columns at or past min(ceil(L_s / bs), col_limit) are
+// left alone (the attention never reads them).
 __global__ void __launch_bounds__(kKvwThreads)
-    dequant_prefill_blocks_kernel(const uint4 *__restrict__ pool, uint4 *__restrict__ scratch,
-                                  int32_t *__restrict__ table, const int32_t *__restrict__ bt,
-                                  int32_t bt_stride, const int32_t *__restrict__ seq_lens,
-                                  int32_t first_seq, int32_t max_blocks, int32_t block_size,
-                                  int32_t num_kv_heads, int32_t head_chunks, int64_t num_blocks,
-                                  int32_t hnd)
+    dequant_blocks_kernel(const uint4 *__restrict__ pool, uint4 *__restrict__ scratch,
+                          int32_t *__restrict__ table, const int32_t *__restrict__ bt,
+                          int32_t bt_stride, const int32_t *__restrict__ seq_lens,
+                          int32_t first_row, int32_t row_blocks, int32_t col_limit,
+                          int64_t dst_base, int32_t table_stride, int32_t block_size,
+                          int32_t num_kv_heads, int32_t head_chunks, int64_t num_blocks,
+                          int32_t hnd)
 {
     const int32_t p = blockIdx.y, n = blockIdx.x;
-    const int32_t s = first_seq + p;
+    const int32_t s = first_row + p;
     const int32_t L = seq_lens[s];
-    if (n == 0 && threadIdx.x == 0 && int64_t(L) > int64_t(max_blocks) * block_size)
+    if (n == 0 && threadIdx.x == 0 && col_limit == row_blocks &&
+        int64_t(L) > int64_t(row_blocks) * block_size)
         flag_error(kErrBadMetadata);  // longer than max_seq_len: its tail was not copied
-    if (n * block_size >= L)
+    if (n >= col_limit || n * block_size >= L)
         return;
-    const int64_t dst_blk = int64_t(p) * max_blocks + n;
+    const int64_t dst_blk = dst_base + int64_t(p) * row_blocks + n;
     if (threadIdx.x == 0)
-        table[int64_t(s) * max_blocks + n] = static_cast<int32_t>(dst_blk);
+        table[int64_t(s) * table_stride + n] = static_cast<int32_t>(dst_blk);
     const int32_t src_blk = bt[int64_t(s) * bt_stride + n];
     if (src_blk < 0 || src_blk >= num_blocks) {
         if (threadIdx.x == 0)
@@ -213,18 +216,18 @@ __global__ void __launch_bounds__(kKvwThreads)
     }
 }
 
-cudaError_t launch_dequant_prefill_blocks(const Fwd &f, void *scratch, int32_t *table,
-                                          int32_t max_blocks)
+cudaError_t launch_dequant_blocks(const Fwd &f, void *scratch, int32_t *table, int32_t first_row,
+                                  int32_t num_rows, int32_t row_blocks, int32_t col_limit,
+                                  int64_t dst_base, int32_t table_stride)
 {
-    const int32_t nprefill = f.num_seqs - f.num_decodes;
-    if (nprefill <= 0 || max_blocks <= 0)
+    if (num_rows <= 0 || col_limit <= 0)
         return cudaSuccess;
     count_launch();
-    dim3 grid(static_cast<unsigned>(max_blocks), static_cast<unsigned>(nprefill));
-    dequant_prefill_blocks_kernel<<<grid, kKvwThreads, 0, f.stream>>>(
+    dim3 grid(static_cast<unsigned>(col_limit), static_cast<unsigned>(num_rows));
+    dequant_blocks_kernel<<<grid, kKvwThreads, 0, f.stream>>>(
         static_cast<const uint4 *>(f.kv_cache), static_cast<uint4 *>(scratch), table,
-        f.block_table, f.bt_stride, f.seq_lens, f.num_decodes, max_blocks, f.block_size,
-        f.num_kv_heads, f.head_size / 16, f.num_blocks, f.kv_hnd);
+        f.block_table, f.bt_stride, f.seq_lens, first_row, row_blocks, col_limit, dst_base,
+        table_stride, f.block_size, f.num_kv_heads, f.head_size / 16, f.num_blocks, f.kv_hnd);
     return cudaGetLastError();
 }
 

@@ -182,8 +182,8 @@ def test_fused_forward_arguments(lib):
 
 def test_fp8_pool_arguments(lib):
     """kv_dtype is one of the two pool element types; an fp8 pool needs
-    positive finite scales and is served at head_size 128 without a shared
-    prefix (UNSUPPORTED otherwise, before any work)."""
+    positive finite scales and is served at head_size 128 (UNSUPPORTED
+    otherwise, before any work)."""
     fp8 = dict(kv_dtype=pka.KV_FP8_E4M3, k_scale=0.5, v_scale=2.0)
     assert pka._CMeta().kv_dtype == pka.KV_BF16  # a zero-initialised meta is bf16
     assert _fwd(lib, _meta(kv_dtype=2)) == -1
@@ -192,7 +192,11 @@ def test_fp8_pool_arguments(lib):
         assert _fwd(lib, _meta(**{**fp8, "k_scale": bad}), D=128) == -1
         assert _fwd(lib, _meta(**{**fp8, "v_scale": bad}), D=128) == -1
     assert _fwd(lib, _meta(**fp8), D=64) == -2                        # head_size 64
-    assert _fwd(lib, _meta(common_prefix_len=16, **fp8), D=128) == -2  # cascade
+    # a cascade over fp8 is served: its shared prefix gets a bf16 copy too
+    casc8 = _meta(common_prefix_len=16, **fp8)
+    w_c8 = lib.pka_workspace_size(ctypes.byref(casc8), 2, 8, 2, 128, 16)
+    w_c16 = lib.pka_workspace_size(ctypes.byref(_meta(common_prefix_len=16)), 2, 8, 2, 128, 16)
+    assert w_c8 - w_c16 >= 1 * 2 * 16 * 2 * 128 * 2  # one prefix block
     assert lib.pka_workspace_size(ctypes.byref(_meta(**fp8)), 2, 8, 2, 64, 16) == 0
     # a bf16 meta ignores the scales
     assert lib.pka_workspace_size(ctypes.byref(_meta(k_scale=-1.0)), 2, 8, 2, 64, 16) > 0
@@ -206,9 +210,9 @@ def test_fp8_pool_arguments(lib):
     assert w8 - w16 >= blocks * 2 * 16 * 2 * 128 * 2 + 2 * blocks * 4
     assert _fwd(lib, mixed8, T=5, D=128) == -3  # served, but needs that workspace
     # the fused entry refuses an unserved fp8 batch before writing anything
-    m = _meta(num_decodes=0, max_query_len=4, common_prefix_len=16, **fp8)
+    m = _meta(num_decodes=0, max_query_len=4, **fp8)
     assert lib.pka_paged_attn_forward_fused(256, 256, 256, 256, 512, ctypes.byref(m), 1024, None,
-                                            5, 8, 2, 128, 16, 64, 0.125, 1, None, 0, None) == -2
+                                            5, 8, 2, 64, 16, 64, 0.125, 1, None, 0, None) == -2
 
 
 def test_fp8_cache_write_arguments(lib):

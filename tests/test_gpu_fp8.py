@@ -44,6 +44,7 @@ def run_fp8(batch, pool8, k_scale, v_scale, split_kv_tokens=0, fused=False, quer
     slots = torch.from_numpy(batch.slot_mapping).to(dev)
     meta = pka.Meta.from_host(batch.query_start_loc, batch.seq_lens, batch.block_table,
                               sp.num_decodes, dev, split_kv_tokens=split_kv_tokens,
+                              common_prefix_len=sp.common_prefix_len,
                               kv_layout=sp.kv_layout, kv_dtype="fp8", k_scale=k_scale,
                               v_scale=v_scale)
     T = batch.num_tokens
@@ -241,19 +242,35 @@ def test_fp8_mixed_full_size_sampled(oracle):
     G.assert_close(res, "mixed fp8")
 
 
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+@pytest.mark.parametrize("kind", ["decodes", "mixed", "prefills"])
+def test_fp8_cascade(oracle, layout, kind):
+    """A shared-prefix cascade over an fp8 pool: the prefix pass and the
+    prefill suffixes run on bf16 copies of their blocks (the prefix read through
+    row 0: a decode's blocks copied for it, or a prefill's own copy), the decode
+    suffixes read the codes and merge the prefix partials in the kernel."""
+    P = 256
+    dec = {"decodes": [P + 3, P + 40, P + 700, P + 33], "mixed": [P + 10, P + 500],
+           "prefills": []}[kind]
+    pre = {"decodes": [], "mixed": [(40, P), (150, P + 20)], "prefills": [(60, P), (129, P + 5)]}[kind]
+    sp = W.BatchSpec(f"fp8_casc_{kind}_{layout}", 32, 8, 128, 16, decode_ctx=dec, prefill=pre,
+                     common_prefix_len=P, kv_layout=layout)
+    b = W.make_batch(sp, seed=8950 + len(dec) + len(pre))
+    check_fp8(oracle, b, 0.05, 0.04, label=f"cascade {kind} {layout}")
+    check_fp8(oracle, b, 0.05, 0.04, fused=True, label=f"cascade {kind} {layout} fused")
+
+
 def test_fp8_unserved_batches_are_refused(oracle):
     import torch
 
     import paged_kv_attention_33_gb300 as pka
 
-    sp = W.BatchSpec("fp8_cascade", 16, 4, 128, 16, decode_ctx=[40, 50], prefill=[(20, 35)],
-                     common_prefix_len=32)
+    sp = W.BatchSpec("fp8_d64", 16, 4, 64, 16, decode_ctx=[40, 50], prefill=[(20, 35)])
     b = W.make_batch(sp, seed=8500)
     dev = G.device()
     pool = torch.from_numpy(fp8_pool(oracle, b, 0.1, 0.1)).to(dev)
     meta = pka.Meta.from_host(b.query_start_loc, b.seq_lens, b.block_table, sp.num_decodes,
-                              dev, common_prefix_len=32, kv_dtype="fp8", k_scale=0.1,
-                              v_scale=0.1)
+                              dev, kv_dtype="fp8", k_scale=0.1, v_scale=0.1)
     q = G.to_dev(b.query, dev)
     with pytest.raises(pka.PkaError) as e:
         pka.paged_attn_forward(q, pool, meta, torch.empty_like(q))
