@@ -663,6 +663,13 @@ def measure_workloads(args, dev, peaks):
                       "cascade_GBps_step": casc * row / (ms * 1e-3) / 1e9,
                       "naive_equivalent_GBps_step": naive * row / (ms * 1e-3) / 1e9,
                       "bytes_read_cascade": casc * row, "bytes_read_naive": naive * row}
+    # the same over an fp8 pool (the prefix pass runs on a bf16 copy of its blocks)
+    to_fp8_pool(st)
+    ms, kms = timed_steps(torch, pka, st, 20)
+    res["cascade_fp8"] = {"ms_per_step": ms, "decode_kernel_ms": kms[0],
+                          "prefix_pass_ms": kms[1],
+                          "suffix_GBps": kv / 2 / (kms[0] * 1e-3) / 1e9,
+                          "note": "step includes the copy of the prefix blocks to bf16"}
     del st
     torch.cuda.empty_cache()
     st = Step("decode_heavy", dev)
