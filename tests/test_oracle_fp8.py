@@ -110,3 +110,43 @@ def test_fp8_cache_write_is_the_quantised_row(oracle):
     for slot in b.slot_mapping:
         mask[slot // sp.block_size, :, slot % sp.block_size] = True
     assert not cache8[~mask].any()
+
+
+@pytest.mark.parametrize("k_scale,v_scale", [(0.0371, 0.0173), (1.3, 0.77)])
+def test_fp8_attention_equals_dense_softmax_with_any_scale(oracle, k_scale, v_scale):
+    """With scales that are not powers of two the dequantised values are not
+    bf16 values; the fp8 attention must still be the dense softmax over
+    code_value * scale (gathered through the block table, causal), computed
+    here in numpy float64 from the codes."""
+    sp = W.BatchSpec("fp8dense", 4, 2, 128, 16, decode_ctx=[7, 33], prefill=[(5, 20)])
+    b = W.make_batch(sp, seed=63)
+    cache = b.cache.copy()
+    oracle.reshape_and_cache(b.key, b.value, cache, b.slot_mapping)
+    cache[np.isnan(W.bf16_bits_to_f32(cache))] = 0
+    codes = np.empty(cache.shape, dtype=np.uint8)
+    codes[:, 0] = oracle.quantize_e4m3(cache[:, 0], k_scale)
+    codes[:, 1] = oracle.quantize_e4m3(cache[:, 1], v_scale)
+    o8, l8 = oracle.paged_attention_fp8(b.query, codes, k_scale, v_scale, b.query_start_loc,
+                                        b.seq_lens, b.block_table, sp.softmax_scale)
+    table = oracle.e4m3_value(np.arange(256, dtype=np.uint8))
+    q = W.bf16_bits_to_f32(b.query).astype(np.float64)
+    H, Hkv, D, bs = sp.num_heads, sp.num_kv_heads, sp.head_size, sp.block_size
+    g = H // Hkv
+    for s in range(len(b.seq_lens)):
+        L = int(b.seq_lens[s])
+        t0, t1 = int(b.query_start_loc[s]), int(b.query_start_loc[s + 1])
+        keys = np.arange(L)
+        blk = b.block_table[s][keys // bs]
+        K = table[codes[blk, 0, keys % bs]] * np.float64(np.float32(k_scale))  # [L, Hkv, D]
+        V = table[codes[blk, 1, keys % bs]] * np.float64(np.float32(v_scale))
+        for i, t in enumerate(range(t0, t1)):
+            allowed = L - (t1 - t0) + i + 1  # bottom-right causal
+            for h in range(H):
+                x = sp.softmax_scale * (K[:allowed, h // g] @ q[t, h])
+                m = x.max()
+                w = np.exp(x - m)
+                lse = m + np.log(w.sum())
+                out = (w / w.sum()) @ V[:allowed, h // g]
+                r = t * H + h
+                assert abs(l8[r] - lse) <= 1e-12 * max(1.0, abs(lse))
+                assert np.max(np.abs(o8[r] - out)) <= 1e-12
