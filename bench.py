@@ -606,6 +606,32 @@ def timed_steps(torch, pka, st, steps, kernels=(0, 1), run=None):
     return ms, kms
 
 
+def graph_step_ms(torch, st, steps):
+    """Mean step time when the step is captured once in a CUDA graph and
+    replayed (how a serving loop removes the per-launch host overhead)."""
+    st.run()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            st.run()
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    st.pka.check_status()
+    return e0.elapsed_time(e1) / steps
+
+
 def measure_workloads(args, dev, peaks):
     """The other configurations of the method, one short timed run each (20 steps
     after 3 warm-ups, CUDA events): tiny_decode (latency), mixed (decode GB/s and
@@ -622,7 +648,8 @@ def measure_workloads(args, dev, peaks):
     st = Step("tiny_decode", dev)
     ms, kms = timed_steps(torch, pka, st, 20)
     res["tiny_decode"] = {"ms_per_step": ms, "decode_kernel_ms": kms[0],
-                          "bound": "latency (0.2 MB of KV)"}
+                          "bound": "latency (0.2 MB of KV)",
+                          "graph_replay_ms_per_step": graph_step_ms(torch, st, 20)}
     del st
     st = Step("mixed", dev)
     kv, fl = units(st.spec)
