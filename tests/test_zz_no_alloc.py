@@ -85,3 +85,38 @@ def test_noalloc_rejects_batches_above_its_scratch():
     assert rc == -3
     msg = lib.pka_last_error().decode()
     assert "16777216" in msg and str(need) in msg
+
+
+@pytest.mark.gpu
+def test_noalloc_over_an_fp8_pool(oracle):
+    """An fp8 mixed batch small enough that its partials and the bf16 copy of
+    its prefill blocks fit the built-in scratch: the same rows as the
+    workspace entry point, twice in a row."""
+    import torch
+
+    spec = W.BatchSpec("na8", 16, 4, 128, 16, decode_ctx=[40, 700], prefill=[(64, 100)])
+    b = W.make_batch(spec, seed=5002)
+    c = G.host_bits(b.cache)
+    p8 = np.empty(c.shape, dtype=np.uint8)
+    p8[:, 0] = oracle.quantize_e4m3(np.ascontiguousarray(c[:, 0]), 0.05)
+    p8[:, 1] = oracle.quantize_e4m3(np.ascontiguousarray(c[:, 1]), 0.03)
+    dev = "cuda"
+    pool = torch.from_numpy(p8).to(dev)
+    pka.reshape_and_cache_fp8(G.to_dev(b.key, dev), G.to_dev(b.value, dev), pool,
+                              torch.from_numpy(b.slot_mapping).to(dev), 0.05, 0.03)
+    meta = pka.Meta.from_host(b.query_start_loc, b.seq_lens, b.block_table, spec.num_decodes,
+                              dev, kv_dtype="fp8", k_scale=0.05, v_scale=0.03)
+    need = pka.workspace_size(meta, b.num_tokens, spec.num_heads, spec.num_kv_heads,
+                              spec.head_size, spec.block_size)
+    assert 0 < need <= 16 << 20
+    q = G.to_dev(b.query, dev)
+    ref = torch.empty_like(q)
+    ref_lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+    pka.paged_attn_forward(q, pool, meta, ref, ref_lse, scale=spec.softmax_scale)
+    for _ in range(2):
+        out = torch.full_like(q, float("nan"))
+        lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device=dev)
+        pka.paged_attn_forward_noalloc(q, pool, meta, out, lse, scale=spec.softmax_scale)
+        pka.check_status()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+        assert torch.equal(lse, ref_lse)
