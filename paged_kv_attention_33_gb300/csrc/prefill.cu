@@ -525,7 +525,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     tc_fence_after();
     const uint32_t tbase = *tmem_holder;
 
-    if (warp < 4) {
+    // All 512 columns belong to this CTA, so the allocation starts at lane 0,
+    // column 0: the MMA issuer's TMEM addresses are compile-time constants.
+    if (tbase != 0) {
+        if (threadIdx.x == 0)
+            flag_error(kErrTmemAlloc);
+    } else if (warp < 4) {
         reg_dealloc<104>();
         if (warp == 0) {
             // ============================================================ producer
@@ -643,15 +648,21 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             }
         } else if (warp == 1) {
             // ============================================================ MMA issuer
-            // Operand descriptors are built once; a k-step or a stage only moves
-            // the start-address field (16-byte units, no carry out of 14 bits as
-            // every tile lies below 256 KB), so each MMA costs one 64-bit add.
-            const uint64_t dQ0 = smem_desc_sw128(smem_addr(smem + Cfg::kQOff), 16, 1024);
-            const uint64_t dK0 = smem_desc_sw128(smem_addr(smem + Cfg::kKOff), 16, 1024);
-            const uint64_t dV0 =
-                smem_desc_sw128(smem_addr(smem + Cfg::kVOff), Cfg::kHalfBytes, 1024);
-            constexpr uint64_t kTileStep = Cfg::kTileBytes >> 4;
+            // One elected lane issues every MMA and commit.  At N = 128 an MMA
+            // runs 64 cycles, so the issue has to keep up while the softmax warps
+            // of the same sub-partitions compete for the scheduler: TMEM addresses
+            // are constants (the allocation starts at 0) and a shared-memory
+            // descriptor is its low word alone (start address and LBO; the high
+            // word is common to all operands), so that a k-step or a stage costs
+            // one 32-bit add.  Every tile lies below 256 KB of shared memory, so
+            // the add never carries out of the 14-bit start-address field.
+            const uint32_t q_lo0 = smem_desc_lo(smem_addr(smem + Cfg::kQOff), 16);
+            const uint32_t k_lo0 = smem_desc_lo(smem_addr(smem + Cfg::kKOff), 16);
+            const uint32_t v_lo0 = smem_desc_lo(smem_addr(smem + Cfg::kVOff), Cfg::kHalfBytes);
+            constexpr uint32_t kTileStep = Cfg::kTileBytes >> 4;
             uint32_t li = 0, kv_it = 0;
+            // per Q tile: P tiles consumed, items that used the tile (registers:
+            // the tile loop below is unrolled, so every index is a constant)
             uint32_t p_cnt[2] = {0, 0}, item_cnt[2] = {0, 0};
             PfItem it;
             bool ok = true;
@@ -666,6 +677,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     break;
                 tc_fence_after();
                 const int n = it.n_kv_all;
+                const int nk[2] = {it.n_kv[0], it.n_kv[1]};
+                const int kv_lo = it.kv_lo, kv_hi = it.kv_hi;
                 for (int jt = 0; jt <= n && ok; ++jt) {
                     const uint32_t kn = kv_it + jt;
                     const int st = kn % kPfStages;
@@ -676,21 +689,24 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                         }
                         tc_fence_after();
                     }
-                    for (int tl = 0; tl < 2 && ok; ++tl) {
-                        const int nk = it.n_kv[tl];
+#pragma unroll
+                    for (int tl = 0; tl < 2; ++tl) {
                         // ---- O_tl += P_tl V of the previous K/V tile
-                        if (jt > 0 && jt - 1 < nk) {
+                        if (jt > 0 && jt - 1 < nk[tl]) {
                             const int jp = jt - 1;
                             const uint32_t pn = kv_it + jp;
                             const int pst = pn % kPfStages;
+                            // tile B reads the V tile that tile A has just waited for
+                            // when both attend it
+                            const bool first_reader = tl == 0 || jp >= nk[0];
                             if (!pf_wait(&bars.p_full[tl], p_cnt[tl] & 1, abort_flag) ||
-                                !pf_wait(&bars.v_full[pst], (pn / kPfStages) & 1, abort_flag)) {
+                                (first_reader &&
+                                 !pf_wait(&bars.v_full[pst], (pn / kPfStages) & 1, abort_flag))) {
                                 ok = false;
                                 break;
                             }
                             ++p_cnt[tl];
-                            const int nvalid = it.kv_hi - (it.kv_lo + jp * kBN);
-                            const bool first_reader = tl == 0 || jp >= it.n_kv[0];
+                            const int nvalid = kv_hi - (kv_lo + jp * kBN);
                             if (jp == n - 1 && nvalid < kBN && first_reader) {
                                 // rows past the last key may hold anything (or nothing
                                 // was loaded there): zero them once, before the first
@@ -712,34 +728,39 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                                 break;
                             }
                             tc_fence_after();
-                            const uint64_t dV = dV0 + pst * kTileStep;
-                            if (lane == 0) {
-                                const uint32_t tO_ = tbase + 256 + tl * D;
-                                const uint32_t tP_ = tbase + tl * 128;
-                                mma_ts(tO_, tP_, dV, Cfg::kIdescPV, jp > 0 ? 1u : 0u);
+                            const uint32_t v_lo = v_lo0 + pst * kTileStep;
+                            const uint32_t tO_ = 256 + tl * D;
+                            const uint32_t tP_ = tl * 128;
+                            const uint32_t acc0 = jp > 0 ? 1u : 0u;
+                            const bool last_v = tl == (jp < nk[1] ? 1 : 0);
+                            if (elect_one()) {
+                                mma_ts(tO_, tP_, v_lo, Cfg::kIdescPV, acc0);
 #pragma unroll
                                 for (int k = 1; k < kBN / 16; ++k)
-                                    mma_ts(tO_, tP_ + k * 8, dV + uint64_t(k * 2048 >> 4),
+                                    mma_ts(tO_, tP_ + k * 8, v_lo + uint32_t(k * 2048 >> 4),
                                            Cfg::kIdescPV, 1u);
                                 mma_commit(&bars.o_done[tl]);
-                                if (tl == (jp < it.n_kv[1] ? 1 : 0))
+                                if (last_v)
                                     mma_commit(&bars.v_empty[pst]);  // last reader of V(jp)
                             }
                             __syncwarp();
                         }
                         // ---- S_tl = Q_tl K^T of this K/V tile
-                        if (jt < nk) {
-                            const uint64_t dK = dK0 + st * kTileStep;
-                            const uint64_t dQ = dQ0 + tl * kTileStep;
-                            if (lane == 0) {
-                                const uint32_t tS_ = tbase + tl * 128;
+                        if (jt < nk[tl]) {
+                            const uint32_t k_lo = k_lo0 + st * kTileStep;
+                            const uint32_t tS_ = tl * 128;
+                            const uint32_t q_lo = q_lo0 + tl * kTileStep;
+                            const bool last_k = tl == (jt < nk[1] ? 1 : 0);
+                            if (elect_one()) {
 #pragma unroll
                                 for (int k = 0; k < D / 16; ++k) {
-                                    const uint64_t off = ((k >> 2) * Cfg::kHalfBytes + (k & 3) * 32) >> 4;
-                                    mma_ss(tS_, dQ + off, dK + off, Cfg::kIdescS, k > 0 ? 1u : 0u);
+                                    const uint32_t off =
+                                        ((k >> 2) * Cfg::kHalfBytes + (k & 3) * 32) >> 4;
+                                    mma_ss(tS_, q_lo + off, k_lo + off, Cfg::kIdescS,
+                                           k > 0 ? 1u : 0u);
                                 }
                                 mma_commit(&bars.s_full[tl]);
-                                if (tl == (jt < it.n_kv[1] ? 1 : 0))
+                                if (last_k)
                                     mma_commit(&bars.k_empty[st]);  // last reader of K(jt)
                             }
                             __syncwarp();
@@ -747,20 +768,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     }
                     if (!ok)
                         break;
-                    if (lane == 0 && jt == n - 1)
+                    if (jt == n - 1 && elect_one())
                         mma_commit(bars.q_empty);  // Q is free once the last S is done
                     __syncwarp();
                 }
                 if (!ok)
                     break;
+#pragma unroll
                 for (int tl = 0; tl < 2; ++tl)
-                    if (it.n_kv[tl] > 0)
+                    if (nk[tl] > 0)
                         ++item_cnt[tl];
                 kv_it += n;
                 ++li;
             }
-            if (lane == 0) {
-                mma_commit(bars.drain);  // fires once every issued MMA has finished
+            if (elect_one()) {
+                // the issuing lane's commit fires once every MMA it issued has finished
+                mma_commit(bars.drain);
                 mbar_wait(bars.drain, 0);
             }
             __syncwarp();

@@ -16,19 +16,18 @@
 namespace pka {
 
 // ------------------------------------------------------------ descriptors
-// Shared-memory matrix descriptor: start address, LBO and SBO in 16-byte
-// units, descriptor version 1 (bits 46-47), 128-byte swizzle (layout 2 in
-// bits 61-63), base offset 0 (tiles are 1024-byte aligned).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,
-                                                    uint32_t sbo_bytes)
+// Shared-memory matrix descriptor: start address (bits 0-13), LBO (16-29) and
+// SBO (32-45) in 16-byte units, descriptor version 1 (bit 46), 128-byte
+// swizzle (layout 2 in bits 61-63), base offset 0 (tiles are 1024-byte
+// aligned).  Every operand here has SBO = 1024 B, so all descriptors share one
+// high word and differ only in the low word (start address and LBO); the MMA
+// wrappers below take the low word alone, which makes a k-step or a stage
+// change one 32-bit add.
+constexpr uint32_t kDescHiSw128 = (1024u >> 4) | (1u << 14) | (2u << 29);
+
+__device__ __forceinline__ uint32_t smem_desc_lo(uint32_t saddr, uint32_t lbo_bytes)
 {
-    uint64_t d = 0;
-    d |= uint64_t((saddr >> 4) & 0x3FFFu);
-    d |= uint64_t((lbo_bytes >> 4) & 0x3FFFu) << 16;
-    d |= uint64_t((sbo_bytes >> 4) & 0x3FFFu) << 32;
-    d |= uint64_t(1) << 46;
-    d |= uint64_t(2) << 61;
-    return d;
+    return ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
 }
 
 // Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulator.
@@ -75,28 +74,38 @@ __device__ __forceinline__ void tc_fence_after() {
 
 
 // ------------------------------------------------------------ MMA
-// D[tmem] (+)= A[smem desc] * B[smem desc]
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate)
+// One lane of a converged warp (the lowest active one; the same lane every
+// time the whole warp executes it).
+__device__ __forceinline__ bool elect_one()
 {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+    uint32_t p;
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}"
+                 : "=r"(p));
+    return p != 0;
 }
 
-// D[tmem] (+)= A[tmem] * B[smem desc]
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+// D[tmem] (+)= A[smem desc] * B[smem desc]; descriptors given by low word.
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
                                        uint32_t idesc, uint32_t accumulate)
 {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+        "mov.b64 da, {%1, %5};\n\tmov.b64 db, {%2, %5};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHiSw128));
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc]; B's descriptor given by low word.
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                       uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "mov.b64 db, {%2, %5};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHiSw128));
 }
 
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
