@@ -48,6 +48,15 @@ constexpr int kBM = 128;             // query rows per tile
 constexpr int kBN = 128;             // keys per tile
 constexpr int kSuper = 2 * kBM;      // query rows per work item (tiles A and B)
 constexpr int kPfThreads = 384;
+// Register split by setmaxnreg: warps 0-3 (TMA producer, MMA issuer, TMEM
+// allocator, spare) drop to kPfRegsLow, the eight softmax warps rise to
+// kPfRegsHigh.  setmaxnreg.inc draws on the registers the block was launched
+// with, so the split has to fit in kPfThreads x (registers per thread at
+// launch), or the softmax warps would wait for registers forever: 168 under
+// __launch_bounds__(384, 1), checked again at launch against the compiled kernel.
+constexpr uint32_t kPfRegsLow = 104, kPfRegsHigh = 200;
+constexpr uint32_t kPfRegsSplit = 4 * 32 * kPfRegsLow + 8 * 32 * kPfRegsHigh;
+static_assert(kPfRegsSplit <= uint32_t(kPfThreads) * 168, "setmaxnreg split");
 constexpr int kPfStages = 2;
 constexpr int kMaxPrefillSeqs = 4096;
 constexpr uint32_t kTmemCols = 512;
@@ -531,7 +540,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (threadIdx.x == 0)
             flag_error(kErrTmemAlloc);
     } else if (warp < 4) {
-        reg_dealloc<104>();
+        reg_dealloc<kPfRegsLow>();
         if (warp == 0) {
             // ============================================================ producer
             if (lane == 0) {
@@ -789,7 +798,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             __syncwarp();
         }
     } else {
-        reg_alloc<200>();
+        reg_alloc<kPfRegsHigh>();
         const int tl = (warp - 4) / 4;  // warps 4-7: tile A, warps 8-11: tile B
         pf_softmax<D>(p, prefix, nseq, bars, tl, tbase + tl * 128, tbase + 256 + tl * D,
                       abort_flag);
@@ -816,6 +825,12 @@ static cudaError_t launch_prefill_d(const Fwd &f, const PrefillParams &p, int gr
                                              static_cast<int>(Cfg::kSmemBytes));
         if (e != cudaSuccess)
             return e;
+        cudaFuncAttributes attr;
+        e = cudaFuncGetAttributes(&attr, prefill_tc_kernel<D, kHnd>);
+        if (e != cudaSuccess)
+            return e;
+        if (uint32_t(attr.numRegs) * kPfThreads < kPfRegsSplit)
+            return cudaErrorInvalidConfiguration;  // the register split would never be granted
         configured_device = dev;
     }
     CUtensorMap q_map, kv_map;
