@@ -75,10 +75,20 @@ static double e4m3_value(uint8_t c)
     double v;
     if (ex == 15 && man == 7)
         return NAN;
+#if ORACLE_MUTANT == 13
+    if (ex == 0)
+        v = ldexp((double)man, -10);
+#else
     if (ex == 0)
         v = ldexp((double)man, -9); /* subnormal: man/8 * 2^-6 */
+#endif
+#if ORACLE_MUTANT == 15
+    else
+        v = ldexp(8.0 + man, ex - 11);
+#else
     else
         v = ldexp(8.0 + man, ex - 10); /* (1 + man/8) * 2^(ex-7) */
+#endif
     return sign ? -v : v;
 }
 
@@ -95,12 +105,20 @@ static uint8_t e4m3_encode(float y, const double *mag)
     double a = fabs((double)y);
     uint8_t best = 0;
     if (a >= 448.0) {
+#if ORACLE_MUTANT == 11
+        best = 0x7f;
+#else
         best = 0x7e;
+#endif
     } else {
         double best_d = a; /* distance to code 0 */
         for (int c = 1; c <= 0x7e; ++c) {
             double d = fabs(mag[c] - a);
+#if ORACLE_MUTANT == 10
+            if (d <= best_d) {
+#else
             if (d < best_d || (d == best_d && (c & 1) == 0)) {
+#endif
                 best = (uint8_t)c;
                 best_d = d;
             }
@@ -117,7 +135,11 @@ void oracle_quantize_e4m3(const uint16_t *x, int64_t n, float scale, uint8_t *ou
         mag[c] = e4m3_value((uint8_t)c);
     for (int64_t i = 0; i < n; ++i) {
         float xf = (float)bf16_value(x[i]);
+#if ORACLE_MUTANT == 12
+        volatile float y = xf * scale;
+#else
         volatile float y = xf / scale; /* fp32 division, as stored */
+#endif
         out[i] = e4m3_encode(y, mag);
     }
 }
@@ -137,8 +159,13 @@ static double pool_elem(const pool_view *pv, int64_t block, int64_t kv, int64_t 
                         int64_t head, int64_t e)
 {
     int64_t row = ((block * 2 + kv) * pv->block_size + offset) * pv->num_kv_heads + head;
+#if ORACLE_MUTANT == 14
+    if (pv->codes8)
+        return e4m3_value(pv->codes8[row * pv->head_size + e]) * (kv ? pv->k_scale : pv->v_scale);
+#else
     if (pv->codes8)
         return e4m3_value(pv->codes8[row * pv->head_size + e]) * (kv ? pv->v_scale : pv->k_scale);
+#endif
     return bf16_value(pv->bf16[row * pv->head_size + e]);
 }
 
