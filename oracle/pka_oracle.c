@@ -488,15 +488,24 @@ int oracle_cascade_attention(const uint16_t *query, const uint16_t *cache, const
     double *l_s = (double *)malloc((size_t)total * sizeof(double));
     int rc = -3;
     if (o_p && o_s && l_p && l_s) {
+#if ORACLE_MUTANT == 17
+        const int64_t prefix_hi = common_prefix_len - 1;
+#else
+        const int64_t prefix_hi = common_prefix_len;
+#endif
+#if ORACLE_MUTANT == 16
+        const int64_t suffix_lo = common_prefix_len + 1;
+#else
+        const int64_t suffix_lo = common_prefix_len;
+#endif
         rc = oracle_paged_attention(query, cache, qsl, seq_lens, block_table, block_table_stride,
                                     num_seqs, num_heads, num_kv_heads, head_size, block_size,
-                                    num_blocks, scale, 0, 0, common_prefix_len, rows, num_rows,
-                                    o_p, l_p);
+                                    num_blocks, scale, 0, 0, prefix_hi, rows, num_rows, o_p, l_p);
         if (rc == 0)
             rc = oracle_paged_attention(query, cache, qsl, seq_lens, block_table,
                                         block_table_stride, num_seqs, num_heads, num_kv_heads,
                                         head_size, block_size, num_blocks, scale, causal,
-                                        common_prefix_len, -1, rows, num_rows, o_s, l_s);
+                                        suffix_lo, -1, rows, num_rows, o_s, l_s);
         if (rc == 0)
             oracle_lse_merge(o_p, l_p, o_s, l_s, total, head_size, out, lse);
     }

@@ -3,9 +3,10 @@
 The oracle source has build-time switches (ORACLE_MUTANT=n) that plant one
 plausible mistake each; this test compiles every variant on the CPU and checks
 that the pin set rejects it, so that the pins are known to be able to catch
-the kind of error they guard against.  Mistakes 1-9 are in the attention and
-cache-write oracle (checked against the pin set of oracle_pins.py), 10-15 in
-its fp8 e4m3 functions (checked against the fp8 pins of test_oracle_fp8.py).
+the kind of error they guard against.  Mistakes 1-9, 16 and 17 are in the
+attention, merge, cascade and cache-write oracle (checked against the pin set
+of oracle_pins.py), 10-15 in its fp8 e4m3 functions (checked against the fp8
+pins of test_oracle_fp8.py).
 """
 import pytest
 
@@ -22,6 +23,8 @@ MUTANTS = {
     7: "log-sum-exp in base 2",
     8: "merge drops the second term",
     9: "cache write to the wrong slot",
+    16: "cascade suffix starts one key late",
+    17: "cascade prefix pass stops one key early",
 }
 
 
