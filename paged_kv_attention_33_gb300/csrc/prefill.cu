@@ -35,6 +35,7 @@
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256, 256+D), O_B [256+D, 256+2D).
 #include <math.h>
 
+#include <atomic>
 #include <algorithm>
 #include <numeric>
 
@@ -816,10 +817,13 @@ template <int D, bool kHnd>
 static cudaError_t launch_prefill_d(const Fwd &f, const PrefillParams &p, int grid)
 {
     using Cfg = PfCfg<D>;
-    static int configured_device = -1;
+    // devices (bit d for device d < 64) on which this instantiation's launch
+    // attributes are set; atomic, since several host threads may launch
+    static std::atomic<uint64_t> configured{0};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (configured_device != dev) {
+    const uint64_t dev_bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+    if (dev_bit == 0 || (configured.load(std::memory_order_acquire) & dev_bit) == 0) {
         cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, kHnd>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(Cfg::kSmemBytes));
@@ -831,7 +835,7 @@ static cudaError_t launch_prefill_d(const Fwd &f, const PrefillParams &p, int gr
             return e;
         if (uint32_t(attr.numRegs) * kPfThreads < kPfRegsSplit)
             return cudaErrorInvalidConfiguration;  // the register split would never be granted
-        configured_device = dev;
+        configured.fetch_or(dev_bit, std::memory_order_release);
     }
     CUtensorMap q_map, kv_map;
     if (encode_3d_bf16(&q_map, f.query, D, f.num_heads, f.num_tokens, uint64_t(D) * 2,
