@@ -82,7 +82,8 @@ typedef enum {
  *                   query token each ([FA/FI] "Responsabilidades": decode
  *                   first, then prefill).
  *  max_query_len    host upper bound on q_s over the prefill sequences.
- *  max_seq_len      host upper bound on L_s over all sequences.
+ *  max_seq_len      host upper bound on L_s over all sequences (0 only in a
+ *                   batch of decodes that all have L_s = 0).
  *  common_prefix_len  0, or a multiple of block_size P such that the first
  *                   P/bs block-table entries of every sequence are the same
  *                   blocks and P <= c_s for every s ([blog] "Que aporta
@@ -307,7 +308,10 @@ pka_status pka_paged_attn_forward_fused(const void *query, const void *key, cons
  *    PKA_ERR_WORKSPACE (and a message naming both sizes); nothing is enqueued.
  *  - The first call on a device looks up the buffer's device address once
  *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture.
+ *    before any stream capture.  The address is kept with the CUDA context it
+ *    belongs to: the first call after the device's context was torn down and
+ *    made anew (cudaDeviceReset, say) looks it up again, so that call too
+ *    belongs before any capture.
  *  - Every call shares the one buffer and leaves its contents behind; each
  *    call clears what must start at zero (its per-sequence counters) and
  *    writes all the rest before reading it.  Calls that overlap on the GPU

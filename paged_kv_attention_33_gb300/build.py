@@ -44,37 +44,48 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
+def _obj(src: str) -> str:
+    return os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+
+
+def commands(ptxas_info: bool = False, out: str | None = None) -> list:
+    """The nvcc command lines of a build: one compile per source, then the link
+    into `out` (default: libpka.so)."""
+    nvcc = _nvcc()
+    common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+                     "-I", INCLUDE, "-I", CSRC]
+    if ptxas_info:
+        common += ["-Xptxas", "-v"]
+    cmds = [[nvcc] + common + ["-c", os.path.join(CSRC, src), "-o", _obj(src)]
+            for src in SOURCES]
+    cmds.append([nvcc] + ARCH + ["-shared", "-o", out or LIB] + [_obj(s) for s in SOURCES])
+    return cmds
+
+
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     """Compile (if needed) and return the path of libpka.so."""
     deps = _deps()
     if not force and not _stale(LIB, deps):
         return LIB
     os.makedirs(BUILD, exist_ok=True)
-    nvcc = _nvcc()
-    common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-                     "-I", INCLUDE, "-I", CSRC]
-    if ptxas_info:
-        common += ["-Xptxas", "-v"]
+    tmp = LIB + f".tmp{os.getpid()}"
+    cmds = commands(ptxas_info, out=tmp)
 
-    def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-        cmd = [nvcc] + common + ["-c", os.path.join(CSRC, src), "-o", obj]
+    def compile_one(cmd):
+        src = cmd[-3]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
-        return obj, r.stderr
+        return cmd[-1], r.stderr
 
     with ThreadPoolExecutor(len(SOURCES)) as ex:
-        results = list(ex.map(compile_one, SOURCES))
+        results = list(ex.map(compile_one, cmds[:-1]))
     if ptxas_info:
         for _, err in results:
             sys.stderr.write(err)
-    objs = [o for o, _ in results]
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
-    r = subprocess.run(cmd, capture_output=True, text=True)
+    r = subprocess.run(cmds[-1], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)

@@ -249,8 +249,11 @@ static pka_status check_shape(const pka_meta *m, int32_t num_tokens, int32_t num
         return fail(PKA_ERR_INVALID_ARG,
                     "inconsistent sizes: num_tokens %d, num_seqs %d, num_decodes %d", num_tokens,
                     m->num_seqs, m->num_decodes);
-    if (m->num_seqs > 0 && m->max_seq_len < 1)
-        return fail(PKA_ERR_INVALID_ARG, "max_seq_len must be >= 1");
+    // a decode may hold no key (L_s = 0: a context-parallel rank's empty
+    // shard), so max_seq_len 0 is a valid bound for a decode-only batch
+    if (m->max_seq_len < 0 || (m->num_seqs > m->num_decodes && m->max_seq_len < 1))
+        return fail(PKA_ERR_INVALID_ARG,
+                    "max_seq_len must be >= 0, and >= 1 when prefills are present");
     if (m->num_seqs > m->num_decodes && m->max_query_len < 1)
         return fail(PKA_ERR_INVALID_ARG, "max_query_len must be >= 1 when prefills are present");
     if (m->common_prefix_len < 0 || m->common_prefix_len % block_size != 0 ||
@@ -682,7 +685,8 @@ pka_status pka_check_status(void *stream)
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "stream synchronize");
-    const uint32_t bits = kv_write_take_error() | decode_take_error() | prefill_take_error();
+    const uint32_t bits =
+        kv_write_take_error() | decode_take_error() | prefill_take_error() | merge_take_error();
     if (bits == 0)
         return PKA_OK;
     char buf[256] = "";
@@ -696,6 +700,8 @@ pka_status pka_check_status(void *stream)
         strcat(buf, " tensor-memory allocation failed;");
     if (bits & kErrBadMetadata)
         strcat(buf, " seq_lens/query_start_loc outside the stated bounds;");
+    if (bits & kErrBadPartial)
+        strcat(buf, " a merge input's lse is +inf or NaN;");
     return fail(PKA_ERR_DEVICE_CHECK, "device check failed:%s", buf);
 }
 

@@ -21,6 +21,7 @@ enum DeviceError : uint32_t {
     kErrWaitTimeout = 1u << 2,     // a pipeline wait exceeded its time limit
     kErrTmemAlloc = 1u << 3,       // tensor-memory allocation failed
     kErrBadMetadata = 1u << 4,     // seq_lens / query_start_loc outside the stated bounds
+    kErrBadPartial = 1u << 5,      // a merge input's lse is +inf or NaN
 };
 
 // One copy per translation unit (no relocatable device code); each unit

@@ -58,6 +58,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <atomic>
 #include <type_traits>
 
 #include "common.cuh"
@@ -1071,16 +1072,19 @@ static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Wor
                                    bool cascade)
 {
     using Cfg = DecodeCfg<D, kFp8>;
-    static int configured_device = -1;
+    // devices (bit d for device d < 64) on which this instantiation's launch
+    // attribute is set; atomic, since several host threads may launch
+    static std::atomic<uint64_t> configured{0};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (configured_device != dev) {
+    const uint64_t dev_bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+    if (dev_bit == 0 || (configured.load(std::memory_order_acquire) & dev_bit) == 0) {
         cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D, kHnd, kFp8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(Cfg::kSmemBytes));
         if (e != cudaSuccess)
             return e;
-        configured_device = dev;
+        configured.fetch_or(dev_bit, std::memory_order_release);
     }
     DecodeParams p;
     p.query = static_cast<const uint32_t *>(f.query);

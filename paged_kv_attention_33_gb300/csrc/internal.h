@@ -133,6 +133,7 @@ cudaError_t launch_merge_partials(const void *outs, const float *lses, int32_t n
                                   void *out, float *lse_out, int32_t num_tokens,
                                   int32_t num_heads, int32_t head_size, int32_t base2,
                                   cudaStream_t st);
+uint32_t merge_take_error();
 
 // Set the thread-local message pka_last_error() returns (api.cu).
 void set_last_error(const char *fmt, ...);

@@ -8,6 +8,10 @@
 // lse base to be known -- here the natural log.  Per row:
 //     lse = ln(e^lse_a + e^lse_b),  out = e^(lse_a-lse) out_a + e^(lse_b-lse) out_b.
 // One warp per (token, head) row, 16-byte vectors along head_size.
+// An lse of +inf or NaN is no partial attention at all (a corrupt input, say
+// from a remote rank): the row is still computed, and the kernel raises the
+// sticky device error (pka_check_status reports it) instead of letting the
+// NaN pass unnoticed.
 #include <math.h>
 
 #include "common.cuh"
@@ -25,6 +29,9 @@ __global__ void __launch_bounds__(256)
     if (r >= rows)
         return;
     const float la = lse_a[r], lb = lse_b[r];
+    // -inf (an empty side) and finite values pass; +inf and NaN do not
+    if (lane == 0 && !(la < INFINITY && lb < INFINITY))
+        flag_error(kErrBadPartial);
     const float m = fmaxf(la, lb);
     float ca = 0.f, cb = 0.f, l = -INFINITY;
     if (m != -INFINITY) {
@@ -73,8 +80,14 @@ __global__ void __launch_bounds__(256)
     // b^x as e^(x ln b): exact scaling of the exponent for b = 2
     const float ln_b = base2 ? 0.69314718055994530942f : 1.f;
     float m = -INFINITY;
-    for (int q = 0; q < num_parts; ++q)
-        m = fmaxf(m, lses[int64_t(q) * rows + r]);
+    bool bad = false;
+    for (int q = 0; q < num_parts; ++q) {
+        const float l = lses[int64_t(q) * rows + r];
+        bad = bad || !(l < INFINITY);  // +inf or NaN
+        m = fmaxf(m, l);
+    }
+    if (lane == 0 && bad)
+        flag_error(kErrBadPartial);
     float wsum = 0.f;
     if (m != -INFINITY)
         for (int q = 0; q < num_parts; ++q) {
@@ -141,5 +154,7 @@ cudaError_t launch_cascade_merge(const void *out_a, const float *lse_a, const vo
         static_cast<uint4 *>(out), lse_out, rows, head_size * 2 / 16);
     return cudaGetLastError();
 }
+
+uint32_t merge_take_error() { return take_device_error(); }
 
 }  // namespace pka

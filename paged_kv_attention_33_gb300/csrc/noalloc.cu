@@ -21,27 +21,58 @@ constexpr size_t kNoallocScratchBytes = size_t(16) << 20;  // 16 MiB
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
+// The driver's cuCtxGetCurrent, found once through the runtime (the library
+// does not link libcuda directly).
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+
+static CtxGetCurrentFn ctx_get_current()
+{
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    });
+    return fn;
+}
+
 // Device address of g_noalloc_scratch on the current device.  In host code
 // the symbol's name stands for a host-side shadow, not for device memory, so
 // the address is looked up once per device (with that device current) and
-// cached.
+// cached together with the context it belongs to: when the device's context
+// has been torn down and made again (cudaDeviceReset, a released and retained
+// primary context), the context differs and the address is looked up anew.
 static cudaError_t noalloc_scratch(void **out)
 {
     static std::mutex mu;
     static void *ptrs[64] = {};
+    static CUcontext ctxs[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
     if (dev < 0 || dev >= 64)
         return cudaErrorInvalidDevice;
+    CtxGetCurrentFn get = ctx_get_current();
+    auto current = [&]() -> CUcontext {
+        CUcontext c = nullptr;
+        return get && get(&c) == CUDA_SUCCESS ? c : nullptr;
+    };
     std::lock_guard<std::mutex> lock(mu);
-    if (!ptrs[dev]) {
+    const CUcontext ctx = current();
+    if (!ptrs[dev] || !ctx || ctxs[dev] != ctx) {
+        // (the lookup makes the runtime's context current if it was not yet;
+        // a context that cannot be named is looked up on every call)
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess)
             return e;
         ptrs[dev] = p;
+        ctxs[dev] = current();
     }
     *out = ptrs[dev];
     return cudaSuccess;

@@ -17,6 +17,10 @@ that the combine must use the lse base the partials were made in.  Here:
   * lse base: the forward reports natural-log lse; the merge takes the base as
     an argument (LSE_BASE_E, or LSE_BASE_2 for partials in log2 units).
 
+This module holds the integer sharding and the collective calls only: every
+step of the arithmetic (the local attention, an empty shard's out = 0 and
+lse = -inf, the merge) runs in the library's kernels.
+
 Only decodes are sharded (the name's "decode"): a prefill query's causal limit
 is a global key position, which a rank-local sequence does not carry.
 """
@@ -25,8 +29,6 @@ from __future__ import annotations
 import math
 
 import numpy as np
-
-LN2 = math.log(2.0)
 
 
 def shard_decode_metadata(seq_lens, block_table, block_size: int, rank: int, world: int):
@@ -45,15 +47,6 @@ def shard_decode_metadata(seq_lens, block_table, block_size: int, rank: int, wor
             table[s, i] = block_table[s, n]
             lens[s] += min(block_size, L - n * block_size)
     return lens, table
-
-
-def ln_to_log2(lse):
-    """lse in natural-log units -> log2 units (x / ln 2)."""
-    return lse / LN2
-
-
-def log2_to_ln(lse):
-    return lse * LN2
 
 
 def dcp_decode_step(local_partial, merge, group=None):
@@ -77,17 +70,14 @@ def dcp_decode_step(local_partial, merge, group=None):
 
 
 def gpu_local_partial(query, kv_cache, local_meta, scale=None, workspace=None):
-    """The rank's partial on its GPU through the library: (out bf16, lse fp32 ln)."""
+    """The rank's partial on its GPU through the library: (out bf16, lse fp32 ln).
+    A shard with no key of some (or every) sequence is served by the library
+    too: those rows come back as out = 0, lse = -inf, the merge's identity."""
     import torch
 
     import paged_kv_attention_33_gb300 as pka
 
     T, H, D = query.shape
-    if local_meta.max_seq_len < 1:
-        # the rank holds no key of any sequence: attention over an empty key
-        # set is out = 0, lse = -inf (the merge's identity)
-        return (torch.zeros((T, H, D), dtype=torch.bfloat16, device=query.device),
-                torch.full((T, H), float("-inf"), dtype=torch.float32, device=query.device))
     out = torch.empty((T, H, D), dtype=torch.bfloat16, device=query.device)
     lse = torch.empty((T, H), dtype=torch.float32, device=query.device)
     pka.paged_attn_forward(query, kv_cache, local_meta, out, lse, scale=scale, causal=True,

@@ -42,11 +42,13 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, s)
 
 
-def test_library_is_built_for_sm103a():
-    out = subprocess.run(["cuobjdump", "--list-elf", pbuild.LIB], capture_output=True, text=True)
-    if out.returncode != 0:
-        pytest.skip("cuobjdump unavailable")
-    assert "sm_103a" in out.stdout
+def test_library_is_built_for_sm103a_only():
+    """Every translation unit and the link step take exactly one target,
+    sm_103a machine code (no PTX to be compiled for another GPU at load)."""
+    assert pbuild.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    cmds = pbuild.commands()
+    assert cmds and all(c.count("-gencode") == 1 and "arch=compute_103a,code=sm_103a" in c
+                        for c in cmds)
 
 
 def _meta(**kw):
@@ -95,7 +97,9 @@ def test_group_rules(lib):
 
 def test_inconsistent_sizes(lib):
     assert _fwd(lib, _meta(num_decodes=3)) == -1
-    assert _fwd(lib, _meta(max_seq_len=0)) == -1
+    assert _fwd(lib, _meta(max_seq_len=-1)) == -1
+    # 0 bounds a decode-only batch whose decodes hold no key, not a prefill
+    assert _fwd(lib, _meta(num_decodes=1, max_query_len=1, max_seq_len=0)) == -1
     assert _fwd(lib, _meta(block_table_stride=2)) == -1
     assert _fwd(lib, _meta(common_prefix_len=8)) == -1
     assert _fwd(lib, _meta(common_prefix_len=100)) == -1

@@ -6,12 +6,28 @@ another), their partials merged by pka_merge_partials and compared with the
 fp64 oracle's unsharded attention; the lse-base flag is checked both ways
 (the "AttentionBackend" page, "Limites y fallos": a wrong base breaks the
 softmax denominator across shards)."""
+import math
+
 import numpy as np
 import pytest
 
 from paged_kv_attention_33_gb300 import dcp
 from paged_kv_attention_33_gb300 import workloads as W
 from tests import gpu_util as G
+
+
+# lse unit changes of the base-flag checks (test-side only: the library takes
+# the base as an argument and converts nothing in Python)
+_LN2 = math.log(2.0)
+
+
+def _ln_to_log2(lse):
+    return lse / _LN2
+
+
+def _log2_to_ln(lse):
+    return lse * _LN2
+
 
 pytestmark = pytest.mark.gpu
 
@@ -66,12 +82,12 @@ def test_dcp_lse_base_flag():
     b = W.make_batch(sp, seed=8100)
     outs, lses = _partials(b, 3, "cuda")
     o_e, l_e = dcp.gpu_merge(outs, lses, lse_base=pka.LSE_BASE_E)
-    o_2, l_2 = dcp.gpu_merge(outs, dcp.ln_to_log2(lses), lse_base=pka.LSE_BASE_2)
+    o_2, l_2 = dcp.gpu_merge(outs, _ln_to_log2(lses), lse_base=pka.LSE_BASE_2)
     diff = (o_e.float() - o_2.float()).abs().max().item()
     assert diff <= 1e-2, diff
-    assert (dcp.log2_to_ln(l_2) - l_e).abs().max().item() <= 1e-4
+    assert (_log2_to_ln(l_2) - l_e).abs().max().item() <= 1e-4
     # log2 partials merged as if natural-log: visibly wrong
-    o_bad, _ = dcp.gpu_merge(outs, dcp.ln_to_log2(lses), lse_base=pka.LSE_BASE_E)
+    o_bad, _ = dcp.gpu_merge(outs, _ln_to_log2(lses), lse_base=pka.LSE_BASE_E)
     assert (o_bad.float() - o_e.float()).abs().max().item() > 5e-2
 
 
@@ -146,3 +162,61 @@ def test_dcp_over_an_fp8_pool(oracle, world):
     rows = np.arange(b.num_tokens * sp.num_heads, dtype=np.int64)
     res = G.compare(W.to_host_bits(out), lse.cpu().numpy(), o_ref, l_ref, rows, sp.num_heads)
     G.assert_close(res, f"dcp fp8 world={world}")
+
+
+@pytest.mark.parametrize("H,Hkv,D,bs", [(32, 8, 128, 16), (8, 2, 64, 64)])
+def test_dcp_shard_without_any_key(oracle, H, Hkv, D, bs):
+    """Every sequence fits in one page, so ranks 1 and 2 hold no key at all
+    (their max_seq_len is 0): the library itself returns out = 0, lse = -inf
+    for those shards (one kv head per warp, and several warps per kv head),
+    and the merge gives the unsharded result."""
+    import torch
+
+    import paged_kv_attention_33_gb300 as pka
+
+    sp = W.BatchSpec("dcp_empty", H, Hkv, D, bs, decode_ctx=[0, 3, bs - 1])
+    b = W.make_batch(sp, seed=8200 + bs)
+    outs, lses = _partials(b, 3, "cuda")
+    for r in (1, 2):
+        lens, _ = dcp.shard_decode_metadata(b.seq_lens, b.block_table, bs, r, 3)
+        assert int(lens.max()) == 0
+        assert torch.all(outs[r].float() == 0) and torch.all(torch.isneginf(lses[r]))
+    out, lse = dcp.gpu_merge(outs, lses)
+    pka.check_status()
+    o_ref, l_ref = _reference(oracle, b)
+    rows = np.arange(b.num_tokens * H, dtype=np.int64)
+    G.assert_close(G.compare(W.to_host_bits(out), lse.cpu().numpy(), o_ref, l_ref, rows, H),
+                   "dcp empty shards")
+
+
+@pytest.mark.parametrize("bad", [float("inf"), float("nan")])
+def test_merges_flag_a_non_finite_lse(bad):
+    """A partial whose lse is +inf or NaN is no attention result (a corrupt
+    input): both merge kernels report it through the device error word
+    instead of spreading NaN unnoticed; -inf (an empty part) stays valid."""
+    import torch
+
+    import paged_kv_attention_33_gb300 as pka
+
+    T, H, D = 5, 4, 64
+    dev = "cuda"
+    g = torch.Generator(device=dev)
+    g.manual_seed(8300)
+    outs = torch.randn((2, T, H, D), generator=g, device=dev).to(torch.bfloat16)
+    lses = torch.randn((2, T, H), generator=g, device=dev)
+    lses[0, 1, 2] = float("-inf")
+    out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    pka.merge_partials(outs, lses, out, lse)
+    pka.cascade_merge(outs[0], lses[0], outs[1], lses[1], out, lse)
+    pka.check_status()  # -inf is an empty part, not an error
+    lses[1, 3, 0] = bad
+    pka.merge_partials(outs, lses, out, lse)
+    with pytest.raises(pka.PkaError) as e:
+        pka.check_status()
+    assert e.value.status == -5 and "+inf or NaN" in str(e.value)
+    pka.cascade_merge(outs[0], lses[0], outs[1], lses[1], out, lse)
+    with pytest.raises(pka.PkaError) as e:
+        pka.check_status()
+    assert e.value.status == -5
+    pka.check_status()  # the error word was cleared

@@ -60,15 +60,15 @@ def test_noalloc_matches_workspace_entry_point(case):
                            prefill=[(100, 128), (70, 200)], common_prefix_len=128)
         split = 64
     ref, ref_lse, results = _run_both(spec, seed=5001, split=split)
-    r = W.bf16_bits_to_f32(W.to_host_bits(ref)).astype(np.float64)
-    rl = ref_lse.cpu().numpy().astype(np.float64)
+    import torch
+
+    # the same plan, kernels and split layout as the workspace entry point, so
+    # the rows agree bit for bit; a partial-slot mix-up or a stale leftover of
+    # the first call would show in the second
     for k, (out, lse) in enumerate(results):
-        o = W.bf16_bits_to_f32(W.to_host_bits(out)).astype(np.float64)
-        lo = lse.cpu().numpy().astype(np.float64)
-        assert np.all(np.isfinite(o)) and np.all(np.isfinite(lo)), f"call {k}"
-        err = np.abs(o - r)
-        assert err.max() <= G.OUT_MAX_ABS and err.mean() <= G.OUT_MEAN_ABS, f"call {k}"
-        assert np.abs(lo - rl).max() <= G.LSE_ABS, f"call {k}"
+        assert torch.isfinite(out).all() and torch.isfinite(lse).all(), f"call {k}"
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), f"call {k}"
+        assert torch.equal(lse, ref_lse), f"call {k}"
 
 
 def test_noalloc_rejects_batches_above_its_scratch():
