@@ -42,8 +42,7 @@ from paged_kv_attention_33_gb300 import workloads as W  # noqa: E402
 
 METRIC = "paged-attn decode KV GB/s & prefill TFLOP/s, % of GB300 roofline"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-SEED_OF = {"tiny_decode": 1001, "decode_heavy": 1002, "prefill": 1003, "mixed": 1004,
-           "cascade": 1005}
+SEED_OF = W.NAMED_SEEDS
 
 
 def load_peaks():
@@ -241,16 +240,26 @@ def oracle_sample_rows(batch, seqs):
     return np.asarray(rows, dtype=np.int64)
 
 
-def time_oracle(name, seqs, threads):
+class OracleStep:
+    """The workload's batch on the host, its new rows written by the oracle
+    (set-up, untimed), for timing the oracle's attention."""
+
+    def __init__(self, name):
+        from oracle import Oracle
+
+        self.name = name
+        self.spec = W.named_spec(name)
+        self.batch = W.make_batch(self.spec, seed=SEED_OF[name], device="cpu")
+        self.oracle = Oracle()
+        b = self.batch
+        self.oracle.reshape_and_cache(b.key, b.value, b.cache, b.slot_mapping)
+
+
+def time_oracle(name, seqs, threads, prepared=None):
     """Oracle on the whole heads of `seqs` of the workload; returns
     (seconds, KV bytes those sequences read, sample description)."""
-    from oracle import Oracle
-
-    spec = W.named_spec(name)
-    b = W.make_batch(spec, seed=SEED_OF[name], device="cpu")
-    cache = b.cache
-    orc = Oracle()
-    orc.reshape_and_cache(b.key, b.value, cache, b.slot_mapping)
+    st = prepared or OracleStep(name)
+    spec, b, orc, cache = st.spec, st.batch, st.oracle, st.batch.cache
     rows = oracle_sample_rows(b, seqs)
     t0 = time.perf_counter()
     orc.paged_attention(b.query, cache, b.query_start_loc, b.seq_lens, b.block_table,
@@ -271,11 +280,14 @@ def run_reference(args):
     threads = oracle.cpu_threads()
     name = args.workload
     spec = W.named_spec(name)
-    per_step = list(range(0, min(spec.num_decodes, 16)))  # bounded sample per step
+    # every sequence of the workload per step (decode_heavy: about 0.4 s on 16
+    # host cores); the batch is drawn once, before the timed steps
+    per_step = list(range(spec.num_decodes)) if spec.num_decodes else [0]
+    prepared = OracleStep(name)
     times = []
     nbytes = 0
     for i in range(args.warmup + args.steps):
-        dt, nb, desc = time_oracle(name, per_step, threads)
+        dt, nb, desc = time_oracle(name, per_step, threads, prepared)
         if i >= args.warmup:
             times.append(dt)
             nbytes = nb

@@ -84,6 +84,13 @@ class BatchSpec:
         return self.scale if self.scale is not None else 1.0 / math.sqrt(self.head_size)
 
 
+# Seeds of the five workloads: the lengths of named_spec(name) are drawn from
+# NAMED_SEEDS[name], and the benchmark draws the batch's values with the same
+# seed (make_batch(named_spec(name), seed=NAMED_SEEDS[name])).
+NAMED_SEEDS = {"tiny_decode": 1001, "decode_heavy": 1002, "prefill": 1003, "mixed": 1004,
+               "cascade": 1005}
+
+
 def named_spec(name: str, seed: int | None = None) -> BatchSpec:
     """The five synthetic workloads of the method (lengths drawn from `seed`).
 
@@ -95,9 +102,7 @@ def named_spec(name: str, seed: int | None = None) -> BatchSpec:
     cascade       256 decodes sharing a 4096-token prefix, private suffix ~ U[64,1024]
                   (the new token included); H=64, Hkv=8, D=128, bs=128
     """
-    seeds = {"tiny_decode": 1001, "decode_heavy": 1002, "prefill": 1003, "mixed": 1004,
-             "cascade": 1005}
-    rng = np.random.Generator(np.random.PCG64(seeds[name] if seed is None else seed))
+    rng = np.random.Generator(np.random.PCG64(NAMED_SEEDS[name] if seed is None else seed))
     if name == "tiny_decode":
         lens = rng.integers(1, 200, size=4, endpoint=True)
         return BatchSpec(name, 8, 2, 64, 16, decode_ctx=[int(x) - 1 for x in lens],

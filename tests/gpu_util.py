@@ -126,3 +126,64 @@ def check_batch(oracle, batch: W.Batch, split_kv_tokens=0, rows=None, label="", 
     res = compare(out, lse, o_ref, l_ref, rows, H)
     assert_close(res, label)
     return res
+
+
+def tile_cover_rows(batch: W.Batch, seed: int, tile: int = 128) -> np.ndarray:
+    """Rows r = t*H + h for a dense check of a batch too large to check whole:
+    every decode row (all heads); one random row of every (128-query tile,
+    head) of every prefill sequence, i.e. of every work item of the
+    tensor-core pass and each of its two softmax tiles; and every row of each
+    prefill sequence's last, ragged tile for one random head."""
+    H = batch.spec.num_heads
+    nd = batch.spec.num_decodes
+    qsl = np.asarray(batch.query_start_loc, dtype=np.int64)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    heads = np.arange(H, dtype=np.int64)
+    rows = [np.arange(qsl[nd] * H, dtype=np.int64)]
+    for s in range(nd, len(qsl) - 1):
+        t0, n = int(qsl[s]), int(qsl[s + 1] - qsl[s])
+        for a in range(0, n, tile):
+            t = t0 + rng.integers(a, min(n, a + tile), size=H)
+            rows.append(t * H + heads)
+        if n > 0:
+            last = (n - 1) // tile * tile
+            rows.append(np.arange(t0 + last, t0 + n, dtype=np.int64) * H + rng.integers(0, H))
+    return np.unique(np.concatenate(rows))
+
+
+def run_fused(batch: W.Batch, pool=None, k_scale=None, v_scale=None):
+    """One step as the benchmark makes it: paged_attn_forward_fused (the cache
+    write inside the decode launch) with a workspace of pka_workspace_size
+    bytes, over the batch's pool (a clone of it) or over `pool` (an fp8 pool of
+    uint8 codes when k_scale is given), updated in place.  Returns the pool
+    (device), out and lse (device)."""
+    import torch
+
+    import paged_kv_attention_33_gb300 as pka
+
+    dev = device()
+    sp = batch.spec
+    fp8 = k_scale is not None
+    if pool is None:
+        pool = to_dev(batch.cache, dev)
+        if not isinstance(batch.cache, np.ndarray):
+            pool = pool.clone()
+    meta = pka.Meta.from_host(batch.query_start_loc, batch.seq_lens, batch.block_table,
+                              sp.num_decodes, dev, common_prefix_len=sp.common_prefix_len,
+                              kv_dtype="fp8" if fp8 else "bf16",
+                              k_scale=k_scale if fp8 else 1.0,
+                              v_scale=v_scale if fp8 else 1.0)
+    T = batch.num_tokens
+    need = pka.workspace_size(meta, T, sp.num_heads, sp.num_kv_heads, sp.head_size,
+                              sp.block_size)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    out = torch.full((T, sp.num_heads, sp.head_size), float("nan"), dtype=torch.bfloat16,
+                     device=dev)
+    lse = torch.full((T, sp.num_heads), float("nan"), dtype=torch.float32, device=dev)
+    pka.paged_attn_forward_fused(to_dev(batch.query, dev), to_dev(batch.key, dev),
+                                 to_dev(batch.value, dev),
+                                 torch.from_numpy(batch.slot_mapping).to(dev), pool, meta, out,
+                                 lse, scale=sp.softmax_scale, causal=sp.causal, workspace=ws)
+    pka.check_status()
+    return pool, out, lse
+

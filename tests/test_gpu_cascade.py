@@ -53,14 +53,6 @@ def test_cascade_equals_plain(oracle):
     assert res_c["out_max_abs"] <= 2e-2 and res_p["out_max_abs"] <= 2e-2
 
 
-def test_cascade_named_full_size_sampled(oracle):
-    """256 decodes sharing a 4096-token prefix (bs 128, H 64, Hkv 8) at full
-    size, in the benchmark's launch configuration, on sampled rows."""
-    b = W.make_batch(W.named_spec("cascade"), seed=1005, device="cuda")
-    rows = W.sample_rows(b, 512, seed=6)
-    G.check_batch(oracle, b, rows=rows, label="cascade full", threads=16)
-
-
 def test_cascade_precondition_is_flagged():
     """A prefill chunk whose queries start inside the shared prefix breaks the
     cascade's premise; the kernel flags it instead of computing garbage."""

@@ -54,15 +54,6 @@ def test_decode_many_splits_ragged(oracle):
     G.check_batch(oracle, b, label="auto")
 
 
-def test_decode_heavy_full_size_sampled(oracle):
-    """The decode-heavy batch at full size in the benchmark's launch
-    configuration (automatic split), checked on sampled rows."""
-    spec = W.named_spec("decode_heavy")
-    b = W.make_batch(spec, seed=1002, device="cuda")
-    rows = W.sample_rows(b, 384, seed=3)
-    G.check_batch(oracle, b, rows=rows, label="decode_heavy", threads=16)
-
-
 def test_out_of_pool_slot_is_flagged():
     import torch
 

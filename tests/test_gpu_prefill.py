@@ -45,17 +45,3 @@ def test_mixed_decode_first_batch(oracle):
 def test_non_causal_prefill(oracle):
     sp = W.BatchSpec("nc", 8, 2, 64, 16, prefill=[(70, 0), (130, 45)], causal=False)
     G.check_batch(oracle, W.make_batch(sp, seed=3400), label="non-causal")
-
-
-def test_prefill_named_full_size_sampled(oracle):
-    """The varlen prefill batch (8 prompts, 1024..8192 tokens) at full size,
-    in the benchmark's launch configuration, checked on sampled rows."""
-    b = W.make_batch(W.named_spec("prefill"), seed=1003, device="cuda")
-    rows = W.sample_rows(b, 256, seed=4)
-    G.check_batch(oracle, b, rows=rows, label="prefill full", threads=16)
-
-
-def test_mixed_named_full_size_sampled(oracle):
-    b = W.make_batch(W.named_spec("mixed"), seed=1004, device="cuda")
-    rows = W.sample_rows(b, 256, seed=5)
-    G.check_batch(oracle, b, rows=rows, label="mixed full", threads=16)
