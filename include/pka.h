@@ -389,6 +389,19 @@ pka_status pka_check_status(void *stream);
 enum { PKA_KERNEL_DECODE = 0, PKA_KERNEL_PREFILL = 1 };
 pka_status pka_set_kernel_events(int32_t kernel, void *start, void *stop);
 
+/*
+ * Test hook of the failure path (bounded waits).  With on != 0, the decode and
+ * prefill kernels that later pka_paged_attn_forward calls on this thread
+ * launch issue no TMA copy and publish no work: the first bounded wait of
+ * every CTA runs out after its time limit (2 s), the CTA raises the abort flag,
+ * winds down with nothing in flight (no copy issued, no MMA issued, its TMEM
+ * freed) and returns; no output row is written, and the next pka_check_status
+ * returns PKA_ERR_DEVICE_CHECK ("pipeline wait timed out").  The GPU context
+ * stays usable.  on = 0 turns the hook off.  For tests only; never set it in
+ * production.  The pages have no counterpart of this call.
+ */
+pka_status pka_test_skip_copies(int32_t on);
+
 /* Number of kernels the library has launched from this thread so far
  * (instrumentation; counts every launch of every entry point). */
 uint64_t pka_kernel_launches(void);

@@ -27,7 +27,7 @@ __all__ = ["Meta", "PkaError", "LAYOUT_NHD", "LAYOUT_HND", "KV_BF16", "KV_FP8_E4
            "paged_attn_forward_noalloc", "paged_attn_forward_fused", "workspace_size",
            "merge_partials", "LSE_BASE_E",
            "LSE_BASE_2", "check_status", "set_kernel_events", "kernel_launches",
-           "load_library",
+           "load_library", "test_skip_copies",
            "library_path", "KERNEL_DECODE", "KERNEL_PREFILL"]
 
 _P = ctypes.c_void_p
@@ -131,6 +131,8 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pka_cascade_merge.restype = ctypes.c_int
         lib.pka_set_kernel_events.argtypes = [_I32, _P, _P]
         lib.pka_set_kernel_events.restype = ctypes.c_int
+        lib.pka_test_skip_copies.argtypes = [_I32]
+        lib.pka_test_skip_copies.restype = ctypes.c_int
         lib.pka_kernel_launches.argtypes = []
         lib.pka_kernel_launches.restype = ctypes.c_uint64
         lib.pka_check_status.argtypes = [_P]
@@ -343,6 +345,13 @@ def set_kernel_events(kernel: int, start=None, stop=None) -> None:
         return None if e is None else ctypes.c_void_p(e.cuda_event)
 
     _check(load_library().pka_set_kernel_events(kernel, raw(start), raw(stop)))
+
+
+def test_skip_copies(on: bool) -> None:
+    """Failure-path test hook (pka_test_skip_copies): while on, the kernels of
+    later forwards on this thread issue no copies, so their first bounded wait
+    runs out and check_status() raises PKA_ERR_DEVICE_CHECK.  Tests only."""
+    _check(load_library().pka_test_skip_copies(1 if on else 0))
 
 
 def kernel_launches() -> int:

@@ -27,6 +27,8 @@ static thread_local cudaEvent_t g_ev_start[2] = {nullptr, nullptr};
 static thread_local cudaEvent_t g_ev_stop[2] = {nullptr, nullptr};
 
 static thread_local uint64_t g_launches = 0;
+// Failure-path test hook (pka_test_skip_copies).
+static thread_local int32_t g_test_skip_copies = 0;
 void count_launch() { ++g_launches; }
 
 static void record_start(int which, cudaStream_t st)
@@ -305,6 +307,12 @@ pka_status pka_set_kernel_events(int32_t kernel, void *start, void *stop)
     return PKA_OK;
 }
 
+pka_status pka_test_skip_copies(int32_t on)
+{
+    g_test_skip_copies = on ? 1 : 0;
+    return PKA_OK;
+}
+
 pka_status pka_reshape_and_cache(const void *key, const void *value, void *kv_cache,
                                  const int64_t *slot_mapping, int32_t num_tokens,
                                  int32_t num_kv_heads, int32_t head_size, int32_t block_size,
@@ -474,6 +482,7 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
     f.causal = causal;
     f.stream = static_cast<cudaStream_t>(stream);
     f.num_sms = sm_count();
+    f.test_skip_copies = g_test_skip_copies;
     if (fuse) {
         f.fuse_write = 1;
         f.new_key = fuse->key;

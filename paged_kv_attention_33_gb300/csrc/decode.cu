@@ -103,6 +103,7 @@ struct DecodeParams {
     // fp8 pool: element value = code value x scale (K, V)
     float k_scale;
     float v_scale;
+    int32_t test_skip_copies;  // failure-path test: the producer issues nothing
 };
 
 constexpr int kConsumerWarps = 8;
@@ -544,9 +545,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                            : (blk * 2 + kv) * p.block_size + (ks % p.block_size);
             }
         };
+        // stages [lo, armed) have been armed (expect_tx) and their copies issued
+        int64_t armed = lo;
         int row_next, c1_next, live_next;
         lookup(lo, s, row_next, c1_next, live_next);
-        for (int64_t x = lo; x < hi; ++x) {
+        for (int64_t x = p.test_skip_copies ? hi : lo; x < hi; ++x) {
             const int i = int(x - lo);
             const int row = row_next, c1 = c1_next, live16 = live_next;
             const int slot = i % Cfg::kStages;
@@ -564,12 +567,23 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 tma_load_3d(dst, &kv_map, &full[slot], half * (128 / (kFp8 ? 1 : 2)), c1, row,
                             policy);
             }
+            armed = x + 1;
             // the next stage's blocks are looked up after this one is issued
             if (x + 1 < hi) {
                 while (prefix[s + 1] <= x + 1)
                     ++s;
                 lookup(x + 1, s, row_next, c1_next, live_next);
             }
+        }
+        // Wind-down: the CTA must not exit while a copy it issued still writes
+        // its shared memory.  A stage is refilled only after the consumers
+        // freed it, which they do after its copies landed, so only the last
+        // kStages armed stages can still be in flight: wait for their full
+        // barriers (bounded, whatever the abort flag says).  On the normal
+        // path they completed long ago and each test succeeds at once.
+        for (int64_t x = armed - Cfg::kStages > lo ? armed - Cfg::kStages : lo; x < armed; ++x) {
+            const int i = int(x - lo);
+            mbar_wait(&full[i % Cfg::kStages], (i / Cfg::kStages) & 1);
         }
         return;
     }
@@ -1118,6 +1132,7 @@ static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Wor
     p.num_decodes_all = f.num_decodes;
     p.k_scale = f.k_scale;
     p.v_scale = f.v_scale;
+    p.test_skip_copies = f.test_skip_copies;
     // one launch per chunk of at most kMaxDecodeChunk decodes (stream ordered,
     // so chunks reuse the same partial slots and counters)
     for (int32_t seq0 = 0; seq0 < f.num_decodes; seq0 += dp.chunk) {

@@ -46,6 +46,9 @@ struct Fwd {
     int32_t causal;
     cudaStream_t stream;
     int num_sms;
+    // test hook of the failure path (pka_test_skip_copies): the kernels' TMA
+    // producers issue nothing, so the first bounded wait of every CTA runs out
+    int32_t test_skip_copies = 0;
 };
 
 // Plan of the decode part of a batch (persistent stream-K grid).

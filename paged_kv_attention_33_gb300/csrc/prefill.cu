@@ -95,6 +95,7 @@ struct PrefillParams {
     int32_t *item_counter;  // work items claimed so far (zeroed before each launch)
     int32_t kv_splits;      // shared_prefix: key chunks, split_tiles key tiles each
     int32_t split_tiles;
+    int32_t test_skip_copies;  // failure-path test: the producer issues nothing
 };
 
 template <int D>
@@ -551,8 +552,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const uint64_t pol_kv = l2_policy_evict_last();
             const uint64_t pol_q = l2_policy_evict_first();
             uint32_t li = 0, kv_it = 0, n_pub = 0;
+            // copies armed so far: Q loads, K and V stages (for the wind-down)
+            uint32_t q_armed = 0, k_armed = 0, v_armed = 0;
             PfItem it;
             for (;;) {
+                if (p.test_skip_copies)
+                    break;  // publish no item: the other roles' first wait runs out
                 // claim the next work item (dynamic: a CTA that finishes early
                 // takes more) and hand its index to the MMA and softmax warps
                 int item = 0;
@@ -595,6 +600,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 int blk_next = lane_block(0);
                 if (li > 0 && !pf_wait(bars.q_empty, (li - 1) & 1, abort_flag))
                     break;
+                ++q_armed;
                 if (lane == 0) {
                     const int ntiles = it.rows[1] > 0 ? 2 : 1;
                     mbar_arrive_expect_tx(bars.q_full, ntiles * Cfg::kTileBytes);
@@ -623,6 +629,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     if (lane == 0)
                         mbar_arrive_expect_tx(bar, bytes);
                     __syncwarp();
+                    (which ? v_armed : k_armed) = n + 1;
                     if (lane < nbox) {
                         // coordinates in the pool map: NHD (head, page*bs + offset),
                         // HND (offset, page*Hkv + head), page = block*2 + (K|V)
@@ -656,6 +663,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     break;
                 ++li;
             }
+            // Wind-down: the CTA must not exit (nor free its TMEM) while a copy
+            // this warp issued still writes shared memory.  A K or V stage is
+            // refilled only after the MMAs that read it completed, and a Q tile
+            // only after the last S of its item, so only the last kPfStages K
+            // and V stages and the last Q load can still be in flight: wait for
+            // their full barriers (bounded, whatever the abort flag says).  On
+            // the normal path each test succeeds at once.
+            for (uint32_t n = k_armed > kPfStages ? k_armed - kPfStages : 0; n < k_armed; ++n)
+                mbar_wait(&bars.k_full[n % kPfStages], (n / kPfStages) & 1);
+            for (uint32_t n = v_armed > kPfStages ? v_armed - kPfStages : 0; n < v_armed; ++n)
+                mbar_wait(&bars.v_full[n % kPfStages], (n / kPfStages) & 1);
+            if (q_armed > 0)
+                mbar_wait(bars.q_full, (q_armed - 1) & 1);
         } else if (warp == 1) {
             // ============================================================ MMA issuer
             // One elected lane issues every MMA and commit.  At N = 128 an MMA
@@ -885,6 +905,7 @@ cudaError_t launch_prefill(const Fwd &f, const PrefillPass &pass)
     p.item_counter = pass.item_counter;
     p.kv_splits = 1;
     p.split_tiles = 0;
+    p.test_skip_copies = f.test_skip_copies;
     if (pass.shared_prefix) {
         const int tiles = (pass.kv_cap - pass.kv_lo + kBN - 1) / kBN;
         p.kv_splits = std::max(1, pass.kv_splits);
