@@ -143,26 +143,96 @@ CUresult encode_kv_map(CUtensorMap *map, const void *cache, int32_t head_size,
     return encode_3d(map, dt, cache, D, Hkv, pages * bs, row, row * Hkv, box0, 1, box_rows);
 }
 
-// ------------------------------------------------------------ planning
-int32_t plan_prefix_splits(int32_t num_tokens, int32_t num_heads, int32_t prefix_len,
-                           int num_sms)
+CUresult encode_kv_map_heads(CUtensorMap *map, const void *cache, int32_t head_size,
+                             int32_t num_kv_heads, int32_t block_size, int64_t num_blocks,
+                             int32_t hnd, int32_t elem_bytes)
 {
+    const uint64_t D = uint64_t(head_size), Hkv = uint64_t(num_kv_heads),
+                   bs = uint64_t(block_size), pages = uint64_t(num_blocks) * 2;
+    const uint64_t row = D * uint64_t(elem_bytes);  // bytes of one (slot, head) row
+    const CUtensorMapDataType dt =
+        elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint32_t box0 = 128u / uint32_t(elem_bytes);  // one 128-byte swizzle row
+    if (hnd)  // (dim, offset, page*Hkv + head): a head's page is bs contiguous rows
+        return encode_3d(map, dt, cache, D, bs, pages * Hkv, row, row * bs, box0, 16,
+                         uint32_t(Hkv));
+    // (dim, page*bs + offset, head): the head is the outer dimension, one row apart
+    return encode_3d(map, dt, cache, D, pages * bs, Hkv, row * Hkv, row, box0, 16,
+                     uint32_t(Hkv));
+}
+
+// ------------------------------------------------------------ planning
+CascadePlan plan_cascade(int32_t num_tokens, int32_t num_heads, int32_t num_kv_heads,
+                         int32_t head_size, int32_t prefix_len, int32_t num_decodes,
+                         int32_t max_seq_len, bool kv_fp8, bool single_decode_launch,
+                         int num_sms)
+{
+    CascadePlan c;
     if (prefix_len <= 0 || num_tokens <= 0)
-        return 1;
-    const int64_t items = (int64_t(num_tokens) + 255) / 256 * num_heads;
+        return c;
+    const int64_t base_items = (int64_t(num_tokens) + 255) / 256 * num_heads;
     const int64_t tiles = (int64_t(prefix_len) + 127) / 128;
-    if (items >= num_sms)
-        return 1;
-    int64_t s = std::min<int64_t>(num_sms / items, std::max<int64_t>(1, tiles / 4));
-    const int64_t per = (tiles + s - 1) / s;  // tiles per chunk; no chunk is empty
-    s = (tiles + per - 1) / per;
-    return static_cast<int32_t>(std::max<int64_t>(1, s));
+    // Cost model in cycles.  A prefix work item of n key tiles costs about
+    // n + 1 tile pairs (one pair of start-up) of kPairCycles each; the suffix
+    // decode streams its KV at kSmBytesPerCycle per SM, at most
+    // kHbmBytesPerCycle over the chip, after a fixed start-up and tail.  The
+    // suffix length is not known on the host: half of max_seq_len - prefix_len
+    // per decode is taken (lengths spread evenly).  (Measured on GB300: the
+    // decode kernel streams ~80 GB/s per SM when HBM is not the limit, ~70 of
+    // fp8 codes, and saturates HBM on about 100 SMs; a tile pair of the
+    // tensor-core pass takes ~4,250 cycles.)
+    constexpr double kPairCycles = 4250.0;
+    constexpr double kPrefixStartCycles = 8000.0;
+    constexpr double kDecodeStartCycles = 30000.0;
+    const double kSmBytesPerCycle = kv_fp8 ? 34.0 : 39.0;
+    constexpr double kHbmBytesPerCycle = 3250.0;  // ~6.7 TB/s at ~2.07 GHz
+    const double suffix_keys =
+        double(num_decodes) * std::max(1.0, 0.5 * double(max_seq_len - prefix_len + 1));
+    const double dec_bytes = suffix_keys * num_kv_heads * head_size * 2.0 * (kv_fp8 ? 1.0 : 2.0);
+    auto t_dec = [&](int ctas) {
+        return ctas <= 0 ? 1e30
+                         : kDecodeStartCycles +
+                               dec_bytes / std::min(kHbmBytesPerCycle, ctas * kSmBytesPerCycle);
+    };
+    auto t_pre = [&](int64_t chunks, int ctas) {
+        const int64_t items = base_items * chunks;
+        const int64_t per = (tiles + chunks - 1) / chunks;
+        const int64_t waves = (items + ctas - 1) / ctas;
+        return kPrefixStartCycles + double(waves) * double(per + 1) * kPairCycles;
+    };
+    // serial: the prefix pass on every SM, then the decode on every SM
+    double best = 1e30;
+    for (int64_t s = 1; s <= kMaxPrefixSplits && tiles / s >= 2; ++s) {
+        const double t = t_pre(s, num_sms) + (num_decodes > 0 ? t_dec(num_sms) : 0.0);
+        if (t < best) {
+            best = t;
+            c.pre_splits = int32_t(s);
+            c.pre_ctas = num_sms;
+            c.overlap = false;
+        }
+    }
+    // side by side: the prefix pass on pre_ctas SMs, the decode on the rest
+    if (num_decodes > 0 && single_decode_launch && num_sms >= 16) {
+        for (int64_t s = 1; s <= kMaxPrefixSplits && tiles / s >= 2; ++s)
+            for (int x = 8; x <= num_sms - 8; ++x) {
+                const double t = std::max(t_pre(s, x), t_dec(num_sms - x));
+                if (t < best * 0.999) {
+                    best = t;
+                    c.pre_splits = int32_t(s);
+                    c.pre_ctas = x;
+                    c.overlap = true;
+                }
+            }
+    }
+    return c;
 }
 
 Workspace plan_workspace(const DecodePlan &dp, int32_t num_tokens, int32_t num_decodes,
                          int32_t num_heads, int32_t head_size, bool cascade,
                          int32_t pre_splits)
 {
+    // (a cascade: pre_splits shared-prefix partials and one suffix partial
+    // for every token, decodes included)
     Workspace w;
     size_t off = 0;
     // one partial per (CTA, sequence) piece: slot ids b + s < grid + chunk
@@ -180,7 +250,7 @@ Workspace plan_workspace(const DecodePlan &dp, int32_t num_tokens, int32_t num_d
     off = round256(off + rows_all * head_size * 4);
     w.lse_pre = off;
     off = round256(off + rows_all * 4);
-    const size_t rows_pf = cascade ? size_t(num_tokens - num_decodes) * num_heads : 0;
+    const size_t rows_pf = cascade ? size_t(num_tokens) * num_heads : 0;
     w.o_suf = off;
     off = round256(off + rows_pf * head_size * 4);
     w.lse_suf = off;
@@ -286,6 +356,36 @@ static pka_status check_shape(const pka_meta *m, int32_t num_tokens, int32_t num
                         head_size);
     }
     return PKA_OK;
+}
+
+// The whole host plan of one forward (pka_workspace_size and the forward
+// itself make the same one): decode grid, cascade split, workspace carve-up.
+struct ForwardPlan {
+    DecodePlan dp;
+    CascadePlan cp;
+    Workspace ws;
+};
+
+static ForwardPlan plan_forward(const pka_meta *m, int32_t num_tokens, int32_t num_heads,
+                                int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                int sms)
+{
+    ForwardPlan fp;
+    const bool cascade = m->common_prefix_len > 0;
+    const bool fp8 = m->kv_dtype == PKA_KV_FP8_E4M3;
+    fp.dp = plan_decode(m->split_kv_tokens, m->num_decodes, num_kv_heads, sms);
+    if (cascade) {
+        fp.cp = plan_cascade(num_tokens, num_heads, num_kv_heads, head_size,
+                             m->common_prefix_len, m->num_decodes, m->max_seq_len, fp8,
+                             fp.dp.chunk == m->num_decodes, sms);
+        if (fp.cp.overlap)
+            fp.dp.grid = sms - fp.cp.pre_ctas;  // the decode takes the SMs the prefix leaves
+    }
+    fp.ws = plan_workspace(fp.dp, num_tokens, m->num_decodes, num_heads, head_size, cascade,
+                           fp.cp.pre_splits);
+    plan_fp8_prefill(fp.ws, fp8, m->num_seqs, m->num_decodes, m->max_seq_len,
+                     m->common_prefix_len, block_size, num_kv_heads, head_size);
+    return fp;
 }
 
 }  // namespace pka
@@ -397,17 +497,9 @@ size_t pka_workspace_size(const pka_meta *meta, int32_t num_tokens, int32_t num_
 {
     if (check_shape(meta, num_tokens, num_heads, num_kv_heads, head_size, block_size) != PKA_OK)
         return 0;
-    const bool cascade = meta->common_prefix_len > 0;
-    const int32_t kv_begin = meta->common_prefix_len;
-    const int sms = sm_count();
-    DecodePlan dp = plan_decode(meta->split_kv_tokens, meta->num_decodes, num_kv_heads, sms);
-    const int32_t pre_splits = plan_prefix_splits(num_tokens, num_heads, kv_begin, sms);
-    Workspace w = plan_workspace(dp, num_tokens, meta->num_decodes, num_heads, head_size, cascade,
-                                 pre_splits);
-    plan_fp8_prefill(w, meta->kv_dtype == PKA_KV_FP8_E4M3, meta->num_seqs, meta->num_decodes,
-                     meta->max_seq_len, meta->common_prefix_len, block_size, num_kv_heads,
-                     head_size);
-    return w.total;
+    return plan_forward(meta, num_tokens, num_heads, num_kv_heads, head_size, block_size,
+                        sm_count())
+        .ws.total;
 }
 
 // This step's new K/V rows for pka_paged_attn_forward_fused.
@@ -491,13 +583,11 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
         f.kv_cache_w = fuse->kv_cache;
     }
 
-    DecodePlan dp = plan_decode(meta->split_kv_tokens, meta->num_decodes, num_kv_heads,
-                                f.num_sms);
-    const int32_t pre_splits = plan_prefix_splits(num_tokens, num_heads, kv_begin, f.num_sms);
-    Workspace ws = plan_workspace(dp, num_tokens, meta->num_decodes, num_heads, head_size, cascade,
-                                  pre_splits);
-    plan_fp8_prefill(ws, f.kv_fp8 != 0, meta->num_seqs, meta->num_decodes, meta->max_seq_len,
-                     meta->common_prefix_len, block_size, num_kv_heads, head_size);
+    const ForwardPlan plan = plan_forward(meta, num_tokens, num_heads, num_kv_heads, head_size,
+                                          block_size, f.num_sms);
+    const DecodePlan &dp = plan.dp;
+    const CascadePlan &cp = plan.cp;
+    const Workspace &ws = plan.ws;
     if (ws.fp8_scratch_blocks * 2 * block_size >= (int64_t(1) << 31))
         return fail(PKA_ERR_UNSUPPORTED, "fp8 prefill copy has more than 2^31 rows");
     if (ws.total > 0 && (!workspace || workspace_bytes < ws.total || !aligned(workspace, 256)))
@@ -506,8 +596,8 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
     char *wsp = static_cast<char *>(workspace);
 
     CUtensorMap kv_map;
-    CUresult cr = encode_kv_map(&kv_map, kv_cache, head_size, num_kv_heads, block_size, num_blocks,
-                                f.kv_hnd, 16, f.kv_fp8 ? 1 : 2);
+    CUresult cr = encode_kv_map_heads(&kv_map, kv_cache, head_size, num_kv_heads, block_size,
+                                      num_blocks, f.kv_hnd, f.kv_fp8 ? 1 : 2);
     if (cr != CUDA_SUCCESS)
         return fail(PKA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(cr));
 
@@ -540,29 +630,58 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
         if (e != cudaSuccess)
             return cuda_fail(e, "fp8 block copy launch");
     }
+    // [blog] "Que aporta FlashInfer: JIT y cascade attention": with a shared
+    // prefix P, the prefix keys [0, P) are attended once for every query (a
+    // tensor-core pass with no mask), each sequence's own suffix [P, L_s) by
+    // the decode / prefill passes, and the parts are merged by log-sum-exp.
+    // The prefix pass is bound by the tensor cores and the suffix decode by
+    // HBM, so when the plan says so they run side by side on disjoint SMs: the
+    // decode is launched as the prefix pass's dependent (it starts on the SMs
+    // the pass leaves free and completes after it), its rows go out as fp32
+    // partials, and one combine kernel merges every token's parts at the end.
+    DecodeOut dout;
     if (cascade) {
-        // [blog] "Que aporta FlashInfer: JIT y cascade attention": the shared
-        // prefix once for every query (tensor cores, no mask), each sequence's
-        // own suffix [P, L_s), then a log-sum-exp merge of the parts.
+        dout.o_suf = reinterpret_cast<float *>(wsp + ws.o_suf);
+        dout.lse_suf = reinterpret_cast<float *>(wsp + ws.lse_suf);
+        dout.after_prefix = cp.overlap;
+        if (cp.overlap) {
+            // nothing may stand between the two launches: zero the decode's
+            // counters first
+            e = cudaMemsetAsync(wsp + ws.counters, 0, size_t(dp.chunk) * 4, f.stream);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "counter reset");
+            dout.counters_zeroed = true;
+            // the two passes run at the same time: both timing brackets
+            // (instrumentation) cover the pair
+            record_start(PKA_KERNEL_PREFILL, f.stream);
+            record_start(PKA_KERNEL_DECODE, f.stream);
+        }
         PrefillPass pre{0, kv_begin, 0, true, reinterpret_cast<float *>(wsp + ws.o_pre),
                         reinterpret_cast<float *>(wsp + ws.lse_pre), 0,
-                        reinterpret_cast<int32_t *>(wsp + ws.pf_counters) + 1, pre_splits};
-        record_start(PKA_KERNEL_PREFILL, f.stream);
+                        reinterpret_cast<int32_t *>(wsp + ws.pf_counters) + 1, cp.pre_splits};
+        pre.max_ctas = cp.overlap ? cp.pre_ctas : 0;
+        pre.trigger_dependents = cp.overlap;
+        if (!cp.overlap)
+            record_start(PKA_KERNEL_PREFILL, f.stream);
         e = launch_prefill(fp, pre);
-        record_stop(PKA_KERNEL_PREFILL, f.stream);
+        if (!cp.overlap)
+            record_stop(PKA_KERNEL_PREFILL, f.stream);
         if (e != cudaSuccess)
             return cuda_fail(e, "cascade prefix launch");
     }
-    record_start(PKA_KERNEL_DECODE, f.stream);
-    e = launch_decode(f, dp, ws, wsp, kv_map, kv_begin, cascade);
+    if (!cp.overlap)
+        record_start(PKA_KERNEL_DECODE, f.stream);
+    e = launch_decode(f, dp, ws, wsp, kv_map, kv_begin, dout);
     record_stop(PKA_KERNEL_DECODE, f.stream);
+    if (cp.overlap)
+        record_stop(PKA_KERNEL_PREFILL, f.stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "decode launch");
     if (num_prefills > 0) {
         PrefillPass pf{kv_begin, INT32_MAX, causal ? 1 : 0, false,
                        cascade ? reinterpret_cast<float *>(wsp + ws.o_suf) : nullptr,
-                       cascade ? reinterpret_cast<float *>(wsp + ws.lse_suf) : nullptr,
-                       meta->num_decodes, reinterpret_cast<int32_t *>(wsp + ws.pf_counters)};
+                       cascade ? reinterpret_cast<float *>(wsp + ws.lse_suf) : nullptr, 0,
+                       reinterpret_cast<int32_t *>(wsp + ws.pf_counters)};
         // fp8 after the decode launch (which wrote this step's rows): the
         // prefill sequences' blocks
         if (f.kv_fp8 && meta->num_decodes > 0) {
@@ -580,7 +699,7 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
             return cuda_fail(e, "prefill launch");
     }
     if (cascade) {
-        e = launch_cascade_prefill_combine(f, ws, wsp);
+        e = launch_cascade_combine(f, ws, wsp);
         if (e != cudaSuccess)
             return cuda_fail(e, "cascade combine launch");
     }

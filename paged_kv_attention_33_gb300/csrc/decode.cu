@@ -20,11 +20,16 @@
 // CTA: 8 consumer warps + 1 producer warp.  A pipeline stage holds 8 "units";
 // unit u is 16 consecutive keys of kv head k = u % Hkv, slice r = u / Hkv of the
 // stage's 16*(8/Hkv) keys (so every warp works in every stage).  The producer
-// issues, per unit, one TMA box {64 dims, 1 head, 16 rows} per 64-dim half for
-// K and for V out of the pool viewed as a 3-D tensor
-// (head_size, num_kv_heads, num_blocks*2*block_size) -- the "FlashAttention y
-// FlashInfer" page's cache shape with (block, kv, offset) flattened -- with
-// 128-byte swizzling so that the ldmatrix reads below are conflict free.
+// issues, per slice and 64-dim half, one TMA box {64 dims, 16 keys, Hkv heads}
+// for K and one for V: the pool is viewed as a 3-D tensor whose outermost
+// dimension is the kv head (NHD: (head_size, num_blocks*2*block_size,
+// num_kv_heads), the head stride being one row; HND: (head_size, block_size,
+// num_blocks*2*num_kv_heads)) -- the "FlashAttention y FlashInfer" page's
+// cache shape with (block, kv, offset) flattened.  One box thus lands every
+// head's 16-key tile of the slice, head after head, 128-byte swizzled so that
+// the ldmatrix reads below are conflict free; a few large boxes per stage let
+// one SM stream almost twice the bytes that one small box per unit and half
+// did, so HBM is saturated long before every SM decodes.
 // Pages are found through the block table ("Como lee el backend el KV
 // paginado": the kernel gathers physical blocks, no contiguous KV).
 //
@@ -82,16 +87,21 @@ struct DecodeParams {
     int32_t nseq;         // decodes in this launch (<= kMaxDecodeChunk)
     int32_t kv_begin;     // first key (cascade suffix: the shared prefix length)
     int32_t target_keys;  // 0, or keys per CTA to aim for (fewer CTAs)
-    int32_t cascade;      // merge the shared-prefix partial into every row
     float scale_log2;     // softmax scale * log2(e)
     __nv_bfloat16 *out;
     float *lse;
+    // cascade suffix: each decode row's result over keys [kv_begin, L) goes to
+    // o_suf [T, H, D] as a normalised fp32 partial with its log2-sum-exp in
+    // lse_suf [T, H] (merged with the shared prefix later), not to out / lse
+    float *o_suf;
+    float *lse_suf;
+    // launched as the dependent of the cascade's shared-prefix pass, which
+    // runs on the other SMs at the same time: the grid completes only after
+    // that pass completed (griddepcontrol.wait before every CTA exits)
+    int32_t after_prefix;
     float *o_part;        // [slots, R, H, D] normalised partials
     float *lse_part;      // [slots, R, H], log2 units
-    int32_t *counters;    // [nseq] pieces finished per sequence (zeroed per launch)
-    const float *o_pre;   // cascade: shared-prefix partials [pre_splits][T, H, D]
-    const float *lse_pre; // [pre_splits][T, H], log2 units
-    int32_t pre_splits;   // cascade: shared-prefix partials per row
+    int32_t *counters;    // [nseq] pieces finished per sequence (zeroed before the launch)
     // fused cache write (pka_paged_attn_forward_fused): this step's K/V rows
     // [T, Hkv, D] and their slots; the pool is written through `pool`
     int32_t fuse_write;
@@ -120,7 +130,11 @@ struct DecodeCfg {
     static constexpr int kUnitKeys = kFp8 ? 32 : 16;               // keys of one unit
     static constexpr int kRowBytes = D * (kFp8 ? 1 : 2);           // one key of one head
     static constexpr int kHalves = kRowBytes / 128;                // 128-byte TMA boxes per row
-    static constexpr int kBoxes = kHalves * kUnitKeys / 16;        // 2 KB boxes per unit
+    static constexpr int kBoxes = kHalves * kUnitKeys / 16;        // 2 KB tiles of a unit
+    // Shared-memory layout of K (and of V) in a stage: for each slice r, box b
+    // (a 64-dim half, or an fp8 unit's 16-key half) and head k, the 16-key
+    // tile of 2 KB at ((r * kBoxes + b) * Hkv + k) * 2048; unit (k, r) starts
+    // at r * Hkv * kUnitBytes + k * 2048 and its box b is Hkv * 2048 further.
     static constexpr int kUnitBytes = kUnitKeys * kRowBytes;
     static constexpr int kKvBytes = kConsumerWarps * kUnitBytes;   // all units of K (or V)
     static constexpr int kStageBytes = 2 * kKvBytes;
@@ -204,13 +218,13 @@ __device__ __forceinline__ float warp_sum32(float v)
 }
 
 // Merge the partials of decode s (token t): its nparts pieces -- part q lives
-// in slot (bf + q / R + s), sub-row q % R -- and, in a cascade, the
-// pre_splits partials of the shared prefix (key chunk c at rows c*T*H + t*H +
-// h).  Warp w takes heads w, w+8, ..., kHB of them at a time, lanes along
-// head_size.  The parts are folded in rounds of kQB: every load of a round
-// (kQB x kHB log2-sum-exps and rows) is issued before any is used, so a merge
-// costs about one L2 round trip per round -- it runs at the end of a CTA's
-// range, while the other SMs still stream, where each round trip is long.
+// in slot (bf + q / R + s), sub-row q % R.  Warp w takes heads w, w+8, ..., kHB
+// of them at a time, lanes along head_size.  The parts are folded in rounds of
+// kQB: every load of a round (kQB x kHB log2-sum-exps and rows) is issued
+// before any is used, so a merge costs about one L2 round trip per round -- it
+// runs at the end of a CTA's range, while the other SMs still stream, where
+// each round trip is long.  The merged row goes to out / lse (bf16, ln), or in
+// a cascade suffix to o_suf / lse_suf (fp32, log2).
 template <int D, int kQB = 2, int kHB = 4>  // kQB: parts per round, kHB: heads per batch
 __device__ __forceinline__ void merge_pieces(const DecodeParams &p, int t, int s, int bf,
                                              int nparts, int R, int warp, int lane)
@@ -218,11 +232,6 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, int t, int s
     constexpr int kPer = D / 32;  // dims per lane
     using Vec = typename std::conditional<kPer == 4, float4, float2>::type;
     const int H = p.num_heads;
-    const int ntot = nparts + (p.cascade ? p.pre_splits : 0);
-    auto row_of = [&](int q, int h) -> int64_t {  // row of part q, head h
-        return q < nparts ? (int64_t(bf + q / R + s) * R + q % R) * H + h
-                          : (int64_t(q - nparts) * p.num_tokens + t) * H + h;
-    };
     for (int h0 = warp; h0 < H; h0 += kHB * kConsumerWarps) {
         float M[kHB], W[kHB], acc[kHB][kPer];
 #pragma unroll
@@ -233,21 +242,19 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, int t, int s
             for (int e = 0; e < kPer; ++e)
                 acc[j][e] = 0.f;
         }
-        for (int q0 = 0; q0 < ntot; q0 += kQB) {
+        for (int q0 = 0; q0 < nparts; q0 += kQB) {
             float lq[kQB][kHB];
             Vec v[kQB][kHB];
 #pragma unroll
             for (int i = 0; i < kQB; ++i) {
-                const int q = q0 + i;
+                const int q = q0 + i < nparts ? q0 + i : 0;
                 // the kHB heads of part q are rows row0 + 8j: one base address
-                const int64_t row0 = row_of(q < ntot ? q : 0, h0);
-                const float *lq_p = (q < nparts ? p.lse_part : p.lse_pre) + row0;
-                const Vec *v_p =
-                    reinterpret_cast<const Vec *>((q < nparts ? p.o_part : p.o_pre) + row0 * D) +
-                    lane;
+                const int64_t row0 = (int64_t(bf + q / R + s) * R + q % R) * H + h0;
+                const float *lq_p = p.lse_part + row0;
+                const Vec *v_p = reinterpret_cast<const Vec *>(p.o_part + row0 * D) + lane;
 #pragma unroll
                 for (int j = 0; j < kHB; ++j) {
-                    if (q < ntot && h0 + j * kConsumerWarps < H) {
+                    if (q0 + i < nparts && h0 + j * kConsumerWarps < H) {
                         lq[i][j] = __ldcg(lq_p + j * kConsumerWarps);
                         v[i][j] = __ldcg(v_p + j * kConsumerWarps * (D / kPer));
                     } else {
@@ -289,69 +296,28 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, int t, int s
                 continue;
             const int64_t row_out = int64_t(t) * H + h;
             const float inv = W[j] > 0.f ? 1.f / W[j] : 0.f;
+            const float lse2 = W[j] > 0.f ? M[j] + log2f(W[j]) : kNegInf;
+            if (p.o_suf) {
+                float *dst = p.o_suf + row_out * D + lane * kPer;
+                Vec r;
+                float *rr = reinterpret_cast<float *>(&r);
+#pragma unroll
+                for (int e = 0; e < kPer; ++e)
+                    rr[e] = acc[j][e] * inv;
+                *reinterpret_cast<Vec *>(dst) = r;
+                if (lane == 0)
+                    p.lse_suf[row_out] = lse2;
+                continue;
+            }
             __nv_bfloat16 *dst = p.out + row_out * D + lane * kPer;
 #pragma unroll
             for (int e = 0; e < kPer; e += 2)
                 *reinterpret_cast<__nv_bfloat162 *>(dst + e) =
                     __floats2bfloat162_rn(acc[j][e] * inv, acc[j][e + 1] * inv);
             if (lane == 0 && p.lse)
-                p.lse[row_out] = W[j] > 0.f ? (M[j] + log2f(W[j])) * kLn2 : kNegInf;
+                p.lse[row_out] = lse2 * kLn2;
         }
     }
-}
-
-// Cascade, a sequence finished inside one warp: fold the pre_splits prefix
-// partials of its two heads (rows h0, h1 of token t) into this thread's slice
-// of the transposed accumulator o (dims 16*mt + gq and +8; o[mt][0|2] head h0,
-// o[mt][1|3] head h1), whose rows still need the scales sc0 / sc1 and whose
-// log2-sum-exps are ls0 / ls1.  On return o * sc is the merged row and ls its
-// log2-sum-exp.
-template <int D>
-__device__ __forceinline__ void merge_prefix_direct(const DecodeParams &p, int t, int h0, int h1,
-                                                    int gq, float (&o)[D / 16][4], float &sc0,
-                                                    float &sc1, float &ls0, float &ls1)
-{
-    const int64_t split_rows = int64_t(p.num_tokens) * p.num_heads;
-    const int64_t r0 = int64_t(t) * p.num_heads + h0;
-    const int64_t r1 = int64_t(t) * p.num_heads + h1;
-    float M0 = ls0, M1 = ls1;
-    for (int c = 0; c < p.pre_splits; ++c) {
-        M0 = fmaxf(M0, __ldg(p.lse_pre + c * split_rows + r0));
-        M1 = fmaxf(M1, __ldg(p.lse_pre + c * split_rows + r1));
-    }
-    // an empty part adds nothing
-    const float a0 = ls0 == kNegInf ? 0.f : exp2f(ls0 - M0);
-    const float a1 = ls1 == kNegInf ? 0.f : exp2f(ls1 - M1);
-    float W0 = a0, W1 = a1;
-    const float f0 = sc0 * a0, f1 = sc1 * a1;
-#pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) {
-        o[mt][0] *= f0;
-        o[mt][2] *= f0;
-        o[mt][1] *= f1;
-        o[mt][3] *= f1;
-    }
-    for (int c = 0; c < p.pre_splits; ++c) {
-        const float l0 = __ldg(p.lse_pre + c * split_rows + r0);
-        const float l1 = __ldg(p.lse_pre + c * split_rows + r1);
-        const float w0 = l0 == kNegInf ? 0.f : exp2f(l0 - M0);
-        const float w1 = l1 == kNegInf ? 0.f : exp2f(l1 - M1);
-        W0 += w0;
-        W1 += w1;
-        const float *b0 = p.o_pre + (c * split_rows + r0) * D + gq;
-        const float *b1 = p.o_pre + (c * split_rows + r1) * D + gq;
-#pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
-            o[mt][0] += w0 * __ldg(b0 + 16 * mt);
-            o[mt][2] += w0 * __ldg(b0 + 16 * mt + 8);
-            o[mt][1] += w1 * __ldg(b1 + 16 * mt);
-            o[mt][3] += w1 * __ldg(b1 + 16 * mt + 8);
-        }
-    }
-    sc0 = W0 > 0.f ? 1.f / W0 : 0.f;
-    sc1 = W1 > 0.f ? 1.f / W1 : 0.f;
-    ls0 = W0 > 0.f ? M0 + log2f(W0) : kNegInf;
-    ls1 = W1 > 0.f ? M1 + log2f(W1) : kNegInf;
 }
 
 // 16 e4m3 codes of chunk c (elements 16c..16c+15) of token tk's row of kv
@@ -409,9 +375,9 @@ __device__ __forceinline__ void write_pool_row(const DecodeParams &p, int64_t tk
     }
 }
 
+// The work of one CTA (the kernel below adds the wait of a dependent launch).
 template <int D, bool kHnd, bool kFp8>
-__global__ void __launch_bounds__(kDecodeThreads, 1)
-    paged_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p)
+__device__ __forceinline__ void decode_cta(const CUtensorMap &kv_map, const DecodeParams &p)
 {
     static_assert(!kFp8 || D == 128, "the fp8 tile addressing assumes 128-byte rows");
     using Cfg = DecodeCfg<D, kFp8>;
@@ -501,28 +467,25 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
-        // lane = one 2 KB box (16 keys x 128 bytes) of every stage: (unit, K|V,
-        // box), box = the 128-byte half of a bf16 row, or the 16-key half of an
-        // fp8 unit; its block id is looked up for the next stage before waiting
-        // for a free slot
+        // lane = one box of every stage: (slice r, K|V, box b), box = the
+        // 128-byte half of a bf16 row, or the 16-key half of an fp8 unit, over
+        // all Hkv heads (2 KB per head); its block id is looked up for the next
+        // stage before waiting for a free slot
         if (lane == 0)
             tma_prefetch_desc(&kv_map);
         const uint64_t policy = l2_policy_evict_first();
-        constexpr int kOps = kConsumerWarps * 2 * Cfg::kBoxes;  // <= 32
-        static_assert(kOps <= 32, "one box per lane");
-        const int u = lane % kConsumerWarps;
-        const int kv = (lane / kConsumerWarps) & 1;
-        const int box = lane / (2 * kConsumerWarps);
+        const int ops = R * 2 * Cfg::kBoxes;  // <= 8 * 2 * 2
+        const int r = lane / (2 * Cfg::kBoxes);
+        const int kv = (lane / Cfg::kBoxes) & 1;
+        const int box = lane % Cfg::kBoxes;
         const int half = kFp8 ? 0 : box;          // 128-byte half of the row
         const int key_off = kFp8 ? 16 * box : 0;  // first key of the box in the unit
-        const int r = u / Hkv;
-        const int k = u % Hkv;
         int s = s_first;
-        // TMA coordinates of the box's 16 keys in the pool map: NHD (head,
-        // page*bs + offset), HND (offset, page*Hkv + head), page = block*2 + (K|V);
-        // row = -1: no keys (a box whose first key is past the end is not loaded,
-        // its block-table entry is not valid); live16 = loaded 16-key blocks of
-        // each kv head, the same for all lanes
+        // TMA coordinates of the box's 16 keys in the pool map: NHD (page*bs +
+        // offset, head 0), HND (offset, page*Hkv + head 0), page = block*2 +
+        // (K|V); row = -1: no keys (a box whose first key is past the end is not
+        // loaded, its block-table entry is not valid); live16 = loaded 16-key
+        // blocks of each kv head, the same for all lanes
         auto lookup = [&](int64_t x, int seq, int &row, int &c1, int &live16) {
             // the table entry is read before the length is known (the row of
             // the table is in bounds), so that both loads are in flight at once
@@ -530,19 +493,24 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             const int ks = k0 + Cfg::kUnitKeys * r + key_off;
             const int col = ks / p.block_size;
             const int32_t *bt = p.block_table + int64_t(p.seq0 + seq) * p.bt_stride;
-            const int blk_raw = lane < kOps && col < p.bt_stride ? bt[col] : -1;
+            const int blk_raw = lane < ops && col < p.bt_stride ? bt[col] : -1;
             const int L = p.seq_lens[p.seq0 + seq];
             live16 = max(0, min(R * Cfg::kUnitKeys / 16, (L - k0 + 15) / 16));
             row = -1;
-            c1 = kHnd ? ks % p.block_size : k;
-            if (lane < kOps && ks < L) {
+            c1 = 0;
+            if (lane < ops && ks < L) {
                 int blk = blk_raw;
                 if (blk < 0 || blk >= p.num_blocks) {
                     flag_error(kErrBlockOutOfPool);
                     blk = 0;  // keep the transaction count whole; result is flagged
                 }
-                row = kHnd ? (blk * 2 + kv) * Hkv + k
-                           : (blk * 2 + kv) * p.block_size + (ks % p.block_size);
+                if (kHnd) {
+                    c1 = ks % p.block_size;
+                    row = (blk * 2 + kv) * Hkv;
+                } else {
+                    c1 = (blk * 2 + kv) * p.block_size + (ks % p.block_size);
+                    row = 0;
+                }
             }
         };
         // stages [lo, armed) have been armed (expect_tx) and their copies issued
@@ -563,7 +531,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             __syncwarp();
             if (row >= 0) {
                 uint8_t *dst = smem + slot * Cfg::kStageBytes + kv * Cfg::kKvBytes +
-                               u * Cfg::kUnitBytes + box * 2048;
+                               (r * Cfg::kBoxes + box) * Hkv * 2048;
                 tma_load_3d(dst, &kv_map, &full[slot], half * (128 / (kFp8 ? 1 : 2)), c1, row,
                             policy);
             }
@@ -596,6 +564,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const int tq = lane & 3;   // thread-in-quad
     const int gq = lane >> 2;  // quad index
     const int H = p.num_heads;
+    const uint32_t bstride = uint32_t(Hkv) * 2048;  // from one box of a unit to the next
 
     // ldmatrix lane addressing (rows = keys of the unit tile)
     const uint32_t k_row = (lane & 7) + ((lane >> 3) & 1) * 8;  // K: non-transposed A
@@ -720,8 +689,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const int ks = p.kv_begin + int(x - prefix[s]) * stage_keys + Cfg::kUnitKeys * r;
         const int valid = min(Cfg::kUnitKeys, L - ks);
         if (ok && valid > 0) {
-            const uint32_t kbase =
-                smem_addr(smem + slot * Cfg::kStageBytes + u * Cfg::kUnitBytes);
+            // this unit's first 16-key tile of K; its box b lies b * bstride on
+            const uint32_t kbase = smem_addr(smem + slot * Cfg::kStageBytes +
+                                             r * Hkv * Cfg::kUnitBytes + k * 2048);
             const uint32_t vbase = kbase + Cfg::kKvBytes;
             if (p.fuse_write && L - 1 < ks + Cfg::kUnitKeys) {
                 // this stage holds the decode's new key (key L-1): the pool may
@@ -743,9 +713,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                         else
                             nr = __ldg((kv ? p.new_value : p.new_key) +
                                        (int64_t(t) * Hkv + k) * kChunks + c);
-                        const uint32_t o = (c >> 3) * 2048 + swz128(L - 1 - ks, c & 7);
+                        // the row's 16-byte chunk c: box = its half (bf16) or its
+                        // 16-key half (fp8), then row and chunk in that tile
+                        const int kr = L - 1 - ks;
+                        const uint32_t o = (kFp8 ? kr >> 4 : c >> 3) * bstride +
+                                           swz128(kr & 15, c & 7);
                         uint8_t *tile = smem + slot * Cfg::kStageBytes + kv * Cfg::kKvBytes +
-                                        u * Cfg::kUnitBytes;
+                                        r * Hkv * Cfg::kUnitBytes + k * 2048;
                         *reinterpret_cast<uint4 *>(tile + o) = nr;
                         // the stage is refilled by TMA later: order this generic
                         // write before the async proxy's
@@ -771,8 +745,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                     float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int hh = 0; hh < D / 64; ++hh) {
-                        const uint4 kr0 = lds128(kbase + swz128(16 * t2 + ka, 4 * hh + tq));
-                        const uint4 kr1 = lds128(kbase + swz128(16 * t2 + ka + 2, 4 * hh + tq));
+                        const uint4 kr0 = lds128(kbase + t2 * bstride + swz128(ka, 4 * hh + tq));
+                        const uint4 kr1 =
+                            lds128(kbase + t2 * bstride + swz128(ka + 2, 4 * hh + tq));
 #pragma unroll
                         for (int m = 0; m < 4; ++m) {
                             uint32_t a0, a1, a2, a3;
@@ -831,7 +806,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 #pragma unroll
                     for (int mt = 0; mt < D / 16; ++mt) {
                         uint32_t v[4];  // [tile 0: dim gq, dim gq+8, tile 1: dim gq, dim gq+8]
-                        ldsm_x2_trans_b8(vbase + swz128(vrow, mt), v[0], v[1], v[2], v[3]);
+                        ldsm_x2_trans_b8(vbase + (vrow >> 4) * bstride + swz128(vrow & 15, mt),
+                                         v[0], v[1], v[2], v[3]);
                         if constexpr (decltype(masked)::value) {
                             v[0] &= mk0;
                             v[1] &= mk0;
@@ -858,7 +834,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t ch = 2 * kk + k_chunk;
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4(kbase + (ch >> 3) * 2048 + swz128(k_row, ch & 7), a0, a1, a2, a3);
+                    ldsm_x4(kbase + (ch >> 3) * bstride + swz128(k_row, ch & 7), a0, a1, a2, a3);
                     mma_bf16_16816(c, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
                 }
                 const bool va = gq < valid, vb = gq + 8 < valid;
@@ -888,7 +864,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                     for (int mt = 0; mt < D / 16; ++mt) {
                         const uint32_t ch = 2 * mt + v_chunk;
                         uint32_t a0, a1, a2, a3;
-                        ldsm_x4_trans(vbase + (ch >> 3) * 2048 + swz128(v_row, ch & 7), a0, a1,
+                        ldsm_x4_trans(vbase + (ch >> 3) * bstride + swz128(v_row, ch & 7), a0, a1,
                                       a2, a3);
                         if constexpr (decltype(masked)::value) {
                             a0 &= mlo;
@@ -918,7 +894,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const int bl = cta_of_stage(prefix[s + 1] - 1, total, grid);
         const int np = bl - bf + 1;
         // a sequence inside one CTA (and one warp per kv head) is finished from
-        // registers; in a cascade its prefix partials are merged in right here
+        // registers
         const bool direct = np == 1 && R == 1;
         const int n0 = 2 * tq, n1 = 2 * tq + 1;  // the two heads of this thread
         // row scales of the output (an fp8 pool's V dequantisation folded in)
@@ -927,30 +903,41 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const float i1 = lr1 > 0.f ? vsc / lr1 : 0.f;
         if (direct) {
             if (ok) {
-                float sc0 = i0, sc1 = i1;  // row scales of the output
-                float ls0 = m0 + log2f(lr0), ls1 = m1 + log2f(lr1);  // log2-sum-exp
-                if (p.cascade)  // (both pools: o holds dims 16*mt + gq and +8)
-                    merge_prefix_direct<D>(p, t, k * g + min(n0, g - 1), k * g + min(n1, g - 1),
-                                           gq, o, sc0, sc1, ls0, ls1);
+                // log2-sum-exp of the two heads (-inf: no key)
+                const float ls0 = lr0 > 0.f ? m0 + log2f(lr0) : kNegInf;
+                const float ls1 = lr1 > 0.f ? m1 + log2f(lr1) : kNegInf;
+                const int64_t r0 = int64_t(t) * H + k * g + n0;
+                const int64_t r1 = r0 + 1;
 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt) {  // dims 16*mt + gq and +8
                     const int d = 16 * mt + gq;
+                    if (p.o_suf) {  // cascade suffix: fp32 partial rows
+                        if (n0 < g) {
+                            p.o_suf[r0 * D + d] = o[mt][0] * i0;
+                            p.o_suf[r0 * D + d + 8] = o[mt][2] * i0;
+                        }
+                        if (n1 < g) {
+                            p.o_suf[r1 * D + d] = o[mt][1] * i1;
+                            p.o_suf[r1 * D + d + 8] = o[mt][3] * i1;
+                        }
+                        continue;
+                    }
                     if (n0 < g) {
-                        __nv_bfloat16 *dst = p.out + (int64_t(t) * H + k * g + n0) * D;
-                        dst[d] = __float2bfloat16_rn(o[mt][0] * sc0);
-                        dst[d + 8] = __float2bfloat16_rn(o[mt][2] * sc0);
+                        p.out[r0 * D + d] = __float2bfloat16_rn(o[mt][0] * i0);
+                        p.out[r0 * D + d + 8] = __float2bfloat16_rn(o[mt][2] * i0);
                     }
                     if (n1 < g) {
-                        __nv_bfloat16 *dst = p.out + (int64_t(t) * H + k * g + n1) * D;
-                        dst[d] = __float2bfloat16_rn(o[mt][1] * sc1);
-                        dst[d + 8] = __float2bfloat16_rn(o[mt][3] * sc1);
+                        p.out[r1 * D + d] = __float2bfloat16_rn(o[mt][1] * i1);
+                        p.out[r1 * D + d + 8] = __float2bfloat16_rn(o[mt][3] * i1);
                     }
                 }
-                if (gq == 0 && p.lse) {
-                    if (n0 < g)
-                        p.lse[int64_t(t) * H + k * g + n0] = ls0 * kLn2;
-                    if (n1 < g)
-                        p.lse[int64_t(t) * H + k * g + n1] = ls1 * kLn2;
+                if (gq == 0) {
+                    float *dst = p.o_suf ? p.lse_suf : p.lse;
+                    const float u = p.o_suf ? 1.f : kLn2;  // log2 partial, or ln
+                    if (dst && n0 < g)
+                        dst[r0] = ls0 * u;
+                    if (dst && n1 < g)
+                        dst[r1] = ls1 * u;
                 }
             }
         } else {
@@ -1000,61 +987,82 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     }
 }
 
+template <int D, bool kHnd, bool kFp8>
+__global__ void __launch_bounds__(kDecodeThreads, 1)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p)
+{
+    decode_cta<D, kHnd, kFp8>(kv_map, p);
+    // A cascade's suffix pass runs beside the shared-prefix pass (a dependent
+    // launch that starts while the prefix pass holds its SMs); its CTAs wait
+    // here for that grid to complete, so that the kernels after this one see
+    // both passes' partials.  The prefix pass never waits on this grid.
+    if (p.after_prefix)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // --------------------------------------------------------------------- combine
-// Cascade only: every prefill token's suffix partial (from the prefill kernel)
-// merged with its pre_splits shared-prefix partials -- the log-sum-exp merge.
-// One warp per (token, head) row, lanes along head_size.
+// Cascade: every token's suffix partial (over keys [P, L), from the decode
+// kernel or the prefill kernel) merged with its pre_splits shared-prefix
+// partials (keys [0, P), one per key chunk) -- the log-sum-exp merge of the
+// "El especialista del plato estrella" blog ("Que aporta FlashInfer: JIT y
+// cascade attention").  One warp per (token, head) row, lanes along
+// head_size; every log2-sum-exp of a row is loaded before any is used, then
+// every part's row, so a row costs about two memory round trips.
 struct CombineParams {
     int32_t num_tokens;
-    int32_t num_decodes;
     int32_t num_heads;
-    int32_t pre_splits;
-    const float *o_pre;  // [pre_splits][T, H, D]
-    const float *lse_pre;
-    const float *o_suf;  // [T - num_decodes, H, D]
-    const float *lse_suf;
+    int32_t pre_splits;   // <= kMaxPrefixSplits
+    const float *o_pre;   // [pre_splits][T, H, D]
+    const float *lse_pre; // [pre_splits][T, H], log2 units
+    const float *o_suf;   // [T, H, D]
+    const float *lse_suf; // [T, H], log2 units
     __nv_bfloat16 *out;
     float *lse;
 };
 
 template <int D>
-__global__ void __launch_bounds__(256) cascade_prefill_combine_kernel(const CombineParams p)
+__global__ void __launch_bounds__(256) cascade_combine_kernel(const CombineParams p)
 {
     constexpr int kPer = D / 32;
-    const int64_t gw = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    constexpr int kParts = 1 + kMaxPrefixSplits;  // part 0: the suffix, 1 + c: prefix chunk c
+    using Vec = typename std::conditional<kPer == 4, float4, float2>::type;
+    const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t nrows = int64_t(p.num_tokens - p.num_decodes) * p.num_heads;
-    if (gw >= nrows)
+    const int64_t rows = int64_t(p.num_tokens) * p.num_heads;
+    if (row >= rows)
         return;
-    const int64_t row = int64_t(p.num_decodes) * p.num_heads + gw;
-    const int64_t split_rows = int64_t(p.num_tokens) * p.num_heads;
-    const int nparts = 1 + p.pre_splits;  // part 0: the suffix, part 1 + c: prefix chunk c
-    auto lse_of = [&](int q) {
-        return q == 0 ? p.lse_suf[gw] : p.lse_pre[(q - 1) * split_rows + row];
-    };
-    auto o_of = [&](int q) {
-        return (q == 0 ? p.o_suf + gw * D : p.o_pre + ((q - 1) * split_rows + row) * D) +
-               lane * kPer;
-    };
+    const int nparts = 1 + p.pre_splits;
+    float l[kParts];
+#pragma unroll
+    for (int q = 0; q < kParts; ++q)
+        l[q] = q >= nparts ? kNegInf
+                           : q == 0 ? __ldcg(p.lse_suf + row)
+                                    : __ldcg(p.lse_pre + (q - 1) * rows + row);
     float mx = kNegInf;
-    for (int q = 0; q < nparts; ++q)
-        mx = fmaxf(mx, lse_of(q));
+#pragma unroll
+    for (int q = 0; q < kParts; ++q)
+        mx = fmaxf(mx, l[q]);
+    Vec v[kParts];
+#pragma unroll
+    for (int q = 0; q < kParts; ++q) {
+        // an empty part (lse = -inf) adds nothing: its row is not read
+        const float *src = q == 0 ? p.o_suf + row * D : p.o_pre + ((q - 1) * rows + row) * D;
+        v[q] = l[q] != kNegInf ? __ldcg(reinterpret_cast<const Vec *>(src) + lane) : Vec{};
+    }
     float acc[kPer];
 #pragma unroll
     for (int e = 0; e < kPer; ++e)
         acc[e] = 0.f;
     float ws = 0.f;
     if (mx != kNegInf) {
-        for (int q = 0; q < nparts; ++q) {
-            const float lq = lse_of(q);
-            if (lq == kNegInf)
-                continue;  // an empty part adds nothing (warp-uniform)
-            const float w = exp2f(lq - mx);
+#pragma unroll
+        for (int q = 0; q < kParts; ++q) {
+            const float w = l[q] == kNegInf ? 0.f : exp2f(l[q] - mx);
             ws += w;
-            const float *src = o_of(q);
+            const float *x = reinterpret_cast<const float *>(&v[q]);
 #pragma unroll
             for (int e = 0; e < kPer; ++e)
-                acc[e] += w * src[e];
+                acc[e] += w * x[e];
         }
     }
     const float inv = ws > 0.f ? 1.f / ws : 0.f;
@@ -1083,7 +1091,7 @@ DecodePlan plan_decode(int32_t split_kv_tokens, int32_t num_decodes, int32_t num
 template <int D, bool kHnd, bool kFp8>
 static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Workspace &ws,
                                    char *wsp, const CUtensorMap &kv_map, int32_t kv_begin,
-                                   bool cascade)
+                                   const DecodeOut &dout)
 {
     using Cfg = DecodeCfg<D, kFp8>;
     // devices (bit d for device d < 64) on which this instantiation's launch
@@ -1114,16 +1122,14 @@ static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Wor
     p.num_blocks = static_cast<int32_t>(f.num_blocks);
     p.kv_begin = kv_begin;
     p.target_keys = dp.target_keys;
-    p.cascade = cascade ? 1 : 0;
     p.scale_log2 = f.scale * 1.4426950408889634f;
     p.out = static_cast<__nv_bfloat16 *>(f.out);
     p.lse = f.lse;
     p.o_part = reinterpret_cast<float *>(wsp + ws.o_part);
     p.lse_part = reinterpret_cast<float *>(wsp + ws.lse_part);
     p.counters = reinterpret_cast<int32_t *>(wsp + ws.counters);
-    p.o_pre = reinterpret_cast<const float *>(wsp + ws.o_pre);
-    p.lse_pre = reinterpret_cast<const float *>(wsp + ws.lse_pre);
-    p.pre_splits = ws.pre_splits;
+    p.o_suf = dout.o_suf;
+    p.lse_suf = dout.lse_suf;
     p.fuse_write = f.fuse_write;
     p.new_key = static_cast<const uint4 *>(f.new_key);
     p.new_value = static_cast<const uint4 *>(f.new_value);
@@ -1138,13 +1144,28 @@ static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Wor
     for (int32_t seq0 = 0; seq0 < f.num_decodes; seq0 += dp.chunk) {
         p.seq0 = seq0;
         p.nseq = std::min(dp.chunk, f.num_decodes - seq0);
-        cudaError_t e = cudaMemsetAsync(p.counters, 0, size_t(p.nseq) * 4, f.stream);
+        cudaError_t e = cudaSuccess;
+        if (seq0 > 0 || !dout.counters_zeroed)
+            e = cudaMemsetAsync(p.counters, 0, size_t(p.nseq) * 4, f.stream);
         if (e != cudaSuccess)
             return e;
+        // the first launch may be the dependent of the shared-prefix pass
+        // enqueued just before it (it then starts on the SMs that pass leaves)
+        p.after_prefix = seq0 == 0 && dout.after_prefix ? 1 : 0;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        cfg.gridDim = dim3(dp.grid);
+        cfg.blockDim = dim3(kDecodeThreads);
+        cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+        cfg.stream = f.stream;
+        if (p.after_prefix) {
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+        }
         count_launch();
-        paged_decode_kernel<D, kHnd, kFp8>
-            <<<dp.grid, kDecodeThreads, Cfg::kSmemBytes, f.stream>>>(kv_map, p);
-        e = cudaGetLastError();
+        e = cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, kHnd, kFp8>, kv_map, p);
         if (e != cudaSuccess)
             return e;
     }
@@ -1152,7 +1173,7 @@ static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Wor
 }
 
 cudaError_t launch_decode(const Fwd &f, const DecodePlan &dp, const Workspace &ws, char *wsp,
-                          const CUtensorMap &kv_map, int32_t kv_begin, bool cascade)
+                          const CUtensorMap &kv_map, int32_t kv_begin, const DecodeOut &dout)
 {
     if (f.num_decodes == 0)
         return cudaSuccess;
@@ -1160,25 +1181,26 @@ cudaError_t launch_decode(const Fwd &f, const DecodePlan &dp, const Workspace &w
         if (f.head_size != 128)
             return cudaErrorInvalidValue;
         return f.kv_hnd
-                   ? launch_decode_d<128, true, true>(f, dp, ws, wsp, kv_map, kv_begin, cascade)
-                   : launch_decode_d<128, false, true>(f, dp, ws, wsp, kv_map, kv_begin, cascade);
+                   ? launch_decode_d<128, true, true>(f, dp, ws, wsp, kv_map, kv_begin, dout)
+                   : launch_decode_d<128, false, true>(f, dp, ws, wsp, kv_map, kv_begin, dout);
     }
     if (f.head_size == 128)
         return f.kv_hnd
-                   ? launch_decode_d<128, true, false>(f, dp, ws, wsp, kv_map, kv_begin, cascade)
-                   : launch_decode_d<128, false, false>(f, dp, ws, wsp, kv_map, kv_begin, cascade);
-    return f.kv_hnd ? launch_decode_d<64, true, false>(f, dp, ws, wsp, kv_map, kv_begin, cascade)
-                    : launch_decode_d<64, false, false>(f, dp, ws, wsp, kv_map, kv_begin, cascade);
+                   ? launch_decode_d<128, true, false>(f, dp, ws, wsp, kv_map, kv_begin, dout)
+                   : launch_decode_d<128, false, false>(f, dp, ws, wsp, kv_map, kv_begin, dout);
+    return f.kv_hnd ? launch_decode_d<64, true, false>(f, dp, ws, wsp, kv_map, kv_begin, dout)
+                    : launch_decode_d<64, false, false>(f, dp, ws, wsp, kv_map, kv_begin, dout);
 }
 
-cudaError_t launch_cascade_prefill_combine(const Fwd &f, const Workspace &ws, char *wsp)
+cudaError_t launch_cascade_combine(const Fwd &f, const Workspace &ws, char *wsp)
 {
-    const int64_t warps = int64_t(f.num_tokens - f.num_decodes) * f.num_heads;
+    const int64_t warps = int64_t(f.num_tokens) * f.num_heads;
     if (warps == 0)
         return cudaSuccess;
+    if (ws.pre_splits < 1 || ws.pre_splits > kMaxPrefixSplits)
+        return cudaErrorInvalidValue;
     CombineParams p;
     p.num_tokens = f.num_tokens;
-    p.num_decodes = f.num_decodes;
     p.num_heads = f.num_heads;
     p.pre_splits = ws.pre_splits;
     p.o_pre = reinterpret_cast<const float *>(wsp + ws.o_pre);
@@ -1190,9 +1212,9 @@ cudaError_t launch_cascade_prefill_combine(const Fwd &f, const Workspace &ws, ch
     const unsigned grid = static_cast<unsigned>((warps * 32 + 255) / 256);
     count_launch();
     if (f.head_size == 128)
-        cascade_prefill_combine_kernel<128><<<grid, 256, 0, f.stream>>>(p);
+        cascade_combine_kernel<128><<<grid, 256, 0, f.stream>>>(p);
     else
-        cascade_prefill_combine_kernel<64><<<grid, 256, 0, f.stream>>>(p);
+        cascade_combine_kernel<64><<<grid, 256, 0, f.stream>>>(p);
     return cudaGetLastError();
 }
 

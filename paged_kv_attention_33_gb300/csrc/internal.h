@@ -83,11 +83,20 @@ struct Workspace {
 
 DecodePlan plan_decode(int32_t split_kv_tokens, int32_t num_decodes, int32_t num_kv_heads,
                        int num_sms);
-// Cascade: the shared-prefix pass has ceil(T/256)*H work items; when they
-// fill less than one wave of the persistent grid, the prefix keys are cut into
-// chunks (at least 4 key tiles each) so that items x chunks fill about one wave.
-int32_t plan_prefix_splits(int32_t num_tokens, int32_t num_heads, int32_t prefix_len,
-                           int num_sms);
+// Cascade (the shared-prefix pass and the suffix passes): how many key chunks
+// the prefix is cut into (each chunk's partial is merged later), and whether
+// the prefix pass runs on pre_ctas SMs beside the suffix decode on the other
+// SMs (overlap: the decode is a dependent launch that starts at once) or on
+// every SM before it.  Chosen on a cost model of both passes; host sizes only.
+struct CascadePlan {
+    int32_t pre_splits = 1;
+    int32_t pre_ctas = 0;  // 0: every SM
+    bool overlap = false;
+};
+CascadePlan plan_cascade(int32_t num_tokens, int32_t num_heads, int32_t num_kv_heads,
+                         int32_t head_size, int32_t prefix_len, int32_t num_decodes,
+                         int32_t max_seq_len, bool kv_fp8, bool single_decode_launch,
+                         int num_sms);
 Workspace plan_workspace(const DecodePlan &dp, int32_t num_tokens, int32_t num_decodes,
                          int32_t num_heads, int32_t head_size, bool cascade,
                          int32_t pre_splits);
@@ -117,13 +126,31 @@ cudaError_t launch_dequant_blocks(const Fwd &f, void *scratch, int32_t *table, i
                                   int64_t dst_base, int32_t table_stride);
 uint32_t kv_write_take_error();
 
+// Most key chunks of a cascade's shared-prefix pass (partials per row).
+constexpr int32_t kMaxPrefixSplits = 8;
+
+// Where the decode launch puts its rows.
+struct DecodeOut {
+    // nullptr: bf16 out / ln lse.  Else (cascade suffix) fp32 normalised
+    // partials [T, H, D] and log2 lse [T, H], merged with the prefix later.
+    float *o_suf = nullptr;
+    float *lse_suf = nullptr;
+    // the launch is the dependent of the shared-prefix pass enqueued just
+    // before it (programmatic stream serialisation: it starts on the SMs that
+    // pass leaves free, and its grid completes after that pass)
+    bool after_prefix = false;
+    // the first launch's per-sequence counters were zeroed by the caller
+    // (before the prefix pass, so that nothing stands between the two kernels)
+    bool counters_zeroed = false;
+};
+
 // decode.cu: paged decode of sequences [0, num_decodes) over keys
-// [kv_begin, L_s), stream-K over a persistent grid with the split combine
-// fused in; cascade: every row is also merged with its shared-prefix partial.
+// [kv_begin, L_s), stream-K over a persistent grid of dp.grid CTAs with the
+// split combine fused in.
 cudaError_t launch_decode(const Fwd &f, const DecodePlan &dp, const Workspace &ws, char *wsp,
-                          const CUtensorMap &kv_map, int32_t kv_begin, bool cascade);
-// Cascade: merge every prefill token's suffix partial with its prefix partial.
-cudaError_t launch_cascade_prefill_combine(const Fwd &f, const Workspace &ws, char *wsp);
+                          const CUtensorMap &kv_map, int32_t kv_begin, const DecodeOut &dout);
+// Cascade: merge every token's suffix partial with its shared-prefix partials.
+cudaError_t launch_cascade_combine(const Fwd &f, const Workspace &ws, char *wsp);
 uint32_t decode_take_error();
 
 // merge.cu
@@ -162,6 +189,10 @@ struct PrefillPass {
     int32_t token_base;
     int32_t *item_counter;  // device int32 for the dynamic work queue (zeroed per launch)
     int32_t kv_splits = 1;  // shared_prefix: key chunks
+    int32_t max_ctas = 0;   // 0: one CTA per SM; else at most this many CTAs
+    // let a dependent launch (the cascade's suffix decode) start as soon as
+    // every CTA of this pass is resident
+    bool trigger_dependents = false;
 };
 cudaError_t launch_prefill(const Fwd &f, const PrefillPass &pass);
 uint32_t prefill_take_error();
@@ -183,5 +214,16 @@ CUresult encode_3d_bf16(CUtensorMap *map, const void *base, uint64_t d0, uint64_
 CUresult encode_kv_map(CUtensorMap *map, const void *cache, int32_t head_size,
                        int32_t num_kv_heads, int32_t block_size, int64_t num_blocks, int32_t hnd,
                        uint32_t box_rows, int32_t elem_bytes = 2);
+// The pool as a 3-D tensor whose outermost dimension is the kv head, box
+// {128 bytes, 16 keys, num_kv_heads}: one box reads 16 consecutive keys of one
+// page for every head, head after head (2 KB each), 128-byte swizzled -- the
+// decode kernel's view:
+//   NHD  (head_size, pages*block_size, num_kv_heads), coordinates
+//        (dim, page*block_size + offset, 0); the head stride is one row;
+//   HND  (head_size, block_size, pages*num_kv_heads), coordinates
+//        (dim, offset, page*num_kv_heads).
+CUresult encode_kv_map_heads(CUtensorMap *map, const void *cache, int32_t head_size,
+                             int32_t num_kv_heads, int32_t block_size, int64_t num_blocks,
+                             int32_t hnd, int32_t elem_bytes);
 
 }  // namespace pka

@@ -96,6 +96,7 @@ struct PrefillParams {
     int32_t kv_splits;      // shared_prefix: key chunks, split_tiles key tiles each
     int32_t split_tiles;
     int32_t test_skip_copies;  // failure-path test: the producer issues nothing
+    int32_t trigger_dependents;  // the cascade's suffix decode may start beside this pass
 };
 
 template <int D>
@@ -483,6 +484,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int nseq = p.shared_prefix ? 0 : p.num_seqs - p.first_seq;
+
+    // The dependent launch (a cascade's suffix decode, which never reads what
+    // this pass writes) may be scheduled on the free SMs right away.
+    if (p.trigger_dependents)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // ---- prefix sums of 256-query super-tiles per prefill sequence
     {
@@ -906,6 +912,7 @@ cudaError_t launch_prefill(const Fwd &f, const PrefillPass &pass)
     p.kv_splits = 1;
     p.split_tiles = 0;
     p.test_skip_copies = f.test_skip_copies;
+    p.trigger_dependents = pass.trigger_dependents ? 1 : 0;
     if (pass.shared_prefix) {
         const int tiles = (pass.kv_cap - pass.kv_lo + kBN - 1) / kBN;
         p.kv_splits = std::max(1, pass.kv_splits);
@@ -919,8 +926,10 @@ cudaError_t launch_prefill(const Fwd &f, const PrefillPass &pass)
     else
         items = (int64_t(f.num_tokens - f.num_decodes) + int64_t(nseq) * (kSuper - 1)) /
                 kSuper * f.num_heads;
-    // persistent grid: one CTA per SM, but no more CTAs than work items
-    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(f.num_sms, items)));
+    // persistent grid: one CTA per SM (or the pass's share of the SMs), but no
+    // more CTAs than work items
+    const int ctas = pass.max_ctas > 0 ? std::min(pass.max_ctas, f.num_sms) : f.num_sms;
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ctas, items)));
     if (f.head_size == 128)
         return f.kv_hnd ? launch_prefill_d<128, true>(f, p, grid)
                         : launch_prefill_d<128, false>(f, p, grid);
