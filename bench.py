@@ -590,11 +590,23 @@ def measure_fp8_decode(args, dev, peaks, peaks_kind):
 
 def timed_steps(torch, pka, st, steps, kernels=(0, 1), run=None):
     """Mean step time and mean per-launch kernel times (CUDA events; the library
-    records the decode (0) and prefill (1) kernels' events on their stream)."""
+    records the decode (0) and prefill (1) kernels' events on their stream).
+    The step time comes from a loop without the per-kernel events (their
+    records cost host time between launches); the kernel times from a second,
+    instrumented loop."""
     run = st.run if run is None else run
     for _ in range(3):
         run()
     torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    pka.check_status()
+    ms = e0.elapsed_time(e1) / steps
     ev = {k: ([torch.cuda.Event(enable_timing=True) for _ in range(steps)],
               [torch.cuda.Event(enable_timing=True) for _ in range(steps)]) for k in kernels}
     for a, b in ev.values():
@@ -613,7 +625,6 @@ def timed_steps(torch, pka, st, steps, kernels=(0, 1), run=None):
     e1.record()
     torch.cuda.synchronize()
     pka.check_status()
-    ms = e0.elapsed_time(e1) / steps
     kms = {k: sum(x.elapsed_time(y) for x, y in zip(a, b)) / steps for k, (a, b) in ev.items()}
     return ms, kms
 
@@ -719,15 +730,21 @@ def measure_workloads(args, dev, peaks):
             e["passes"] = "one after the other"
         return e
 
+    def graph_ms():
+        try:
+            return graph_step_ms(torch, st, 20)
+        except Exception as e:  # reported, not fatal: the eager step stands
+            return f"capture failed: {e}"
+
     ms, kms = timed_steps(torch, pka, st, 20)
-    res["cascade"] = {**cascade_entry(ms, kms, kv),
+    res["cascade"] = {**cascade_entry(ms, kms, kv), "graph_replay_ms_per_step": graph_ms(),
                       "cascade_GBps_step": casc * row / (ms * 1e-3) / 1e9,
                       "naive_equivalent_GBps_step": naive * row / (ms * 1e-3) / 1e9,
                       "bytes_read_cascade": casc * row, "bytes_read_naive": naive * row}
     # the same over an fp8 pool (the prefix pass runs on a bf16 copy of its blocks)
     to_fp8_pool(st)
     ms, kms = timed_steps(torch, pka, st, 20)
-    res["cascade_fp8"] = {**cascade_entry(ms, kms, kv // 2),
+    res["cascade_fp8"] = {**cascade_entry(ms, kms, kv // 2), "graph_replay_ms_per_step": graph_ms(),
                           "note": "step includes the copy of the prefix blocks to bf16"}
     del st
     torch.cuda.empty_cache()

@@ -207,6 +207,20 @@ size_t pka_workspace_size(const pka_meta *meta, int32_t num_tokens, int32_t num_
                           int32_t num_kv_heads, int32_t head_size, int32_t block_size);
 
 /*
+ * The smallest workspace pka_paged_attn_forward accepts for this batch (same
+ * arguments; 0 when they are invalid).  pka_workspace_size can be larger: with
+ * a bf16 pool of 16-key pages and query-heavy prefills (at least 256 query
+ * tokens per prefill sequence on average) it adds room for a copy of the
+ * prefill sequences' keys in 128-key blocks, which the tensor-core prefill
+ * then reads with one TMA box per tile half instead of one per page.  Given a
+ * workspace of at least this size but below pka_workspace_size, the forward
+ * reads the pages as they are; the results are the same bit for bit.  The
+ * pages have no counterpart of this call.
+ */
+size_t pka_workspace_size_min(const pka_meta *meta, int32_t num_tokens, int32_t num_heads,
+                              int32_t num_kv_heads, int32_t head_size, int32_t block_size);
+
+/*
  * Attention forward of one layer over the paged pool ([backend] "Archivos
  * clave": AttentionImpl.forward(layer, query, key, value, kv_cache,
  * attn_metadata, output); [FA/FI] "Responsabilidades": Q/K/V reshaped to
@@ -235,8 +249,9 @@ size_t pka_workspace_size(const pka_meta *meta, int32_t num_tokens, int32_t num_
  *             or NULL
  *  scale      softmax scale (1/sqrt(head_size) in the usual case)
  *  causal     1: bottom-right causal mask; 0: every key [0, L_s) admitted
- *  workspace  device buffer of at least pka_workspace_size(...) bytes,
- *             256-byte aligned (may be NULL when that size is 0)
+ *  workspace  device buffer of pka_workspace_size(...) bytes (at least
+ *             pka_workspace_size_min(...): see there), 256-byte aligned (may be
+ *             NULL when that size is 0)
  *
  * Served shapes: head_size 64 or 128; num_kv_heads in {1, 2, 4, 8};
  * num_heads/num_kv_heads <= 8 for decodes; block_size a multiple of 16

@@ -25,6 +25,7 @@ from . import build as _build
 __all__ = ["Meta", "PkaError", "LAYOUT_NHD", "LAYOUT_HND", "KV_BF16", "KV_FP8_E4M3",
            "reshape_and_cache", "reshape_and_cache_fp8", "paged_attn_forward", "cascade_merge",
            "paged_attn_forward_noalloc", "paged_attn_forward_fused", "workspace_size",
+           "workspace_size_min",
            "merge_partials", "LSE_BASE_E",
            "LSE_BASE_2", "check_status", "set_kernel_events", "kernel_launches",
            "load_library", "test_skip_copies",
@@ -112,6 +113,9 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pka_reshape_and_cache_fp8.restype = ctypes.c_int
         lib.pka_workspace_size.argtypes = [ctypes.POINTER(_CMeta), _I32, _I32, _I32, _I32, _I32]
         lib.pka_workspace_size.restype = ctypes.c_size_t
+        lib.pka_workspace_size_min.argtypes = [ctypes.POINTER(_CMeta), _I32, _I32, _I32, _I32,
+                                               _I32]
+        lib.pka_workspace_size_min.restype = ctypes.c_size_t
         lib.pka_paged_attn_forward.argtypes = [_P, _P, ctypes.POINTER(_CMeta), _P, _P, _I32,
                                                _I32, _I32, _I32, _I32, _I64, ctypes.c_float,
                                                _I32, _P, ctypes.c_size_t, _P]
@@ -246,6 +250,15 @@ def workspace_size(meta: Meta, num_tokens, num_heads, num_kv_heads, head_size, b
     cm = meta._c()
     return int(lib.pka_workspace_size(ctypes.byref(cm), num_tokens, num_heads, num_kv_heads,
                                       head_size, block_size))
+
+
+def workspace_size_min(meta: Meta, num_tokens, num_heads, num_kv_heads, head_size,
+                       block_size) -> int:
+    """The smallest workspace the forward accepts (pka_workspace_size_min)."""
+    lib = load_library()
+    cm = meta._c()
+    return int(lib.pka_workspace_size_min(ctypes.byref(cm), num_tokens, num_heads,
+                                          num_kv_heads, head_size, block_size))
 
 
 def paged_attn_forward(query, kv_cache, meta: Meta, out, lse=None, scale=None, causal=True,

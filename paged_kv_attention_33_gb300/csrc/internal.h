@@ -78,6 +78,12 @@ struct Workspace {
     int32_t fp8_blocks_per_seq;
     int32_t fp8_prefix_blocks;
     int64_t fp8_scratch_blocks;
+    // bf16 pool of small pages: the prefill sequences' keys re-blocked into
+    // 128-key NHD blocks (reblock_blocks_per_seq = ceil(max_seq_len / 128) per
+    // prefill sequence) and their block table ([num_seqs, blocks_per_seq])
+    size_t reblock_scratch, reblock_table;
+    int32_t reblock_blocks_per_seq;
+    int64_t reblock_blocks;
     size_t total;
 };
 
@@ -100,6 +106,15 @@ CascadePlan plan_cascade(int32_t num_tokens, int32_t num_heads, int32_t num_kv_h
 Workspace plan_workspace(const DecodePlan &dp, int32_t num_tokens, int32_t num_decodes,
                          int32_t num_heads, int32_t head_size, bool cascade,
                          int32_t pre_splits);
+// A bf16 pool of small pages read by a query-heavy prefill pass: the 128-key
+// re-blocking of the prefill sequences' keys (none otherwise), appended.
+void plan_reblock(Workspace &w, bool kv_fp8, int32_t num_tokens, int32_t num_seqs,
+                  int32_t num_decodes, int32_t max_seq_len, int32_t block_size,
+                  int32_t num_kv_heads, int32_t head_size);
+// The smallest workspace a forward accepts (without the re-blocking copy);
+// 0 when the arguments are invalid.
+size_t workspace_size_min(const pka_meta *m, int32_t num_tokens, int32_t num_heads,
+                          int32_t num_kv_heads, int32_t head_size, int32_t block_size);
 // The fp8 prefill copy: blocks per prefill sequence and bytes of the bf16 scratch pool
 // (0 when the pool is bf16 or there are no prefills); appended to a planned workspace.
 void plan_fp8_prefill(Workspace &w, bool kv_fp8, int32_t num_seqs, int32_t num_decodes,
@@ -124,6 +139,13 @@ cudaError_t launch_reshape_and_cache_fp8(const void *key, const void *value, voi
 cudaError_t launch_dequant_blocks(const Fwd &f, void *scratch, int32_t *table, int32_t first_row,
                                   int32_t num_rows, int32_t row_blocks, int32_t col_limit,
                                   int64_t dst_base, int32_t table_stride);
+// The prefill sequences' keys of a bf16 pool of small pages (block_size a
+// divisor of 128) copied into 128-key NHD blocks of a scratch pool: block-table
+// rows [first_row, first_row + num_rows), destination block dst_base +
+// p * row_blocks + n of row p, table rows of stride table_stride.
+cudaError_t launch_reblock(const Fwd &f, void *scratch, int32_t *table, int32_t first_row,
+                           int32_t num_rows, int32_t row_blocks, int64_t dst_base,
+                           int32_t table_stride);
 uint32_t kv_write_take_error();
 
 // Most key chunks of a cascade's shared-prefix pass (partials per row).

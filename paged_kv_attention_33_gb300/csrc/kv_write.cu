@@ -231,6 +231,87 @@ cudaError_t launch_dequant_blocks(const Fwd &f, void *scratch, int32_t *table, i
     return cudaGetLastError();
 }
 
+// Re-blocking of a bf16 pool with small pages for the tensor-core prefill.
+// A prefill work item reads its K and V tiles (128 keys of one kv head) with
+// one TMA box per page and 64-dim half; at 16-key pages that is 16 boxes of
+// 2 KB per tile, and the tensor-core pass is then bound by how fast one SM
+// issues boxes, not by its MMAs.  Copying the prefill sequences' keys into
+// 128-key blocks first (2 x 140 MB of traffic for a 34K-token batch, against
+// about a millisecond of MMAs) lets the pass read one box per tile half.
+// One CTA per 128-key destination block of one sequence: block-table row
+// first_row + p, destination block dst_base + p * row_blocks + n (NHD, every
+// kv head), its id stored at table[(first_row + p) * table_stride + n]; keys
+// at and past L are not copied (the prefill pass never admits them).
+constexpr int kReblockKeys = 128;
+
+__global__ void __launch_bounds__(kKvwThreads)
+    reblock_kernel(const uint4 *__restrict__ pool, uint4 *__restrict__ scratch,
+                   int32_t *__restrict__ table, const int32_t *__restrict__ bt,
+                   int32_t bt_stride, const int32_t *__restrict__ seq_lens, int32_t first_row,
+                   int32_t row_blocks, int64_t dst_base, int32_t table_stride,
+                   int32_t block_size, int32_t num_kv_heads, int32_t head_chunks,
+                   int64_t num_blocks, int32_t hnd)
+{
+    __shared__ int32_t src_blk[kReblockKeys];  // source block of each key's page (-1: none)
+    const int32_t p = blockIdx.y, n = blockIdx.x;
+    const int32_t s = first_row + p;
+    const int32_t L = seq_lens[s];
+    if (n == 0 && threadIdx.x == 0 && int64_t(L) > int64_t(row_blocks) * kReblockKeys)
+        flag_error(kErrBadMetadata);  // longer than max_seq_len: its tail was not copied
+    if (n >= row_blocks || n * kReblockKeys >= L)
+        return;
+    const int32_t keys = min(kReblockKeys, L - n * kReblockKeys);
+    const int64_t dst_blk = dst_base + int64_t(p) * row_blocks + n;
+    if (threadIdx.x == 0)
+        table[int64_t(s) * table_stride + n] = static_cast<int32_t>(dst_blk);
+    const int32_t pages = (keys + block_size - 1) / block_size;  // block_size divides 128
+    if (threadIdx.x < pages) {
+        // (a column past the table is a length above max_seq_len: flagged too)
+        const int32_t col = n * (kReblockKeys / block_size) + threadIdx.x;
+        int32_t b = col < bt_stride ? bt[int64_t(s) * bt_stride + col] : -1;
+        if (b < 0 || b >= num_blocks) {
+            flag_error(kErrBlockOutOfPool);
+            b = -1;
+        }
+        src_blk[threadIdx.x] = b;
+    }
+    __syncthreads();
+    // 16-byte chunk i: (K|V, key, head, chunk); a key's row of every head is
+    // row_chunks chunks, contiguous in the destination (and in an NHD source)
+    const int32_t row_chunks = num_kv_heads * head_chunks;
+    const int32_t per_kv = keys * row_chunks;
+    for (int32_t i = threadIdx.x; i < 2 * per_kv; i += kKvwThreads) {
+        const int32_t kv = i / per_kv, r = i % per_kv;
+        const int32_t key = r / row_chunks, c = r % row_chunks;
+        const int32_t b = src_blk[key / block_size];
+        if (b < 0)
+            continue;  // flagged above; the row is left as it was
+        const int32_t off = key % block_size;
+        const int64_t src =
+            hnd ? ((int64_t(b) * 2 + kv) * num_kv_heads + c / head_chunks) * block_size * head_chunks +
+                      int64_t(off) * head_chunks + c % head_chunks
+                : ((int64_t(b) * 2 + kv) * block_size + off) * row_chunks + c;
+        scratch[((dst_blk * 2 + kv) * kReblockKeys + key) * row_chunks + c] = pool[src];
+    }
+}
+
+cudaError_t launch_reblock(const Fwd &f, void *scratch, int32_t *table, int32_t first_row,
+                           int32_t num_rows, int32_t row_blocks, int64_t dst_base,
+                           int32_t table_stride)
+{
+    if (num_rows <= 0 || row_blocks <= 0)
+        return cudaSuccess;
+    if (kReblockKeys % f.block_size != 0)
+        return cudaErrorInvalidValue;
+    count_launch();
+    dim3 grid(static_cast<unsigned>(row_blocks), static_cast<unsigned>(num_rows));
+    reblock_kernel<<<grid, kKvwThreads, 0, f.stream>>>(
+        static_cast<const uint4 *>(f.kv_cache), static_cast<uint4 *>(scratch), table,
+        f.block_table, f.bt_stride, f.seq_lens, first_row, row_blocks, dst_base, table_stride,
+        f.block_size, f.num_kv_heads, f.head_size * 2 / 16, f.num_blocks, f.kv_hnd);
+    return cudaGetLastError();
+}
+
 uint32_t kv_write_take_error() { return take_device_error(); }
 
 }  // namespace pka

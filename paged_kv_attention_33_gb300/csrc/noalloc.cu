@@ -85,8 +85,10 @@ extern "C" pka_status pka_paged_attn_forward_noalloc(
     int32_t num_tokens, int32_t num_heads, int32_t num_kv_heads, int32_t head_size,
     int32_t block_size, int64_t num_blocks, float scale, int32_t causal, void *stream)
 {
-    const size_t need = pka_workspace_size(meta, num_tokens, num_heads, num_kv_heads, head_size,
-                                           block_size);
+    // the smallest workspace the forward accepts (it leaves out optional
+    // copies that do not fit)
+    const size_t need = pka::workspace_size_min(meta, num_tokens, num_heads, num_kv_heads,
+                                                head_size, block_size);
     if (need > pka::kNoallocScratchBytes) {
         pka::set_last_error("pka_paged_attn_forward_noalloc: this batch needs %zu bytes of "
                             "scratch, more than the %zu-byte built-in buffer; use "

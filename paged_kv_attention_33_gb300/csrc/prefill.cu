@@ -891,9 +891,11 @@ cudaError_t launch_prefill(const Fwd &f, const PrefillPass &pass)
     p.num_heads = f.num_heads;
     p.group = f.num_heads / f.num_kv_heads;
     p.block_size = f.block_size;
-    // boxes never straddle a block: key offsets are multiples of both
-    // block_size (prefix length) and 128 (tile), so use their gcd
-    p.box_rows = std::gcd(f.block_size, 128);
+    // boxes never straddle a block: key offsets are multiples of block_size,
+    // of 128 (tile) and of the first key kv_lo (a cascade suffix starts at the
+    // prefix length, a multiple of the pool's block size, which a re-blocked
+    // copy of 128-key blocks need not share), so use their gcd
+    p.box_rows = std::gcd(std::gcd(f.block_size, 128), pass.kv_lo);
     p.num_blocks = static_cast<int32_t>(f.num_blocks);
     p.num_kv_heads = f.num_kv_heads;
     p.kv_lo = pass.kv_lo;

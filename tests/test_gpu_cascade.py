@@ -71,3 +71,14 @@ def test_cascade_precondition_is_flagged():
     with pytest.raises(pka.PkaError) as e:
         pka.check_status()
     assert e.value.status == -5
+
+
+def test_cascade_small_pages_prefix_off_the_tile_grid(oracle):
+    """A cascade over 16-key pages whose shared prefix (80 keys) is not a
+    multiple of 128, with query-heavy prefill suffixes: the suffix pass reads
+    the 128-key re-blocked copy from key 80, so its TMA boxes shrink to
+    gcd(16, 128, 80) = 16 rows and never straddle a copied block."""
+    P = 80
+    sp = W.BatchSpec("casc_reblock", 16, 4, 128, 16, decode_ctx=[P + 5, P + 300],
+                     prefill=[(300, P), (400, P + 50)], common_prefix_len=P)
+    G.check_batch(oracle, W.make_batch(sp, seed=4400), label="cascade re-blocked suffix")

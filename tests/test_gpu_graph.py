@@ -88,3 +88,24 @@ def test_graph_replay_over_an_fp8_pool(oracle):
     assert torch.equal(oe.view(torch.int16), og.view(torch.int16))
     assert torch.equal(le, lg)
     assert torch.equal(pe, pg)
+
+
+def test_graph_replay_of_a_cascade_step():
+    """A shared-prefix cascade whose prefix pass and suffix decode run side by
+    side (the decode a programmatic dependent launch) is captured and replayed
+    with the same results as eager, bit for bit."""
+    import torch
+
+    import paged_kv_attention_33_gb300 as pka
+
+    P = 2048
+    sp = W.BatchSpec("graph_cascade", 64, 8, 128, 128,
+                     decode_ctx=[P + 3, P + 100, P + 700, P + 1023, P + 64, P + 300],
+                     common_prefix_len=P)
+    b = W.make_batch(sp, seed=9302)
+    meta = pka.Meta.from_host(b.query_start_loc, b.seq_lens, b.block_table, sp.num_decodes,
+                              "cuda", common_prefix_len=P)
+    (oe, le, pe), (og, lg, pg) = _eager_and_replayed(b, G.to_dev(b.cache, "cuda"), meta, sp)
+    assert torch.equal(oe.view(torch.int16), og.view(torch.int16))
+    assert torch.equal(le, lg)
+    assert torch.equal(pe.view(torch.int16), pg.view(torch.int16))

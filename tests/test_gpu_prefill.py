@@ -45,3 +45,48 @@ def test_mixed_decode_first_batch(oracle):
 def test_non_causal_prefill(oracle):
     sp = W.BatchSpec("nc", 8, 2, 64, 16, prefill=[(70, 0), (130, 45)], causal=False)
     G.check_batch(oracle, W.make_batch(sp, seed=3400), label="non-causal")
+
+
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+def test_small_pages_reblocked_and_direct(oracle, layout):
+    """A bf16 pool of 16-key pages under query-heavy prefills: with the
+    workspace pka_workspace_size asks for, the prefill pass reads a copy of
+    its sequences' keys in 128-key blocks; with pka_workspace_size_min it reads
+    the pages as they are.  Both match the oracle on every row, and each other
+    bit for bit."""
+    import torch
+
+    import paged_kv_attention_33_gb300 as pka
+
+    sp = W.BatchSpec("reblock", 16, 4, 128, 16, decode_ctx=[100, 1000],
+                     prefill=[(300, 0), (700, 37), (257, 1000), (129, 5)], table_pad=2,
+                     kv_layout=layout)
+    b = W.make_batch(sp, seed=3500)
+    dev = "cuda"
+    cache = W.to_layout(G.to_dev(b.cache, dev), layout)
+    pka.reshape_and_cache(G.to_dev(b.key, dev), G.to_dev(b.value, dev), cache,
+                          torch.from_numpy(b.slot_mapping).to(dev), kv_layout=layout)
+    meta = pka.Meta.from_host(b.query_start_loc, b.seq_lens, b.block_table, sp.num_decodes, dev,
+                              kv_layout=layout)
+    T, H, D = b.num_tokens, sp.num_heads, sp.head_size
+    full = pka.workspace_size(meta, T, H, sp.num_kv_heads, D, sp.block_size)
+    small = pka.workspace_size_min(meta, T, H, sp.num_kv_heads, D, sp.block_size)
+    assert full > small > 0  # the copy is planned
+    q = G.to_dev(b.query, dev)
+    results = []
+    for nbytes in (full, small):
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        out = torch.full_like(q, float("nan"))
+        lse = torch.full((T, H), float("nan"), dtype=torch.float32, device=dev)
+        pka.paged_attn_forward(q, cache, meta, out, lse, scale=sp.softmax_scale, workspace=ws)
+        pka.check_status()
+        results.append((out, lse))
+    want = G.host_bits(b.cache).copy()
+    oracle.reshape_and_cache(b.key, b.value, want, b.slot_mapping)
+    rows = np.arange(T * H, dtype=np.int64)
+    o_ref, l_ref = G.oracle_expected(oracle, b, want, rows=rows)
+    for label, (out, lse) in zip(("re-blocked", "direct"), results):
+        G.assert_close(G.compare(W.to_host_bits(out), lse.cpu().numpy(), o_ref, l_ref, rows, H),
+                       f"{layout} {label}")
+    assert torch.equal(results[0][0].view(torch.int16), results[1][0].view(torch.int16))
+    assert torch.equal(results[0][1], results[1][1])

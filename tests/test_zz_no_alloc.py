@@ -78,8 +78,9 @@ def test_noalloc_rejects_batches_above_its_scratch():
     # a cascade over 8192 prefill tokens: the shared-prefix partials alone are
     # 8192 x 32 heads x 128 x 4 bytes
     m = pka._CMeta(16, 16, 16, 1024, 2, 0, 4096, 16384, 16, 0)
-    need = lib.pka_workspace_size(ctypes.byref(m), 8192, 32, 8, 128, 16)
-    assert need > 16 << 20
+    # the smallest workspace the forward accepts (no optional prefill copy)
+    need = lib.pka_workspace_size_min(ctypes.byref(m), 8192, 32, 8, 128, 16)
+    assert 16 << 20 < need <= lib.pka_workspace_size(ctypes.byref(m), 8192, 32, 8, 128, 16)
     rc = lib.pka_paged_attn_forward_noalloc(256, 512, ctypes.byref(m), 1024, None, 8192, 32, 8,
                                             128, 16, 100000, 0.088, 1, None)
     assert rc == -3
