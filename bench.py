@@ -310,24 +310,28 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------------- our arm
-def kernel_source_hash():
+KERNEL_SOURCES = {"decode": ("decode.cu", "common.cuh"),
+                  "prefill": ("prefill.cu", "common.cuh", "tcgen05.cuh")}
+
+
+def kernel_source_hash(kernel="decode"):
     h = hashlib.sha256()
-    for f in ("decode.cu", "common.cuh"):
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "paged_kv_attention_33_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def committed_traffic(workload, kv_dtype="bf16"):
-    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary,
-    or None when the kernel source changed since it was taken."""
+def committed_traffic(workload, kv_dtype="bf16", kernel="decode"):
+    """Per-launch DRAM bytes of the kernel from the committed ncu summary, or
+    None when the kernel source changed since it was taken."""
     suffix = "" if kv_dtype == "bf16" else f"_{kv_dtype}"
-    path = os.path.join(ROOT, "profiles", f"decode_kernel_{workload}{suffix}_traffic.json")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_kernel_{workload}{suffix}_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f)
-    if rec.get("kernel_source_hash") != kernel_source_hash():
+    if rec.get("kernel_source_hash") != kernel_source_hash(kernel):
         return None
     return rec.get("traffic_bytes_per_launch")
 
@@ -804,7 +808,10 @@ def measure_prefill(args, dev, peaks, peaks_kind):
             "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel", "achieved": achieved,
                          "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                          "peak_source": f"{peaks_kind} dense bf16 burst (bf16_tflops)",
-                         "kernel_ms": k_ms, "traffic": None}}
+                         "kernel_ms": k_ms,
+                         "traffic": committed_traffic("prefill", kernel="prefill")},
+            "note": "the step includes the copy of the prompts' keys into 128-key blocks "
+                    "(16-key pool pages) that the prefill kernel reads"}
 
 
 def run_profile(args, st):

@@ -327,7 +327,7 @@ void plan_reblock(Workspace &w, bool kv_fp8, int32_t num_tokens, int32_t num_seq
     w.reblock_blocks_per_seq = 0;
     w.reblock_blocks = 0;
     const int32_t nprefill = num_seqs - num_decodes;
-    if (kv_fp8 || nprefill <= 0 || block_size >= 32 || 128 % block_size != 0)
+    if (kv_fp8 || nprefill <= 0 || block_size >= 32 || 32 % block_size != 0)
         return;
     if (int64_t(num_tokens) - num_decodes < int64_t(256) * nprefill)
         return;

@@ -140,7 +140,7 @@ cudaError_t launch_dequant_blocks(const Fwd &f, void *scratch, int32_t *table, i
                                   int32_t num_rows, int32_t row_blocks, int32_t col_limit,
                                   int64_t dst_base, int32_t table_stride);
 // The prefill sequences' keys of a bf16 pool of small pages (block_size a
-// divisor of 128) copied into 128-key NHD blocks of a scratch pool: block-table
+// divisor of 32) copied into 128-key NHD blocks of a scratch pool: block-table
 // rows [first_row, first_row + num_rows), destination block dst_base +
 // p * row_blocks + n of row p, table rows of stride table_stride.
 cudaError_t launch_reblock(const Fwd &f, void *scratch, int32_t *table, int32_t first_row,

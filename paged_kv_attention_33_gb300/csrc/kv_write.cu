@@ -238,11 +238,15 @@ cudaError_t launch_dequant_blocks(const Fwd &f, void *scratch, int32_t *table, i
 // issues boxes, not by its MMAs.  Copying the prefill sequences' keys into
 // 128-key blocks first (2 x 140 MB of traffic for a 34K-token batch, against
 // about a millisecond of MMAs) lets the pass read one box per tile half.
-// One CTA per 128-key destination block of one sequence: block-table row
-// first_row + p, destination block dst_base + p * row_blocks + n (NHD, every
-// kv head), its id stored at table[(first_row + p) * table_stride + n]; keys
-// at and past L are not copied (the prefill pass never admits them).
+// One CTA per quarter (32 keys) of a 128-key destination block of one
+// sequence: block-table row first_row + p, destination block dst_base +
+// p * row_blocks + n (NHD, every kv head), its id stored at
+// table[(first_row + p) * table_stride + n]; keys at and past L are not
+// copied (the prefill pass never admits them).  A warp copies whole key rows
+// (every head's K or V row of one key), lanes along the row.
 constexpr int kReblockKeys = 128;
+constexpr int kReblockSplit = 4;  // CTAs per destination block
+constexpr int kReblockCtaKeys = kReblockKeys / kReblockSplit;
 
 __global__ void __launch_bounds__(kKvwThreads)
     reblock_kernel(const uint4 *__restrict__ pool, uint4 *__restrict__ scratch,
@@ -252,22 +256,24 @@ __global__ void __launch_bounds__(kKvwThreads)
                    int32_t block_size, int32_t num_kv_heads, int32_t head_chunks,
                    int64_t num_blocks, int32_t hnd)
 {
-    __shared__ int32_t src_blk[kReblockKeys];  // source block of each key's page (-1: none)
-    const int32_t p = blockIdx.y, n = blockIdx.x;
+    __shared__ int32_t src_blk[kReblockCtaKeys];  // source block of each page (-1: none)
+    const int32_t p = blockIdx.y;
+    const int32_t n = blockIdx.x / kReblockSplit, quarter = blockIdx.x % kReblockSplit;
     const int32_t s = first_row + p;
     const int32_t L = seq_lens[s];
-    if (n == 0 && threadIdx.x == 0 && int64_t(L) > int64_t(row_blocks) * kReblockKeys)
+    if (blockIdx.x == 0 && threadIdx.x == 0 && int64_t(L) > int64_t(row_blocks) * kReblockKeys)
         flag_error(kErrBadMetadata);  // longer than max_seq_len: its tail was not copied
-    if (n >= row_blocks || n * kReblockKeys >= L)
+    const int32_t key0 = n * kReblockKeys + quarter * kReblockCtaKeys;  // first key copied
+    if (n >= row_blocks || key0 >= L)
         return;
-    const int32_t keys = min(kReblockKeys, L - n * kReblockKeys);
+    const int32_t keys = min(kReblockCtaKeys, L - key0);
     const int64_t dst_blk = dst_base + int64_t(p) * row_blocks + n;
-    if (threadIdx.x == 0)
+    if (quarter == 0 && threadIdx.x == 0)
         table[int64_t(s) * table_stride + n] = static_cast<int32_t>(dst_blk);
-    const int32_t pages = (keys + block_size - 1) / block_size;  // block_size divides 128
+    const int32_t pages = (keys + block_size - 1) / block_size;  // block_size divides 32
     if (threadIdx.x < pages) {
         // (a column past the table is a length above max_seq_len: flagged too)
-        const int32_t col = n * (kReblockKeys / block_size) + threadIdx.x;
+        const int32_t col = key0 / block_size + threadIdx.x;
         int32_t b = col < bt_stride ? bt[int64_t(s) * bt_stride + col] : -1;
         if (b < 0 || b >= num_blocks) {
             flag_error(kErrBlockOutOfPool);
@@ -276,22 +282,31 @@ __global__ void __launch_bounds__(kKvwThreads)
         src_blk[threadIdx.x] = b;
     }
     __syncthreads();
-    // 16-byte chunk i: (K|V, key, head, chunk); a key's row of every head is
-    // row_chunks chunks, contiguous in the destination (and in an NHD source)
-    const int32_t row_chunks = num_kv_heads * head_chunks;
-    const int32_t per_kv = keys * row_chunks;
-    for (int32_t i = threadIdx.x; i < 2 * per_kv; i += kKvwThreads) {
-        const int32_t kv = i / per_kv, r = i % per_kv;
-        const int32_t key = r / row_chunks, c = r % row_chunks;
+    const int32_t row_chunks = num_kv_heads * head_chunks;  // 16-byte chunks of a key row
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int32_t r = warp; r < 2 * keys; r += kKvwThreads / 32) {
+        const int32_t kv = r >= keys ? 1 : 0;
+        const int32_t key = r - kv * keys;  // within this CTA's keys
         const int32_t b = src_blk[key / block_size];
         if (b < 0)
             continue;  // flagged above; the row is left as it was
-        const int32_t off = key % block_size;
-        const int64_t src =
-            hnd ? ((int64_t(b) * 2 + kv) * num_kv_heads + c / head_chunks) * block_size * head_chunks +
-                      int64_t(off) * head_chunks + c % head_chunks
-                : ((int64_t(b) * 2 + kv) * block_size + off) * row_chunks + c;
-        scratch[((dst_blk * 2 + kv) * kReblockKeys + key) * row_chunks + c] = pool[src];
+        const int32_t off = (key0 + key) % block_size;
+        uint4 *dst = scratch + ((dst_blk * 2 + kv) * kReblockKeys + quarter * kReblockCtaKeys +
+                                key) * row_chunks;
+        if (!hnd) {  // the row is contiguous in the pool too
+            const uint4 *src = pool + ((int64_t(b) * 2 + kv) * block_size + off) * row_chunks;
+#pragma unroll 4
+            for (int32_t c = lane; c < row_chunks; c += 32)
+                dst[c] = __ldcs(src + c);
+        } else {  // one head's row at a time, block_size rows apart
+            const uint4 *src = pool + (int64_t(b) * 2 + kv) * num_kv_heads * block_size * head_chunks +
+                               int64_t(off) * head_chunks;
+#pragma unroll 4
+            for (int32_t c = lane; c < row_chunks; c += 32) {
+                const int32_t h = c / head_chunks;
+                dst[c] = __ldcs(src + (int64_t(h) * block_size * head_chunks + (c - h * head_chunks)));
+            }
+        }
     }
 }
 
@@ -301,10 +316,10 @@ cudaError_t launch_reblock(const Fwd &f, void *scratch, int32_t *table, int32_t 
 {
     if (num_rows <= 0 || row_blocks <= 0)
         return cudaSuccess;
-    if (kReblockKeys % f.block_size != 0)
+    if (kReblockCtaKeys % f.block_size != 0)
         return cudaErrorInvalidValue;
     count_launch();
-    dim3 grid(static_cast<unsigned>(row_blocks), static_cast<unsigned>(num_rows));
+    dim3 grid(static_cast<unsigned>(row_blocks * kReblockSplit), static_cast<unsigned>(num_rows));
     reblock_kernel<<<grid, kKvwThreads, 0, f.stream>>>(
         static_cast<const uint4 *>(f.kv_cache), static_cast<uint4 *>(scratch), table,
         f.block_table, f.bt_stride, f.seq_lens, first_row, row_blocks, dst_base, table_stride,
