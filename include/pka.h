@@ -277,12 +277,13 @@ pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const
  * write folded into the forward's launches ([FA/FI] "Responsabilidades": the
  * FlashAttention kernel writes the KV cache itself,
  * forward_includes_kv_cache_update).  Same results, bit for bit in the pool,
- * as the two calls.  When the batch has decodes, the decode kernel writes
- * every new row: each decode's new K/V row is copied from `key`/`value` into
- * the tile its attention reads (the pool need not hold it yet) and stored at
- * its slot, and the prefill tokens' rows are stored before the prefill pass
- * reads them -- no separate write launch.  A batch without decodes writes
- * first and then attends (two launches).
+ * as the two calls.  Each decode's new K/V row is written by the decode
+ * kernel itself: copied from `key`/`value` into the tile its attention reads
+ * (the pool need not hold it yet) and stored at its slot.  The prefill
+ * tokens' rows are written by the cache-write kernel before the forward's
+ * other launches (one warp per token over the whole GPU; written by the
+ * decode CTAs they would hold back the decode's first copies).  A batch of
+ * decodes only is thus one launch for write and attention.
  *
  *  key, value     device bf16 [num_tokens, num_kv_heads, head_size], as in
  *                 pka_reshape_and_cache

@@ -657,6 +657,7 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
         f.slots = fuse->slots;
         f.kv_cache_w = fuse->kv_cache;
     }
+    const bool fuse_prefill_rows = fuse && num_tokens > meta->num_decodes;
 
     ForwardPlan plan = plan_forward(meta, num_tokens, num_heads, num_kv_heads, head_size,
                                     block_size, f.num_sms);
@@ -683,6 +684,27 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
         return fail(PKA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(cr));
 
     cudaError_t e;
+    if (fuse_prefill_rows) {
+        // The prefill tokens' new rows go first, through the cache-write
+        // kernel (one warp per token over the whole GPU); the decode launch
+        // writes only each decode's own row, into the tile it attends over and
+        // into the pool.  Written inside the decode launch, those rows held
+        // back its first copies (measured: the decode of a batch with 8,192
+        // prefill tokens ran 4% slower over a bf16 pool, 19% over fp8).
+        const size_t row = size_t(num_kv_heads) * head_size * 2;  // bytes of a bf16 row
+        const int32_t nd = meta->num_decodes;
+        const char *k = static_cast<const char *>(fuse->key) + size_t(nd) * row;
+        const char *v = static_cast<const char *>(fuse->value) + size_t(nd) * row;
+        e = f.kv_fp8 ? launch_reshape_and_cache_fp8(k, v, fuse->kv_cache, fuse->slots + nd,
+                                                     num_tokens - nd, num_kv_heads, head_size,
+                                                     block_size, num_blocks, f.kv_hnd, f.k_scale,
+                                                     f.v_scale, f.stream)
+                     : launch_reshape_and_cache(k, v, fuse->kv_cache, fuse->slots + nd,
+                                                num_tokens - nd, num_kv_heads, head_size,
+                                                block_size, num_blocks, f.kv_hnd, f.stream);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cache write launch");
+    }
     // An fp8 pool: the tensor-core prefill (prefill sequences, the cascade's
     // shared prefix) runs on bf16 copies of the blocks it reads, made in the
     // workspace as exact code values, with k_scale in the score scale and

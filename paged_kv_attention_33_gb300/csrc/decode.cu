@@ -103,13 +103,13 @@ struct DecodeParams {
     float *lse_part;      // [slots, R, H], log2 units
     int32_t *counters;    // [nseq] pieces finished per sequence (zeroed before the launch)
     // fused cache write (pka_paged_attn_forward_fused): this step's K/V rows
-    // [T, Hkv, D] and their slots; the pool is written through `pool`
+    // [T, Hkv, D] and their slots; each decode's own row is written through
+    // `pool` (the prefill tokens' rows are written before this launch)
     int32_t fuse_write;
     const uint4 *new_key;
     const uint4 *new_value;
     const int64_t *slots;
     uint4 *pool;
-    int32_t num_decodes_all;  // tokens [num_decodes_all, T) are prefill tokens
     // fp8 pool: element value = code value x scale (K, V)
     float k_scale;
     float v_scale;
@@ -345,36 +345,6 @@ __device__ __forceinline__ int64_t pool_chunk(const DecodeParams &p, int64_t sl,
     return row * kChunks + c;
 }
 
-// Heads [h0, h1) of token tk's new K and V rows into the pool at slot sl
-// (block sl / bs, offset sl % bs), 16 bytes per lane, NHD or HND order -- the
-// cache write of the "FlashAttention y FlashInfer" page ("Responsabilidades":
-// the cache-update op), done inside the forward; an fp8 pool gets the codes.
-// A negative slot is padding; a slot past the pool is skipped and flagged.
-template <int D, bool kHnd, bool kFp8>
-__device__ __forceinline__ void write_pool_row(const DecodeParams &p, int64_t tk, int64_t sl,
-                                               int lane, int h0, int h1)
-{
-    if (sl < 0)
-        return;
-    if (sl >= int64_t(p.num_blocks) * p.block_size) {
-        if (lane == 0)
-            flag_error(kErrSlotOutOfPool);
-        return;
-    }
-    constexpr int kChunks = D / (kFp8 ? 16 : 8);  // 16-byte chunks of one head's row
-    for (int i = lane; i < (h1 - h0) * kChunks; i += 32) {
-        const int h = h0 + i / kChunks, c = i % kChunks;
-        for (int kv = 0; kv < 2; ++kv) {
-            uint4 v;
-            if constexpr (kFp8)
-                v = quantized_chunk<D>(p, tk, h, c, kv);
-            else
-                v = __ldg((kv ? p.new_value : p.new_key) + (tk * p.num_kv_heads + h) * kChunks + c);
-            p.pool[pool_chunk<kHnd>(p, sl, kv, h, c, kChunks)] = v;
-        }
-    }
-}
-
 // The work of one CTA (the kernel below adds the wait of a dependent launch).
 template <int D, bool kHnd, bool kFp8>
 __device__ __forceinline__ void decode_cta(const CUtensorMap &kv_map, const DecodeParams &p)
@@ -396,15 +366,6 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap &kv_map, const Deco
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int nseq = p.nseq;
-
-    if (p.fuse_write && p.seq0 == 0) {
-        // the prefill tokens' new rows, one token per warp over the grid (the
-        // prefill kernel reads them after this launch; nothing here does)
-        const int64_t nw = int64_t(gridDim.x) * (kDecodeThreads / 32);
-        for (int64_t tk = p.num_decodes_all + int64_t(blockIdx.x) * (kDecodeThreads / 32) + warp;
-             tk < p.num_tokens; tk += nw)
-            write_pool_row<D, kHnd, kFp8>(p, tk, p.slots[tk], lane, 0, Hkv);
-    }
 
     // ---- stage prefix sums over the decodes of this launch: each thread sums a
     // run of decodes, then a block-wide exclusive scan of the run sums
@@ -1135,7 +1096,6 @@ static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Wor
     p.new_value = static_cast<const uint4 *>(f.new_value);
     p.slots = f.slots;
     p.pool = static_cast<uint4 *>(f.kv_cache_w);
-    p.num_decodes_all = f.num_decodes;
     p.k_scale = f.k_scale;
     p.v_scale = f.v_scale;
     p.test_skip_copies = f.test_skip_copies;
