@@ -156,12 +156,17 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *c
     return cudaGetLastError();
 }
 
+// CTAs per copied block (a shared prefix of a few large blocks is copied by
+// more CTAs than it has blocks).
+constexpr int kDequantSplit = 8;
+
 // Blocks of an fp8 pool as bf16 code values (no scale: every e4m3 value is
 // exact in bf16; the attention applies k_scale and v_scale) in a dense NHD
-// scratch pool: CTA (p, n) takes block column n of block-table row s =
-// first_row + p, copies pool block bt[s][n] to scratch block dst_base +
-// p*row_blocks + n and writes that id into the scratch table at [s][n] (row
-// stride table_stride).  Columns at or past min(ceil(L_s / bs), col_limit) are
+// scratch pool: the kDequantSplit CTAs (p, n*kDequantSplit + part) take block
+// column n of block-table row s = first_row + p, copy (each a part of its
+// chunks) pool block bt[s][n] to scratch block dst_base + p*row_blocks + n, and
+// part 0 writes that id into the scratch table at [s][n] (row stride
+// table_stride).  Columns at or past min(ceil(L_s / bs), col_limit) are
 // left alone (the attention never reads them).
 __global__ void __launch_bounds__(kKvwThreads)
     dequant_blocks_kernel(const uint4 *__restrict__ pool, uint4 *__restrict__ scratch,
@@ -172,26 +177,28 @@ __global__ void __launch_bounds__(kKvwThreads)
                           int32_t num_kv_heads, int32_t head_chunks, int64_t num_blocks,
                           int32_t hnd)
 {
-    const int32_t p = blockIdx.y, n = blockIdx.x;
+    // block n of row p, part `part` of its kDequantSplit slices of chunks
+    const int32_t p = blockIdx.y, n = blockIdx.x / kDequantSplit, part = blockIdx.x % kDequantSplit;
     const int32_t s = first_row + p;
     const int32_t L = seq_lens[s];
-    if (n == 0 && threadIdx.x == 0 && col_limit == row_blocks &&
+    if (blockIdx.x == 0 && threadIdx.x == 0 && col_limit == row_blocks &&
         int64_t(L) > int64_t(row_blocks) * block_size)
         flag_error(kErrBadMetadata);  // longer than max_seq_len: its tail was not copied
     if (n >= col_limit || n * block_size >= L)
         return;
     const int64_t dst_blk = dst_base + int64_t(p) * row_blocks + n;
-    if (threadIdx.x == 0)
+    if (part == 0 && threadIdx.x == 0)
         table[int64_t(s) * table_stride + n] = static_cast<int32_t>(dst_blk);
     const int32_t src_blk = bt[int64_t(s) * bt_stride + n];
     if (src_blk < 0 || src_blk >= num_blocks) {
-        if (threadIdx.x == 0)
+        if (part == 0 && threadIdx.x == 0)
             flag_error(kErrBlockOutOfPool);
         return;
     }
     // 16-code chunk i of the block in NHD order: (kv, offset, head, chunk)
     const int32_t per_kv = block_size * num_kv_heads * head_chunks;
-    for (int32_t i = threadIdx.x; i < 2 * per_kv; i += kKvwThreads) {
+    for (int32_t i = part * kKvwThreads + threadIdx.x; i < 2 * per_kv;
+         i += kDequantSplit * kKvwThreads) {
         const int32_t kv = i / per_kv, r = i % per_kv;
         const int32_t off = r / (num_kv_heads * head_chunks);
         const int32_t h = (r / head_chunks) % num_kv_heads, c = r % head_chunks;
@@ -223,7 +230,7 @@ cudaError_t launch_dequant_blocks(const Fwd &f, void *scratch, int32_t *table, i
     if (num_rows <= 0 || col_limit <= 0)
         return cudaSuccess;
     count_launch();
-    dim3 grid(static_cast<unsigned>(col_limit), static_cast<unsigned>(num_rows));
+    dim3 grid(static_cast<unsigned>(col_limit * kDequantSplit), static_cast<unsigned>(num_rows));
     dequant_blocks_kernel<<<grid, kKvwThreads, 0, f.stream>>>(
         static_cast<const uint4 *>(f.kv_cache), static_cast<uint4 *>(scratch), table,
         f.block_table, f.bt_stride, f.seq_lens, first_row, row_blocks, col_limit, dst_base,
