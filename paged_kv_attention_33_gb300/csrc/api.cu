@@ -197,13 +197,17 @@ CascadePlan plan_cascade(int32_t num_tokens, int32_t num_heads, int32_t num_kv_h
     // kHbmBytesPerCycle over the chip, after a fixed start-up and tail.  The
     // suffix length is not known on the host: half of max_seq_len - prefix_len
     // per decode is taken (lengths spread evenly).  (Measured on GB300: the
-    // decode kernel streams ~80 GB/s per SM when HBM is not the limit, ~70 of
-    // fp8 codes, and saturates HBM on about 100 SMs; a tile pair of the
-    // tensor-core pass takes ~4,250 cycles.)
+    // decode kernel streams ~80 GB/s per SM when HBM is not the limit and
+    // saturates HBM on about 100 SMs; a tile pair of the tensor-core pass takes
+    // ~4,250 cycles.  The per-SM rates below are the ones that gave the
+    // fastest steps on the 256-decode, 4096-token-prefix batch: 39 B/cycle of
+    // bf16 K/V (a 64-CTA prefix pass beside an 88-CTA decode, 0.122 ms), 28 of
+    // fp8 codes (the same split, 0.103 ms; 34 picked 5 key chunks on 80 CTAs
+    // and took 0.122 ms).)
     constexpr double kPairCycles = 4250.0;
     constexpr double kPrefixStartCycles = 8000.0;
     constexpr double kDecodeStartCycles = 30000.0;
-    const double kSmBytesPerCycle = kv_fp8 ? 34.0 : 39.0;
+    const double kSmBytesPerCycle = kv_fp8 ? 28.0 : 39.0;
     constexpr double kHbmBytesPerCycle = 3250.0;  // ~6.7 TB/s at ~2.07 GHz
     const double suffix_keys =
         double(num_decodes) * std::max(1.0, 0.5 * double(max_seq_len - prefix_len + 1));
