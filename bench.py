@@ -314,11 +314,38 @@ KERNEL_SOURCES = {"decode": ("decode.cu", "common.cuh"),
                   "prefill": ("prefill.cu", "common.cuh", "tcgen05.cuh")}
 
 
+def code_only(text):
+    """C/C++/CUDA source with comments removed and whitespace runs collapsed
+    (string and character literals kept as written): what the compiler sees,
+    so that editing a comment does not change a kernel's key."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash(kernel="decode"):
+    """Key of a kernel's code (its source files, comments and whitespace aside)."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "paged_kv_attention_33_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "paged_kv_attention_33_gb300", "csrc", f)) as fh:
+            h.update(code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

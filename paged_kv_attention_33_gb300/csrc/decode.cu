@@ -7,7 +7,8 @@
 // for all query heads of its kv head at the same time (GQA packing), and is
 // staged into shared memory by TMA ahead of use.
 //
-// Grid: persistent, one CTA per SM, stream-K.  The decodes' keys
+// Grid: persistent, one CTA per SM (or, beside a cascade's shared-prefix pass,
+// one per SM that pass leaves), stream-K.  The decodes' keys
 // [kv_begin, L_s) are cut into stages of 16*(8/Hkv) keys; the flattened list
 // of all stages (sequence after sequence) is divided into equal, contiguous
 // ranges, one per CTA, so every CTA streams the same number of bytes and its
@@ -20,8 +21,9 @@
 // CTA: 8 consumer warps + 1 producer warp.  A pipeline stage holds 8 "units";
 // unit u is 16 consecutive keys of kv head k = u % Hkv, slice r = u / Hkv of the
 // stage's 16*(8/Hkv) keys (so every warp works in every stage).  The producer
-// issues, per slice and 64-dim half, one TMA box {64 dims, 16 keys, Hkv heads}
-// for K and one for V: the pool is viewed as a 3-D tensor whose outermost
+// issues, per slice and 64-dim half (fp8: per 16-key half of a slice), one TMA
+// box {128 bytes, 16 keys, Hkv heads} for K and one for V: the pool is viewed
+// as a 3-D tensor whose outermost
 // dimension is the kv head (NHD: (head_size, num_blocks*2*block_size,
 // num_kv_heads), the head stride being one row; HND: (head_size, block_size,
 // num_blocks*2*num_kv_heads)) -- the "FlashAttention y FlashInfer" page's
@@ -55,8 +57,13 @@
 // every call, which would convert each code once per Q or P term.)
 //
 // At the end of a piece every warp writes its rows straight from registers:
-// the final bf16 rows and lse, or (several pieces, or Hkv < 8 where several
-// warps share a kv head) a normalised fp32 partial and its log2-sum-exp.
+// the final bf16 rows and lse (a cascade's suffix: fp32 rows and log2-sum-exp,
+// merged with the shared prefix by a later kernel), or (several pieces, or
+// Hkv < 8 where several warps share a kv head) a normalised fp32 partial and
+// its log2-sum-exp.
+// Fused cache write: the stage holding a decode's new key (key L-1) gets that
+// row from the step's K/V rows, and the row is stored at the token's slot, so
+// the pool need not hold it before the launch.
 // Failure path: every wait is bounded; a warp whose wait gives up raises a
 // CTA-wide abort flag, stops computing and writing, but still walks the same
 // stage and piece sequence so that every named barrier is reached by all.

@@ -10,8 +10,12 @@
 //
 // Work item: (sequence s, 256-query super-tile, query head h) = two 128-row
 // tiles A and B that share every K/V tile, in a persistent grid (one CTA per
-// SM).  Items are claimed dynamically from a global counter (the heaviest
-// causal tiles of each sequence first), so CTAs that draw light items take more.
+// SM, or a cascade prefix pass's share of the SMs).  Items are claimed
+// dynamically from a global counter (the heaviest causal tiles of each
+// sequence first), so CTAs that draw light items take more.  The pool it reads
+// may be the forward's 128-key re-blocking of a 16-key-page pool (one box per
+// tile half instead of one per page: at 16-key pages one SM's TMA box rate,
+// not the MMAs, bounded this kernel).
 // Roles (384 threads, three warpgroups):
 //   warp 0      TMA producer: Q tiles once per item, K and V tiles of 128 keys
 //               into two-stage rings (K one tile ahead of V, each freed by its
