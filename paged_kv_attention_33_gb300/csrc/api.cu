@@ -751,6 +751,7 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
         dout.o_suf = reinterpret_cast<float *>(wsp + ws.o_suf);
         dout.lse_suf = reinterpret_cast<float *>(wsp + ws.lse_suf);
         dout.after_prefix = cp.overlap;
+        dout.combine_follows = true;
         if (cp.overlap) {
             // nothing may stand between the two launches: zero the decode's
             // counters first

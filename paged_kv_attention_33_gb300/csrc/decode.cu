@@ -106,6 +106,7 @@ struct DecodeParams {
     // runs on the other SMs at the same time: the grid completes only after
     // that pass completed (griddepcontrol.wait before every CTA exits)
     int32_t after_prefix;
+    int32_t trigger_dependents;  // the cascade's combine follows as a dependent launch
     float *o_part;        // [slots, R, H, D] normalised partials
     float *lse_part;      // [slots, R, H], log2 units
     int32_t *counters;    // [nseq] pieces finished per sequence (zeroed before the launch)
@@ -959,6 +960,11 @@ template <int D, bool kHnd, bool kFp8>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p)
 {
+    // The cascade's combine (launched after this grid as its dependent) may be
+    // scheduled on SMs as they free up; it waits for this grid to complete
+    // before it reads anything.
+    if (p.trigger_dependents)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     decode_cta<D, kHnd, kFp8>(kv_map, p);
     // A cascade's suffix pass runs beside the shared-prefix pass (a dependent
     // launch that starts while the prefix pass holds its SMs); its CTAs wait
@@ -994,6 +1000,9 @@ __global__ void __launch_bounds__(256) cascade_combine_kernel(const CombineParam
     constexpr int kPer = D / 32;
     constexpr int kParts = 1 + kMaxPrefixSplits;  // part 0: the suffix, 1 + c: prefix chunk c
     using Vec = typename std::conditional<kPer == 4, float4, float2>::type;
+    // a dependent launch: the passes that write the partials may still run
+    // (this grid's CTAs start as theirs finish); wait until they completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const int64_t rows = int64_t(p.num_tokens) * p.num_heads;
@@ -1106,6 +1115,7 @@ static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Wor
     p.k_scale = f.k_scale;
     p.v_scale = f.v_scale;
     p.test_skip_copies = f.test_skip_copies;
+    p.trigger_dependents = dout.combine_follows ? 1 : 0;
     // one launch per chunk of at most kMaxDecodeChunk decodes (stream ordered,
     // so chunks reuse the same partial slots and counters)
     for (int32_t seq0 = 0; seq0 < f.num_decodes; seq0 += dp.chunk) {
@@ -1176,13 +1186,22 @@ cudaError_t launch_cascade_combine(const Fwd &f, const Workspace &ws, char *wsp)
     p.lse_suf = reinterpret_cast<const float *>(wsp + ws.lse_suf);
     p.out = static_cast<__nv_bfloat16 *>(f.out);
     p.lse = f.lse;
-    const unsigned grid = static_cast<unsigned>((warps * 32 + 255) / 256);
+    // launched as the dependent of the kernel before it (the suffix decode or
+    // the prefill pass), so that its CTAs take SMs as that grid drains
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(static_cast<unsigned>((warps * 32 + 255) / 256));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = f.stream;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     count_launch();
     if (f.head_size == 128)
-        cascade_combine_kernel<128><<<grid, 256, 0, f.stream>>>(p);
-    else
-        cascade_combine_kernel<64><<<grid, 256, 0, f.stream>>>(p);
-    return cudaGetLastError();
+        return cudaLaunchKernelEx(&cfg, cascade_combine_kernel<128>, p);
+    return cudaLaunchKernelEx(&cfg, cascade_combine_kernel<64>, p);
 }
 
 uint32_t decode_take_error() { return take_device_error(); }

@@ -164,6 +164,8 @@ struct DecodeOut {
     // the first launch's per-sequence counters were zeroed by the caller
     // (before the prefix pass, so that nothing stands between the two kernels)
     bool counters_zeroed = false;
+    // the cascade's combine follows: let it be scheduled as this grid drains
+    bool combine_follows = false;
 };
 
 // decode.cu: paged decode of sequences [0, num_decodes) over keys

@@ -42,6 +42,34 @@ def test_mixed_decode_first_batch(oracle):
     G.check_batch(oracle, W.make_batch(sp, seed=3300), label="mixed")
 
 
+@pytest.mark.parametrize("gain", [6.0, 40.0])
+def test_prefill_logits_rising_past_the_first_tile(oracle, gain):
+    """Keys of a later tile scaled by `gain` raise the logits there (log2
+    units) by ~12 at gain 6 and by ~100 at gain 40 above the first tile's max:
+    the softmax's reference max moves (past its threshold) and O, already
+    holding the earlier tiles' PV, is rescaled; at gain 40 the earlier tiles'
+    weights underflow to nothing."""
+    sp = W.BatchSpec("rise", 8, 2, 128, 16, prefill=[(512, 0), (300, 40)])
+    b = W.make_batch(sp, seed=3600)
+    k = W.bf16_bits_to_f32(b.key)
+    q0, q1 = int(b.query_start_loc[0]), int(b.query_start_loc[1])
+    k[q0 + 256:q0 + 384] *= gain  # keys 256..383 of the first prompt (its third tile)
+    k[q1 + 120:q1 + 200] *= gain  # keys 160..239 of the second (40 cached keys first)
+    b.key = W.f32_to_bf16_bits(k)
+    G.check_batch(oracle, b, label=f"rising logits x{gain}")
+
+
+def test_many_prefill_sequences(oracle):
+    """600 short prefill chunks with cached context beside two decodes: the
+    prefill kernel maps its work items to sequences through a per-CTA prefix
+    table of super-tiles; every row matches the oracle."""
+    rng = np.random.default_rng(3700)
+    prefill = [(int(q), int(c)) for q, c in zip(rng.integers(1, 40, 600),
+                                                 rng.integers(0, 60, 600))]
+    sp = W.BatchSpec("many", 8, 2, 64, 16, decode_ctx=[10, 300], prefill=prefill)
+    G.check_batch(oracle, W.make_batch(sp, seed=3701), label="600 prefill sequences")
+
+
 def test_non_causal_prefill(oracle):
     sp = W.BatchSpec("nc", 8, 2, 64, 16, prefill=[(70, 0), (130, 45)], causal=False)
     G.check_batch(oracle, W.make_batch(sp, seed=3400), label="non-causal")
