@@ -798,13 +798,19 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
             if (e != cudaSuccess)
                 return cuda_fail(e, "fp8 block copy launch");
         }
-        // a bf16 pool of small pages: the pass reads the re-blocked copy
+        // the fused call over a bf16 pool: key tiles of this step's keys only
+        // are read from its key/value rows (identical to what was just
+        // written into the pool)
+        pf.new_from_input = f.fuse_write && !f.kv_fp8;
+        // a bf16 pool of small pages: the pass reads the re-blocked copy (of the
+        // tiles it still reads from the pool)
         Fwd fr = fp;
         if (ws.reblock_blocks > 0) {
             int32_t *rtable = reinterpret_cast<int32_t *>(wsp + ws.reblock_table);
             void *rscratch = wsp + ws.reblock_scratch;
             const int32_t rb = ws.reblock_blocks_per_seq;
-            e = launch_reblock(f, rscratch, rtable, meta->num_decodes, num_prefills, rb, 0, rb);
+            e = launch_reblock(f, rscratch, rtable, meta->num_decodes, num_prefills, rb, 0, rb,
+                               pf.new_from_input ? kv_begin : -1);
             if (e != cudaSuccess)
                 return cuda_fail(e, "prefill re-block launch");
             fr.kv_cache = rscratch;
@@ -859,21 +865,8 @@ pka_status pka_paged_attn_forward_fused(const void *query, const void *key, cons
         return fail(PKA_ERR_INVALID_ARG, "null pointer argument");
     if (!aligned(key, 16) || !aligned(value, 16) || !aligned(slot_mapping, 8))
         return fail(PKA_ERR_INVALID_ARG, "misaligned pointer (16 bytes required)");
-    if (meta->num_decodes == 0) {
-        // no decode launch to carry the write: write first, then attend
-        st = meta->kv_dtype == PKA_KV_FP8_E4M3
-                 ? pka_reshape_and_cache_fp8(key, value, kv_cache, slot_mapping, num_tokens,
-                                             num_kv_heads, head_size, block_size, num_blocks,
-                                             meta->kv_layout, meta->k_scale, meta->v_scale, stream)
-                 : pka_reshape_and_cache_ex(key, value, kv_cache, slot_mapping, num_tokens,
-                                            num_kv_heads, head_size, block_size, num_blocks,
-                                            meta->kv_layout, stream);
-        if (st != PKA_OK)
-            return st;
-        return forward_impl(query, kv_cache, meta, out, lse, num_tokens, num_heads, num_kv_heads,
-                            head_size, block_size, num_blocks, scale, causal, workspace,
-                            workspace_bytes, stream, nullptr);
-    }
+    // the prefill tokens' rows are written by the cache-write kernel first,
+    // each decode's by the decode launch
     const FuseArgs fa{key, value, slot_mapping, kv_cache};
     return forward_impl(query, kv_cache, meta, out, lse, num_tokens, num_heads, num_kv_heads,
                         head_size, block_size, num_blocks, scale, causal, workspace,

@@ -142,10 +142,13 @@ cudaError_t launch_dequant_blocks(const Fwd &f, void *scratch, int32_t *table, i
 // The prefill sequences' keys of a bf16 pool of small pages (block_size a
 // divisor of 32) copied into 128-key NHD blocks of a scratch pool: block-table
 // rows [first_row, first_row + num_rows), destination block dst_base +
-// p * row_blocks + n of row p, table rows of stride table_stride.
+// p * row_blocks + n of row p, table rows of stride table_stride.  With
+// context_lo >= 0 only the blocks that a pass starting at key context_lo still
+// reads from the pool when it takes the tiles of this step's keys from the
+// step's rows (those below a sequence's context, plus one) are copied.
 cudaError_t launch_reblock(const Fwd &f, void *scratch, int32_t *table, int32_t first_row,
                            int32_t num_rows, int32_t row_blocks, int64_t dst_base,
-                           int32_t table_stride);
+                           int32_t table_stride, int32_t context_lo = -1);
 uint32_t kv_write_take_error();
 
 // Most key chunks of a cascade's shared-prefix pass (partials per row).
@@ -217,6 +220,9 @@ struct PrefillPass {
     // let a dependent launch (the cascade's suffix decode) start as soon as
     // every CTA of this pass is resident
     bool trigger_dependents = false;
+    // a bf16 pool written this step (the fused call): key tiles that hold only
+    // this step's keys are read from its key/value rows, not from the pool
+    bool new_from_input = false;
 };
 cudaError_t launch_prefill(const Fwd &f, const PrefillPass &pass);
 uint32_t prefill_take_error();

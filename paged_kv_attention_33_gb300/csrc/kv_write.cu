@@ -249,8 +249,12 @@ cudaError_t launch_dequant_blocks(const Fwd &f, void *scratch, int32_t *table, i
 // sequence: block-table row first_row + p, destination block dst_base +
 // p * row_blocks + n (NHD, every kv head), its id stored at
 // table[(first_row + p) * table_stride + n]; keys at and past L are not
-// copied (the prefill pass never admits them).  A warp copies whole key rows
-// (every head's K or V row of one key), lanes along the row.
+// copied (the prefill pass never admits them).  With context_lo >= 0 (the
+// pass reads every key tile that starts at or after the sequence's context
+// ctx = L - q from the step's own rows) only the blocks that such a pass still
+// reads here are copied: none when ctx <= context_lo (its first key), else
+// those that start below ctx + 127.  A warp copies whole key rows (every
+// head's K or V row of one key), lanes along the row.
 constexpr int kReblockKeys = 128;
 constexpr int kReblockSplit = 4;  // CTAs per destination block
 constexpr int kReblockCtaKeys = kReblockKeys / kReblockSplit;
@@ -258,7 +262,8 @@ constexpr int kReblockCtaKeys = kReblockKeys / kReblockSplit;
 __global__ void __launch_bounds__(kKvwThreads)
     reblock_kernel(const uint4 *__restrict__ pool, uint4 *__restrict__ scratch,
                    int32_t *__restrict__ table, const int32_t *__restrict__ bt,
-                   int32_t bt_stride, const int32_t *__restrict__ seq_lens, int32_t first_row,
+                   int32_t bt_stride, const int32_t *__restrict__ seq_lens,
+                   const int32_t *__restrict__ qsl, int32_t context_lo, int32_t first_row,
                    int32_t row_blocks, int64_t dst_base, int32_t table_stride,
                    int32_t block_size, int32_t num_kv_heads, int32_t head_chunks,
                    int64_t num_blocks, int32_t hnd)
@@ -273,6 +278,11 @@ __global__ void __launch_bounds__(kKvwThreads)
     const int32_t key0 = n * kReblockKeys + quarter * kReblockCtaKeys;  // first key copied
     if (n >= row_blocks || key0 >= L)
         return;
+    if (context_lo >= 0) {
+        const int32_t ctx = L - (qsl[s + 1] - qsl[s]);
+        if (ctx <= context_lo || n * kReblockKeys >= ctx + kReblockKeys - 1)
+            return;
+    }
     const int32_t keys = min(kReblockCtaKeys, L - key0);
     const int64_t dst_blk = dst_base + int64_t(p) * row_blocks + n;
     if (quarter == 0 && threadIdx.x == 0)
@@ -319,7 +329,7 @@ __global__ void __launch_bounds__(kKvwThreads)
 
 cudaError_t launch_reblock(const Fwd &f, void *scratch, int32_t *table, int32_t first_row,
                            int32_t num_rows, int32_t row_blocks, int64_t dst_base,
-                           int32_t table_stride)
+                           int32_t table_stride, int32_t context_lo)
 {
     if (num_rows <= 0 || row_blocks <= 0)
         return cudaSuccess;
@@ -329,8 +339,8 @@ cudaError_t launch_reblock(const Fwd &f, void *scratch, int32_t *table, int32_t 
     dim3 grid(static_cast<unsigned>(row_blocks * kReblockSplit), static_cast<unsigned>(num_rows));
     reblock_kernel<<<grid, kKvwThreads, 0, f.stream>>>(
         static_cast<const uint4 *>(f.kv_cache), static_cast<uint4 *>(scratch), table,
-        f.block_table, f.bt_stride, f.seq_lens, first_row, row_blocks, dst_base, table_stride,
-        f.block_size, f.num_kv_heads, f.head_size * 2 / 16, f.num_blocks, f.kv_hnd);
+        f.block_table, f.bt_stride, f.seq_lens, f.qsl, context_lo, first_row, row_blocks, dst_base,
+        table_stride, f.block_size, f.num_kv_heads, f.head_size * 2 / 16, f.num_blocks, f.kv_hnd);
     return cudaGetLastError();
 }
 

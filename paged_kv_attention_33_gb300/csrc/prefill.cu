@@ -100,6 +100,10 @@ struct PrefillParams {
     int32_t kv_splits;      // shared_prefix: key chunks, split_tiles key tiles each
     int32_t split_tiles;
     int32_t test_skip_copies;  // failure-path test: the producer issues nothing
+    // 1: a K/V tile that starts at or after its sequence's context (all its
+    // keys are this step's) is read from the step's key/value rows
+    // ([num_tokens, Hkv, D], one box of 128 tokens per half) instead of the pool
+    int32_t new_from_input;
     int32_t trigger_dependents;  // the cascade's suffix decode may start beside this pass
 };
 
@@ -459,7 +463,9 @@ __device__ __forceinline__ void pf_softmax(const PrefillParams &p, const int32_t
 template <int D, bool kHnd>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
-                      const __grid_constant__ CUtensorMap kv_map, const PrefillParams p)
+                      const __grid_constant__ CUtensorMap kv_map,
+                      const __grid_constant__ CUtensorMap kin_map,
+                      const __grid_constant__ CUtensorMap vin_map, const PrefillParams p)
 {
     using Cfg = PfCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -558,6 +564,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             if (lane == 0) {
                 tma_prefetch_desc(&q_map);
                 tma_prefetch_desc(&kv_map);
+                if (p.new_from_input) {
+                    tma_prefetch_desc(&kin_map);
+                    tma_prefetch_desc(&vin_map);
+                }
             }
             const uint64_t pol_kv = l2_policy_evict_last();
             const uint64_t pol_q = l2_policy_evict_first();
@@ -594,10 +604,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 const int kv_hi = it.kv_hi;
                 // lane b owns TMA box b of every K/V tile; its block id is looked
                 // up for the next tile before waiting for a free stage
+                // a tile of this step's keys only: read from the step's rows
+                auto from_input = [&](int key0) { return p.new_from_input && key0 >= it.ctx; };
                 auto lane_block = [&](int jt) -> int {
                     const int key0 = it.kv_lo + jt * kBN;
                     const int nbox = (min(kBN, kv_hi - key0) + p.box_rows - 1) / p.box_rows;
-                    if (lane >= nbox)
+                    if (lane >= nbox || from_input(key0))
                         return -1;
                     const int col = (key0 + lane * p.box_rows) / p.block_size;
                     int blk = col < p.bt_stride ? bt[col] : -1;
@@ -633,9 +645,25 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     if (rnd > 0 && !pf_wait(emp, (rnd - 1) & 1, abort_flag))
                         return false;
                     const int key0 = it.kv_lo + jt * kBN;
+                    uint64_t *bar = which ? &bars.v_full[st] : &bars.k_full[st];
+                    uint8_t *tile = smem + (which ? Cfg::kVOff : Cfg::kKOff) + st * Cfg::kTileBytes;
+                    if (from_input(key0)) {
+                        // token of key key0: the sequence's first query token is
+                        // the step row of its first new key (key ctx); rows past
+                        // the sequence's end are masked, V's zeroed by the MMA warp
+                        const int tok = it.t0 - it.qidx0 + (key0 - it.ctx);
+                        if (lane == 0) {
+                            mbar_arrive_expect_tx(bar, kBN * 128 * Cfg::kHalves);
+                            for (int hf = 0; hf < Cfg::kHalves; ++hf)
+                                tma_load_3d(tile + hf * Cfg::kHalfBytes, which ? &vin_map : &kin_map,
+                                            bar, hf * 64, kvh, tok, pol_kv);
+                        }
+                        __syncwarp();
+                        (which ? v_armed : k_armed) = n + 1;
+                        return true;
+                    }
                     const int nbox = (min(kBN, kv_hi - key0) + p.box_rows - 1) / p.box_rows;
                     const uint32_t bytes = nbox * p.box_rows * 128 * Cfg::kHalves;
-                    uint64_t *bar = which ? &bars.v_full[st] : &bars.k_full[st];
                     if (lane == 0)
                         mbar_arrive_expect_tx(bar, bytes);
                     __syncwarp();
@@ -647,8 +675,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                         const int c1 = kHnd ? key % p.block_size : kvh;
                         const int row = kHnd ? (blk * 2 + which) * p.num_kv_heads + kvh
                                              : (blk * 2 + which) * p.block_size + key % p.block_size;
-                        uint8_t *dst = smem + (which ? Cfg::kVOff : Cfg::kKOff) +
-                                       st * Cfg::kTileBytes + lane * p.box_rows * 128;
+                        uint8_t *dst = tile + lane * p.box_rows * 128;
                         for (int hf = 0; hf < Cfg::kHalves; ++hf)
                             tma_load_3d(dst + hf * Cfg::kHalfBytes, &kv_map, bar, hf * 64, c1,
                                         row, pol_kv);
@@ -875,7 +902,19 @@ static cudaError_t launch_prefill_d(const Fwd &f, const PrefillParams &p, int gr
                       f.kv_hnd, uint32_t(p.box_rows)) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     count_launch();
-    prefill_tc_kernel<D, kHnd><<<grid, kPfThreads, Cfg::kSmemBytes, f.stream>>>(q_map, kv_map, p);
+    // the step's key and value rows as (dim, head, token), one box of 128
+    // tokens per 64-dim half (unused unless p.new_from_input)
+    CUtensorMap kin_map = kv_map, vin_map = kv_map;
+    if (p.new_from_input) {
+        const uint64_t row = uint64_t(D) * 2;
+        if (encode_3d_bf16(&kin_map, f.new_key, D, f.num_kv_heads, f.num_tokens, row,
+                           row * f.num_kv_heads, 64, 1, kBN) != CUDA_SUCCESS ||
+            encode_3d_bf16(&vin_map, f.new_value, D, f.num_kv_heads, f.num_tokens, row,
+                           row * f.num_kv_heads, 64, 1, kBN) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    prefill_tc_kernel<D, kHnd><<<grid, kPfThreads, Cfg::kSmemBytes, f.stream>>>(
+        q_map, kv_map, kin_map, vin_map, p);
     return cudaGetLastError();
 }
 
@@ -919,6 +958,7 @@ cudaError_t launch_prefill(const Fwd &f, const PrefillPass &pass)
     p.split_tiles = 0;
     p.test_skip_copies = f.test_skip_copies;
     p.trigger_dependents = pass.trigger_dependents ? 1 : 0;
+    p.new_from_input = pass.new_from_input && !pass.shared_prefix && f.new_key && f.new_value ? 1 : 0;
     if (pass.shared_prefix) {
         const int tiles = (pass.kv_cap - pass.kv_lo + kBN - 1) / kBN;
         p.kv_splits = std::max(1, pass.kv_splits);
