@@ -53,6 +53,14 @@ CASES = {
                     prefill=[(50, 256)], common_prefix_len=256),
     "hnd_large_pages": dict(H=32, Hkv=8, D=128, bs=256, decode_ctx=[10, 255, 256, 1500],
                             prefill=[(200, 100)], kv_layout="HND"),
+    # 16-key pages under query-heavy prefills with prior context that ends inside a
+    # 128-key tile: the context's blocks go through the re-blocking copy, the tiles
+    # of this step's keys come from the step's rows
+    "small_pages_context": dict(H=16, Hkv=4, D=128, bs=16, decode_ctx=[5, 300],
+                                prefill=[(400, 0), (300, 70), (300, 200), (129, 37)]),
+    "hnd_small_pages_context": dict(H=16, Hkv=4, D=64, bs=16, decode_ctx=[40],
+                                    prefill=[(400, 130), (300, 0), (300, 255)],
+                                    kv_layout="HND"),
 }
 
 
