@@ -283,12 +283,17 @@ pka_status pka_paged_attn_forward(const void *query, const void *kv_cache, const
  * tokens' rows are written by the cache-write kernel before the forward's
  * other launches (one warp per token over the whole GPU; written by the
  * decode CTAs they would hold back the decode's first copies).  A batch of
- * decodes only is thus one launch for write and attention.
+ * decodes only is thus one launch for write and attention.  Over a bf16 pool
+ * the prefill pass reads a 128-key tile that holds only this step's keys
+ * (one that starts at or after its sequence's prior context) from
+ * `key`/`value` rather than from the pool, the same values.
  *
  *  key, value     device bf16 [num_tokens, num_kv_heads, head_size], as in
- *                 pka_reshape_and_cache
- *  slot_mapping   device int64 [num_tokens]; for a decode token the slot of
- *                 its sequence's last key (key L_s - 1 through block_table),
+ *                 pka_reshape_and_cache; 16-byte aligned, read until the
+ *                 forward's last launch
+ *  slot_mapping   device int64 [num_tokens]; the slot of each token's key
+ *                 through block_table: token qsl[s] + i is key
+ *                 L_s - q_s + i of sequence s (for a decode, key L_s - 1),
  *                 which is what makes the fused and the two-call results agree
  *  kv_cache       device pool, written in place (layout meta->kv_layout);
  *                 for an fp8 pool the rows are stored as pka_reshape_and_cache_fp8
