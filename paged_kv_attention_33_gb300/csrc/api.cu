@@ -252,6 +252,63 @@ CascadePlan plan_cascade(int32_t num_tokens, int32_t num_heads, int32_t num_kv_h
     return c;
 }
 
+// Decodes and prefills of one batch (no cascade).  The decode is bound by HBM
+// and the prefill pass by its SMs (tensor cores and shared memory), and one SM
+// of the decode streams ~39 B/cycle (~80 GB/s; 28 of fp8 codes) while HBM
+// takes ~3,250 B/cycle: on every SM the decode holds 152 SMs for its bytes at
+// the chip's rate, on x SMs only x.  So the decode may run on x SMs beside the
+// prefill pass on the others, the pass (its programmatic dependent, one CTA per
+// SM, work items claimed from a counter) taking over the decode's SMs as they
+// free up: the step then costs about the pass's SM-time plus the decode's bytes
+// at the per-SM rate, over the chip.  The host does not see the lengths: every
+// sequence's keys are taken as half of max_seq_len, the decode's bytes with a
+// 25% margin (a decode that ends after the pass holds the whole step, one that
+// ends before it only lends its SMs to the pass later).  A tile pair of the
+// pass (two 128-query tiles against a 128-key tile) takes ~4,250 cycles:
+// ~3,950 flops per SM and cycle at head_size 128.  Chosen only when the model
+// saves at least 5%.  (Measured on the mixed batch of 64 decodes and four
+// 2,048-query chunks: 1.426 ms one after the other; side by side with the
+// decode on 16 / 24 / 31 / 40 / 48 / 64 / 80 SMs 1.612 / 1.132 / 1.149 / 1.147
+// / 1.145 / 1.160 / 1.232 ms; the model picks 31.)
+MixedPlan plan_mixed(int32_t num_tokens, int32_t num_heads, int32_t num_kv_heads,
+                     int32_t head_size, int32_t num_decodes, int32_t num_seqs,
+                     int32_t max_seq_len, bool kv_fp8, bool single_decode_launch, int num_sms)
+{
+    MixedPlan mp;
+    const int64_t prefill_tokens = int64_t(num_tokens) - num_decodes;
+    if (num_decodes <= 0 || num_seqs <= num_decodes || prefill_tokens <= 0 ||
+        !single_decode_launch || num_sms < 32)
+        return mp;
+    constexpr double kPassFlopsPerSmCycle = 3950.0;
+    constexpr double kPassStartCycles = 8000.0;
+    constexpr double kDecodeStartCycles = 30000.0;
+    const double kSmBytesPerCycle = kv_fp8 ? 28.0 : 39.0;
+    constexpr double kHbmBytesPerCycle = 3250.0;
+    const double half = std::max(1.0, 0.5 * double(max_seq_len));
+    const double dec_bytes = 1.25 * double(num_decodes) * half * num_kv_heads * head_size *
+                             (kv_fp8 ? 2.0 : 4.0);
+    const double pass_sm_cycles =
+        double(prefill_tokens) * half * 4.0 * head_size * num_heads / kPassFlopsPerSmCycle;
+    auto t_dec = [&](int ctas) {
+        return kDecodeStartCycles + dec_bytes / std::min(kHbmBytesPerCycle, ctas * kSmBytesPerCycle);
+    };
+    const double t_serial = t_dec(num_sms) + kPassStartCycles + pass_sm_cycles / num_sms;
+    double best = 0.95 * t_serial;
+    for (int x = 16; x <= num_sms - 16; ++x) {
+        const double td = t_dec(x);
+        const double beside = double(num_sms - x) * std::max(0.0, td - kPassStartCycles);
+        const double t = pass_sm_cycles <= beside
+                             ? td
+                             : td + (pass_sm_cycles - beside) / num_sms;
+        if (t < best) {
+            best = t;
+            mp.overlap = true;
+            mp.dec_ctas = x;
+        }
+    }
+    return mp;
+}
+
 Workspace plan_workspace(const DecodePlan &dp, int32_t num_tokens, int32_t num_decodes,
                          int32_t num_heads, int32_t head_size, bool cascade,
                          int32_t pre_splits)
@@ -420,6 +477,7 @@ static pka_status check_shape(const pka_meta *m, int32_t num_tokens, int32_t num
 struct ForwardPlan {
     DecodePlan dp;
     CascadePlan cp;
+    MixedPlan mp;
     Workspace ws;
 };
 
@@ -437,6 +495,11 @@ static ForwardPlan plan_forward(const pka_meta *m, int32_t num_tokens, int32_t n
                              fp.dp.chunk == m->num_decodes, sms);
         if (fp.cp.overlap)
             fp.dp.grid = sms - fp.cp.pre_ctas;  // the decode takes the SMs the prefix leaves
+    } else {
+        fp.mp = plan_mixed(num_tokens, num_heads, num_kv_heads, head_size, m->num_decodes,
+                           m->num_seqs, m->max_seq_len, fp8, fp.dp.chunk == m->num_decodes, sms);
+        if (fp.mp.overlap)
+            fp.dp.grid = fp.mp.dec_ctas;
     }
     fp.ws = plan_workspace(fp.dp, num_tokens, m->num_decodes, num_heads, head_size, cascade,
                            fp.cp.pre_splits);
@@ -672,6 +735,7 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
                             f.num_sms, false);
     const DecodePlan &dp = plan.dp;
     const CascadePlan &cp = plan.cp;
+    const MixedPlan &mp = plan.mp;
     const Workspace &ws = plan.ws;
     if (ws.fp8_scratch_blocks * 2 * block_size >= (int64_t(1) << 31) ||
         ws.reblock_blocks * 2 * 128 >= (int64_t(1) << 31))
@@ -751,7 +815,7 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
         dout.o_suf = reinterpret_cast<float *>(wsp + ws.o_suf);
         dout.lse_suf = reinterpret_cast<float *>(wsp + ws.lse_suf);
         dout.after_prefix = cp.overlap;
-        dout.combine_follows = true;
+        dout.dependent_follows = true;  // the combine
         if (cp.overlap) {
             // nothing may stand between the two launches: zero the decode's
             // counters first
@@ -777,52 +841,82 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
         if (e != cudaSuccess)
             return cuda_fail(e, "cascade prefix launch");
     }
+    // The prefill pass of the sequences [num_decodes, S).  With decodes beside it
+    // (the mixed plan) it is the decode's programmatic dependent: it starts on
+    // the SMs the decode leaves and takes the decode's SMs as they free up, so
+    // its counter, the re-blocking copy and the timing brackets go first --
+    // nothing may stand between the two launches.
+    PrefillPass pf{kv_begin, INT32_MAX, causal ? 1 : 0, false,
+                   cascade ? reinterpret_cast<float *>(wsp + ws.o_suf) : nullptr,
+                   cascade ? reinterpret_cast<float *>(wsp + ws.lse_suf) : nullptr, 0,
+                   reinterpret_cast<int32_t *>(wsp + ws.pf_counters)};
+    // the fused call over a bf16 pool: key tiles of this step's keys only are
+    // read from its key/value rows (identical to what was just written into
+    // the pool)
+    pf.new_from_input = f.fuse_write && !f.kv_fp8;
+    // a bf16 pool of small pages: the pass reads the re-blocked copy (of the
+    // tiles it still reads from the pool)
+    Fwd fr = fp;
+    auto reblock = [&]() -> cudaError_t {
+        int32_t *rtable = reinterpret_cast<int32_t *>(wsp + ws.reblock_table);
+        void *rscratch = wsp + ws.reblock_scratch;
+        const int32_t rb = ws.reblock_blocks_per_seq;
+        const cudaError_t re = launch_reblock(f, rscratch, rtable, meta->num_decodes,
+                                              num_prefills, rb, 0, rb,
+                                              pf.new_from_input ? kv_begin : -1);
+        fr.kv_cache = rscratch;
+        fr.block_table = rtable;
+        fr.bt_stride = rb;
+        fr.num_blocks = ws.reblock_blocks;
+        fr.block_size = 128;
+        fr.kv_hnd = 0;
+        return re;
+    };
+    const bool beside = mp.overlap && num_prefills > 0 && !cascade;
+    if (beside) {
+        e = cudaMemsetAsync(pf.item_counter, 0, sizeof(int32_t), f.stream);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "counter reset");
+        pf.counter_zeroed = true;
+        pf.after_decode = true;
+        if (ws.reblock_blocks > 0 && (e = reblock()) != cudaSuccess)
+            return cuda_fail(e, "prefill re-block launch");
+        // an fp8 pool: the prefill sequences' blocks as bf16 (the decode writes
+        // only its own sequences' new rows, into their last blocks)
+        if (f.kv_fp8 &&
+            (e = launch_dequant_blocks(f, fp8_scratch, fp8_table, meta->num_decodes,
+                                       num_prefills, mb, mb, 0, mb)) != cudaSuccess)
+            return cuda_fail(e, "fp8 block copy launch");
+        dout.dependent_follows = true;
+        // the two passes run at the same time: both timing brackets
+        // (instrumentation) cover the pair
+        record_start(PKA_KERNEL_PREFILL, f.stream);
+    }
     if (!cp.overlap)
         record_start(PKA_KERNEL_DECODE, f.stream);
     e = launch_decode(f, dp, ws, wsp, kv_map, kv_begin, dout);
-    record_stop(PKA_KERNEL_DECODE, f.stream);
+    if (!beside)
+        record_stop(PKA_KERNEL_DECODE, f.stream);
     if (cp.overlap)
         record_stop(PKA_KERNEL_PREFILL, f.stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "decode launch");
     if (num_prefills > 0) {
-        PrefillPass pf{kv_begin, INT32_MAX, causal ? 1 : 0, false,
-                       cascade ? reinterpret_cast<float *>(wsp + ws.o_suf) : nullptr,
-                       cascade ? reinterpret_cast<float *>(wsp + ws.lse_suf) : nullptr, 0,
-                       reinterpret_cast<int32_t *>(wsp + ws.pf_counters)};
         // fp8 after the decode launch (which wrote this step's rows): the
-        // prefill sequences' blocks
-        if (f.kv_fp8 && meta->num_decodes > 0) {
+        // prefill sequences' blocks (beside the decode: copied before it)
+        if (f.kv_fp8 && meta->num_decodes > 0 && !beside) {
             e = launch_dequant_blocks(f, fp8_scratch, fp8_table, meta->num_decodes, num_prefills,
                                       mb, mb, 0, mb);
             if (e != cudaSuccess)
                 return cuda_fail(e, "fp8 block copy launch");
         }
-        // the fused call over a bf16 pool: key tiles of this step's keys only
-        // are read from its key/value rows (identical to what was just
-        // written into the pool)
-        pf.new_from_input = f.fuse_write && !f.kv_fp8;
-        // a bf16 pool of small pages: the pass reads the re-blocked copy (of the
-        // tiles it still reads from the pool)
-        Fwd fr = fp;
-        if (ws.reblock_blocks > 0) {
-            int32_t *rtable = reinterpret_cast<int32_t *>(wsp + ws.reblock_table);
-            void *rscratch = wsp + ws.reblock_scratch;
-            const int32_t rb = ws.reblock_blocks_per_seq;
-            e = launch_reblock(f, rscratch, rtable, meta->num_decodes, num_prefills, rb, 0, rb,
-                               pf.new_from_input ? kv_begin : -1);
-            if (e != cudaSuccess)
-                return cuda_fail(e, "prefill re-block launch");
-            fr.kv_cache = rscratch;
-            fr.block_table = rtable;
-            fr.bt_stride = rb;
-            fr.num_blocks = ws.reblock_blocks;
-            fr.block_size = 128;
-            fr.kv_hnd = 0;
-        }
-        if (!cascade)
+        if (!beside && ws.reblock_blocks > 0 && (e = reblock()) != cudaSuccess)
+            return cuda_fail(e, "prefill re-block launch");
+        if (!cascade && !beside)
             record_start(PKA_KERNEL_PREFILL, f.stream);
         e = launch_prefill(fr, pf);
+        if (beside)
+            record_stop(PKA_KERNEL_DECODE, f.stream);
         if (!cascade)
             record_stop(PKA_KERNEL_PREFILL, f.stream);
         if (e != cudaSuccess)

@@ -106,7 +106,7 @@ struct DecodeParams {
     // runs on the other SMs at the same time: the grid completes only after
     // that pass completed (griddepcontrol.wait before every CTA exits)
     int32_t after_prefix;
-    int32_t trigger_dependents;  // the cascade's combine follows as a dependent launch
+    int32_t trigger_dependents;  // a programmatic dependent launch follows
     float *o_part;        // [slots, R, H, D] normalised partials
     float *lse_part;      // [slots, R, H], log2 units
     int32_t *counters;    // [nseq] pieces finished per sequence (zeroed before the launch)
@@ -960,9 +960,10 @@ template <int D, bool kHnd, bool kFp8>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p)
 {
-    // The cascade's combine (launched after this grid as its dependent) may be
-    // scheduled on SMs as they free up; it waits for this grid to complete
-    // before it reads anything.
+    // The launch after this grid, its programmatic dependent (the cascade's
+    // combine, or a prefill pass beside this decode), may be scheduled on SMs
+    // as they free up; it waits for this grid to complete before it reads this
+    // grid's results or exits.
     if (p.trigger_dependents)
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     decode_cta<D, kHnd, kFp8>(kv_map, p);
@@ -1115,7 +1116,7 @@ static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Wor
     p.k_scale = f.k_scale;
     p.v_scale = f.v_scale;
     p.test_skip_copies = f.test_skip_copies;
-    p.trigger_dependents = dout.combine_follows ? 1 : 0;
+    p.trigger_dependents = dout.dependent_follows ? 1 : 0;
     // one launch per chunk of at most kMaxDecodeChunk decodes (stream ordered,
     // so chunks reuse the same partial slots and counters)
     for (int32_t seq0 = 0; seq0 < f.num_decodes; seq0 += dp.chunk) {

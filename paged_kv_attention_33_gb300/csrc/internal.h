@@ -99,6 +99,16 @@ struct CascadePlan {
     int32_t pre_ctas = 0;  // 0: every SM
     bool overlap = false;
 };
+// Decodes and prefills of one batch (no cascade) side by side: the
+// decode on dec_ctas SMs, the prefill pass as its programmatic dependent on the
+// others, taking over the decode's SMs as they free up.
+struct MixedPlan {
+    bool overlap = false;
+    int32_t dec_ctas = 0;
+};
+MixedPlan plan_mixed(int32_t num_tokens, int32_t num_heads, int32_t num_kv_heads,
+                     int32_t head_size, int32_t num_decodes, int32_t num_seqs,
+                     int32_t max_seq_len, bool kv_fp8, bool single_decode_launch, int num_sms);
 CascadePlan plan_cascade(int32_t num_tokens, int32_t num_heads, int32_t num_kv_heads,
                          int32_t head_size, int32_t prefix_len, int32_t num_decodes,
                          int32_t max_seq_len, bool kv_fp8, bool single_decode_launch,
@@ -167,8 +177,9 @@ struct DecodeOut {
     // the first launch's per-sequence counters were zeroed by the caller
     // (before the prefix pass, so that nothing stands between the two kernels)
     bool counters_zeroed = false;
-    // the cascade's combine follows: let it be scheduled as this grid drains
-    bool combine_follows = false;
+    // a programmatic dependent launch follows (the cascade's combine, or the
+    // prefill pass beside this decode): let it be scheduled as this grid drains
+    bool dependent_follows = false;
 };
 
 // decode.cu: paged decode of sequences [0, num_decodes) over keys
@@ -223,6 +234,12 @@ struct PrefillPass {
     // a bf16 pool written this step (the fused call): key tiles that hold only
     // this step's keys are read from its key/value rows, not from the pool
     bool new_from_input = false;
+    // launched as the programmatic dependent of the decode just before it
+    // (beside it on the SMs it leaves); the pass completes after the decode
+    bool after_decode = false;
+    // item_counter was zeroed by the caller (nothing may stand between the
+    // decode and this launch)
+    bool counter_zeroed = false;
 };
 cudaError_t launch_prefill(const Fwd &f, const PrefillPass &pass);
 uint32_t prefill_take_error();

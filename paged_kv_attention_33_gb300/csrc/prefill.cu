@@ -105,6 +105,7 @@ struct PrefillParams {
     // ([num_tokens, Hkv, D], one box of 128 tokens per half) instead of the pool
     int32_t new_from_input;
     int32_t trigger_dependents;  // the cascade's suffix decode may start beside this pass
+    int32_t after_decode;        // the dependent of the decode just before it: wait for it at the end
 };
 
 template <int D>
@@ -867,6 +868,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     tc_fence_after();
     if (warp == 2)
         tmem_dealloc(tbase, kTmemCols);
+    // Beside a decode (this pass is its programmatic dependent, started on the
+    // SMs the decode left free): the grid completes only after the decode's,
+    // so that the launches after it see both passes' rows.
+    if (p.after_decode)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // --------------------------------------------------------------------- host
@@ -913,9 +919,20 @@ static cudaError_t launch_prefill_d(const Fwd &f, const PrefillParams &p, int gr
                            row * f.num_kv_heads, 64, 1, kBN) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    prefill_tc_kernel<D, kHnd><<<grid, kPfThreads, Cfg::kSmemBytes, f.stream>>>(
-        q_map, kv_map, kin_map, vin_map, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kPfThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.stream = f.stream;
+    if (p.after_decode) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, kHnd>, q_map, kv_map, kin_map, vin_map,
+                              p);
 }
 
 cudaError_t launch_prefill(const Fwd &f, const PrefillPass &pass)
@@ -959,13 +976,15 @@ cudaError_t launch_prefill(const Fwd &f, const PrefillPass &pass)
     p.test_skip_copies = f.test_skip_copies;
     p.trigger_dependents = pass.trigger_dependents ? 1 : 0;
     p.new_from_input = pass.new_from_input && !pass.shared_prefix && f.new_key && f.new_value ? 1 : 0;
+    p.after_decode = pass.after_decode ? 1 : 0;
     if (pass.shared_prefix) {
         const int tiles = (pass.kv_cap - pass.kv_lo + kBN - 1) / kBN;
         p.kv_splits = std::max(1, pass.kv_splits);
         p.split_tiles = (tiles + p.kv_splits - 1) / p.kv_splits;
     }
-    if (cudaError_t e = cudaMemsetAsync(p.item_counter, 0, sizeof(int32_t), f.stream))
-        return e;
+    if (!pass.counter_zeroed)
+        if (cudaError_t e = cudaMemsetAsync(p.item_counter, 0, sizeof(int32_t), f.stream))
+            return e;
     int64_t items;
     if (pass.shared_prefix)
         items = int64_t((f.num_tokens + kSuper - 1) / kSuper) * f.num_heads * p.kv_splits;
