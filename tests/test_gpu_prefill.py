@@ -70,6 +70,17 @@ def test_many_prefill_sequences(oracle):
     G.check_batch(oracle, W.make_batch(sp, seed=3701), label="600 prefill sequences")
 
 
+def test_decodes_with_a_long_prompt(oracle):
+    """Two decodes beside a 16K-token prompt: the forward's plan runs the decode
+    and the prefill pass one after the other here (the prompt's work dwarfs the
+    decode's), where smaller mixed batches run them side by side.  One row of
+    every 128-query tile and head, and every decode row, against the oracle."""
+    sp = W.BatchSpec("long_prompt", 16, 2, 64, 16, decode_ctx=[10, 3000],
+                     prefill=[(16384, 0)])
+    b = W.make_batch(sp, seed=3800)
+    G.check_batch(oracle, b, rows=G.tile_cover_rows(b, seed=3801), label="long prompt")
+
+
 def test_non_causal_prefill(oracle):
     sp = W.BatchSpec("nc", 8, 2, 64, 16, prefill=[(70, 0), (130, 45)], causal=False)
     G.check_batch(oracle, W.make_batch(sp, seed=3400), label="non-causal")
