@@ -934,19 +934,32 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap &kv_map, const Deco
                         p.lse_part[prow + n1] = lr1 > 0.f ? m1 + log2f(lr1) : kNegInf;
                 }
             }
-            __threadfence();
+            // The piece's rows are written (the barrier orders every consumer's
+            // writes before thread 0's); thread 0 releases them to the GPU
+            // with one fence before it counts the piece, and the last piece's
+            // thread 0 acquires the others' rows with one fence after it: the
+            // barrier then orders those before every consumer's reads.
             consumer_sync();  // all eight warps reach it, failed or not
-            if (threadIdx.x == 0)
+            if (threadIdx.x == 0) {
+                __threadfence();
                 *last_flag = (atomicAdd(&p.counters[s], 1) == np - 1) ? 1 : 0;
+                __threadfence();
+            }
             consumer_sync();
             if (*last_flag && !*abort_flag) {
                 // every piece of this sequence is written: merge them, one warp
                 // per head (warp-shuffle max/sum of the parts' log2-sum-exp,
-                // then the weighted sum of their rows, lanes along head_size)
-                __threadfence();
-                // (the fp8 stage loop leaves fewer registers: one part per
-                // round, two heads per batch)
-                merge_pieces<D, kFp8 ? 1 : 2, kFp8 ? 2 : 4>(p, t, s, bf, np * R, R, warp, lane);
+                // then the weighted sum of their rows, lanes along head_size).
+                // A round of a merge holds kQB x kHB rows in registers: with one
+                // head per warp (H <= 8) the rounds take more parts instead of
+                // more heads, so that the np x R parts of a short batch cost
+                // one or two L2 round trips.  (The fp8 stage loop leaves fewer
+                // registers: two rows per round.)
+                if (H <= kConsumerWarps)
+                    merge_pieces<D, kFp8 ? 2 : 8, 1>(p, t, s, bf, np * R, R, warp, lane);
+                else
+                    merge_pieces<D, kFp8 ? 1 : 2, kFp8 ? 2 : 4>(p, t, s, bf, np * R, R, warp,
+                                                                 lane);
             }
         }
         if (x + 1 < hi) {
