@@ -781,6 +781,24 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
     int32_t *fp8_table = reinterpret_cast<int32_t *>(wsp + ws.fp8_table);
     void *fp8_scratch = wsp + ws.fp8_scratch;
     const int32_t mb = ws.fp8_blocks_per_seq;
+    // A cascade over an fp8 pool whose passes run side by side: the prefix
+    // pass is the copy's programmatic dependent (it waits for the copy before
+    // it reads the blocks), so the suffix decode, the pass's own dependent,
+    // starts beside the copy instead of after it.  Nothing may stand between
+    // the launches: both work counters are zeroed and the timing brackets
+    // (instrumentation) opened before the copy.
+    const bool copy_chained = cascade && cp.overlap && f.kv_fp8 && ws.fp8_scratch_blocks > 0 &&
+                              meta->num_decodes > 0;
+    if (copy_chained) {
+        e = cudaMemsetAsync(wsp + ws.counters, 0, size_t(dp.chunk) * 4, f.stream);
+        if (e == cudaSuccess)
+            e = cudaMemsetAsync(reinterpret_cast<int32_t *>(wsp + ws.pf_counters) + 1, 0,
+                                sizeof(int32_t), f.stream);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "counter reset");
+        record_start(PKA_KERNEL_PREFILL, f.stream);
+        record_start(PKA_KERNEL_DECODE, f.stream);
+    }
     if (f.kv_fp8 && ws.fp8_scratch_blocks > 0) {
         fp.kv_cache = fp8_scratch;
         fp.block_table = fp8_table;
@@ -797,7 +815,7 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
             e = launch_dequant_blocks(f, fp8_scratch, fp8_table, 0, num_prefills, mb, mb, 0, mb);
         else
             e = launch_dequant_blocks(f, fp8_scratch, fp8_table, 0, 1, 0, ws.fp8_prefix_blocks,
-                                      int64_t(num_prefills) * mb, mb);
+                                      int64_t(num_prefills) * mb, mb, copy_chained);
         if (e != cudaSuccess)
             return cuda_fail(e, "fp8 block copy launch");
     }
@@ -818,21 +836,25 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
         dout.dependent_follows = true;  // the combine
         if (cp.overlap) {
             // nothing may stand between the two launches: zero the decode's
-            // counters first
-            e = cudaMemsetAsync(wsp + ws.counters, 0, size_t(dp.chunk) * 4, f.stream);
-            if (e != cudaSuccess)
-                return cuda_fail(e, "counter reset");
+            // counters first (before the copy when it is chained)
+            if (!copy_chained) {
+                e = cudaMemsetAsync(wsp + ws.counters, 0, size_t(dp.chunk) * 4, f.stream);
+                if (e != cudaSuccess)
+                    return cuda_fail(e, "counter reset");
+                // the two passes run at the same time: both timing brackets
+                // (instrumentation) cover the pair
+                record_start(PKA_KERNEL_PREFILL, f.stream);
+                record_start(PKA_KERNEL_DECODE, f.stream);
+            }
             dout.counters_zeroed = true;
-            // the two passes run at the same time: both timing brackets
-            // (instrumentation) cover the pair
-            record_start(PKA_KERNEL_PREFILL, f.stream);
-            record_start(PKA_KERNEL_DECODE, f.stream);
         }
         PrefillPass pre{0, kv_begin, 0, true, reinterpret_cast<float *>(wsp + ws.o_pre),
                         reinterpret_cast<float *>(wsp + ws.lse_pre), 0,
                         reinterpret_cast<int32_t *>(wsp + ws.pf_counters) + 1, cp.pre_splits};
         pre.max_ctas = cp.overlap ? cp.pre_ctas : 0;
         pre.trigger_dependents = cp.overlap;
+        pre.after_copy = copy_chained;
+        pre.counter_zeroed = copy_chained;
         if (!cp.overlap)
             record_start(PKA_KERNEL_PREFILL, f.stream);
         e = launch_prefill(fp, pre);

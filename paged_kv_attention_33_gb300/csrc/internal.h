@@ -146,9 +146,12 @@ cudaError_t launch_reshape_and_cache_fp8(const void *key, const void *value, voi
 // dense NHD scratch pool and its block table: block-table rows [first_row,
 // first_row + num_rows), columns below min(ceil(L/bs), col_limit), row p at
 // scratch blocks dst_base + p*row_blocks + n, table rows of stride table_stride.
+// dependent_follows: the next launch is its programmatic dependent (started at
+// once; it waits for this grid before it reads the copy).
 cudaError_t launch_dequant_blocks(const Fwd &f, void *scratch, int32_t *table, int32_t first_row,
                                   int32_t num_rows, int32_t row_blocks, int32_t col_limit,
-                                  int64_t dst_base, int32_t table_stride);
+                                  int64_t dst_base, int32_t table_stride,
+                                  bool dependent_follows = false);
 // The prefill sequences' keys of a bf16 pool of small pages (block_size a
 // divisor of 32) copied into 128-key NHD blocks of a scratch pool: block-table
 // rows [first_row, first_row + num_rows), destination block dst_base +
@@ -240,6 +243,10 @@ struct PrefillPass {
     // item_counter was zeroed by the caller (nothing may stand between the
     // decode and this launch)
     bool counter_zeroed = false;
+    // launched as the programmatic dependent of the fp8 block copy just before
+    // it: the pass waits for the copy's grid before it reads anything the copy
+    // writes (its blocks and block table)
+    bool after_copy = false;
 };
 cudaError_t launch_prefill(const Fwd &f, const PrefillPass &pass);
 uint32_t prefill_take_error();

@@ -167,7 +167,9 @@ constexpr int kDequantSplit = 8;
 // chunks) pool block bt[s][n] to scratch block dst_base + p*row_blocks + n, and
 // part 0 writes that id into the scratch table at [s][n] (row stride
 // table_stride).  Columns at or past min(ceil(L_s / bs), col_limit) are
-// left alone (the attention never reads them).
+// left alone (the attention never reads them).  With `trigger` the launch after
+// it (its programmatic dependent, which waits for this grid before it reads the
+// copy) may start at once.
 __global__ void __launch_bounds__(kKvwThreads)
     dequant_blocks_kernel(const uint4 *__restrict__ pool, uint4 *__restrict__ scratch,
                           int32_t *__restrict__ table, const int32_t *__restrict__ bt,
@@ -175,8 +177,10 @@ __global__ void __launch_bounds__(kKvwThreads)
                           int32_t first_row, int32_t row_blocks, int32_t col_limit,
                           int64_t dst_base, int32_t table_stride, int32_t block_size,
                           int32_t num_kv_heads, int32_t head_chunks, int64_t num_blocks,
-                          int32_t hnd)
+                          int32_t hnd, int32_t trigger)
 {
+    if (trigger)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // block n of row p, part `part` of its kDequantSplit slices of chunks
     const int32_t p = blockIdx.y, n = blockIdx.x / kDequantSplit, part = blockIdx.x % kDequantSplit;
     const int32_t s = first_row + p;
@@ -225,7 +229,7 @@ __global__ void __launch_bounds__(kKvwThreads)
 
 cudaError_t launch_dequant_blocks(const Fwd &f, void *scratch, int32_t *table, int32_t first_row,
                                   int32_t num_rows, int32_t row_blocks, int32_t col_limit,
-                                  int64_t dst_base, int32_t table_stride)
+                                  int64_t dst_base, int32_t table_stride, bool dependent_follows)
 {
     if (num_rows <= 0 || col_limit <= 0)
         return cudaSuccess;
@@ -234,7 +238,8 @@ cudaError_t launch_dequant_blocks(const Fwd &f, void *scratch, int32_t *table, i
     dequant_blocks_kernel<<<grid, kKvwThreads, 0, f.stream>>>(
         static_cast<const uint4 *>(f.kv_cache), static_cast<uint4 *>(scratch), table,
         f.block_table, f.bt_stride, f.seq_lens, first_row, row_blocks, col_limit, dst_base,
-        table_stride, f.block_size, f.num_kv_heads, f.head_size / 16, f.num_blocks, f.kv_hnd);
+        table_stride, f.block_size, f.num_kv_heads, f.head_size / 16, f.num_blocks, f.kv_hnd,
+        dependent_follows ? 1 : 0);
     return cudaGetLastError();
 }
 

@@ -106,6 +106,7 @@ struct PrefillParams {
     int32_t new_from_input;
     int32_t trigger_dependents;  // the cascade's suffix decode may start beside this pass
     int32_t after_decode;        // the dependent of the decode just before it: wait for it at the end
+    int32_t after_copy;          // the dependent of the block copy just before it: wait for it first
 };
 
 template <int D>
@@ -553,6 +554,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     tc_fence_after();
     const uint32_t tbase = *tmem_holder;
 
+    // The programmatic dependent of the fp8 block copy: everything above
+    // overlapped the copy; its blocks and block table are read from here on.
+    if (p.after_copy)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+
     // All 512 columns belong to this CTA, so the allocation starts at lane 0,
     // column 0: the MMA issuer's TMEM addresses are compile-time constants.
     if (tbase != 0) {
@@ -925,7 +931,7 @@ static cudaError_t launch_prefill_d(const Fwd &f, const PrefillParams &p, int gr
     cfg.blockDim = dim3(kPfThreads);
     cfg.dynamicSmemBytes = Cfg::kSmemBytes;
     cfg.stream = f.stream;
-    if (p.after_decode) {
+    if (p.after_decode || p.after_copy) {
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
@@ -977,6 +983,7 @@ cudaError_t launch_prefill(const Fwd &f, const PrefillPass &pass)
     p.trigger_dependents = pass.trigger_dependents ? 1 : 0;
     p.new_from_input = pass.new_from_input && !pass.shared_prefix && f.new_key && f.new_value ? 1 : 0;
     p.after_decode = pass.after_decode ? 1 : 0;
+    p.after_copy = pass.after_copy ? 1 : 0;
     if (pass.shared_prefix) {
         const int tiles = (pass.kv_cap - pass.kv_lo + kBN - 1) / kBN;
         p.kv_splits = std::max(1, pass.kv_splits);
