@@ -127,6 +127,12 @@ struct DecodeParams {
 constexpr int kConsumerWarps = 8;
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxDecodeChunk = 4096;
+// A batch of at most one stage per SM whose longest sequence has at most this
+// many stages is divided one sequence per CTA instead of evenly: no sequence
+// is split over CTAs, so none waits on a cross-CTA merge (a fence, an atomic
+// count and an L2 round trip of partials, several microseconds), while one CTA
+// streams a few stages in well under that.
+constexpr int kAlignedMaxStages = 8;
 constexpr float kNegInf = -INFINITY;
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -393,6 +399,16 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap &kv_map, const Deco
     }
     const int64_t total = prefix[nseq];
     int grid = gridDim.x;
+    // a small batch (at most one stage per SM, so at most one sequence per
+    // thread here): one sequence per CTA unless one of them is long; the same
+    // choice in every CTA
+    bool aligned = false;
+    if (p.target_keys == 0 && total <= grid) {
+        const int k = threadIdx.x;
+        aligned = !__syncthreads_or(k < nseq && prefix[k + 1] - prefix[k] > kAlignedMaxStages);
+    }
+    if (aligned)
+        grid = nseq;
     if (p.target_keys > 0) {
         const int64_t per_cta = (int64_t(p.target_keys) + stage_keys - 1) / stage_keys;
         const int64_t want = (total + per_cta - 1) / per_cta;
@@ -405,13 +421,13 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap &kv_map, const Deco
     const int b = blockIdx.x;
     if (b >= grid)
         return;  // whole CTA (uniform): not needed for this batch
-    const int64_t lo = int64_t(b) * total / grid;
-    const int64_t hi = int64_t(b + 1) * total / grid;
+    const int64_t lo = aligned ? prefix[b] : int64_t(b) * total / grid;
+    const int64_t hi = aligned ? prefix[b + 1] : int64_t(b + 1) * total / grid;
     if (lo >= hi)
         return;  // whole CTA (uniform): no stage falls in its range
     // first sequence of the range: the largest s with prefix[s] <= lo
-    int s_first;
-    {
+    int s_first = b;
+    if (!aligned) {
         int a = 0, e = nseq;
         while (e - a > 1) {
             const int mid = (a + e) >> 1;
@@ -859,8 +875,8 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap &kv_map, const Deco
         // ------------------------------------------------------------ end of a piece
         const float lr0 = warp_sum_heads(l0);
         const float lr1 = warp_sum_heads(l1);
-        const int bf = cta_of_stage(prefix[s], total, grid);
-        const int bl = cta_of_stage(prefix[s + 1] - 1, total, grid);
+        const int bf = aligned ? s : cta_of_stage(prefix[s], total, grid);
+        const int bl = aligned ? s : cta_of_stage(prefix[s + 1] - 1, total, grid);
         const int np = bl - bf + 1;
         // a sequence inside one CTA (and one warp per kv head) is finished from
         // registers
@@ -938,15 +954,19 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap &kv_map, const Deco
             // writes before thread 0's); thread 0 releases them to the GPU
             // with one fence before it counts the piece, and the last piece's
             // thread 0 acquires the others' rows with one fence after it: the
-            // barrier then orders those before every consumer's reads.
+            // barrier then orders those before every consumer's reads.  A
+            // sequence inside this CTA (its parts are the warps' rows) needs
+            // only the barrier: no count, no fence.
             consumer_sync();  // all eight warps reach it, failed or not
-            if (threadIdx.x == 0) {
-                __threadfence();
-                *last_flag = (atomicAdd(&p.counters[s], 1) == np - 1) ? 1 : 0;
-                __threadfence();
+            if (np > 1) {
+                if (threadIdx.x == 0) {
+                    __threadfence();
+                    *last_flag = (atomicAdd(&p.counters[s], 1) == np - 1) ? 1 : 0;
+                    __threadfence();
+                }
+                consumer_sync();
             }
-            consumer_sync();
-            if (*last_flag && !*abort_flag) {
+            if ((np == 1 || *last_flag) && !*abort_flag) {
                 // every piece of this sequence is written: merge them, one warp
                 // per head (warp-shuffle max/sum of the parts' log2-sum-exp,
                 // then the weighted sum of their rows, lanes along head_size).
