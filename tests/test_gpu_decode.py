@@ -45,6 +45,29 @@ def test_decode_edges(oracle, H, Hkv, D, bs):
         G.check_batch(oracle, b, split_kv_tokens=split, label=f"split {split}")
 
 
+# A small batch (at most one 16*(8/Hkv)-key stage per SM) whose longest
+# sequence has at most 8 stages is divided one sequence per CTA; one more stage
+# (or more stages than SMs) and it is divided evenly again, its sequences split
+# over CTAs.  Both sides of each boundary, for one, two and eight kv heads.
+@pytest.mark.parametrize("H,Hkv,D,bs", [(8, 2, 64, 16), (32, 8, 128, 16), (8, 1, 128, 32)])
+@pytest.mark.parametrize("stages", [8, 9])
+def test_decode_small_batch_division(oracle, H, Hkv, D, bs, stages):
+    sk = 16 * (8 // Hkv)  # keys per stage
+    ctx = [stages * sk - 1, 3 * sk, sk - 1, 0, 2 * sk + 5]  # L = ctx + 1
+    b = W.make_batch(_spec(H, Hkv, D, bs, ctx), seed=2300 + Hkv + stages)
+    G.check_batch(oracle, b, label=f"longest {stages} stages")
+
+
+@pytest.mark.parametrize("n", [152, 153])
+def test_decode_one_stage_per_sm(oracle, n):
+    """n one-stage decodes: one per SM (each CTA one sequence), or one more than
+    the SMs (divided evenly)."""
+    rng = np.random.Generator(np.random.PCG64(n))
+    ctx = rng.integers(0, 16, size=n).tolist()
+    b = W.make_batch(_spec(32, 8, 128, 16, ctx), seed=2400 + n)
+    G.check_batch(oracle, b, label=f"{n} one-stage decodes")
+
+
 def test_decode_many_splits_ragged(oracle):
     rng = np.random.Generator(np.random.PCG64(5))
     ctx = rng.integers(1, 3000, size=24).tolist()

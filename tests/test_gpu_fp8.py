@@ -128,6 +128,18 @@ def test_fp8_decode_heads(oracle, Hkv, g):
               label=f"Hkv={Hkv} g={g} split 48, non-power-of-two scales")
 
 
+@pytest.mark.parametrize("Hkv,g", [(8, 4), (2, 8)])
+@pytest.mark.parametrize("stages", [8, 9])
+def test_fp8_decode_small_batch_division(oracle, Hkv, g, stages):
+    """Both sides of the small-batch boundary (one sequence per CTA while the
+    longest has at most 8 stages of 32*(8/Hkv) keys) over an fp8 pool."""
+    sk = 32 * (8 // Hkv)
+    ctx = [stages * sk - 1, 3 * sk, sk - 1, 0, 2 * sk + 5]  # L = ctx + 1
+    sp = _decode_spec(f"fp8_small_{Hkv}_{g}_{stages}", Hkv * g, Hkv, 16, ctx)
+    b = W.make_batch(sp, seed=8500 + 10 * Hkv + stages)
+    check_fp8(oracle, b, 0.0625, 0.03125, label=f"Hkv={Hkv} longest {stages} stages")
+
+
 @pytest.mark.parametrize("layout", ["NHD", "HND"])
 @pytest.mark.parametrize("bs", [16, 64, 256, 1024])
 def test_fp8_decode_layouts_and_pages(oracle, layout, bs):
