@@ -914,6 +914,20 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
         // (instrumentation) cover the pair
         record_start(PKA_KERNEL_PREFILL, f.stream);
     }
+    // A decode-only batch of a few long decodes (at least 4 SMs per decode, more
+    // stages than SMs by the longest length): each decode spreads over many
+    // CTAs, and their pieces are merged by a launch over the whole GPU after the
+    // decode's rather than each by the decode's last CTA (measured on 8 of
+    // decode_heavy's decodes: that merge folds ~19 parts, 2 per L2 round trip,
+    // and ended ~12 us after the rest of the grid).
+    if (!cascade && num_prefills == 0 && meta->num_decodes > 0 &&
+        dp.chunk >= meta->num_decodes && dp.target_keys == 0) {
+        const int64_t sk = int64_t(f.kv_fp8 ? 32 : 16) * (8 / num_kv_heads);  // keys per stage
+        const int64_t longest = (int64_t(meta->max_seq_len) + sk - 1) / sk;
+        if (int64_t(dp.grid) >= 4 * int64_t(meta->num_decodes) &&
+            int64_t(meta->num_decodes) * longest > dp.grid)
+            dout.defer_merge = true;
+    }
     if (!cp.overlap)
         record_start(PKA_KERNEL_DECODE, f.stream);
     e = launch_decode(f, dp, ws, wsp, kv_map, kv_begin, dout);

@@ -110,6 +110,10 @@ struct DecodeParams {
     float *o_part;        // [slots, R, H, D] normalised partials
     float *lse_part;      // [slots, R, H], log2 units
     int32_t *counters;    // [nseq] pieces finished per sequence (zeroed before the launch)
+    // 1: a sequence split over several CTAs is not merged here; its pieces'
+    // partials are left for the merge launch that follows (counters[s] then
+    // holds its first CTA | pieces << 16, or 0 when it was not split)
+    int32_t defer_merge;
     // fused cache write (pka_paged_attn_forward_fused): this step's K/V rows
     // [T, Hkv, D] and their slots; each decode's own row is written through
     // `pool` (the prefill tokens' rows are written before this launch)
@@ -418,6 +422,14 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap &kv_map, const Deco
     // CTAs [bf, bl] of a sequence are exactly its pieces
     if (total < grid)
         grid = static_cast<int>(total);
+    if (p.defer_merge && blockIdx.x == 0) {
+        // where the merge launch finds each split sequence's pieces
+        for (int k = threadIdx.x; k < nseq; k += kDecodeThreads) {
+            const int kf = aligned ? k : cta_of_stage(prefix[k], total, grid);
+            const int kl = aligned ? k : cta_of_stage(prefix[k + 1] - 1, total, grid);
+            p.counters[k] = kl > kf ? kf | ((kl - kf + 1) << 16) : 0;
+        }
+    }
     const int b = blockIdx.x;
     if (b >= grid)
         return;  // whole CTA (uniform): not needed for this batch
@@ -957,29 +969,33 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap &kv_map, const Deco
             // barrier then orders those before every consumer's reads.  A
             // sequence inside this CTA (its parts are the warps' rows) needs
             // only the barrier: no count, no fence.
-            consumer_sync();  // all eight warps reach it, failed or not
-            if (np > 1) {
-                if (threadIdx.x == 0) {
-                    __threadfence();
-                    *last_flag = (atomicAdd(&p.counters[s], 1) == np - 1) ? 1 : 0;
-                    __threadfence();
+            // (a split sequence's pieces are left for the merge launch after
+            // this grid when it defers them)
+            if (np == 1 || !p.defer_merge) {
+                consumer_sync();  // all eight warps reach it, failed or not
+                if (np > 1) {
+                    if (threadIdx.x == 0) {
+                        __threadfence();
+                        *last_flag = (atomicAdd(&p.counters[s], 1) == np - 1) ? 1 : 0;
+                        __threadfence();
+                    }
+                    consumer_sync();
                 }
-                consumer_sync();
-            }
-            if ((np == 1 || *last_flag) && !*abort_flag) {
-                // every piece of this sequence is written: merge them, one warp
-                // per head (warp-shuffle max/sum of the parts' log2-sum-exp,
-                // then the weighted sum of their rows, lanes along head_size).
-                // A round of a merge holds kQB x kHB rows in registers: with one
-                // head per warp (H <= 8) the rounds take more parts instead of
-                // more heads, so that the np x R parts of a short batch cost
-                // one or two L2 round trips.  (The fp8 stage loop leaves fewer
-                // registers: two rows per round.)
-                if (H <= kConsumerWarps)
-                    merge_pieces<D, kFp8 ? 2 : 8, 1>(p, t, s, bf, np * R, R, warp, lane);
-                else
-                    merge_pieces<D, kFp8 ? 1 : 2, kFp8 ? 2 : 4>(p, t, s, bf, np * R, R, warp,
-                                                                 lane);
+                if ((np == 1 || *last_flag) && !*abort_flag) {
+                    // every piece of this sequence is written: merge them, one warp
+                    // per head (warp-shuffle max/sum of the parts' log2-sum-exp,
+                    // then the weighted sum of their rows, lanes along head_size).
+                    // A round of a merge holds kQB x kHB rows in registers: with one
+                    // head per warp (H <= 8) the rounds take more parts instead of
+                    // more heads, so that the np x R parts of a short batch cost
+                    // one or two L2 round trips.  (The fp8 stage loop leaves fewer
+                    // registers: two rows per round.)
+                    if (H <= kConsumerWarps)
+                        merge_pieces<D, kFp8 ? 2 : 8, 1>(p, t, s, bf, np * R, R, warp, lane);
+                    else
+                        merge_pieces<D, kFp8 ? 1 : 2, kFp8 ? 2 : 4>(p, t, s, bf, np * R, R,
+                                                                     warp, lane);
+                }
             }
         }
         if (x + 1 < hi) {
@@ -1099,6 +1115,93 @@ DecodePlan plan_decode(int32_t split_kv_tokens, int32_t num_decodes, int32_t num
     return dp;
 }
 
+// The pieces of every decode that the launch before split over several CTAs
+// (a batch of a few long decodes: each spreads over many SMs), merged by one
+// warp per (decode, head) over the whole GPU instead of by the decode's last
+// CTA, which would fold its many parts a few per L2 round trip while the rest
+// of the GPU idles.  A programmatic dependent of that launch: its CTAs start
+// as the decode's finish and wait for the whole grid before reading.
+struct PieceMergeParams {
+    const float *o_part;    // [slots, R, H, D] normalised partials
+    const float *lse_part;  // [slots, R, H], log2 units
+    const int32_t *table;   // [nseq]: first CTA | pieces << 16, or 0 (not split)
+    const int32_t *qsl;
+    int32_t seq0, nseq, num_heads, R;
+    __nv_bfloat16 *out;
+    float *lse;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) decode_merge_kernel(const PieceMergeParams p)
+{
+    constexpr int kPer = D / 32;  // dims per lane
+    constexpr int kQB = 8;        // parts per round: every load of a round in flight at once
+    using Vec = typename std::conditional<kPer == 4, float4, float2>::type;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int64_t unit = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const int H = p.num_heads;
+    if (unit >= int64_t(p.nseq) * H)
+        return;
+    const int s = static_cast<int>(unit / H), h = static_cast<int>(unit % H);
+    const int32_t e = __ldcg(p.table + s);
+    if (e == 0)
+        return;  // finished by the decode launch
+    const int bf = e & 0xFFFF, nparts = (e >> 16) * p.R;
+    float M = kNegInf, W = 0.f, acc[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k)
+        acc[k] = 0.f;
+    for (int q0 = 0; q0 < nparts; q0 += kQB) {
+        float lq[kQB];
+        Vec v[kQB];
+#pragma unroll
+        for (int i = 0; i < kQB; ++i) {
+            const int q = q0 + i;
+            if (q < nparts) {
+                // part q: slot bf + q / R + s, sub-row q % R
+                const int64_t row = (int64_t(bf + q / p.R + s) * p.R + q % p.R) * H + h;
+                lq[i] = __ldcg(p.lse_part + row);
+                v[i] = __ldcg(reinterpret_cast<const Vec *>(p.o_part + row * D) + lane);
+            } else {
+                lq[i] = kNegInf;
+                v[i] = Vec{};
+            }
+        }
+        float mr = M;
+#pragma unroll
+        for (int i = 0; i < kQB; ++i)
+            mr = fmaxf(mr, lq[i]);
+        if (mr == kNegInf)
+            continue;  // every part so far is empty
+        const float a = exp2f(M - mr);
+        W *= a;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k)
+            acc[k] *= a;
+#pragma unroll
+        for (int i = 0; i < kQB; ++i) {
+            // an empty part adds nothing, whatever its row holds
+            const float w = lq[i] == kNegInf ? 0.f : exp2f(lq[i] - mr);
+            W += w;
+            const float *x = reinterpret_cast<const float *>(&v[i]);
+#pragma unroll
+            for (int k = 0; k < kPer; ++k)
+                acc[k] += w * x[k];
+        }
+        M = mr;
+    }
+    const int64_t row_out = int64_t(p.qsl[p.seq0 + s]) * H + h;
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    __nv_bfloat16 *dst = p.out + row_out * D + lane * kPer;
+#pragma unroll
+    for (int k = 0; k < kPer; k += 2)
+        *reinterpret_cast<__nv_bfloat162 *>(dst + k) =
+            __floats2bfloat162_rn(acc[k] * inv, acc[k + 1] * inv);
+    if (lane == 0 && p.lse)
+        p.lse[row_out] = W > 0.f ? (M + log2f(W)) * kLn2 : kNegInf;
+}
+
 template <int D, bool kHnd, bool kFp8>
 static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Workspace &ws,
                                    char *wsp, const CUtensorMap &kv_map, int32_t kv_begin,
@@ -1149,7 +1252,8 @@ static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Wor
     p.k_scale = f.k_scale;
     p.v_scale = f.v_scale;
     p.test_skip_copies = f.test_skip_copies;
-    p.trigger_dependents = dout.dependent_follows ? 1 : 0;
+    p.trigger_dependents = dout.dependent_follows || dout.defer_merge ? 1 : 0;
+    p.defer_merge = dout.defer_merge ? 1 : 0;
     // one launch per chunk of at most kMaxDecodeChunk decodes (stream ordered,
     // so chunks reuse the same partial slots and counters)
     for (int32_t seq0 = 0; seq0 < f.num_decodes; seq0 += dp.chunk) {
@@ -1179,6 +1283,35 @@ static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Wor
         e = cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, kHnd, kFp8>, kv_map, p);
         if (e != cudaSuccess)
             return e;
+        if (p.defer_merge) {
+            // the split decodes' pieces, merged over the whole GPU as the
+            // decode's programmatic dependent (nothing may stand between them)
+            PieceMergeParams m;
+            m.o_part = p.o_part;
+            m.lse_part = p.lse_part;
+            m.table = p.counters;
+            m.qsl = p.qsl;
+            m.seq0 = p.seq0;
+            m.nseq = p.nseq;
+            m.num_heads = p.num_heads;
+            m.R = kConsumerWarps / p.num_kv_heads;
+            m.out = p.out;
+            m.lse = p.lse;
+            const int64_t warps = int64_t(p.nseq) * p.num_heads;
+            cudaLaunchConfig_t mc = {};
+            cudaLaunchAttribute ma[1];
+            mc.gridDim = dim3(static_cast<unsigned>((warps * 32 + 255) / 256));
+            mc.blockDim = dim3(256);
+            mc.stream = f.stream;
+            ma[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            ma[0].val.programmaticStreamSerializationAllowed = 1;
+            mc.attrs = ma;
+            mc.numAttrs = 1;
+            count_launch();
+            e = cudaLaunchKernelEx(&mc, decode_merge_kernel<D>, m);
+            if (e != cudaSuccess)
+                return e;
+        }
     }
     return cudaSuccess;
 }

@@ -183,6 +183,10 @@ struct DecodeOut {
     // a programmatic dependent launch follows (the cascade's combine, or the
     // prefill pass beside this decode): let it be scheduled as this grid drains
     bool dependent_follows = false;
+    // a decode-only batch of a few long decodes: the pieces of a decode split
+    // over several CTAs are merged by a launch over the whole GPU after the
+    // decode's (its programmatic dependent), not by the decode's last CTA
+    bool defer_merge = false;
 };
 
 // decode.cu: paged decode of sequences [0, num_decodes) over keys

@@ -68,6 +68,17 @@ def test_decode_one_stage_per_sm(oracle, n):
     G.check_batch(oracle, b, label=f"{n} one-stage decodes")
 
 
+# A decode-only batch of a few long decodes (at least four SMs per decode):
+# every decode spreads over many CTAs and their pieces are merged by a launch
+# over the whole GPU after the decode's.
+@pytest.mark.parametrize("H,Hkv,D,bs", [(32, 8, 128, 16), (8, 2, 64, 64), (8, 1, 128, 32)])
+def test_decode_few_long_decodes(oracle, H, Hkv, D, bs):
+    ctx = [6000, 4097, 2500, 31, 5111]  # one of them inside a single CTA
+    b = W.make_batch(_spec(H, Hkv, D, bs, ctx), seed=2500 + Hkv + D)
+    G.check_batch(oracle, b, label="few long decodes")
+    G.check_batch(oracle, b, split_kv_tokens=4096, label="few long decodes, 4096 keys per CTA")
+
+
 def test_decode_many_splits_ragged(oracle):
     rng = np.random.Generator(np.random.PCG64(5))
     ctx = rng.integers(1, 3000, size=24).tolist()

@@ -140,6 +140,15 @@ def test_fp8_decode_small_batch_division(oracle, Hkv, g, stages):
     check_fp8(oracle, b, 0.0625, 0.03125, label=f"Hkv={Hkv} longest {stages} stages")
 
 
+@pytest.mark.parametrize("fused", [False, True])
+def test_fp8_few_long_decodes(oracle, fused):
+    """A few long decodes over an fp8 pool: their pieces merged by the launch
+    after the decode's."""
+    sp = _decode_spec("fp8_few_long", 32, 8, 16, [7000, 3001, 12, 4500])
+    b = W.make_batch(sp, seed=8600)
+    check_fp8(oracle, b, 0.0625, 0.03125, fused=fused, label=f"few long decodes fused={fused}")
+
+
 @pytest.mark.parametrize("layout", ["NHD", "HND"])
 @pytest.mark.parametrize("bs", [16, 64, 256, 1024])
 def test_fp8_decode_layouts_and_pages(oracle, layout, bs):
