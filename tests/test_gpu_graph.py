@@ -109,3 +109,21 @@ def test_graph_replay_of_a_cascade_step():
     assert torch.equal(oe.view(torch.int16), og.view(torch.int16))
     assert torch.equal(le, lg)
     assert torch.equal(pe.view(torch.int16), pg.view(torch.int16))
+
+
+def test_graph_replay_of_a_few_long_decodes():
+    """A decode-only batch of a few long decodes: the decode launch and the
+    merge launch of its split decodes (its programmatic dependent) captured
+    together."""
+    import torch
+
+    import paged_kv_attention_33_gb300 as pka
+
+    sp = W.BatchSpec("graph_few_long", 32, 8, 128, 16, decode_ctx=[6000, 3500, 20, 4100])
+    b = W.make_batch(sp, seed=9400)
+    meta = pka.Meta.from_host(b.query_start_loc, b.seq_lens, b.block_table, sp.num_decodes,
+                              "cuda")
+    (oe, le, pe), (og, lg, pg) = _eager_and_replayed(b, G.to_dev(b.cache, "cuda"), meta, sp)
+    assert torch.equal(oe.view(torch.int16), og.view(torch.int16))
+    assert torch.equal(le, lg)
+    assert torch.equal(pe.view(torch.int16), pg.view(torch.int16))
