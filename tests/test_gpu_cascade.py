@@ -39,6 +39,20 @@ def test_cascade_split_prefix(oracle, H, Hkv, D, bs, P):
     G.check_batch(oracle, b, split_kv_tokens=64, label=f"cascade split P={P}, 64 keys/CTA")
 
 
+@pytest.mark.parametrize("layout,bs", [("NHD", 16), ("HND", 128)])
+def test_cascade_side_by_side(oracle, layout, bs):
+    """A batch the cascade plan runs side by side (48 decodes sharing a
+    1024-token prefix: the prefix pass on part of the SMs, the suffix decode as
+    its dependent on the rest, then the combine), in both pool layouts."""
+    P = 1024
+    rng = np.random.Generator(np.random.PCG64(bs))
+    ctx = (P + rng.integers(64, 800, size=48)).tolist()
+    sp = W.BatchSpec(f"c_sbs_{layout}", 32, 8, 128, bs, decode_ctx=ctx, common_prefix_len=P,
+                     kv_layout=layout)
+    b = W.make_batch(sp, seed=4400 + bs)
+    G.check_batch(oracle, b, label=f"cascade side by side {layout} bs={bs}")
+
+
 def test_cascade_equals_plain(oracle):
     """The same batch with and without the cascade gives the same rows (both
     within tolerance of the oracle's plain attention)."""

@@ -248,6 +248,21 @@ def test_fp8_cascade(oracle, layout, kind):
     check_fp8(oracle, b, 0.05, 0.04, fused=True, label=f"cascade {kind} {layout} fused")
 
 
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+def test_fp8_cascade_side_by_side(oracle, layout):
+    """A cascade the plan runs side by side over an fp8 pool: the prefix blocks'
+    bf16 copy, the prefix pass as that copy's programmatic dependent, the
+    suffix decode (over the codes) as the pass's, then the combine."""
+    P = 1024
+    rng = np.random.Generator(np.random.PCG64(7))
+    ctx = (P + rng.integers(64, 800, size=48)).tolist()
+    sp = W.BatchSpec(f"fp8_casc_sbs_{layout}", 32, 8, 128, 64, decode_ctx=ctx,
+                     common_prefix_len=P, kv_layout=layout)
+    b = W.make_batch(sp, seed=8990)
+    check_fp8(oracle, b, 0.05, 0.04, label=f"cascade side by side {layout}")
+    check_fp8(oracle, b, 0.05, 0.04, fused=True, label=f"cascade side by side {layout} fused")
+
+
 def test_fp8_unserved_batches_are_refused(oracle):
     import torch
 
