@@ -249,6 +249,19 @@ def test_fp8_cascade(oracle, layout, kind):
 
 
 @pytest.mark.parametrize("layout", ["NHD", "HND"])
+def test_fp8_mixed_side_by_side(oracle, layout):
+    """A mixed batch the plan runs side by side over an fp8 pool: the prefill
+    blocks' bf16 copy, the decode over the codes on part of the SMs, the
+    prefill pass as its programmatic dependent on the rest."""
+    ctx = [2000 + 250 * k for k in range(16)]
+    sp = W.BatchSpec(f"fp8_mixed_sbs_{layout}", 32, 8, 128, 64, decode_ctx=ctx,
+                     prefill=[(256, 1000), (256, 1500)], kv_layout=layout)
+    b = W.make_batch(sp, seed=8995)
+    check_fp8(oracle, b, 0.05, 0.04, label=f"mixed side by side {layout}")
+    check_fp8(oracle, b, 0.05, 0.04, fused=True, label=f"mixed side by side {layout} fused")
+
+
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
 def test_fp8_cascade_side_by_side(oracle, layout):
     """A cascade the plan runs side by side over an fp8 pool: the prefix blocks'
     bf16 copy, the prefix pass as that copy's programmatic dependent, the

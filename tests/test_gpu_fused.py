@@ -61,6 +61,14 @@ CASES = {
     "hnd_small_pages_context": dict(H=16, Hkv=4, D=64, bs=16, decode_ctx=[40],
                                     prefill=[(400, 130), (300, 0), (300, 255)],
                                     kv_layout="HND"),
+    # batches the mixed plan runs side by side: the decode on part of the SMs,
+    # the prefill pass as its programmatic dependent on the rest
+    "mixed_side_by_side": dict(H=32, Hkv=8, D=128, bs=16,
+                               decode_ctx=[2000 + 250 * k for k in range(16)],
+                               prefill=[(256, 1000), (256, 1500)]),
+    "hnd_mixed_side_by_side": dict(H=32, Hkv=8, D=128, bs=64,
+                                   decode_ctx=[6000 - 230 * k for k in range(16)],
+                                   prefill=[(256, 1400), (200, 900)], kv_layout="HND"),
 }
 
 
