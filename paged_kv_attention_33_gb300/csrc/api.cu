@@ -928,6 +928,17 @@ static pka_status forward_impl(const void *query, const void *kv_cache, const pk
             int64_t(meta->num_decodes) * longest > dp.grid)
             dout.defer_merge = true;
     }
+    // A small decode-only batch that the kernel divides one sequence per CTA
+    // (at most kAlignedMaxStages stages per decode and at most one stage per
+    // CTA in all, by max_seq_len) merges no pieces across CTAs: its counters
+    // are not reset (one launch less; the kernel checks the lengths).
+    if (!cascade && num_prefills == 0 && meta->num_decodes > 0 && dp.target_keys == 0 &&
+        dp.chunk >= meta->num_decodes) {
+        const int64_t sk = int64_t(f.kv_fp8 ? 32 : 16) * (8 / num_kv_heads);  // keys per stage
+        const int64_t longest = std::max<int64_t>(1, (int64_t(meta->max_seq_len) + sk - 1) / sk);
+        if (longest <= kAlignedMaxStages && int64_t(meta->num_decodes) * longest <= dp.grid)
+            dout.expect_aligned = true;
+    }
     if (!cp.overlap)
         record_start(PKA_KERNEL_DECODE, f.stream);
     e = launch_decode(f, dp, ws, wsp, kv_map, kv_begin, dout);

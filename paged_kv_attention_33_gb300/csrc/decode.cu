@@ -107,6 +107,9 @@ struct DecodeParams {
     // that pass completed (griddepcontrol.wait before every CTA exits)
     int32_t after_prefix;
     int32_t trigger_dependents;  // a programmatic dependent launch follows
+    // the host did not reset the counters, expecting the one-sequence-per-CTA
+    // division (kAlignedMaxStages); a batch that does not allow it is flagged
+    int32_t expect_aligned;
     float *o_part;        // [slots, R, H, D] normalised partials
     float *lse_part;      // [slots, R, H], log2 units
     int32_t *counters;    // [nseq] pieces finished per sequence (zeroed before the launch)
@@ -131,12 +134,6 @@ struct DecodeParams {
 constexpr int kConsumerWarps = 8;
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxDecodeChunk = 4096;
-// A batch of at most one stage per SM whose longest sequence has at most this
-// many stages is divided one sequence per CTA instead of evenly: no sequence
-// is split over CTAs, so none waits on a cross-CTA merge (a fence, an atomic
-// count and an L2 round trip of partials, several microseconds), while one CTA
-// streams a few stages in well under that.
-constexpr int kAlignedMaxStages = 8;
 constexpr float kNegInf = -INFINITY;
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -410,6 +407,13 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap &kv_map, const Deco
     if (p.target_keys == 0 && total <= grid) {
         const int k = threadIdx.x;
         aligned = !__syncthreads_or(k < nseq && prefix[k + 1] - prefix[k] > kAlignedMaxStages);
+    }
+    if (p.expect_aligned && !aligned) {
+        // (the same in every CTA) a decode longer than max_seq_len: the
+        // counters hold leftovers, so nothing is computed
+        if (blockIdx.x == 0 && threadIdx.x == 0)
+            flag_error(kErrBadMetadata);
+        return;
     }
     if (aligned)
         grid = nseq;
@@ -1254,13 +1258,14 @@ static cudaError_t launch_decode_d(const Fwd &f, const DecodePlan &dp, const Wor
     p.test_skip_copies = f.test_skip_copies;
     p.trigger_dependents = dout.dependent_follows || dout.defer_merge ? 1 : 0;
     p.defer_merge = dout.defer_merge ? 1 : 0;
+    p.expect_aligned = dout.expect_aligned ? 1 : 0;
     // one launch per chunk of at most kMaxDecodeChunk decodes (stream ordered,
     // so chunks reuse the same partial slots and counters)
     for (int32_t seq0 = 0; seq0 < f.num_decodes; seq0 += dp.chunk) {
         p.seq0 = seq0;
         p.nseq = std::min(dp.chunk, f.num_decodes - seq0);
         cudaError_t e = cudaSuccess;
-        if (seq0 > 0 || !dout.counters_zeroed)
+        if (seq0 > 0 || !(dout.counters_zeroed || dout.expect_aligned))
             e = cudaMemsetAsync(p.counters, 0, size_t(p.nseq) * 4, f.stream);
         if (e != cudaSuccess)
             return e;

@@ -166,6 +166,12 @@ uint32_t kv_write_take_error();
 
 // Most key chunks of a cascade's shared-prefix pass (partials per row).
 constexpr int32_t kMaxPrefixSplits = 8;
+// A decode batch of at most one stage per SM whose longest sequence has at most
+// this many stages is divided one sequence per CTA instead of evenly: no
+// sequence is split over CTAs, so none waits on a cross-CTA merge (a fence, an
+// atomic count and an L2 round trip of partials, several microseconds), while
+// one CTA streams a few stages in well under that.
+constexpr int kAlignedMaxStages = 8;
 
 // Where the decode launch puts its rows.
 struct DecodeOut {
@@ -183,6 +189,11 @@ struct DecodeOut {
     // a programmatic dependent launch follows (the cascade's combine, or the
     // prefill pass beside this decode): let it be scheduled as this grid drains
     bool dependent_follows = false;
+    // the batch is small enough, by max_seq_len, for the kernel to divide it
+    // one sequence per CTA (kAlignedMaxStages): no piece is merged across
+    // CTAs, so the per-decode counters are not reset (a batch longer than
+    // max_seq_len says is flagged by the kernel, which then computes nothing)
+    bool expect_aligned = false;
     // a decode-only batch of a few long decodes: the pieces of a decode split
     // over several CTAs are merged by a launch over the whole GPU after the
     // decode's (its programmatic dependent), not by the decode's last CTA

@@ -79,6 +79,62 @@ def test_decode_few_long_decodes(oracle, H, Hkv, D, bs):
     G.check_batch(oracle, b, split_kv_tokens=4096, label="few long decodes, 4096 keys per CTA")
 
 
+def test_small_batch_longer_than_max_seq_len_is_flagged(oracle):
+    """A decode-only batch that max_seq_len says the kernel divides one
+    sequence per CTA skips the counter reset.  A decode longer than
+    max_seq_len (too long for that division) is flagged, nothing is computed,
+    and the next call is served."""
+    import torch
+
+    import paged_kv_attention_33_gb300 as pka
+
+    sp = _spec(8, 2, 64, 16, [1000, 9, 30])  # 1,001 keys: 16 stages of 64 keys
+    b = W.make_batch(sp, seed=2320)
+    meta = pka.Meta.from_host(b.query_start_loc, b.seq_lens, b.block_table, 3, "cuda")
+    meta.max_seq_len = 64  # understated: one stage per decode by this bound
+    q = G.to_dev(b.query, "cuda")
+    out = torch.empty_like(q)
+    pka.paged_attn_forward(q, G.to_dev(b.cache, "cuda"), meta, out, scale=sp.softmax_scale)
+    with pytest.raises(pka.PkaError) as e:
+        pka.check_status()
+    assert e.value.status == -5
+    pka.check_status()
+    G.check_batch(oracle, b, label="the true max_seq_len")
+
+
+def test_one_sequence_per_cta_ignores_counter_leftovers(oracle):
+    """A workspace whose counters hold a split batch's piece counts serves a
+    small batch divided one sequence per CTA (its counters are not reset)."""
+    import torch
+
+    import paged_kv_attention_33_gb300 as pka
+
+    dev = "cuda"
+    ws = torch.zeros(1 << 24, dtype=torch.uint8, device=dev)
+    for ctx, seed in (([3000, 2000, 1500, 700], 2321), ([40, 100, 7, 0], 2322)):
+        b = W.make_batch(_spec(32, 8, 128, 16, ctx), seed=seed)
+        sp = b.spec
+        want = G.host_bits(b.cache).copy()
+        oracle.reshape_and_cache(G.host_bits(b.key), G.host_bits(b.value), want, b.slot_mapping)
+        cache = G.to_dev(b.cache, dev)
+        pka.reshape_and_cache(G.to_dev(b.key, dev), G.to_dev(b.value, dev), cache,
+                              torch.from_numpy(b.slot_mapping).to(dev))
+        meta = pka.Meta.from_host(b.query_start_loc, b.seq_lens, b.block_table,
+                                  sp.num_decodes, dev)
+        T = b.num_tokens
+        out = torch.full((T, sp.num_heads, sp.head_size), float("nan"), dtype=torch.bfloat16,
+                         device=dev)
+        lse = torch.full((T, sp.num_heads), float("nan"), dtype=torch.float32, device=dev)
+        pka.paged_attn_forward(G.to_dev(b.query, dev), cache, meta, out, lse,
+                               scale=sp.softmax_scale, workspace=ws)
+        pka.check_status()
+        rows = np.arange(T * sp.num_heads, dtype=np.int64)
+        o_ref, l_ref = G.oracle_expected(oracle, b, want, rows=rows)
+        res = G.compare(W.to_host_bits(out), lse.cpu().numpy(), o_ref, l_ref, rows,
+                        sp.num_heads)
+        G.assert_close(res, f"ctx {ctx}")
+
+
 def test_decode_many_splits_ragged(oracle):
     rng = np.random.Generator(np.random.PCG64(5))
     ctx = rng.integers(1, 3000, size=24).tolist()
