@@ -993,11 +993,12 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap &kv_map, const Deco
                     // head per warp (H <= 8) the rounds take more parts instead of
                     // more heads, so that the np x R parts of a short batch cost
                     // one or two L2 round trips.  (The fp8 stage loop leaves fewer
-                    // registers: two rows per round.)
+                    // registers: two rows per round with one head per warp, four
+                    // with more.)
                     if (H <= kConsumerWarps)
                         merge_pieces<D, kFp8 ? 2 : 8, 1>(p, t, s, bf, np * R, R, warp, lane);
                     else
-                        merge_pieces<D, kFp8 ? 1 : 2, kFp8 ? 2 : 4>(p, t, s, bf, np * R, R,
+                        merge_pieces<D, 2, kFp8 ? 2 : 4>(p, t, s, bf, np * R, R,
                                                                      warp, lane);
                 }
             }
